@@ -1,0 +1,241 @@
+/*
+ * nvfp4moe.h -- C ABI of the NVFP4 fused mixture-of-experts layer forward (one GPU).
+ *
+ * The operation: a mixture-of-experts layer with routed experts plus one always-on
+ * shared expert and top-k routing (Solar Open 2 on DGX Spark, "Solar Open 2 개요": 320
+ * routed, 1 shared, top-8), NVFP4 weights (packed FP4 codes, FP8 E4M3 block scales of
+ * 16 elements clamped at 448, one FP32 global scale per expert and projection; same
+ * page, "b12x 버전이 실제 NVFP4 체크포인트를 읽어들이도록 만들기"), a fused gate/up
+ * projection followed by silu(gate)*up and a down projection, and expert parallelism by
+ * a contiguous shard of experts selected by local_expert_offset, whose output is the
+ * shard's partial sum (same page, "b12x에서의 Expert Parallelism 구현 추가").
+ *
+ * Conventions for every call:
+ *   - Pointers named *_d are device pointers; all tensors are caller-owned unless stated.
+ *     moe_create copies the weights into its own re-laid-out buffers: the caller may free
+ *     its copies once moe_create returns.
+ *   - Every call is asynchronous and ordered on the given stream (0 = legacy default).
+ *   - Argument errors are reported synchronously, before anything is launched, with
+ *     MOE_ERR_INVALID / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE.  CUDA launch errors give
+ *     MOE_ERR_CUDA.  Errors found on the device (an expert id outside [0, E), a bounded
+ *     wait that ran out) set a status word in the workspace, drop the offending work and
+ *     never trap; moe_get_status reads and clears it.  moe_forward clears the word when
+ *     it starts; the staged calls only add to it, so a new workspace is zero-filled (or
+ *     cleared with moe_get_status) before staged calls are checked.
+ *   - No exceptions cross this boundary.  A handle is immutable after moe_create:
+ *     concurrent calls on one handle are safe with separate workspaces.
+ *   - bf16 tensors are passed as uint16_t bit patterns (void* in signatures).
+ *
+ * Layouts:
+ *   canonical NVFP4 matrix [R][K]: codes uint8 [R][K/2], element 2i in the low nibble and
+ *     2i+1 in the high nibble; block scales uint8 (E4M3) [R][K/16]; the value of an
+ *     element is E2M1(code) * E4M3(scale) / gs, gs the FP32 global (encode) scale.
+ *   padded rows: the grouped GEMMs work on "padded rows" -- the routed (token, expert)
+ *     pairs grouped by local expert (ascending pair index p = t*k + j inside a group),
+ *     each group starting on a multiple of 128 rows, followed by a group of T rows for the
+ *     shared expert.  expert_offsets[g] is the first padded row of group g
+ *     (g = 0..E_loc-1 routed, g = E_loc shared), expert_offsets[E_loc+1] the total.
+ *   tiled NVFP4 activations (the GEMM operand layout): codes uint8 [rows][pitch] with
+ *     pitch = round_up(K/2, 128) bytes; scales in 512-byte atoms, one per (128-row block
+ *     rb, 64-element k-step s) at byte ((rb * K/64) + s) * 512, and inside an atom row m
+ *     (0..127) scale kk (0..3) at byte (m % 32) * 16 + (m / 32) * 4 + kk.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* cudaStream_t without the CUDA headers. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID = 1,        /* bad argument (null pointer, size out of range) */
+    MOE_ERR_UNSUPPORTED = 2,    /* valid but unsupported shape or mode */
+    MOE_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
+    MOE_ERR_WORKSPACE = 4,      /* workspace smaller than moe_workspace_size */
+    MOE_ERR_TIMEOUT = 5,        /* a bounded device wait ran out (see moe_get_status) */
+    MOE_ERR_DEVICE_STATUS = 6   /* the device flagged bad data (see moe_get_status) */
+} moe_status;
+
+typedef enum {
+    MOE_W4A4_DYNAMIC = 0,   /* NVFP4 activations, global scale 2688/amax(x) per call */
+    MOE_W4A4_STATIC = 1,    /* NVFP4 activations, global scale act_global_scale */
+    MOE_W4A16 = 2           /* bf16 activations x NVFP4 weights */
+} moe_act_mode;
+
+/* Device status bits (moe_get_status's *bits). */
+#define MOE_DEV_BAD_EXPERT_ID  0x1u   /* a top-k id outside [0, num_experts): pair dropped */
+#define MOE_DEV_WAIT_TIMEOUT   0x2u   /* a pipeline wait ran out: that tile was abandoned */
+#define MOE_DEV_ROWS_OVERFLOW  0x4u   /* padded rows exceeded capacity: pairs dropped */
+
+typedef struct {
+    int32_t hidden;               /* H: multiple of 128 */
+    int32_t inter;                /* I: multiple of 64 */
+    int32_t num_experts;          /* E: global routed experts, 1..1024 */
+    int32_t top_k;                /* k: 1..min(E, 32) */
+    int32_t num_local_experts;    /* E_loc: experts held by this shard, 0..E */
+    int32_t local_expert_offset;  /* global id of local expert 0; off + E_loc <= E */
+    int32_t has_shared;           /* 1 if the layer has the shared expert */
+    int32_t shared_inter;         /* intermediate size of the shared expert (== inter) */
+    int32_t add_shared;           /* 1: add the shared expert into THIS partial sum */
+    int32_t act_mode;             /* moe_act_mode */
+    float act_global_scale;       /* MOE_W4A4_STATIC only */
+    float inter_global_scale;     /* static global scale of the intermediate (W4A4) */
+    int32_t max_tokens;           /* largest T a call may pass */
+} moe_config;
+
+/* Device pointers, canonical layouts (see above). */
+typedef struct {
+    const void* router_w_d;       /* bf16 [E][H] (global E: routing is global) */
+    const uint8_t* w13_d;         /* [E_loc][2I][H/2]; rows 0..I-1 gate, I..2I-1 up */
+    const uint8_t* w13_sf_d;      /* [E_loc][2I][H/16] */
+    const float* w13_gs_d;        /* [E_loc] */
+    const uint8_t* w2_d;          /* [E_loc][H][I/2] */
+    const uint8_t* w2_sf_d;       /* [E_loc][H][I/16] */
+    const float* w2_gs_d;         /* [E_loc] */
+    const uint8_t* sh13_d;        /* shared expert, [2I][H/2] (NULL when !has_shared) */
+    const uint8_t* sh13_sf_d;     /* [2I][H/16] */
+    const float* sh13_gs_d;       /* [1] */
+    const uint8_t* sh2_d;         /* [H][I/2] */
+    const uint8_t* sh2_sf_d;      /* [H][I/16] */
+    const float* sh2_gs_d;        /* [1] */
+} moe_weights;
+
+typedef struct moe_layer* moe_handle;
+
+/* Validates cfg, allocates the handle and device copies of the weights re-laid out for
+ * the grouped GEMMs (gate/up rows interleaved in blocks of 16 inside each 128-row tile,
+ * scales in 512-byte atoms, one extra expert slot for the shared expert).  Synchronises
+ * the stream before returning.  *out receives the handle (NULL on error). */
+MOE_API moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t stream,
+                      moe_handle* out);
+MOE_API void moe_destroy(moe_handle h);
+
+/* Bytes of workspace a call with T tokens needs (moe_forward and the staged calls).
+ * One workspace may be shared by every layer of a model (calls on one stream). */
+MOE_API size_t moe_workspace_size(const moe_config* cfg, int32_t T);
+
+/* Padded-row capacity for T tokens: every buffer indexed by padded row is sized to it. */
+MOE_API int32_t moe_rows_capacity(const moe_config* cfg, int32_t T);
+
+/* Router (steps: logits, softmax + top-k).  logits = x . Wr^T (+ logit_bias) in fp32, or
+ * logits_in (+ logit_bias) when given.  topk_ids_d[T][k]: the k largest logits,
+ * descending, ties to the lower id; topk_w_d[T][k]: softmax over the selected logits.
+ * logits_out_d (nullable): fp32 [T][E] including the bias.  x_bf16_d may be NULL when
+ * logits_in_d is set.  ws: scratch for the logits when they are computed from x. */
+MOE_API moe_status moe_route_topk(moe_handle h, const void* x_bf16_d, const float* logits_in_d,
+                          const float* logit_bias_d, int32_t T, int32_t* topk_ids_d,
+                          float* topk_w_d, float* logits_out_d, void* ws_d, size_t ws_bytes,
+                          moe_stream_t stream);
+
+/* Local map + grouping (the "compact pre-pass").  Pair p = t*k + j with local expert
+ * e' = topk_ids[p] - local_expert_offset is kept iff 0 <= e' < E_loc (a pair with an id
+ * outside [0, E) is dropped and sets MOE_DEV_BAD_EXPERT_ID).  Outputs:
+ *   expert_counts_d[E_loc+1]  rows of each group (group E_loc: T if the shared expert is
+ *                             added by this shard, else 0)
+ *   expert_offsets_d[E_loc+2] padded first row of each group, [E_loc+1] = total
+ *   perm_src_d[rows_capacity] pair index of each padded row (T*k + t for shared rows,
+ *                             -1 for padding)
+ *   inv_d[T*k]                padded row of each pair, -1 if dropped
+ * ws: the workspace (its tile table is filled here and read by the grouped GEMMs). */
+MOE_API moe_status moe_permute(moe_handle h, const int32_t* topk_ids_d, int32_t T,
+                       int32_t* expert_counts_d, int32_t* expert_offsets_d,
+                       int32_t* perm_src_d, int32_t* inv_d, void* ws_d, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* NVFP4 quantiser of a bf16 matrix [rows][cols] (cols % 64 == 0).  gs_in_d NULL: dynamic
+ * global scale 2688/amax over the whole matrix (written to gs_out_d); else the scale
+ * *gs_in_d.  sf_layout 0: canonical codes [rows][cols/2], scales [rows][cols/16];
+ * sf_layout 1: tiled (pitch-padded codes, 512-byte scale atoms).  ws: scratch for amax. */
+MOE_API moe_status moe_quant_nvfp4(const void* x_bf16_d, int32_t rows, int32_t cols,
+                           const float* gs_in_d, float* gs_out_d, uint8_t* codes_d,
+                           uint8_t* sf_d, int32_t sf_layout, void* ws_d, size_t ws_bytes,
+                           moe_stream_t stream);
+
+/* Gather-quantise: NVFP4-quantise the T rows of x with gs (dynamic or static per the
+ * handle's act_mode) and write row t to every padded row of its local pairs and to its
+ * shared row, in the tiled layout (W4A4).  W4A16: copy the bf16 rows instead
+ * (a_bf16_d [rows_capacity][H]).  gs_out_d receives the scale used (W4A4). */
+MOE_API moe_status moe_gather_activations(moe_handle h, const void* x_bf16_d, int32_t T,
+                                  const int32_t* inv_d, const int32_t* expert_offsets_d,
+                                  uint8_t* a_codes_d, uint8_t* a_sf_d, void* a_bf16_d,
+                                  float* gs_out_d, void* ws_d, size_t ws_bytes,
+                                  moe_stream_t stream);
+
+/* Grouped GEMM gate_up over the padded rows: for group g with expert weights W13_g,
+ * G = A_g . W13_g^T / (gs_a * gs13_g) (W4A4; W4A16: A_g . W13_g^T / gs13_g).
+ *   fuse_epilogue 0: gateup_f32_d [rows_capacity][2I] fp32 (gate cols 0..I-1, up I..2I-1)
+ *   fuse_epilogue 1: s = silu(gate) * up, then
+ *       W4A4 : NVFP4 with inter_global_scale -> inter_codes_d / inter_sf_d (tiled, K = I)
+ *       W4A16: bf16 -> inter_bf16_d [rows_capacity][I]
+ * Padding rows of the outputs are left unwritten. */
+MOE_API moe_status moe_grouped_gemm_gateup(moe_handle h, const uint8_t* a_codes_d,
+                                   const uint8_t* a_sf_d, const float* gs_a_d,
+                                   const void* a_bf16_d, const int32_t* expert_counts_d,
+                                   const int32_t* expert_offsets_d, int32_t fuse_epilogue,
+                                   float* gateup_f32_d, uint8_t* inter_codes_d,
+                                   uint8_t* inter_sf_d, void* inter_bf16_d, int32_t T,
+                                   void* ws_d, size_t ws_bytes, moe_stream_t stream);
+
+/* SwiGLU + NVFP4 requantisation of fp32 gate/up rows [rows][2I] (gate cols 0..I-1):
+ * s = silu(g) * u in fp32, quantised with the static scale gs_i.  sf_layout as for
+ * moe_quant_nvfp4 (0 canonical, 1 tiled). */
+MOE_API moe_status moe_swiglu_requant(const float* gateup_f32_d, int32_t rows, int32_t inter,
+                              float gs_i, uint8_t* codes_d, uint8_t* sf_d, int32_t sf_layout,
+                              moe_stream_t stream);
+
+/* Grouped GEMM down: Y_g = Aq_g . W2_g^T / (gs_i * gs2_g) (W4A16: / gs2_g), each row
+ * multiplied by its routing weight (1 for shared rows) and written to
+ * y_d[perm_src[row]][H] fp32 -- i.e. y is indexed by pair p = t*k + j, shared rows at
+ * T*k + t; rows of dropped pairs are left unwritten. */
+MOE_API moe_status moe_grouped_gemm_down(moe_handle h, const uint8_t* inter_codes_d,
+                                 const uint8_t* inter_sf_d, const void* inter_bf16_d,
+                                 const int32_t* expert_counts_d,
+                                 const int32_t* expert_offsets_d, const int32_t* perm_src_d,
+                                 const float* topk_w_d, float* y_d, int32_t T, void* ws_d,
+                                 size_t ws_bytes, moe_stream_t stream);
+
+/* Combine: out[t] = sum_{j: inv[t*k+j] >= 0} y[t*k+j] + (add_shared ? y[T*k+t] : 0),
+ * summed in ascending j then the shared term in fp32, rounded to bf16. */
+MOE_API moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* inv_d, int32_t T,
+                       void* out_bf16_d, moe_stream_t stream);
+
+/* The whole layer: route, permute, gather-quantise, gate_up (fused SwiGLU+requant),
+ * down, combine.  logits_in_d (nullable): given router logits [T][E] instead of x.Wr^T;
+ * logit_bias_d (nullable) [E].  out_bf16_d [T][H] receives this shard's partial sum. */
+MOE_API moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_in_d,
+                       const float* logit_bias_d, int32_t T, void* out_bf16_d, void* ws_d,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/* Where moe_forward keeps its intermediates inside the workspace (device pointers into
+ * ws_d), so callers can inspect them after a forward.  Any pointer may be NULL. */
+MOE_API moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** topk_ids,
+                               float** topk_w, int32_t** expert_counts,
+                               int32_t** expert_offsets, int32_t** perm_src, int32_t** inv,
+                               float** gs_a, uint8_t** a_codes, uint8_t** a_sf,
+                               uint8_t** inter_codes, uint8_t** inter_sf, float** y);
+
+/* Reads the device status word of ws (synchronises the stream) into *bits (nullable) and
+ * clears it.  Returns MOE_OK, MOE_ERR_TIMEOUT (MOE_DEV_WAIT_TIMEOUT set) or
+ * MOE_ERR_DEVICE_STATUS (other bits set). */
+MOE_API moe_status moe_get_status(moe_handle h, void* ws_d, moe_stream_t stream, uint32_t* bits);
+
+MOE_API const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4MOE_H */

@@ -1,0 +1,694 @@
+// C ABI of the NVFP4 fused mixture-of-experts layer: argument checks, the workspace plan,
+// tensor-map encoding and the launch sequence of the forward.  Every step of the forward
+// runs in this library's kernels; there is no host or library fallback.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+// ---------------------------------------------------------------- driver entry point
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D tensor map over rows of row_bytes (dims in elements of dtype).
+bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dtype, uint64_t inner,
+               uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+               CUtensorMapSwizzle swz)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || rows == 0) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------- workspace plan
+struct Plan {
+    int T, k, E, El, G, H, I, cap, nblk, Tk;
+    size_t status, amax, gs_a, ids, w, logits, hist, blkoff, counts, offsets, mb_start,
+        perm_src, inv, a_codes, a_sf, a_bf16, i_codes, i_sf, i_bf16, y, total;
+};
+
+int rows_cap(const moe_config& c, int T)
+{
+    if (T <= 0) return 0;
+    const int64_t P = (int64_t)T * c.top_k;
+    const int64_t routed =
+        128 * ((P + 127) / 128 + (int64_t)std::min<int64_t>(c.num_local_experts, P));
+    const int64_t shared = (c.has_shared && c.add_shared) ? ((int64_t)T + 127) / 128 * 128 : 0;
+    const int64_t cap = routed + shared;
+    return cap > 0x7fffffff ? -1 : (int)cap;
+}
+
+Plan plan(const moe_config& c, int T)
+{
+    Plan p;
+    p.T = T;
+    p.k = c.top_k;
+    p.E = c.num_experts;
+    p.El = c.num_local_experts;
+    p.G = p.El + 1;
+    p.H = c.hidden;
+    p.I = c.inter;
+    p.cap = rows_cap(c, T);
+    p.Tk = T * c.top_k;
+    p.nblk = std::max(1, ceil_div(p.Tk, kPairsPerBlock));
+    const bool a16 = c.act_mode == MOE_W4A16;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += align256(bytes);
+        return at;
+    };
+    p.status = take(4);
+    p.amax = take(4);
+    p.gs_a = take(4);
+    p.ids = take((size_t)p.Tk * 4);
+    p.w = take((size_t)p.Tk * 4);
+    p.logits = take((size_t)T * p.E * 4);
+    p.hist = take((size_t)p.nblk * p.El * 4);
+    p.blkoff = take((size_t)p.nblk * p.El * 4);
+    p.counts = take((size_t)p.G * 4);
+    p.offsets = take((size_t)(p.G + 1) * 4);
+    p.mb_start = take((size_t)(p.G + 1) * 4);
+    p.perm_src = take((size_t)p.cap * 4);
+    p.inv = take((size_t)p.Tk * 4);
+    p.a_codes = take(a16 ? 0 : (size_t)p.cap * codes_pitch(p.H));
+    p.a_sf = take(a16 ? 0 : (size_t)p.cap * (p.H / 16));
+    p.a_bf16 = take(a16 ? (size_t)p.cap * p.H * 2 : 0);
+    p.i_codes = take(a16 ? 0 : (size_t)p.cap * codes_pitch(p.I));
+    p.i_sf = take(a16 ? 0 : (size_t)p.cap * (p.I / 16));
+    p.i_bf16 = take(a16 ? (size_t)p.cap * p.I * 2 : 0);
+    p.y = take((size_t)(p.Tk + T) * p.H * 4);
+    p.total = o;
+    return p;
+}
+
+template <typename T>
+T* at(void* ws, size_t off)
+{
+    return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+moe_status check_launch()
+{
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- the handle
+struct moe_layer {
+    moe_config cfg;
+    int device = 0, num_sms = 0;
+    uint16_t* router_w = nullptr;              // [E][H] bf16
+    uint8_t *w13 = nullptr, *w13_sf = nullptr;  // tiled, G slots
+    uint8_t *w2 = nullptr, *w2_sf = nullptr;
+    float *gs13 = nullptr, *gs2 = nullptr;     // [G]
+    float* act_gs = nullptr;                   // static activation scale (device copy)
+    CUtensorMap tm_w13, tm_w2;                 // W4A4: 128 B x 128 rows, 128-byte swizzle
+    CUtensorMap tm_w13_raw, tm_w2_raw;         // W4A16: 32 B x 128 rows, no swizzle
+};
+
+namespace {
+
+bool valid_cfg(const moe_config* c, moe_status* why)
+{
+    *why = MOE_ERR_INVALID;
+    if (!c) return false;
+    if (c->hidden <= 0 || c->inter <= 0 || c->num_experts <= 0 || c->top_k <= 0) return false;
+    if (c->num_local_experts < 0 || c->local_expert_offset < 0) return false;
+    if (c->local_expert_offset + c->num_local_experts > c->num_experts) return false;
+    if (c->top_k > c->num_experts) return false;
+    if (c->max_tokens < 0) return false;
+    if (c->act_mode < 0 || c->act_mode > 2) return false;
+    if (c->act_mode == MOE_W4A4_STATIC && !(c->act_global_scale > 0.0f)) return false;
+    if (c->act_mode != MOE_W4A16 && !(c->inter_global_scale > 0.0f)) return false;
+    *why = MOE_ERR_UNSUPPORTED;
+    if (c->hidden % 128 || c->inter % 64) return false;
+    if (c->num_experts > kMaxExperts || c->top_k > kMaxTopK) return false;
+    if (c->has_shared && c->shared_inter != c->inter) return false;
+    if (rows_cap(*c, c->max_tokens) < 0) return false;
+    *why = MOE_OK;
+    return true;
+}
+
+moe_status check_ws(const moe_layer* h, int T, void* ws, size_t ws_bytes)
+{
+    if (!ws) return MOE_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MOE_ERR_INVALID;
+    if (ws_bytes < plan(h->cfg, T).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+bool t_ok(const moe_layer* h, int T) { return T >= 0 && T <= h->cfg.max_tokens; }
+
+int grid_for(int64_t threads, int block) { return (int)std::max<int64_t>(1, (threads + block - 1) / block); }
+
+// Upper bound on the GEMM tile count for T tokens (the exact count is on the device).
+int gemm_grid(const moe_layer* h, int T, int N)
+{
+    const int64_t P = (int64_t)T * h->cfg.top_k;
+    int64_t mb = (P + 127) / 128 + std::min<int64_t>(h->cfg.num_local_experts, P);
+    if (h->cfg.has_shared && h->cfg.add_shared) mb += (T + 127) / 128;
+    const int64_t tiles = mb * (N / 128);
+    return (int)std::max<int64_t>(1, std::min<int64_t>(tiles, h->num_sms));
+}
+
+int shared_rows(const moe_layer* h, int T)
+{
+    return (h->cfg.has_shared && h->cfg.add_shared) ? T : 0;
+}
+
+// ---- launch pieces (no argument checks; callers validated)
+
+moe_status launch_route(const moe_layer* h, const void* x, const float* logits_in,
+                        const float* bias, int T, int32_t* ids, float* w, float* logits_out,
+                        float* logits_scratch, cudaStream_t s)
+{
+    const moe_config& c = h->cfg;
+    const float* src = logits_in;
+    if (!logits_in) {
+        dim3 grid(ceil_div(c.num_experts, 4), ceil_div(T, 64));
+        router_logits_kernel<<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(x), h->router_w,
+                                                  nullptr, T, c.hidden, c.num_experts,
+                                                  logits_scratch);
+        src = logits_scratch;
+    }
+    topk_kernel<<<grid_for((int64_t)T * 32, 256), 256, 0, s>>>(src, bias, T, c.num_experts,
+                                                               c.top_k, ids, w, logits_out);
+    return check_launch();
+}
+
+moe_status launch_permute(const moe_layer* h, const Plan& p, const int32_t* ids, int T,
+                          int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* inv,
+                          void* ws, cudaStream_t s)
+{
+    const moe_config& c = h->cfg;
+    uint32_t* status = at<uint32_t>(ws, p.status);
+    int32_t* hist = at<int32_t>(ws, p.hist);
+    int32_t* blkoff = at<int32_t>(ws, p.blkoff);
+    int32_t* mb_start = at<int32_t>(ws, p.mb_start);
+    perm_hist_kernel<<<p.nblk, 256, 0, s>>>(ids, p.Tk, c.num_experts, c.local_expert_offset,
+                                            p.El, hist, status);
+    perm_scan_kernel<<<1, 1024, 0, s>>>(hist, p.nblk, p.El, T, c.top_k, shared_rows(h, T),
+                                        p.cap, blkoff, counts, offsets, mb_start, perm_src,
+                                        status);
+    perm_scatter_kernel<<<p.nblk, 32, 0, s>>>(ids, p.Tk, c.num_experts, c.local_expert_offset,
+                                              p.El, blkoff, offsets, p.cap, perm_src, inv);
+    return check_launch();
+}
+
+moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T,
+                         const int32_t* inv, const int32_t* offsets, uint8_t* a_codes,
+                         uint8_t* a_sf, void* a_bf16, float* gs_out, void* ws, cudaStream_t s)
+{
+    const moe_config& c = h->cfg;
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    const int add = shared_rows(h, T) > 0 ? 1 : 0;
+    if (c.act_mode == MOE_W4A16) {
+        gather_bf16_kernel<<<grid_for((int64_t)T * 32, 256), 256, 0, s>>>(
+            xb, T, c.hidden, c.top_k, inv, offsets, p.El, add, static_cast<uint16_t*>(a_bf16));
+        return check_launch();
+    }
+    uint32_t* amax = at<uint32_t>(ws, p.amax);
+    const float* gs_static = nullptr;
+    if (c.act_mode == MOE_W4A4_DYNAMIC) {
+        if (cudaMemsetAsync(amax, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+        const int64_t n = (int64_t)T * c.hidden;
+        const int blocks = (int)std::min<int64_t>(2 * h->num_sms, std::max<int64_t>(1, n / 2048));
+        amax_bf16_kernel<<<blocks, 256, 0, s>>>(xb, n, amax);
+    } else {
+        gs_static = h->act_gs;  // the handle's device copy of act_global_scale
+    }
+    gather_quant_kernel<<<grid_for((int64_t)T * 32, 256), 256, 0, s>>>(
+        xb, T, c.hidden, c.top_k, inv, offsets, p.El, add, gs_static, amax, a_codes, a_sf, gs_out);
+    return check_launch();
+}
+
+moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilogue,
+                       const uint8_t* a_codes, const uint8_t* a_sf, const float* gs_a,
+                       const void* a_bf16, const int32_t* counts, const int32_t* offsets,
+                       float* out_f32, uint8_t* out_codes, uint8_t* out_sf, void* out_bf16,
+                       const int32_t* perm_src, const float* topk_w, void* ws, cudaStream_t s)
+{
+    const moe_config& c = h->cfg;
+    const bool a16 = c.act_mode == MOE_W4A16;
+    const int K = gateup ? c.hidden : c.inter;
+    const int N = gateup ? 2 * c.inter : c.hidden;
+    GemmArgs args;
+    memset(&args, 0, sizeof(args));
+    args.a_sf = a_sf;
+    args.b_sf = gateup ? h->w13_sf : h->w2_sf;
+    args.gs_a = gs_a;
+    args.gs_w = gateup ? h->gs13 : h->gs2;
+    args.counts = counts;
+    args.offsets = offsets;
+    args.mb_start = at<int32_t>(ws, p.mb_start);
+    args.G = p.G;
+    args.N = N;
+    args.K = K;
+    args.epilogue = epilogue;
+    args.gs_i = c.inter_global_scale;
+    args.out_f32 = out_f32;
+    args.out_codes = out_codes;
+    args.out_sf = out_sf;
+    args.out_bf16 = static_cast<uint16_t*>(out_bf16);
+    args.perm_src = perm_src;
+    args.topk_w = topk_w;
+    args.Tk = p.Tk;
+    args.status = at<uint32_t>(ws, p.status);
+    CUtensorMap tmA, tmA16;
+    const int grid = gemm_grid(h, p.T, N);
+    if (!a16) {
+        const int pitch = codes_pitch(K);
+        if (!make_tmap(&tmA, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
+                       128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_tmap(&tmA16, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
+                       16, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MOE_ERR_CUDA;
+        gemm_nvf4_kernel<<<grid, kGemmThreads, kNvf4Smem, s>>>(
+            tmA, tmA16, gateup ? h->tm_w13 : h->tm_w2, args);
+    } else {
+        if (!make_tmap(&tmA, a_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, p.cap, (uint64_t)K * 2,
+                       64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_tmap(&tmA16, a_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, p.cap,
+                       (uint64_t)K * 2, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MOE_ERR_CUDA;
+        gemm_w4a16_kernel<<<grid, kBf16Threads, kBf16Smem, s>>>(
+            tmA, tmA16, gateup ? h->tm_w13_raw : h->tm_w2_raw, args);
+    }
+    return check_launch();
+}
+
+}  // namespace
+
+// ================================================================ C ABI
+
+extern "C" {
+
+const char* moe_status_string(moe_status s)
+{
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape or mode";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_DEVICE_STATUS: return "device flagged bad data";
+    }
+    return "unknown status";
+}
+
+int32_t moe_rows_capacity(const moe_config* cfg, int32_t T)
+{
+    if (!cfg || T < 0) return -1;
+    return rows_cap(*cfg, T);
+}
+
+size_t moe_workspace_size(const moe_config* cfg, int32_t T)
+{
+    moe_status why;
+    if (!valid_cfg(cfg, &why) || T < 0) return 0;
+    return plan(*cfg, T).total;
+}
+
+void moe_destroy(moe_handle h)
+{
+    if (!h) return;
+    cudaFree(h->router_w);
+    cudaFree(h->w13);
+    cudaFree(h->w13_sf);
+    cudaFree(h->w2);
+    cudaFree(h->w2_sf);
+    cudaFree(h->gs13);
+    cudaFree(h->gs2);
+    cudaFree(h->act_gs);
+    delete h;
+}
+
+moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t stream,
+                      moe_handle* out)
+{
+    if (!out) return MOE_ERR_INVALID;
+    *out = nullptr;
+    moe_status why;
+    if (!valid_cfg(cfg, &why)) return why;
+    if (!w || !w->router_w_d) return MOE_ERR_INVALID;
+    const int El = cfg->num_local_experts, H = cfg->hidden, I = cfg->inter;
+    if (El > 0 && (!w->w13_d || !w->w13_sf_d || !w->w13_gs_d || !w->w2_d || !w->w2_sf_d ||
+                   !w->w2_gs_d))
+        return MOE_ERR_INVALID;
+    if (cfg->has_shared && (!w->sh13_d || !w->sh13_sf_d || !w->sh13_gs_d || !w->sh2_d ||
+                            !w->sh2_sf_d || !w->sh2_gs_d))
+        return MOE_ERR_INVALID;
+    if (!encode_fn()) return MOE_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    moe_layer* h = new (std::nothrow) moe_layer();
+    if (!h) return MOE_ERR_CUDA;
+    h->cfg = *cfg;
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) !=
+            cudaSuccess) {
+        delete h;
+        return MOE_ERR_CUDA;
+    }
+    const int G = El + 1;
+    const size_t n13 = (size_t)G * 2 * I * codes_pitch(H), s13 = (size_t)G * 2 * I * (H / 16);
+    const size_t n2 = (size_t)G * H * codes_pitch(I), s2 = (size_t)G * H * (I / 16);
+    bool ok = cudaMalloc(&h->router_w, (size_t)cfg->num_experts * H * 2) == cudaSuccess &&
+              cudaMalloc(&h->w13, n13) == cudaSuccess &&
+              cudaMalloc(&h->w13_sf, s13) == cudaSuccess &&
+              cudaMalloc(&h->w2, n2) == cudaSuccess && cudaMalloc(&h->w2_sf, s2) == cudaSuccess &&
+              cudaMalloc(&h->gs13, G * 4) == cudaSuccess &&
+              cudaMalloc(&h->gs2, G * 4) == cudaSuccess &&
+              cudaMalloc(&h->act_gs, 4) == cudaSuccess &&
+              cudaMemcpy(h->act_gs, &cfg->act_global_scale, 4, cudaMemcpyHostToDevice) ==
+                  cudaSuccess;
+    ok = ok && cudaMemsetAsync(h->w13, 0, n13, s) == cudaSuccess &&
+         cudaMemsetAsync(h->w13_sf, 0, s13, s) == cudaSuccess &&
+         cudaMemsetAsync(h->w2, 0, n2, s) == cudaSuccess &&
+         cudaMemsetAsync(h->w2_sf, 0, s2, s) == cudaSuccess &&
+         cudaMemsetAsync(h->gs13, 0, G * 4, s) == cudaSuccess &&
+         cudaMemsetAsync(h->gs2, 0, G * 4, s) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(h->router_w, w->router_w_d, (size_t)cfg->num_experts * H * 2,
+                               cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+    const int blocks = 8 * h->num_sms;
+    if (ok && El > 0) {
+        repack_codes_kernel<<<blocks, 256, 0, s>>>(w->w13_d, El, 2 * I, H, 1, h->w13);
+        repack_sf_kernel<<<blocks, 256, 0, s>>>(w->w13_sf_d, El, 2 * I, H, 1, h->w13_sf);
+        repack_codes_kernel<<<blocks, 256, 0, s>>>(w->w2_d, El, H, I, 0, h->w2);
+        repack_sf_kernel<<<blocks, 256, 0, s>>>(w->w2_sf_d, El, H, I, 0, h->w2_sf);
+        ok = cudaMemcpyAsync(h->gs13, w->w13_gs_d, El * 4, cudaMemcpyDeviceToDevice, s) ==
+                 cudaSuccess &&
+             cudaMemcpyAsync(h->gs2, w->w2_gs_d, El * 4, cudaMemcpyDeviceToDevice, s) ==
+                 cudaSuccess;
+    }
+    if (ok && cfg->has_shared) {
+        repack_codes_kernel<<<blocks, 256, 0, s>>>(w->sh13_d, 1, 2 * I, H, 1,
+                                                   h->w13 + (size_t)El * 2 * I * codes_pitch(H));
+        repack_sf_kernel<<<blocks, 256, 0, s>>>(w->sh13_sf_d, 1, 2 * I, H, 1,
+                                                h->w13_sf + (size_t)El * 2 * I * (H / 16));
+        repack_codes_kernel<<<blocks, 256, 0, s>>>(w->sh2_d, 1, H, I, 0,
+                                                   h->w2 + (size_t)El * H * codes_pitch(I));
+        repack_sf_kernel<<<blocks, 256, 0, s>>>(w->sh2_sf_d, 1, H, I, 0,
+                                                h->w2_sf + (size_t)El * H * (I / 16));
+        ok = cudaMemcpyAsync(h->gs13 + El, w->sh13_gs_d, 4, cudaMemcpyDeviceToDevice, s) ==
+                 cudaSuccess &&
+             cudaMemcpyAsync(h->gs2 + El, w->sh2_gs_d, 4, cudaMemcpyDeviceToDevice, s) ==
+                 cudaSuccess;
+    }
+    ok = ok && cudaGetLastError() == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess;
+    // weight tensor maps (the buffers live as long as the handle)
+    const int p13 = codes_pitch(H), p2 = codes_pitch(I);
+    ok = ok &&
+         make_tmap(&h->tm_w13, h->w13, CU_TENSOR_MAP_DATA_TYPE_UINT8, p13, (uint64_t)G * 2 * I,
+                   p13, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_tmap(&h->tm_w2, h->w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, p2, (uint64_t)G * H, p2, 128,
+                   128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_tmap(&h->tm_w13_raw, h->w13, CU_TENSOR_MAP_DATA_TYPE_UINT8, p13,
+                   (uint64_t)G * 2 * I, p13, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         make_tmap(&h->tm_w2_raw, h->w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, p2, (uint64_t)G * H, p2,
+                   32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok = ok &&
+         cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kNvf4Smem) == cudaSuccess &&
+         cudaFuncSetAttribute(gemm_w4a16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kBf16Smem) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        moe_destroy(h);
+        return MOE_ERR_CUDA;
+    }
+    *out = h;
+    return MOE_OK;
+}
+
+moe_status moe_route_topk(moe_handle h, const void* x_bf16_d, const float* logits_in_d,
+                          const float* logit_bias_d, int32_t T, int32_t* topk_ids_d,
+                          float* topk_w_d, float* logits_out_d, void* ws_d, size_t ws_bytes,
+                          moe_stream_t stream)
+{
+    if (!h || !t_ok(h, T) || !topk_ids_d || !topk_w_d) return MOE_ERR_INVALID;
+    if (!logits_in_d && !x_bf16_d) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;
+    float* scratch = nullptr;
+    if (!logits_in_d) {
+        const moe_status st = check_ws(h, T, ws_d, ws_bytes);
+        if (st != MOE_OK) return st;
+        scratch = at<float>(ws_d, plan(h->cfg, T).logits);
+    }
+    return launch_route(h, x_bf16_d, logits_in_d, logit_bias_d, T, topk_ids_d, topk_w_d,
+                        logits_out_d, scratch, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_permute(moe_handle h, const int32_t* topk_ids_d, int32_t T,
+                       int32_t* expert_counts_d, int32_t* expert_offsets_d,
+                       int32_t* perm_src_d, int32_t* inv_d, void* ws_d, size_t ws_bytes,
+                       moe_stream_t stream)
+{
+    if (!h || !t_ok(h, T) || !topk_ids_d || !expert_counts_d || !expert_offsets_d ||
+        !perm_src_d || !inv_d)
+        return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;  // nothing to do: no workspace needed
+    const moe_status st = check_ws(h, T, ws_d, ws_bytes);
+    if (st != MOE_OK) return st;
+    const Plan p = plan(h->cfg, T);
+    return launch_permute(h, p, topk_ids_d, T, expert_counts_d, expert_offsets_d, perm_src_d,
+                          inv_d, ws_d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_quant_nvfp4(const void* x_bf16_d, int32_t rows, int32_t cols,
+                           const float* gs_in_d, float* gs_out_d, uint8_t* codes_d,
+                           uint8_t* sf_d, int32_t sf_layout, void* ws_d, size_t ws_bytes,
+                           moe_stream_t stream)
+{
+    if (!x_bf16_d || !codes_d || !sf_d || rows < 0 || cols <= 0) return MOE_ERR_INVALID;
+    if (sf_layout != 0 && sf_layout != 1) return MOE_ERR_INVALID;
+    if (cols % 64) return MOE_ERR_UNSUPPORTED;
+    if (!gs_in_d && (!ws_d || ws_bytes < 4)) return MOE_ERR_WORKSPACE;
+    if (rows == 0) return MOE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint16_t* x = static_cast<const uint16_t*>(x_bf16_d);
+    uint32_t* amax = static_cast<uint32_t*>(ws_d);
+    if (!gs_in_d) {
+        if (cudaMemsetAsync(amax, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+        int dev = 0, sms = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int64_t n = (int64_t)rows * cols;
+        const int blocks = (int)std::min<int64_t>(2 * sms, std::max<int64_t>(1, n / 2048));
+        amax_bf16_kernel<<<blocks, 256, 0, s>>>(x, n, amax);
+    }
+    quant_rows_kernel<<<grid_for((int64_t)rows * 32, 256), 256, 0, s>>>(
+        x, rows, cols, gs_in_d, gs_in_d ? nullptr : amax, codes_d, sf_d, sf_layout, gs_out_d);
+    return check_launch();
+}
+
+moe_status moe_gather_activations(moe_handle h, const void* x_bf16_d, int32_t T,
+                                  const int32_t* inv_d, const int32_t* expert_offsets_d,
+                                  uint8_t* a_codes_d, uint8_t* a_sf_d, void* a_bf16_d,
+                                  float* gs_out_d, void* ws_d, size_t ws_bytes,
+                                  moe_stream_t stream)
+{
+    if (!h || !t_ok(h, T) || !x_bf16_d || !inv_d || !expert_offsets_d) return MOE_ERR_INVALID;
+    if (h->cfg.act_mode == MOE_W4A16 ? !a_bf16_d : (!a_codes_d || !a_sf_d || !gs_out_d))
+        return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;  // nothing to do: no workspace needed
+    const moe_status st = check_ws(h, T, ws_d, ws_bytes);
+    if (st != MOE_OK) return st;
+    const Plan p = plan(h->cfg, T);
+    return launch_gather(h, p, x_bf16_d, T, inv_d, expert_offsets_d, a_codes_d, a_sf_d,
+                         a_bf16_d, gs_out_d, ws_d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_grouped_gemm_gateup(moe_handle h, const uint8_t* a_codes_d,
+                                   const uint8_t* a_sf_d, const float* gs_a_d,
+                                   const void* a_bf16_d, const int32_t* expert_counts_d,
+                                   const int32_t* expert_offsets_d, int32_t fuse_epilogue,
+                                   float* gateup_f32_d, uint8_t* inter_codes_d,
+                                   uint8_t* inter_sf_d, void* inter_bf16_d, int32_t T,
+                                   void* ws_d, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!h || !t_ok(h, T) || !expert_counts_d || !expert_offsets_d) return MOE_ERR_INVALID;
+    const bool a16 = h->cfg.act_mode == MOE_W4A16;
+    if (a16 ? !a_bf16_d : (!a_codes_d || !a_sf_d || !gs_a_d)) return MOE_ERR_INVALID;
+    if (fuse_epilogue) {
+        if (a16 ? !inter_bf16_d : (!inter_codes_d || !inter_sf_d)) return MOE_ERR_INVALID;
+    } else if (!gateup_f32_d) {
+        return MOE_ERR_INVALID;
+    }
+    if (T == 0) return MOE_OK;  // nothing to do: no workspace needed
+    const moe_status st = check_ws(h, T, ws_d, ws_bytes);
+    if (st != MOE_OK) return st;
+    const Plan p = plan(h->cfg, T);
+    return launch_gemm(h, p, true, fuse_epilogue ? kEpiGateUpSwiglu : kEpiGateUpF32, a_codes_d,
+                       a_sf_d, gs_a_d, a_bf16_d, expert_counts_d, expert_offsets_d,
+                       gateup_f32_d, inter_codes_d, inter_sf_d, inter_bf16_d, nullptr, nullptr,
+                       ws_d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_swiglu_requant(const float* gateup_f32_d, int32_t rows, int32_t inter,
+                              float gs_i, uint8_t* codes_d, uint8_t* sf_d, int32_t sf_layout,
+                              moe_stream_t stream)
+{
+    if (!gateup_f32_d || !codes_d || !sf_d || rows < 0 || inter <= 0 || !(gs_i > 0.0f))
+        return MOE_ERR_INVALID;
+    if (sf_layout != 0 && sf_layout != 1) return MOE_ERR_INVALID;
+    if (inter % 64) return MOE_ERR_UNSUPPORTED;
+    if (rows == 0) return MOE_OK;
+    swiglu_requant_kernel<<<grid_for((int64_t)rows * 32, 256), 256, 0,
+                            reinterpret_cast<cudaStream_t>(stream)>>>(
+        gateup_f32_d, rows, inter, gs_i, codes_d, sf_d, sf_layout);
+    return check_launch();
+}
+
+moe_status moe_grouped_gemm_down(moe_handle h, const uint8_t* inter_codes_d,
+                                 const uint8_t* inter_sf_d, const void* inter_bf16_d,
+                                 const int32_t* expert_counts_d,
+                                 const int32_t* expert_offsets_d, const int32_t* perm_src_d,
+                                 const float* topk_w_d, float* y_d, int32_t T, void* ws_d,
+                                 size_t ws_bytes, moe_stream_t stream)
+{
+    if (!h || !t_ok(h, T) || !expert_counts_d || !expert_offsets_d || !perm_src_d ||
+        !topk_w_d || !y_d)
+        return MOE_ERR_INVALID;
+    const bool a16 = h->cfg.act_mode == MOE_W4A16;
+    if (a16 ? !inter_bf16_d : (!inter_codes_d || !inter_sf_d)) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;  // nothing to do: no workspace needed
+    const moe_status st = check_ws(h, T, ws_d, ws_bytes);
+    if (st != MOE_OK) return st;
+    const Plan p = plan(h->cfg, T);
+    return launch_gemm(h, p, false, kEpiDown, inter_codes_d, inter_sf_d, nullptr, inter_bf16_d,
+                       expert_counts_d, expert_offsets_d, y_d, nullptr, nullptr, nullptr,
+                       perm_src_d, topk_w_d, ws_d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* inv_d, int32_t T,
+                       void* out_bf16_d, moe_stream_t stream)
+{
+    if (!h || !t_ok(h, T) || !y_d || !inv_d || !out_bf16_d) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;
+    const moe_config& c = h->cfg;
+    combine_kernel<<<grid_for((int64_t)T * (c.hidden / 8), 256), 256, 0,
+                     reinterpret_cast<cudaStream_t>(stream)>>>(
+        y_d, inv_d, T, c.hidden, c.top_k, shared_rows(h, T) > 0 ? 1 : 0,
+        static_cast<uint16_t*>(out_bf16_d));
+    return check_launch();
+}
+
+moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_in_d,
+                       const float* logit_bias_d, int32_t T, void* out_bf16_d, void* ws_d,
+                       size_t ws_bytes, moe_stream_t stream)
+{
+    if (!h || !t_ok(h, T) || !x_bf16_d || !out_bf16_d) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;  // nothing to do: no workspace needed
+    const moe_status st = check_ws(h, T, ws_d, ws_bytes);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const Plan p = plan(h->cfg, T);
+    void* ws = ws_d;
+    int32_t* ids = at<int32_t>(ws, p.ids);
+    float* w = at<float>(ws, p.w);
+    int32_t* counts = at<int32_t>(ws, p.counts);
+    int32_t* offsets = at<int32_t>(ws, p.offsets);
+    int32_t* perm_src = at<int32_t>(ws, p.perm_src);
+    int32_t* inv = at<int32_t>(ws, p.inv);
+    float* gs_a = at<float>(ws, p.gs_a);
+    uint8_t* a_codes = at<uint8_t>(ws, p.a_codes);
+    uint8_t* a_sf = at<uint8_t>(ws, p.a_sf);
+    void* a_bf16 = at<void>(ws, p.a_bf16);
+    uint8_t* i_codes = at<uint8_t>(ws, p.i_codes);
+    uint8_t* i_sf = at<uint8_t>(ws, p.i_sf);
+    void* i_bf16 = at<void>(ws, p.i_bf16);
+    float* y = at<float>(ws, p.y);
+    if (cudaMemsetAsync(at<uint32_t>(ws, p.status), 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    moe_status r = launch_route(h, x_bf16_d, logits_in_d, logit_bias_d, T, ids, w, nullptr,
+                                at<float>(ws, p.logits), s);
+    if (r == MOE_OK) r = launch_permute(h, p, ids, T, counts, offsets, perm_src, inv, ws, s);
+    if (r == MOE_OK)
+        r = launch_gather(h, p, x_bf16_d, T, inv, offsets, a_codes, a_sf, a_bf16, gs_a, ws, s);
+    if (r == MOE_OK)
+        r = launch_gemm(h, p, true, kEpiGateUpSwiglu, a_codes, a_sf, gs_a, a_bf16, counts,
+                        offsets, nullptr, i_codes, i_sf, i_bf16, nullptr, nullptr, ws, s);
+    if (r == MOE_OK)
+        r = launch_gemm(h, p, false, kEpiDown, i_codes, i_sf, nullptr, i_bf16, counts, offsets,
+                        y, nullptr, nullptr, nullptr, perm_src, w, ws, s);
+    if (r == MOE_OK) r = moe_combine(h, y, inv, T, out_bf16_d, stream);
+    return r;
+}
+
+moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** topk_ids,
+                               float** topk_w, int32_t** expert_counts,
+                               int32_t** expert_offsets, int32_t** perm_src, int32_t** inv,
+                               float** gs_a, uint8_t** a_codes, uint8_t** a_sf,
+                               uint8_t** inter_codes, uint8_t** inter_sf, float** y)
+{
+    if (!h || !ws_d || !t_ok(h, T)) return MOE_ERR_INVALID;
+    const Plan p = plan(h->cfg, T);
+    if (topk_ids) *topk_ids = at<int32_t>(ws_d, p.ids);
+    if (topk_w) *topk_w = at<float>(ws_d, p.w);
+    if (expert_counts) *expert_counts = at<int32_t>(ws_d, p.counts);
+    if (expert_offsets) *expert_offsets = at<int32_t>(ws_d, p.offsets);
+    if (perm_src) *perm_src = at<int32_t>(ws_d, p.perm_src);
+    if (inv) *inv = at<int32_t>(ws_d, p.inv);
+    if (gs_a) *gs_a = at<float>(ws_d, p.gs_a);
+    if (a_codes) *a_codes = at<uint8_t>(ws_d, p.a_codes);
+    if (a_sf) *a_sf = at<uint8_t>(ws_d, p.a_sf);
+    if (inter_codes) *inter_codes = at<uint8_t>(ws_d, p.i_codes);
+    if (inter_sf) *inter_sf = at<uint8_t>(ws_d, p.i_sf);
+    if (y) *y = at<float>(ws_d, p.y);
+    return MOE_OK;
+}
+
+moe_status moe_get_status(moe_handle h, void* ws_d, moe_stream_t stream, uint32_t* bits)
+{
+    if (!h || !ws_d) return MOE_ERR_INVALID;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    // the status word is the first entry of every workspace plan
+    if (cudaMemcpyAsync(&v, ws_d, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess || cudaMemsetAsync(ws_d, 0, 4, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (bits) *bits = v;
+    if (v & MOE_DEV_WAIT_TIMEOUT) return MOE_ERR_TIMEOUT;
+    return v ? MOE_ERR_DEVICE_STATUS : MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,573 @@
+// Grouped GEMMs of the expert MLPs on the 5th-generation tensor cores (tcgen05).
+//
+// Rows (M) are the padded rows of one expert group (tokens routed to that expert); columns
+// (N) are 128 rows of that expert's weight matrix; the accumulator lives in TMEM.  One
+// persistent CTA per SM walks the tile list (group, weight tile, row block), with
+// consecutive tiles sharing the same weight tile so the second row block of an expert
+// reads the weights from L2.
+//
+// Warp roles (warp-specialised pipeline):
+//   warp 0   TMA producer: activation tile, weight tile, both scale tiles per k-stage
+//   warp 1   TMEM allocation; one thread issues tcgen05.cp (scales) and tcgen05.mma
+//   warps 2-5 epilogue: TMEM -> registers -> fused output (one TMEM lane quarter each)
+//   (W4A16 only) warps 6-9: FP4 -> bf16 dequantisation of the weight tile into the
+//   swizzled operand layout
+//
+// W4A4 (NVFP4 x NVFP4): kind::mxf4nvf4 block-scaled MMA, K = 64 per instruction, UE4M3
+// scales per 16 elements copied SMEM -> TMEM per k-step.  The global scales are applied in
+// the epilogue as alpha = 1 / (gs_a * gs_w).
+// W4A16: kind::f16 with bf16 operands; the weights are dequantised in the mainloop
+// (E2M1 * E4M3 is exact in bf16) and the global scale is applied in the epilogue.
+//
+// Every pipeline wait is bounded: a wait that runs out sets MOE_DEV_WAIT_TIMEOUT in the
+// status word and makes all roles stop, drain their copies in flight, free TMEM and exit.
+#include <cuda_bf16.h>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+struct TileInfo {
+    int g;       // group (local expert, or the shared slot)
+    int nb;      // 128-row weight tile within the expert
+    int rows;    // valid rows of this row block (1..128)
+    int arow0;   // first padded row of the row block
+    int brow0;   // first weight row (slot * N + 128 * nb)
+};
+
+// Tile t of the list: groups in order; inside a group, weight tiles in order; inside a
+// weight tile, the group's row blocks (so row blocks sharing weights run back to back).
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int NB, int t)
+{
+    int lo = 0, hi = a.G;  // largest g with mb_start[g] * NB <= t
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (a.mb_start[mid] * NB <= t) lo = mid;
+        else hi = mid;
+    }
+    const int g = lo;
+    const int nmb = a.mb_start[g + 1] - a.mb_start[g];
+    const int local = t - a.mb_start[g] * NB;
+    const int nb = local / nmb, mb = local % nmb;
+    TileInfo ti;
+    ti.g = g;
+    ti.nb = nb;
+    ti.rows = min(128, a.counts[g] - 128 * mb);
+    ti.arow0 = a.offsets[g] + 128 * mb;
+    ti.brow0 = g * a.N + 128 * nb;
+    return ti;
+}
+
+// Lane 0 waits, the warp follows (keeps .sync.aligned tcgen05 ops converged).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort)
+{
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    return ok != 0;
+}
+
+// Epilogue of one tile for the 32 rows of TMEM lane quarter q (thread = row).
+template <bool kW4A16>
+__device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& ti,
+                                             uint32_t tacc, int q, int lane)
+{
+    const int m = q * 32 + lane;
+    const bool valid = m < ti.rows;
+    const int64_t prow = (int64_t)ti.arow0 + m;
+    const float gw = a.gs_w[ti.g];
+    float alpha;
+    if (a.epilogue == kEpiDown) alpha = kW4A16 ? __frcp_rn(gw) : __frcp_rn(__fmul_rn(a.gs_i, gw));
+    else alpha = kW4A16 ? __frcp_rn(gw) : __frcp_rn(__fmul_rn(*a.gs_a, gw));
+    int64_t yrow = 0;
+    float wgt = 1.0f;
+    if (a.epilogue == kEpiDown && valid) {
+        yrow = a.perm_src[prow];
+        if (yrow < a.Tk) wgt = a.topk_w[yrow];
+        alpha = __fmul_rn(alpha, wgt);
+    }
+    const int I = a.N / 2;
+    uint32_t sfword = 0;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tacc + ((uint32_t)(q * 32) << 16) + 32 * c, r);
+        tmem_ld_wait();
+        if (!valid) continue;
+        if (a.epilogue == kEpiDown) {
+            float4* dst = reinterpret_cast<float4*>(a.out_f32 + yrow * a.N + 128 * ti.nb + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(__uint_as_float(r[4 * i]) * alpha,
+                                     __uint_as_float(r[4 * i + 1]) * alpha,
+                                     __uint_as_float(r[4 * i + 2]) * alpha,
+                                     __uint_as_float(r[4 * i + 3]) * alpha);
+        } else if (a.epilogue == kEpiGateUpF32) {
+            const int f = 64 * ti.nb + 16 * c;
+            float4* dg = reinterpret_cast<float4*>(a.out_f32 + prow * a.N + f);
+            float4* du = reinterpret_cast<float4*>(a.out_f32 + prow * a.N + I + f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dg[i] = make_float4(__uint_as_float(r[4 * i]) * alpha,
+                                    __uint_as_float(r[4 * i + 1]) * alpha,
+                                    __uint_as_float(r[4 * i + 2]) * alpha,
+                                    __uint_as_float(r[4 * i + 3]) * alpha);
+                du[i] = make_float4(__uint_as_float(r[16 + 4 * i]) * alpha,
+                                    __uint_as_float(r[16 + 4 * i + 1]) * alpha,
+                                    __uint_as_float(r[16 + 4 * i + 2]) * alpha,
+                                    __uint_as_float(r[16 + 4 * i + 3]) * alpha);
+            }
+        } else {
+            const int f = 64 * ti.nb + 16 * c;
+            float s[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                s[i] = silu_mul(__fmul_rn(__uint_as_float(r[i]), alpha),
+                                __fmul_rn(__uint_as_float(r[16 + i]), alpha));
+            if (kW4A16) {
+                uint32_t o[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const __nv_bfloat162 p = __floats2bfloat162_rn(s[2 * i], s[2 * i + 1]);
+                    o[i] = *reinterpret_cast<const uint32_t*>(&p);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + prow * I + f);
+                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            } else {
+                uint32_t cw[2];
+                const uint32_t sb = quant16(s, a.gs_i, cw);
+                *reinterpret_cast<uint2*>(a.out_codes + prow * codes_pitch(I) + f / 2) =
+                    make_uint2(cw[0], cw[1]);
+                sfword |= sb << (8 * c);
+            }
+        }
+    }
+    if (!kW4A16 && a.epilogue == kEpiGateUpSwiglu && valid)
+        *reinterpret_cast<uint32_t*>(a.out_sf + sf_atom_offset(prow, 4 * ti.nb, I)) = sfword;
+}
+
+// Shared-memory carve-up: stages, then barriers, then the TMEM address slot and flags.
+struct Ctl {
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* ready;       // W4A16: weight tile dequantised
+    uint64_t* acc_full;
+    uint64_t* acc_empty;
+    uint64_t* drain;
+    uint32_t* tmem_slot;
+    volatile int* abort_flag;
+    int* zero;
+};
+
+__device__ __forceinline__ Ctl carve(uint8_t* base, int stages)
+{
+    Ctl c;
+    uint64_t* b = reinterpret_cast<uint64_t*>(base);
+    c.full = b;
+    c.empty = b + stages;
+    c.ready = b + 2 * stages;
+    c.acc_full = b + 3 * stages;
+    c.acc_empty = c.acc_full + 2;
+    c.drain = c.acc_empty + 2;
+    c.tmem_slot = reinterpret_cast<uint32_t*>(c.drain + 1);
+    c.abort_flag = reinterpret_cast<volatile int*>(c.tmem_slot + 1);
+    c.zero = reinterpret_cast<int*>(c.tmem_slot + 2);
+    return c;
+}
+
+__device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw)
+{
+    const uint32_t u = smem_u32(raw);
+    return raw + (((u + 1023u) & ~1023u) - u);
+}
+
+// ============================================================== W4A4: NVFP4 x NVFP4
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmA16,
+                     const __grid_constant__ CUtensorMap tmB, GemmArgs args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* stages = aligned_smem(smem_raw);
+    Ctl ctl = carve(stages + kNvf4Stages * kNvf4StageBytes, kNvf4Stages);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NB = args.N / 128;
+    const int KB = (args.K + 255) / 256;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNvf4Stages; ++s) {
+            mbar_init(&ctl.full[s], 1);
+            mbar_init(&ctl.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl.acc_full[b], 1);
+            mbar_init(&ctl.acc_empty[b], 128);
+        }
+        mbar_init(ctl.drain, 1);
+        *ctl.abort_flag = 0;
+        *ctl.zero = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmA16);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(ctl.tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *ctl.tmem_slot;
+    const int ntiles = args.mb_start[args.G] * NB;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const TileInfo ti = decode_tile(args, NB, t);
+                const int nbox = (ti.rows + 15) >> 4;
+                const bool big = nbox > 4;
+                const uint32_t a_bytes = big ? 16384u : (uint32_t)nbox * 2048u;
+                const uint8_t* sfa = args.a_sf + (size_t)(ti.arow0 >> 7) * (args.K / 64) * 512;
+                const uint8_t* sfb = args.b_sf + (size_t)(ti.brow0 >> 7) * (args.K / 64) * 512;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, ctl.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int nk = min(4, (args.K - kb * 256) / 64);
+                    uint8_t* sA = stages + stage * kNvf4StageBytes;
+                    uint8_t* sB = sA + 16384;
+                    uint8_t* sSFA = sB + 16384;
+                    uint8_t* sSFB = sSFA + 2048;
+                    mbar_arrive_expect_tx(&ctl.full[stage], a_bytes + 16384u + 1024u * nk);
+                    if (big) {
+                        tma_load_2d(sA, &tmA, &ctl.full[stage], kb * 128, ti.arow0, pol_a);
+                    } else {
+                        for (int i = 0; i < nbox; ++i)
+                            tma_load_2d(sA + i * 2048, &tmA16, &ctl.full[stage], kb * 128,
+                                        ti.arow0 + 16 * i, pol_a);
+                    }
+                    tma_load_2d(sB, &tmB, &ctl.full[stage], kb * 128, ti.brow0, pol_w);
+                    bulk_load(sSFA, sfa + kb * 2048, 512u * nk, &ctl.full[stage], pol_a);
+                    bulk_load(sSFB, sfb + kb * 2048, 512u * nk, &ctl.full[stage], pol_w);
+                    issued |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kNvf4Stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+                *ctl.abort_flag = 1;
+            }
+            for (int s = 0; s < kNvf4Stages; ++s)  // copies in flight land before exit
+                if ((issued >> s) & 1u) mbar_wait(&ctl.full[s], (issued_par >> s) & 1u, ctl.zero);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_nvf4(128, 128);
+            int stage = 0, it = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+                const int buf = it & 1;
+                const uint32_t acc_par = (it >> 1) & 1;
+                if (!mbar_wait(&ctl.acc_empty[buf], acc_par ^ 1u, ctl.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_t = tmem + buf * 128;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&ctl.full[stage], phase, ctl.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nk = min(4, (args.K - kb * 256) / 64);
+                    uint8_t* sA = stages + stage * kNvf4StageBytes;
+                    uint8_t* sB = sA + 16384;
+                    uint8_t* sSFA = sB + 16384;
+                    uint8_t* sSFB = sSFA + 2048;
+                    const uint32_t sfa_t = tmem + 256 + stage * 32, sfb_t = sfa_t + 16;
+                    for (int j = 0; j < nk; ++j) {
+                        tc_cp_sf(sfa_t + 4 * j, sdesc_sf(smem_u32(sSFA) + 512 * j));
+                        tc_cp_sf(sfb_t + 4 * j, sdesc_sf(smem_u32(sSFB) + 512 * j));
+                    }
+                    const uint64_t ad = sdesc_sw128(smem_u32(sA)), bd = sdesc_sw128(smem_u32(sB));
+                    for (int j = 0; j < nk; ++j)
+                        tc_mma_nvf4(d_t, ad + 2 * j, bd + 2 * j, idesc, sfa_t + 4 * j,
+                                    sfb_t + 4 * j, (kb | j) != 0);
+                    tc_commit(&ctl.empty[stage]);
+                    if (++stage == kNvf4Stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&ctl.acc_full[buf]);
+            }
+            if (!ok) {
+                set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+                *ctl.abort_flag = 1;
+            }
+            tc_commit(ctl.drain);  // every MMA / copy issued above is complete after this
+            mbar_wait(ctl.drain, 0, ctl.zero);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;
+        int it = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+            const TileInfo ti = decode_tile(args, NB, t);
+            const int buf = it & 1;
+            const uint32_t acc_par = (it >> 1) & 1;
+            if (!warp_wait(&ctl.acc_full[buf], acc_par, ctl.abort_flag)) {
+                if (lane == 0) {
+                    set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+                    *ctl.abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            run_epilogue<false>(args, ti, tmem + buf * 128, q, lane);
+            tc_fence_before();
+            mbar_arrive(&ctl.acc_empty[buf]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ============================================================== W4A16: bf16 x NVFP4
+
+// E2M1 code (4 bits) -> fp32: magnitude 0, 0.5, 1, 1.5, 2, 3, 4, 6 from the exponent and
+// mantissa bits (exponent field e = c >> 1 with bias 1, mantissa m = c & 1).
+__device__ __forceinline__ float e2m1_to_f32(uint32_t code)
+{
+    const uint32_t c = code & 7u;
+    // e >= 1: fp32 exponent e + 126, mantissa bit m at bit 22  ==  (c + 252) << 22;
+    // c == 1 (subnormal 0.5): 0x3F000000 == 252 << 22;  c == 0: 0.
+    const uint32_t bits = c == 0 ? 0u : ((c + 252u - (c == 1u ? 1u : 0u)) << 22);
+    return __uint_as_float(bits | ((code & 8u) << 28));
+}
+
+__global__ void __launch_bounds__(kBf16Threads, 1)
+    gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmA16,
+                      const __grid_constant__ CUtensorMap tmB, GemmArgs args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* stages = aligned_smem(smem_raw);
+    Ctl ctl = carve(stages + kBf16Stages * kBf16StageBytes, kBf16Stages);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NB = args.N / 128;
+    const int KB = args.K / 64;
+    // stage layout: A bf16 [128][128 B] | B bf16 [128][128 B] | raw FP4 [128][32 B] | scales
+    constexpr int kOffB = 16384, kOffW = 32768, kOffSF = 36864;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kBf16Stages; ++s) {
+            mbar_init(&ctl.full[s], 1);
+            mbar_init(&ctl.empty[s], 1);
+            mbar_init(&ctl.ready[s], 128);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl.acc_full[b], 1);
+            mbar_init(&ctl.acc_empty[b], 128);
+        }
+        mbar_init(ctl.drain, 1);
+        *ctl.abort_flag = 0;
+        *ctl.zero = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmA16);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(ctl.tmem_slot, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *ctl.tmem_slot;
+    const int ntiles = args.mb_start[args.G] * NB;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const TileInfo ti = decode_tile(args, NB, t);
+                const int nbox = (ti.rows + 15) >> 4;
+                const bool big = nbox > 4;
+                const uint32_t a_bytes = big ? 16384u : (uint32_t)nbox * 2048u;
+                const uint8_t* sfb = args.b_sf + (size_t)(ti.brow0 >> 7) * (args.K / 64) * 512;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, ctl.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = stages + stage * kBf16StageBytes;
+                    mbar_arrive_expect_tx(&ctl.full[stage], a_bytes + 4096u + 512u);
+                    if (big) {
+                        tma_load_2d(st, &tmA, &ctl.full[stage], kb * 64, ti.arow0, pol_a);
+                    } else {
+                        for (int i = 0; i < nbox; ++i)
+                            tma_load_2d(st + i * 2048, &tmA16, &ctl.full[stage], kb * 64,
+                                        ti.arow0 + 16 * i, pol_a);
+                    }
+                    tma_load_2d(st + kOffW, &tmB, &ctl.full[stage], kb * 32, ti.brow0, pol_w);
+                    bulk_load(st + kOffSF, sfb + kb * 512, 512u, &ctl.full[stage], pol_w);
+                    issued |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kBf16Stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+                *ctl.abort_flag = 1;
+            }
+            for (int s = 0; s < kBf16Stages; ++s)
+                if ((issued >> s) & 1u) mbar_wait(&ctl.full[s], (issued_par >> s) & 1u, ctl.zero);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(128, 128);
+            int stage = 0, it = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+                const int buf = it & 1;
+                const uint32_t acc_par = (it >> 1) & 1;
+                if (!mbar_wait(&ctl.acc_empty[buf], acc_par ^ 1u, ctl.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_t = tmem + buf * 128;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&ctl.ready[stage], phase, ctl.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint8_t* st = stages + stage * kBf16StageBytes;
+                    const uint64_t ad = sdesc_sw128(smem_u32(st));
+                    const uint64_t bd = sdesc_sw128(smem_u32(st + kOffB));
+                    for (int j = 0; j < 4; ++j)
+                        tc_mma_bf16(d_t, ad + 2 * j, bd + 2 * j, idesc, (kb | j) != 0);
+                    tc_commit(&ctl.empty[stage]);
+                    if (++stage == kBf16Stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&ctl.acc_full[buf]);
+            }
+            if (!ok) {
+                set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+                *ctl.abort_flag = 1;
+            }
+            tc_commit(ctl.drain);
+            mbar_wait(ctl.drain, 0, ctl.zero);
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        const int q = warp & 3;
+        int it = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+            const TileInfo ti = decode_tile(args, NB, t);
+            const int buf = it & 1;
+            const uint32_t acc_par = (it >> 1) & 1;
+            if (!warp_wait(&ctl.acc_full[buf], acc_par, ctl.abort_flag)) {
+                if (lane == 0) {
+                    set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+                    *ctl.abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            run_epilogue<true>(args, ti, tmem + buf * 128, q, lane);
+            tc_fence_before();
+            mbar_arrive(&ctl.acc_empty[buf]);
+        }
+    } else {
+        // dequantisation: thread n converts weight row n of the stage (64 elements)
+        const int n = (warp - 6) * 32 + lane;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!warp_wait(&ctl.full[stage], phase, ctl.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = stages + stage * kBf16StageBytes;
+                const uint4 w0 = *reinterpret_cast<const uint4*>(st + kOffW + 32 * n);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(st + kOffW + 32 * n + 16);
+                const uint32_t sw =
+                    *reinterpret_cast<const uint32_t*>(st + kOffSF + (n & 31) * 16 + (n >> 5) * 4);
+                const uint32_t by[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                uint8_t* dstrow = st + kOffB + n * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {  // 8 elements (one 16-byte chunk) per step
+                    const float sv = e4m3_to_f32((sw >> (8 * (j >> 1))) & 0xFFu);
+                    uint32_t o[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float lo = e2m1_to_f32(by[j] >> (8 * i)) * sv;
+                        const float hi = e2m1_to_f32(by[j] >> (8 * i + 4)) * sv;
+                        const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+                        o[i] = *reinterpret_cast<const uint32_t*>(&p);
+                    }
+                    *reinterpret_cast<uint4*>(dstrow + ((j ^ (n & 7)) << 4)) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(&ctl.ready[stage]);
+                if (++stage == kBf16Stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+            *ctl.abort_flag = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+}  // namespace moe

@@ -1,0 +1,276 @@
+// NVFP4 quantisation (activations, standalone matrices, SwiGLU requantisation), the
+// weighted combine, and the create-time weight re-layout.
+//
+// NVFP4 (Solar Open 2 on DGX Spark, "b12x 버전이 실제 NVFP4 체크포인트를 읽어들이도록
+// 만들기": packed FP4 values, FP8 block scales clamped at 448, an FP32 global scale):
+// E2M1 codes, one E4M3 scale per 16 consecutive elements, value = code * scale / gs.
+#include <cuda_bf16.h>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------- amax
+// amax over n bf16 values, merged into *amax_bits with an integer max (non-negative
+// floats order like their bit patterns).
+__global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t* __restrict__ x,
+                                                        int64_t n, uint32_t* amax_bits)
+{
+    float m = 0.0f;
+    const int64_t n8 = n / 8;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 v = reinterpret_cast<const uint4*>(x)[i];
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            m = fmaxf(m, fabsf(bf16_bits_to_f32(u[j] & 0xFFFFu)));
+            m = fmaxf(m, fabsf(bf16_bits_to_f32(u[j] >> 16)));
+        }
+    }
+    for (int64_t i = n8 * 8 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        m = fmaxf(m, fabsf(bf16_bits_to_f32(x[i])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ float s[32];
+    if ((threadIdx.x & 31) == 0) s[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        m = threadIdx.x < (blockDim.x >> 5) ? s[threadIdx.x] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(m));
+    }
+}
+
+// Global encode scale: the static one if given, else 2688 / amax (1 when amax == 0).
+__device__ __forceinline__ float global_scale(const float* gs_static, const uint32_t* amax_bits)
+{
+    if (gs_static) return *gs_static;
+    const float a = __uint_as_float(*amax_bits);
+    return a == 0.0f ? 1.0f : __fdiv_rn(2688.0f, a);
+}
+
+// Loads 16 bf16 values (32 bytes) as fp32.
+__device__ __forceinline__ void load16_bf16(const uint16_t* p, float* v)
+{
+    const uint4 a = reinterpret_cast<const uint4*>(p)[0];
+    const uint4 b = reinterpret_cast<const uint4*>(p)[1];
+    const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = bf16_bits_to_f32(u[i] & 0xFFFFu);
+        v[2 * i + 1] = bf16_bits_to_f32(u[i] >> 16);
+    }
+}
+
+// ---------------------------------------------------------------- gather-quantise
+//
+// One warp per token.  Lane l handles the 16-element blocks l, l+32, ... so code stores
+// from a warp are contiguous, and the 4 blocks of one 64-element k-step sit on 4
+// neighbouring lanes (their scale bytes are merged into one 32-bit atom word).
+// Destinations: the padded rows of the token's local pairs (inv) and its shared row.
+__global__ void __launch_bounds__(256) gather_quant_kernel(
+    const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ inv,
+    const int32_t* __restrict__ offsets, int shared_group, int add_shared,
+    const float* gs_static, const uint32_t* amax_bits, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ sf, float* gs_out)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= T) return;
+    const int t = warp;
+    const float gs = global_scale(gs_static, amax_bits);
+    if (t == 0 && lane == 0 && gs_out) *gs_out = gs;
+    int dst[kMaxTopK + 1];
+    int nd = 0;
+    for (int j = 0; j < k; ++j) {
+        const int r = inv[(size_t)t * k + j];
+        if (r >= 0) dst[nd++] = r;
+    }
+    if (add_shared) dst[nd++] = offsets[shared_group] + t;
+    if (nd == 0) return;
+    const int pitch = codes_pitch(H);
+    const int nb = H / 16;
+    for (int b0 = 0; b0 < nb; b0 += 32) {  // warp-uniform loop: every lane shuffles
+        const int b = b0 + lane;
+        const bool act = b < nb;               // nb % 4 == 0: k-step lanes agree
+        float v[16];
+        uint32_t c[2] = {0u, 0u}, s = 0u;
+        if (act) {
+            load16_bf16(x + (size_t)t * H + b * 16, v);
+            s = quant16(v, gs, c);
+        }
+        // merge the 4 scale bytes of this k-step into the lane with b % 4 == 0
+        const uint32_t s1 = __shfl_down_sync(0xffffffffu, s, 1);
+        const uint32_t s2 = __shfl_down_sync(0xffffffffu, s, 2);
+        const uint32_t s3 = __shfl_down_sync(0xffffffffu, s, 3);
+        const uint32_t word = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        if (!act) continue;
+        for (int d = 0; d < nd; ++d) {
+            const int64_t row = dst[d];
+            *reinterpret_cast<uint2*>(codes + row * pitch + b * 8) = make_uint2(c[0], c[1]);
+            if ((b & 3) == 0)
+                *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(row, b, H)) = word;
+        }
+    }
+}
+
+// W4A16: copy token rows (bf16) to the padded rows of their pairs and shared row.
+__global__ void __launch_bounds__(256) gather_bf16_kernel(
+    const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ inv,
+    const int32_t* __restrict__ offsets, int shared_group, int add_shared,
+    uint16_t* __restrict__ out)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= T) return;
+    const int t = warp;
+    int dst[kMaxTopK + 1];
+    int nd = 0;
+    for (int j = 0; j < k; ++j) {
+        const int r = inv[(size_t)t * k + j];
+        if (r >= 0) dst[nd++] = r;
+    }
+    if (add_shared) dst[nd++] = offsets[shared_group] + t;
+    for (int c = lane * 8; c < H; c += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c);
+        for (int d = 0; d < nd; ++d)
+            *reinterpret_cast<uint4*>(out + (size_t)dst[d] * H + c) = v;
+    }
+}
+
+// ---------------------------------------------------------------- standalone quantiser
+// rows x cols bf16 -> NVFP4; layout 0 canonical, 1 tiled.  One warp per row.
+__global__ void __launch_bounds__(256) quant_rows_kernel(
+    const uint16_t* __restrict__ x, int rows, int cols, const float* gs_static,
+    const uint32_t* amax_bits, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+    int layout, float* gs_out)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= rows) return;
+    const float gs = global_scale(gs_static, amax_bits);
+    if (warp == 0 && lane == 0 && gs_out) *gs_out = gs;
+    const int64_t r = warp;
+    const int nb = cols / 16;
+    const int pitch = layout ? codes_pitch(cols) : cols / 2;
+    for (int b = lane; b < nb; b += 32) {
+        float v[16];
+        load16_bf16(x + r * cols + b * 16, v);
+        uint32_t c[2];
+        const uint32_t s = quant16(v, gs, c);
+        *reinterpret_cast<uint2*>(codes + r * pitch + b * 8) = make_uint2(c[0], c[1]);
+        if (layout) sf[sf_atom_offset(r, b, cols)] = (uint8_t)s;
+        else sf[r * nb + b] = (uint8_t)s;
+    }
+}
+
+// ---------------------------------------------------------------- SwiGLU + requant
+// fp32 gate/up rows [rows][2I] (gate cols 0..I-1) -> s = silu(g) * u -> NVFP4 with gs_i.
+__global__ void __launch_bounds__(256) swiglu_requant_kernel(
+    const float* __restrict__ gu, int rows, int I, float gs_i, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ sf, int layout)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= rows) return;
+    const int64_t r = warp;
+    const int nb = I / 16;
+    const int pitch = layout ? codes_pitch(I) : I / 2;
+    for (int b = lane; b < nb; b += 32) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            v[i] = silu_mul(gu[r * 2 * I + b * 16 + i], gu[r * 2 * I + I + b * 16 + i]);
+        uint32_t c[2];
+        const uint32_t s = quant16(v, gs_i, c);
+        *reinterpret_cast<uint2*>(codes + r * pitch + b * 8) = make_uint2(c[0], c[1]);
+        if (layout) sf[sf_atom_offset(r, b, I)] = (uint8_t)s;
+        else sf[r * nb + b] = (uint8_t)s;
+    }
+}
+
+// ---------------------------------------------------------------- combine
+// out[t][h] = sum_{j: inv >= 0} y[t*k+j][h] + (add_shared ? y[T*k+t][h] : 0) -> bf16.
+// One thread per 8 columns of one token.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
+                                                      const int32_t* __restrict__ inv, int T,
+                                                      int H, int k, int add_shared,
+                                                      uint16_t* __restrict__ out)
+{
+    const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    const int per = H / 8;
+    if (i >= (int64_t)T * per) return;
+    const int t = (int)(i / per), c = (int)(i % per) * 8;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j = 0; j < k; ++j) {
+        if (inv[(size_t)t * k + j] < 0) continue;
+        const float4* src = reinterpret_cast<const float4*>(y + ((size_t)t * k + j) * H + c);
+        const float4 a = src[0], b = src[1];
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    if (add_shared) {
+        const float4* src = reinterpret_cast<const float4*>(y + ((size_t)T * k + t) * H + c);
+        const float4 a = src[0], b = src[1];
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+        o[q] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    *reinterpret_cast<uint4*>(out + (size_t)t * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ---------------------------------------------------------------- weight re-layout
+//
+// Canonical [N][K/2] codes and [N][K/16] scales of one expert -> tiled slot: codes
+// [N][pitch] and 512-byte scale atoms per (128-row tile, 64-element k-step).  With
+// interleave (gate/up of w13, N = 2I): destination row 128*nb + 32*c + 16*u + i holds
+// source row u*I + 64*nb + 16*c + i, so each 128-row tile has 4 pairs of 16 gate rows and
+// the 16 matching up rows -- the fused epilogue sees gate and up of the same features.
+__device__ __forceinline__ int64_t src_row(int64_t r, int N, int interleave)
+{
+    if (!interleave) return r;
+    const int I = N / 2;
+    const int nb = (int)(r >> 7), c = (int)((r >> 5) & 3), u = (int)((r >> 4) & 1),
+              i = (int)(r & 15);
+    return (int64_t)u * I + 64 * nb + 16 * c + i;
+}
+
+__global__ void __launch_bounds__(256) repack_codes_kernel(const uint8_t* __restrict__ src,
+                                                           int nexp, int N, int K,
+                                                           int interleave,
+                                                           uint8_t* __restrict__ dst)
+{
+    const int pitch = codes_pitch(K);
+    const int64_t n = (int64_t)nexp * N * pitch;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / pitch;  // destination row over all experts
+        const int c = (int)(i % pitch);
+        const int64_t e = r / N, rl = r % N;
+        dst[i] = c < K / 2 ? src[(e * N + src_row(rl, N, interleave)) * (K / 2) + c] : (uint8_t)0;
+    }
+}
+
+__global__ void __launch_bounds__(256) repack_sf_kernel(const uint8_t* __restrict__ src,
+                                                        int nexp, int N, int K, int interleave,
+                                                        uint8_t* __restrict__ dst)
+{
+    const int64_t n = (int64_t)nexp * N * (K / 16);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / (K / 16);
+        const int b = (int)(i % (K / 16));
+        const int64_t e = r / N, rl = r % N;
+        dst[sf_atom_offset(r, b, K)] = src[(e * N + src_row(rl, N, interleave)) * (K / 16) + b];
+    }
+}
+
+}  // namespace moe

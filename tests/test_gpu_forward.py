@@ -1,0 +1,208 @@
+"""Whole-layer GPU parity against the oracle on every workload: the tiny layer, the
+320-expert decode layer, the prefill chunk (sampled tokens), the expert shard 160-319
+with Zipf popularity (and shard 0-159 + shard 160-319 == full layer), and the W4A16
+decode sweep.  Bar: relative L2 <= 1e-2 and max |err| <= 5e-2 * rms(ref) against the
+oracle's fp64 accumulation; routing ids, grouping and activation codes bit-exact."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_mixture_experts_gb300 as moe
+import oracle
+import synth
+from gpu_util import bits16, dev, host, make_layer, tiled_to_canonical
+from helpers import build_layer, slice_layer, within_layer_tolerance
+
+pytestmark = pytest.mark.gpu
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+INTER = json.load(open(os.path.join(GOLD, "inter_scale.json")))
+
+
+@pytest.fixture(scope="module")
+def big_layer():
+    c = synth.CONFIGS["decode"]
+    return build_layer(0, c["H"], c["I"], c["E"])
+
+
+def _routing_clear(x, wr, bias, k, logits_in=None):
+    """Tokens whose k-th / (k+1)-th logit gap is far above the fp32 logit error."""
+    if logits_in is not None:
+        lg = logits_in.astype(np.float64) + (0 if bias is None else bias)
+        return np.ones(lg.shape[0], bool), lg
+    lg = oracle.router_logits(x, wr, bias)
+    mag = np.abs(synth.bf16_to_f32(x).astype(np.float64)) @ np.abs(
+        synth.bf16_to_f32(wr).astype(np.float64)).T
+    srt = -np.sort(-lg, axis=1)
+    gap = srt[:, k - 1] - srt[:, k]
+    return gap > 2e-5 * mag.max(1), lg
+
+
+def _forward(h, x, T, logits_in=None, bias=None):
+    out = torch.zeros((T, h.cfg.hidden), dtype=torch.int16, device="cuda")
+    h.forward(bits16(x), out=out, logits_in=None if logits_in is None else dev(logits_in),
+              logit_bias=None if bias is None else dev(bias))
+    torch.cuda.synchronize()
+    st, bits = moe.moe_get_status(h.handle, h.ws)
+    assert st == moe.MOE_OK, bits
+    return synth.bf16_to_f32(host(out).view(np.uint16)).astype(np.float64)
+
+
+def _check(got, ref, what):
+    rel, mx = within_layer_tolerance(got, ref)
+    assert rel <= 1e-2 and mx <= 5e-2, (what, rel, mx)
+    return rel, mx
+
+
+def _read_ws(layer, ptr, n, dtype):
+    """n elements of dtype at device address ptr inside layer.ws (a forward intermediate)."""
+    off = ptr - layer.ws.data_ptr()
+    nbytes = n * np.dtype(dtype).itemsize
+    assert 0 <= off and off + nbytes <= layer.ws.numel()
+    return layer.ws[off:off + nbytes].cpu().numpy().view(dtype)
+
+
+def _forward_buffers_check(h, T, ora, clear):
+    """ids, grouping and activation codes of the forward equal the oracle's."""
+    k = h.cfg.top_k
+    b = moe.moe_forward_buffers(h.handle, h.ws, T)
+    ids = _read_ws(h, b["topk_ids"], T * k, np.int32).reshape(T, k)
+    assert np.array_equal(ids[clear], ora.ids[clear])
+    El = h.cfg.num_local_experts
+    counts = _read_ws(h, b["expert_counts"], El + 1, np.int32)
+    offsets = _read_ws(h, b["expert_offsets"], El + 2, np.int32)
+    perm = _read_ws(h, b["perm_src"], int(offsets[-1]), np.int32)
+    if clear.all():
+        assert np.array_equal(counts[:El], ora.counts)
+        got = np.concatenate([perm[offsets[e]:offsets[e] + counts[e]] for e in range(El)])
+        assert np.array_equal(got, ora.pairs)
+    if h.cfg.act_mode != moe.MOE_W4A16:
+        H = h.cfg.hidden
+        gs = _read_ws(h, b["gs_a"], 1, np.float32)[0]
+        assert gs == np.float32(ora.gs_a)
+        rows = int(offsets[-1])
+        pitch = (H // 2 + 127) // 128 * 128
+        ac = _read_ws(h, b["a_codes"], rows * pitch, np.uint8)
+        asf = _read_ws(h, b["a_sf"], rows * H // 16, np.uint8)
+        c, s = tiled_to_canonical(ac, asf, rows, H)
+        valid = np.nonzero(perm >= 0)[0]
+        tok = np.where(perm[valid] < T * k, perm[valid] // k, perm[valid] - T * k)
+        assert np.array_equal(c[valid], ora.x_codes[tok])
+        assert np.array_equal(s[valid], ora.x_sf[tok])
+
+
+def test_tiny_layer_full_parity():
+    c = synth.CONFIGS["tiny"]
+    T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+    gs_i = INTER["tiny"]["inter_global_scale"]
+    layer = build_layer(0, H, I, E)
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(0, T, H)
+    h = make_layer(layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T)
+    got = _forward(h, x, T)
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, inter_gs=gs_i), x, layer, router_w=wr)
+    clear, _ = _routing_clear(x, wr, None, k)
+    assert clear.all()
+    _check(got, ora.out, "tiny")
+    _forward_buffers_check(h, T, ora, clear)
+
+
+def test_empty_batch_is_a_no_op():
+    c = synth.CONFIGS["tiny"]
+    H, I, E, k = c["H"], c["I"], c["E"], c["k"]
+    layer = build_layer(0, H, I, E)
+    h = make_layer(layer, synth.router_weight(0, E, H), H, I, E, k, inter_gs=64.0, max_tokens=4)
+    out = torch.zeros((1, H), dtype=torch.int16, device="cuda")
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    moe.moe_forward(h.handle, out, None, None, 0, out, ws)
+    torch.cuda.synchronize()
+
+
+def test_decode_layer_full_parity(big_layer):
+    c = synth.CONFIGS["decode"]
+    T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+    gs_i = INTER["decode"]["inter_global_scale"]
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(0, T, H)
+    h = make_layer(big_layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T)
+    got = _forward(h, x, T)
+    clear, _ = _routing_clear(x, wr, None, k)
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, inter_gs=gs_i), x, big_layer,
+                             router_w=wr)
+    _check(got[clear], ora.out[clear], "decode")
+    _forward_buffers_check(h, T, ora, clear)
+
+
+def test_shard_partials_and_union(big_layer):
+    c = synth.CONFIGS["shard"]
+    T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+    gs_i = INTER["shard"]["inter_global_scale"]
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(0, T, H)
+    bias = synth.zipf_bias(0, E)
+    full = make_layer(big_layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T)
+    s0 = make_layer(slice_layer(big_layer, 0, 160), wr, H, I, E, k, E_loc=160, off=0,
+                    add_shared=1, inter_gs=gs_i, max_tokens=T)
+    s1 = make_layer(slice_layer(big_layer, 160, 320), wr, H, I, E, k, E_loc=160, off=160,
+                    add_shared=0, inter_gs=gs_i, max_tokens=T)
+    of = _forward(full, x, T, bias=bias)
+    o0 = _forward(s0, x, T, bias=bias)
+    o1 = _forward(s1, x, T, bias=bias)
+    # the two partial sums add up to the full layer (each partial rounded to bf16)
+    _check(o0 + o1, of, "shard 0-159 + shard 160-319 vs full")
+    # the local pair sets are disjoint and cover every pair
+    inv0 = _read_ws(s0, moe.moe_forward_buffers(s0.handle, s0.ws, T)["inv"], T * k, np.int32)
+    inv1 = _read_ws(s1, moe.moe_forward_buffers(s1.handle, s1.ws, T)["inv"], T * k, np.int32)
+    assert np.all((inv0 >= 0) ^ (inv1 >= 0))
+    # shard 160..319 against the oracle's shard on sampled tokens
+    clear, _ = _routing_clear(x, wr, bias, k)
+    tok = np.sort(np.random.default_rng(0).choice(T, 48, replace=False)).astype(np.int32)
+    tok = tok[clear[tok]]
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, E_loc=160, off=160, add_shared=0,
+                                             inter_gs=gs_i),
+                             x, slice_layer(big_layer, 160, 320), router_w=wr, logit_bias=bias,
+                             tokens=tok)
+    _check(o1[tok], ora.out, "shard 160-319")
+    counts = np.bincount(ora.ids.ravel(), minlength=E)
+    assert counts.max() > 4 * counts.mean()  # Zipf popularity: a few hot experts
+
+
+@pytest.mark.parametrize("T", synth.CONFIGS["w4a16"]["sweep"])
+def test_w4a16_decode_sweep(big_layer, T):
+    c = synth.CONFIGS["w4a16"]
+    H, I, E, k = c["H"], c["I"], c["E"], c["k"]
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(0, T, H)
+    lg = synth.logits_normal(0, T, E)
+    h = make_layer(big_layer, wr, H, I, E, k, act_mode=moe.MOE_W4A16, max_tokens=T)
+    got = _forward(h, x, T, logits_in=lg)
+    tok = np.arange(T, dtype=np.int32) if T <= 32 else np.sort(
+        np.random.default_rng(T).choice(T, 32, replace=False)).astype(np.int32)
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, act_mode=2), x, big_layer,
+                             logits_in=lg, tokens=tok)
+    _check(got[tok], ora.out, "w4a16 T=%d" % T)
+
+
+def test_prefill_chunk_sampled_parity(big_layer):
+    c = synth.CONFIGS["prefill"]
+    T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+    gs_i = INTER["prefill"]["inter_global_scale"]
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(0, T, H, outlier_frac=c["outlier_frac"])
+    h = make_layer(big_layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T)
+    got = _forward(h, x, T)
+    clear, _ = _routing_clear(x, wr, None, k)
+    tok = np.sort(np.random.default_rng(1).choice(T, 96, replace=False)).astype(np.int32)
+    tok = tok[clear[tok]]
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, inter_gs=gs_i), x, big_layer,
+                             router_w=wr, tokens=tok)
+    _check(got[tok], ora.out, "prefill")
+    # routing over every token, bit-exact where the fp64 gap is clear
+    ids = _read_ws(h, moe.moe_forward_buffers(h.handle, h.ws, T)["topk_ids"], T * k,
+                   np.int32).reshape(T, k)
+    assert np.array_equal(ids[clear], ora.ids[clear])
+    counts = np.bincount(ora.ids.ravel(), minlength=E)
+    assert 150 < counts.mean() < 260  # ~205 tokens per expert

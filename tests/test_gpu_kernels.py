@@ -1,0 +1,352 @@
+"""GPU parity of each C-ABI call against the oracle, on seeded inputs that span several
+tiles and k-stages with ragged tails.  Integer work (top-k ids, grouping, NVFP4 codes and
+scales) is compared bit for bit; contractions within fp32-accumulation tolerances."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_mixture_experts_gb300 as moe
+import oracle
+import synth
+from gpu_util import (bits16, canonical_to_tiled, dev, host, make_layer,
+                      quant_decisions_near_boundary, tiled_to_canonical)
+from helpers import build_layer
+
+pytestmark = pytest.mark.gpu
+
+
+def _ws(nbytes):
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+
+
+# ---------------------------------------------------------------- quantiser
+
+@pytest.mark.parametrize("R,K,layout", [(300, 512, 0), (300, 512, 1), (1, 64, 0), (129, 4096, 1),
+                                        (64, 1280, 1)])
+def test_quant_nvfp4_dynamic_bit_exact(R, K, layout):
+    x = synth.activations(3, R, K, outlier_frac=0.02)
+    xd = bits16(x)
+    codes = torch.zeros((((R + 127) // 128) * 128 if layout else R) * (
+        (K // 2 + 127) // 128 * 128 if layout else K // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.zeros((((R + 127) // 128) * 128 if layout else R) * (K // 16),
+                     dtype=torch.uint8, device="cuda")
+    gs = torch.zeros(1, dtype=torch.float32, device="cuda")
+    moe.moe_quant_nvfp4(xd, R, K, None, gs, codes, sf, layout, _ws(256))
+    torch.cuda.synchronize()
+    rc, rs, rg = oracle.quant_nvfp4(synth.bf16_to_f32(x))
+    assert float(host(gs)[0]) == rg
+    if layout:
+        c, s = tiled_to_canonical(host(codes), host(sf), R, K)
+    else:
+        c, s = host(codes).reshape(R, K // 2), host(sf).reshape(R, K // 16)
+    assert np.array_equal(s, rs)
+    assert np.array_equal(c, rc)
+
+
+def test_quant_nvfp4_static_scale_and_zero_rows():
+    R, K = 40, 256
+    x = synth.activations(4, R, K)
+    x[5] = 0  # a zero row: every scale 0, every code +0
+    gsv = np.float32(96.0)
+    codes = torch.zeros(R * K // 2, dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(R * K // 16, dtype=torch.uint8, device="cuda")
+    moe.moe_quant_nvfp4(bits16(x), R, K, dev(np.array([gsv])), None, codes, sf, 0, None)
+    rc, rs, _ = oracle.quant_nvfp4(synth.bf16_to_f32(x), gs=float(gsv))
+    assert np.array_equal(host(sf).reshape(R, -1), rs)
+    assert np.array_equal(host(codes).reshape(R, -1), rc)
+    assert not host(codes).reshape(R, -1)[5].any()
+
+
+def test_swiglu_requant_matches_oracle_up_to_boundaries():
+    R, I, gs_i = 150, 256, 64.0
+    rng = np.random.default_rng(8)
+    gu = (rng.standard_normal((R, 2 * I)) * 1.5).astype(np.float32)
+    codes = torch.zeros(R * I // 2, dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(R * I // 16, dtype=torch.uint8, device="cuda")
+    moe.moe_swiglu_requant(dev(gu), R, I, gs_i, codes, sf, 0)
+    rc, rs, s = oracle.swiglu_requant(gu, I, gs_i)
+    gc, gsf = host(codes).reshape(R, -1), host(sf).reshape(R, -1)
+    ok = quant_decisions_near_boundary(s, gs_i, rs, gsf, rc, gc)
+    assert ok.all(), np.argwhere(~ok)[:5]
+    assert (gsf == rs).mean() > 0.999
+
+
+# ---------------------------------------------------------------- routing
+
+def zero_layer(H, I, El):
+    """All-zero NVFP4 experts (valid weights for calls that do not read them)."""
+    z = lambda *shape: np.zeros(shape, np.uint8)
+    one = lambda n: np.ones(n, np.float32)
+    return oracle.Layer(z(El, 2 * I, H // 2), z(El, 2 * I, H // 16), one(El),
+                        z(El, H, I // 2), z(El, H, I // 16), one(El),
+                        z(2 * I, H // 2), z(2 * I, H // 16), 1.0, z(H, I // 2), z(H, I // 16), 1.0)
+
+
+def _tiny_layer_handle(E=320, H=256, I=64, k=8, E_loc=None, **kw):
+    El = E if E_loc is None else E_loc
+    wr = synth.router_weight(0, E, H)
+    return make_layer(zero_layer(H, I, El), wr, H, I, E, k, E_loc=El, inter_gs=64.0, **kw), wr
+
+
+def test_topk_from_given_logits_bit_exact():
+    T, E, k = 300, 320, 8
+    h, _ = _tiny_layer_handle(E=E, k=k)
+    lg = synth.logits_normal(5, T, E)
+    lg[:50] = np.round(lg[:50] * 4) / 4  # exact ties -> lower id first
+    ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(h.handle, None, dev(lg), None, T, ids, w, None, None)
+    rid, rw = oracle.topk(lg.astype(np.float64), k)
+    assert np.array_equal(host(ids), rid)
+    assert np.max(np.abs(host(w) - rw)) <= 1e-6
+    # a bias whose sums are exact in fp32 and fp64 alike
+    bias = (np.arange(E) % 7 * 0.25).astype(np.float32)
+    lgq = (np.round(lg * 1024) / 1024).astype(np.float32)
+    moe.moe_route_topk(h.handle, None, dev(lgq), dev(bias), T, ids, w, None, None)
+    rid, rw = oracle.topk(lgq.astype(np.float64) + bias, k)
+    assert np.array_equal(host(ids), rid)
+
+
+def test_router_logits_and_topk_from_x():
+    T, E, H, k = 200, 320, 4096, 8
+    h, wr = _tiny_layer_handle(E=E, H=H, k=k)
+    x = synth.activations(6, T, H)
+    ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    lo = torch.zeros((T, E), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(h.handle, bits16(x), None, None, T, ids, w, lo,
+                       _ws(h.workspace_bytes(T)))
+    ref = oracle.router_logits(x, wr)
+    got = host(lo).astype(np.float64)
+    # fp32 accumulation of 4096 exact products: error << 1e-4 of the sum of |terms|
+    mag = np.abs(synth.bf16_to_f32(x).astype(np.float64)) @ np.abs(
+        synth.bf16_to_f32(wr).astype(np.float64)).T
+    assert np.all(np.abs(got - ref) <= 1e-5 * mag + 1e-6)
+    rid, rw = oracle.topk(ref, k)
+    srt = -np.sort(-ref, axis=1)
+    gap = srt[:, k - 1] - srt[:, k]
+    clear = gap > 2e-5 * mag.max(1)
+    assert clear.mean() > 0.95
+    assert np.array_equal(host(ids)[clear], rid[clear])
+    assert np.max(np.abs(host(w)[clear] - rw[clear])) <= 1e-5
+
+
+# ---------------------------------------------------------------- grouping
+
+@pytest.mark.parametrize("T,E_loc,off,add_shared", [(1, 320, 0, 1), (64, 320, 0, 1),
+                                                    (300, 160, 160, 0), (2000, 160, 0, 1),
+                                                    (2000, 37, 100, 0)])
+def test_permute_bit_exact(T, E_loc, off, add_shared):
+    E, k = 320, 8
+    h, _ = _tiny_layer_handle(E=E, k=k, E_loc=E_loc, off=off, add_shared=add_shared)
+    rng = np.random.default_rng(T + E_loc)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    cap = h.rows_capacity(T)
+    counts = torch.zeros(E_loc + 1, dtype=torch.int32, device="cuda")
+    offsets = torch.zeros(E_loc + 2, dtype=torch.int32, device="cuda")
+    perm = torch.full((cap,), -7, dtype=torch.int32, device="cuda")
+    inv = torch.zeros(T * k, dtype=torch.int32, device="cuda")
+    ws = _ws(h.workspace_bytes(T))
+    moe.moe_permute(h.handle, dev(ids), T, counts, offsets, perm, inv, ws)
+    rc, rp = oracle.permute(ids, E_loc, off)
+    c, o, p, iv = host(counts), host(offsets), host(perm), host(inv)
+    assert np.array_equal(c[:E_loc], rc)
+    assert c[E_loc] == (T if add_shared else 0)
+    pad = (c + 127) // 128 * 128
+    assert np.array_equal(o, np.concatenate([[0], np.cumsum(pad)]))
+    got_pairs = np.concatenate([p[o[e]:o[e] + c[e]] for e in range(E_loc)]) if E_loc else []
+    assert np.array_equal(got_pairs, rp)
+    for g in range(E_loc + 1):
+        assert np.all(p[o[g] + c[g]:o[g + 1]] == -1)
+    assert np.array_equal(p[o[E_loc]:o[E_loc] + c[E_loc]], T * k + np.arange(c[E_loc]))
+    want_inv = np.full(T * k, -1)
+    rows = np.concatenate([np.arange(o[e], o[e] + c[e]) for e in range(E_loc)]) if E_loc else []
+    want_inv[rp] = rows
+    assert np.array_equal(iv, want_inv)
+    assert moe.moe_get_status(h.handle, ws) == (moe.MOE_OK, 0)
+
+
+def test_permute_drops_and_flags_bad_ids():
+    E, k, T = 320, 8, 10
+    h, _ = _tiny_layer_handle(E=E, k=k)
+    ids = np.stack([np.arange(k) + 10 * t for t in range(T)]).astype(np.int32)
+    ids[3, 2] = 400   # >= E
+    ids[7, 0] = -5
+    cap = h.rows_capacity(T)
+    counts = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    offsets = torch.zeros(E + 2, dtype=torch.int32, device="cuda")
+    perm = torch.zeros(cap, dtype=torch.int32, device="cuda")
+    inv = torch.zeros(T * k, dtype=torch.int32, device="cuda")
+    ws = _ws(h.workspace_bytes(T))
+    moe.moe_permute(h.handle, dev(ids), T, counts, offsets, perm, inv, ws)
+    iv = host(inv)
+    assert iv[3 * k + 2] == -1 and iv[7 * k] == -1
+    assert host(counts)[:E].sum() == T * k - 2
+    st, bits = moe.moe_get_status(h.handle, ws)
+    assert st == moe.MOE_ERR_DEVICE_STATUS and bits & moe.MOE_DEV_BAD_EXPERT_ID
+    assert moe.moe_get_status(h.handle, ws) == (moe.MOE_OK, 0)  # cleared
+
+
+# ---------------------------------------------------------------- grouped GEMMs
+
+class Staged:
+    """Runs the staged calls of one layer up to the grouped GEMMs."""
+
+    def __init__(self, h, x_bits, T, k, logits):
+        self.h, self.T, self.k = h, T, k
+        cfg = h.cfg
+        El = cfg.num_local_experts
+        self.cap = cap = h.rows_capacity(T)
+        self.ws = _ws(h.workspace_bytes(T))
+        self.ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+        self.w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+        moe.moe_route_topk(h.handle, None, dev(logits), None, T, self.ids, self.w, None, None)
+        self.counts = torch.zeros(El + 1, dtype=torch.int32, device="cuda")
+        self.offsets = torch.zeros(El + 2, dtype=torch.int32, device="cuda")
+        self.perm = torch.zeros(cap, dtype=torch.int32, device="cuda")
+        self.inv = torch.zeros(T * k, dtype=torch.int32, device="cuda")
+        moe.moe_permute(h.handle, self.ids, T, self.counts, self.offsets, self.perm, self.inv,
+                        self.ws)
+        H = cfg.hidden
+        self.a_codes = torch.zeros(cap * ((H // 2 + 127) // 128 * 128), dtype=torch.uint8,
+                                   device="cuda")
+        self.a_sf = torch.zeros(cap * H // 16, dtype=torch.uint8, device="cuda")
+        self.a_bf16 = torch.zeros(cap * H, dtype=torch.int16, device="cuda")
+        self.gs = torch.zeros(1, dtype=torch.float32, device="cuda")
+        moe.moe_gather_activations(h.handle, x_bits, T, self.inv, self.offsets, self.a_codes,
+                                   self.a_sf, self.a_bf16, self.gs, self.ws)
+        torch.cuda.synchronize()
+
+    def rows(self):
+        """(padded row, token, group) of every valid row."""
+        c, o, p = host(self.counts), host(self.offsets), host(self.perm)
+        out = []
+        for g in range(len(c)):
+            for i in range(c[g]):
+                r = o[g] + i
+                pair = p[r]
+                tok = pair // self.k if pair < self.T * self.k else pair - self.T * self.k
+                out.append((r, tok, g))
+        return np.array(out, dtype=np.int64).reshape(-1, 3)
+
+
+def _mid_problem(act_mode):
+    H, I, E, k, T = 512, 256, 8, 2, 200
+    layer = build_layer(12, H, I, E)
+    wr = synth.router_weight(12, E, H)
+    x = synth.activations(12, T, H, outlier_frac=0.01)
+    lg = synth.logits_normal(12, T, E)
+    lg[:, 3] += 2.5   # one popular expert: > 128 rows -> two row blocks
+    h = make_layer(layer, wr, H, I, E, k, act_mode=act_mode, inter_gs=32.0)
+    return layer, wr, x, lg, h, (H, I, E, k, T)
+
+
+@pytest.mark.parametrize("act_mode", [0, 2])
+def test_grouped_gemm_gateup_unfused_matches_oracle(act_mode):
+    layer, wr, x, lg, h, (H, I, E, k, T) = _mid_problem(act_mode)
+    st = Staged(h, bits16(x), T, k, lg)
+    rows = st.rows()
+    assert (np.bincount(rows[:, 2], minlength=E + 1) > 128).any()
+    G = torch.zeros((st.cap, 2 * I), dtype=torch.float32, device="cuda")
+    moe.moe_grouped_gemm_gateup(h.handle, st.a_codes, st.a_sf, st.gs, st.a_bf16, st.counts,
+                                st.offsets, 0, G, None, None, None, T, st.ws)
+    Gg = host(G)
+    cfg = oracle.make_cfg(T, H, I, E, k, act_mode=act_mode, inter_gs=32.0)
+    xf = synth.bf16_to_f32(x)
+    xc, xsf, gs_a = oracle.quant_nvfp4(xf) if act_mode != 2 else (None, None, 1.0)
+    if act_mode != 2:
+        assert float(host(st.gs)[0]) == gs_a
+    for g in range(E + 1):
+        sel = rows[rows[:, 2] == g]
+        if len(sel) == 0:
+            continue
+        e = "shared" if g == E else g
+        Go = oracle.expert_rows(cfg, layer, e, x, xc, xsf, gs_a, sel[:, 1].astype(np.int32))[0]
+        got = Gg[sel[:, 0]]
+        err = np.abs(got - Go)
+        scale = np.sqrt(np.mean(Go ** 2))
+        assert np.max(err) <= 2e-5 * scale * np.sqrt(H / 64), (g, np.max(err), scale)
+
+
+@pytest.mark.parametrize("act_mode", [0, 2])
+def test_grouped_gemm_fused_and_down_match_oracle(act_mode):
+    layer, wr, x, lg, h, (H, I, E, k, T) = _mid_problem(act_mode)
+    st = Staged(h, bits16(x), T, k, lg)
+    rows = st.rows()
+    ic = torch.zeros(st.cap * ((I // 2 + 127) // 128 * 128), dtype=torch.uint8, device="cuda")
+    isf = torch.zeros(st.cap * I // 16, dtype=torch.uint8, device="cuda")
+    ib = torch.zeros(st.cap * I, dtype=torch.int16, device="cuda")
+    moe.moe_grouped_gemm_gateup(h.handle, st.a_codes, st.a_sf, st.gs, st.a_bf16, st.counts,
+                                st.offsets, 1, None, ic, isf, ib, T, st.ws)
+    cfg = oracle.make_cfg(T, H, I, E, k, act_mode=act_mode, inter_gs=32.0)
+    xf = synth.bf16_to_f32(x)
+    xc, xsf, gs_a = oracle.quant_nvfp4(xf) if act_mode != 2 else (None, None, 1.0)
+    n = len(rows)
+    ref_ic = np.zeros((n, I // 2), np.uint8)
+    ref_isf = np.zeros((n, I // 16), np.uint8)
+    ref_Y = np.zeros((n, H))
+    ref_s = np.zeros((n, I))
+    for g in range(E + 1):
+        idx = np.nonzero(rows[:, 2] == g)[0]
+        if len(idx) == 0:
+            continue
+        e = "shared" if g == E else g
+        G, c_, s_, Y = oracle.expert_rows(cfg, layer, e, x, xc, xsf, gs_a,
+                                          rows[idx, 1].astype(np.int32))
+        ref_ic[idx], ref_isf[idx], ref_Y[idx] = c_, s_, Y
+        ref_s[idx] = G[:, :I] / (1 + np.exp(-G[:, :I])) * G[:, I:]
+    if act_mode != 2:
+        gc, gsf = tiled_to_canonical(host(ic), host(isf), st.cap, I)
+        gc, gsf = gc[rows[:, 0]], gsf[rows[:, 0]]
+        # fp32 accumulation vs fp64: decisions may differ only next to a boundary
+        same = (gsf == ref_isf)
+        assert same.mean() > 0.995
+        near = quant_decisions_near_boundary(ref_s, 32.0, ref_isf, gsf, ref_ic, gc, rel=5e-5)
+        assert near.mean() > 0.999
+        # the down GEMM alone, fed the oracle's intermediate (tiled as the library expects)
+        full_c = np.zeros((st.cap, I // 2), np.uint8)
+        full_s = np.zeros((st.cap, I // 16), np.uint8)
+        full_c[rows[:, 0]] = ref_ic
+        full_s[rows[:, 0]] = ref_isf
+        ct, stl = canonical_to_tiled(full_c, full_s, st.cap, I)
+        dic, disf = dev(ct.reshape(-1)), dev(stl)
+        dib = None
+    else:
+        gb = host(ib).reshape(st.cap, I)[rows[:, 0]].view(np.uint16)
+        want = np.array([[oracle.bf16_round(v) for v in row] for row in ref_s[:8]], np.uint16)
+        assert np.mean(gb[:8] == want) > 0.99
+        full = np.zeros((st.cap, I), np.uint16)
+        full[rows[:, 0]] = np.array([[oracle.bf16_round(v) for v in row] for row in ref_s],
+                                    np.uint16)
+        dic = disf = None
+        dib = bits16(full.reshape(-1))
+    y = torch.zeros(((T * k + T), H), dtype=torch.float32, device="cuda")
+    moe.moe_grouped_gemm_down(h.handle, dic, disf, dib, st.counts, st.offsets, st.perm, st.w,
+                              y, T, st.ws)
+    yg = host(y)
+    perm = host(st.perm)
+    wts = host(st.w).reshape(-1)
+    for j, (r, tok, g) in enumerate(rows):
+        pair = perm[r]
+        wt = wts[pair] if pair < T * k else 1.0
+        want = ref_Y[j] * wt
+        got = yg[pair]
+        assert np.max(np.abs(got - want)) <= 1e-4 * np.sqrt(np.mean(want ** 2)) * np.sqrt(I / 64) + 1e-9, (j, g)
+
+
+def test_combine_sums_pairs_and_shared():
+    T, k, H = 33, 8, 256
+    h, _ = _tiny_layer_handle(E=320, k=k, H=H)
+    rng = np.random.default_rng(1)
+    y = rng.standard_normal((T * k + T, H)).astype(np.float32)
+    inv = rng.integers(-1, 5, size=T * k).astype(np.int32)  # >= 0 means local
+    out = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+    moe.moe_combine(h.handle, dev(y), dev(inv), T, out)
+    want = np.zeros((T, H), np.float64)
+    for t in range(T):
+        for j in range(k):
+            if inv[t * k + j] >= 0:
+                want[t] += y[t * k + j]
+        want[t] += y[T * k + t]
+    got = synth.bf16_to_f32(host(out).view(np.uint16))
+    assert np.max(np.abs(got - want) / (np.abs(want) + 1e-3)) < 2 ** -7
