@@ -1,0 +1,541 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 fused mixture-of-experts layer forward (tokens/s).
+
+One step = one whole forward of the layer (route, group, quantise, gate_up GEMM with
+fused SwiGLU+requant, down GEMM, combine) over one batch of seeded synthetic tokens.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|...]
+  python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
+
+Prints ONE JSON line (rank 0).  value: tokens/s of the whole job, inputs resident in HBM,
+device time of K CUDA-graph replays (CUDA events).  e2e: the same through the C ABI with
+the batch copied host->device and the output device->host inside the timed region.
+roofline: the gate_up grouped GEMM (the dominant kernel), algorithmic bytes per launch /
+its CUDA-event duration measured here, against the measured HBM copy bandwidth.
+Weights (2.3-2.8 GB per step) exceed the 129 MB L2, so no L2 flush is needed between steps.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "NVFP4 MoE-layer tokens/s at T=64/8192; % of HBM or FP4 tensor roofline"
+INTER = json.load(open(os.path.join(ROOT, "tests", "golden", "inter_scale.json")))
+NVFP4_BYTES = 0.5625  # 4-bit code + one E4M3 scale per 16 elements
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--no-extra", action="store_true", help="skip the prefill side measurement")
+    ap.add_argument("--nvtx", action="store_true",
+                    help="wrap the device-timed steps in an NVTX range named 'timed' (for ncu)")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, src="fallback")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        self.marks = []
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.p:
+            self.p.terminate()
+            self.p.wait()
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.f.name)
+        return rows
+
+
+def summarise_clocks(rows):
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+    def num(s):
+        try:
+            return float(s)
+        except ValueError:
+            return None
+    sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+    mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- GPU layer setup
+
+def gpu_layer(name, seed=0, extra_handles=()):
+    """Seeded weights (N(0, 0.02) masters rounded to bf16) quantised to NVFP4 by the
+    library's own quantiser on the GPU, then handed to moe_create.  Returns the handles
+    for name and for each config in extra_handles (same weights)."""
+    import torch
+
+    import nvfp4_mixture_experts_gb300 as moe
+    c = synth.CONFIGS[name]
+    H, I, E, k = c["H"], c["I"], c["E"], c["k"]
+    experts = list(range(c["off"], c["off"] + c["E_loc"]))
+    El = len(experts)
+    dev = torch.device("cuda")
+    w = dict(w13=torch.empty((El, 2 * I, H // 2), dtype=torch.uint8, device=dev),
+             w13_sf=torch.empty((El, 2 * I, H // 16), dtype=torch.uint8, device=dev),
+             w13_gs=torch.empty(El, dtype=torch.float32, device=dev),
+             w2=torch.empty((El, H, I // 2), dtype=torch.uint8, device=dev),
+             w2_sf=torch.empty((El, H, I // 16), dtype=torch.uint8, device=dev),
+             w2_gs=torch.empty(El, dtype=torch.float32, device=dev))
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+
+    def gen(e):
+        m13, m2 = synth.expert_master(seed, e, H, I) if e != "shared" else \
+            synth.shared_master(seed, H, I)
+        return synth.bf16_bits(m13).view(np.int16), synth.bf16_bits(m2).view(np.int16)
+
+    def quant(m, rows, cols, codes, sf, gs):
+        t = torch.from_numpy(m).to(dev)
+        moe.moe_quant_nvfp4(t, rows, cols, None, gs, codes, sf, 0, ws)
+
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(min(16, os.cpu_count() or 4)) as pool:
+        for i, (m13, m2) in enumerate(pool.map(gen, experts + ["shared"])):
+            if i < El:
+                quant(m13, 2 * I, H, w["w13"][i], w["w13_sf"][i], w["w13_gs"][i:i + 1])
+                quant(m2, H, I, w["w2"][i], w["w2_sf"][i], w["w2_gs"][i:i + 1])
+            else:
+                w["sh13"] = torch.empty((2 * I, H // 2), dtype=torch.uint8, device=dev)
+                w["sh13_sf"] = torch.empty((2 * I, H // 16), dtype=torch.uint8, device=dev)
+                w["sh13_gs"] = torch.empty(1, dtype=torch.float32, device=dev)
+                w["sh2"] = torch.empty((H, I // 2), dtype=torch.uint8, device=dev)
+                w["sh2_sf"] = torch.empty((H, I // 16), dtype=torch.uint8, device=dev)
+                w["sh2_gs"] = torch.empty(1, dtype=torch.float32, device=dev)
+                quant(m13, 2 * I, H, w["sh13"], w["sh13_sf"], w["sh13_gs"])
+                quant(m2, H, I, w["sh2"], w["sh2_sf"], w["sh2_gs"])
+    w["router_w"] = torch.from_numpy(synth.router_weight(seed, E, H).view(np.int16)).to(dev)
+    torch.cuda.synchronize()
+    handles = {}
+    for nm in (name,) + tuple(extra_handles):
+        cc = synth.CONFIGS[nm]
+        cfg = moe.make_config(H, I, E, k, E_loc=El, off=c["off"], has_shared=1,
+                              add_shared=cc["add_shared"], act_mode=cc["act_mode"],
+                              inter_gs=INTER[nm]["inter_global_scale"],
+                              max_tokens=cc["T"])
+        handles[nm] = moe.MoELayer(cfg, w)
+    del w
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return handles
+
+
+def inputs(name, seed=0):
+    c = synth.CONFIGS[name]
+    x = synth.activations(seed, c["T"], c["H"], outlier_frac=c["outlier_frac"])
+    lg = synth.logits_normal(seed, c["T"], c["E"]) if c["logits"] else None
+    bias = synth.zipf_bias(seed, c["E"]) if c["bias"] else None
+    return x, lg, bias
+
+
+def launches_per_forward(c):
+    n = 1 + (0 if c["logits"] else 1)      # router logits (from x) + top-k
+    n += 3                                 # grouping: histogram, scan, scatter
+    n += 2 if c["act_mode"] == 0 else 1    # (amax +) gather-quantise / gather
+    n += 2 + 1                             # two grouped GEMMs + combine
+    return n
+
+
+def gemm_bytes(c, counts, gateup):
+    """Algorithmic bytes of one grouped-GEMM launch: the weights of every expert that has
+    rows, the activation rows it reads and the rows it writes, each once."""
+    H, I, El = c["H"], c["I"], c["E_loc"]
+    touched = int((counts[:El] > 0).sum()) + int(counts[El] > 0)
+    rows = int(counts.sum())
+    w4a16 = c["act_mode"] == 2
+    if gateup:
+        wbytes = touched * 2 * I * H * NVFP4_BYTES
+        a_in = rows * H * (2 if w4a16 else NVFP4_BYTES)
+        a_out = rows * I * (2 if w4a16 else NVFP4_BYTES)
+    else:
+        wbytes = touched * H * I * NVFP4_BYTES
+        a_in = rows * I * (2 if w4a16 else NVFP4_BYTES)
+        a_out = rows * H * 4
+    return wbytes + a_in + a_out, touched, rows
+
+
+def gemm_flops(counts, c, gateup):
+    rows = int(counts.sum())
+    return 2.0 * rows * (2 * c["I"] * c["H"] if gateup else c["H"] * c["I"])
+
+
+def profile_traffic(kernel, workload):
+    """dram bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "%s_%s.json" % (kernel, workload))
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    src = os.path.join(ROOT, "nvfp4_mixture_experts_gb300", "csrc", "gemm.cu")
+    if d.get("gemm_cu_sha1") != hashlib.sha1(open(src, "rb").read()).hexdigest():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def measure_ours(args, rank, world):
+    import torch
+
+    import nvfp4_mixture_experts_gb300 as moe
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    name = args.workload
+    c = synth.CONFIGS[name]
+    T, H, k = c["T"], c["H"], c["k"]
+    extra = () if (args.no_extra or name != "decode") else ("prefill",)
+    handles = gpu_layer(name, extra_handles=extra)
+    layer = handles[name]
+    x, lg, bias = inputs(name, seed=rank)
+    dev = torch.device("cuda")
+    xd = torch.from_numpy(x.view(np.int16)).to(dev)
+    lgd = None if lg is None else torch.from_numpy(lg).to(dev)
+    bd = None if bias is None else torch.from_numpy(bias).to(dev)
+    out = torch.empty((T, H), dtype=torch.int16, device=dev)
+    ws = layer.ensure_workspace(T)
+    stream = torch.cuda.Stream()
+
+    def fwd():
+        moe.moe_forward(layer.handle, xd, lgd, bd, T, out, ws)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            fwd()
+        torch.cuda.synchronize()
+        st, bits = moe.moe_get_status(layer.handle, ws)
+        if st != moe.MOE_OK:
+            raise RuntimeError("device status %#x" % bits)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fwd()
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.3)
+    # ---- device-timed steps (CUDA graph replays)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        barrier()
+        torch.cuda.synchronize()
+        if args.nvtx:
+            torch.cuda.nvtx.range_push("timed")
+        ev0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        ev1.record(stream)
+        if args.nvtx:
+            torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        barrier()
+        # keep the clocks sampled over at least ~1.5 s of the same work
+        t_end = time.time() + max(0.0, 1.5 - ev0.elapsed_time(ev1) / 1e3)
+        while time.time() < t_end:
+            for _ in range(50):
+                g.replay()
+            torch.cuda.synchronize()
+    clocks = summarise_clocks(sampler.stop())
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T / (ms / 1e3)
+
+    # ---- end to end through the C ABI: pinned host x -> device, forward, out -> host
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    oh = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            xd.copy_(xh, non_blocking=True)
+            fwd()
+            oh.copy_(out, non_blocking=True)
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            xd.copy_(xh, non_blocking=True)
+            fwd()
+            oh.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    roof = roofline(layer, c, xd, lgd, bd, ws, stream, args.steps, peaks(), name)
+    res = dict(value=value, ms=ms, ms_e2e=ms_e2e, clocks=clocks, roofline=roof,
+               launches=launches_per_forward(c) * args.steps)
+    if "prefill" in extra and rank == 0:
+        res["prefill"] = measure_prefill(handles["prefill"], stream, max(3, args.steps // 20))
+    return res
+
+
+def staged_counts(layer, ws, T):
+    import torch
+
+    import nvfp4_mixture_experts_gb300 as moe
+    b = moe.moe_forward_buffers(layer.handle, ws, T)
+    G = layer.cfg.num_local_experts + 1
+    off = b["expert_counts"] - ws.data_ptr()
+    return ws[off:off + 4 * G].cpu().numpy().view(np.int32).copy()
+
+
+def roofline(layer, c, xd, lgd, bd, ws, stream, steps, pk, workload):
+    """Times each grouped GEMM launch with CUDA events on its stream over `steps` launches
+    of the staged calls, after one forward has filled the workspace intermediates."""
+    import torch
+
+    import nvfp4_mixture_experts_gb300 as moe
+    T = c["T"]
+    b = moe.moe_forward_buffers(layer.handle, ws, T)
+    counts = staged_counts(layer, ws, T)
+    h = layer.handle
+    lib = moe.load()
+    import ctypes as C
+    nbytes = ws.numel()
+    strm = C.c_void_p(stream.cuda_stream)
+    a16 = c["act_mode"] == 2
+    P = lambda n: C.c_void_p(b[n])
+    times = {"gateup": [], "down": []}
+    with torch.cuda.stream(stream):
+        for i in range(steps + 3):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(stream)
+            st = lib.moe_grouped_gemm_gateup(h, P("a_codes"), P("a_sf"), P("gs_a"),
+                                             P("a_bf16"), P("expert_counts"),
+                                             P("expert_offsets"), 1, None, P("inter_codes"),
+                                             P("inter_sf"), P("inter_bf16"),
+                                             T, C.c_void_p(ws.data_ptr()), nbytes, strm)
+            e[1].record(stream)
+            st |= lib.moe_grouped_gemm_down(h, P("inter_codes"), P("inter_sf"),
+                                            P("inter_bf16"),
+                                            P("expert_counts"), P("expert_offsets"),
+                                            P("perm_src"), P("topk_w"), P("y"), T,
+                                            C.c_void_p(ws.data_ptr()), nbytes, strm)
+            e[2].record(stream)
+            if st:
+                raise RuntimeError("staged GEMM call failed: %d" % st)
+            if i >= 3:
+                times["gateup"].append(e)
+        torch.cuda.synchronize()
+    gu = statistics.mean(x[0].elapsed_time(x[1]) for x in times["gateup"]) / 1e3
+    dn = statistics.mean(x[1].elapsed_time(x[2]) for x in times["gateup"]) / 1e3
+    bytes_gu, touched, rows = gemm_bytes(c, counts, True)
+    bytes_dn, _, _ = gemm_bytes(c, counts, False)
+    ach = bytes_gu / gu / 1e9
+    kern = "gemm_w4a16" if a16 else "gemm_nvf4"
+    fl = gemm_flops(counts, c, True)
+    return {"kernel": kern + "_kernel (gate_up, fused SwiGLU+requant)", "bound": "hbm",
+            "achieved": round(ach, 1), "peak": pk["hbm"], "unit": "GB/s",
+            "frac": round(ach / pk["hbm"], 4), "peak_src": pk["src"],
+            "traffic": profile_traffic(kern + "_gateup", workload),
+            "alg_bytes_per_launch": int(bytes_gu), "launch_us": round(gu * 1e6, 2),
+            "experts_touched": touched, "rows": rows,
+            "fp4_tflops": round(fl / gu / 1e12, 2),
+            "down": {"achieved": round(bytes_dn / dn / 1e9, 1), "launch_us": round(dn * 1e6, 2),
+                     "alg_bytes_per_launch": int(bytes_dn),
+                     "frac": round(bytes_dn / dn / 1e9 / pk["hbm"], 4)}}
+
+
+def measure_prefill(layer, stream, steps):
+    """Side measurement of the prefill chunk (8192 tokens, 1% outlier channels)."""
+    import torch
+
+    import nvfp4_mixture_experts_gb300 as moe
+    c = synth.CONFIGS["prefill"]
+    T, H = c["T"], c["H"]
+    x, _, _ = inputs("prefill")
+    dev = torch.device("cuda")
+    xd = torch.from_numpy(x.view(np.int16)).to(dev)
+    out = torch.empty((T, H), dtype=torch.int16, device=dev)
+    ws = layer.ensure_workspace(T)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            moe.moe_forward(layer.handle, xd, None, None, T, out, ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            moe.moe_forward(layer.handle, xd, None, None, T, out, ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    pk = peaks()
+    roof = roofline(layer, c, xd, None, None, ws, stream, steps, pk, "prefill")
+    counts = staged_counts(layer, ws, T)
+    fl = gemm_flops(counts, c, True) + gemm_flops(counts, c, False)
+    return {"workload": "prefill T=8192", "value": T / (ms / 1e3), "ms_per_step": ms,
+            "roofline": roof, "expert_fp4_tflops": round(fl / (ms / 1e3) / 1e12, 2)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_setup(name, n_tokens, seed=0):
+    """Oracle inputs for a bounded sample: the first n_tokens of the batch; only the experts
+    those tokens reach are quantised (by the oracle, from the same bf16-rounded masters)."""
+    import oracle
+    c = synth.CONFIGS[name]
+    T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+    x, lg, bias = inputs(name, seed)
+    wr = synth.router_weight(seed, E, H)
+    full = lg.astype(np.float64) if lg is not None else oracle.router_logits(x, wr, bias)
+    ids, _ = oracle.topk(full if bias is None or lg is None else full + bias, k)
+    tok = np.arange(n_tokens, dtype=np.int32)
+    El, off = c["E_loc"], c["off"]
+    used = sorted({int(e) - off for e in ids[:n_tokens].ravel() if 0 <= int(e) - off < El})
+    w13 = np.zeros((El, 2 * I, H // 2), np.uint8)
+    w13_sf = np.zeros((El, 2 * I, H // 16), np.uint8)
+    w2 = np.zeros((El, H, I // 2), np.uint8)
+    w2_sf = np.zeros((El, H, I // 16), np.uint8)
+    g13 = np.ones(El, np.float32)
+    g2 = np.ones(El, np.float32)
+    f32 = lambda m: synth.bf16_to_f32(synth.bf16_bits(m))
+    for le in used:
+        m13, m2 = synth.expert_master(seed, le + off, H, I)
+        w13[le], w13_sf[le], g13[le] = oracle.quant_nvfp4(f32(m13))
+        w2[le], w2_sf[le], g2[le] = oracle.quant_nvfp4(f32(m2))
+    s13, s2 = synth.shared_master(seed, H, I)
+    a, b_, cg = oracle.quant_nvfp4(f32(s13))
+    d, e_, fg = oracle.quant_nvfp4(f32(s2))
+    L = oracle.Layer(w13, w13_sf, g13, w2, w2_sf, g2, a, b_, cg, d, e_, fg)
+    cfg = oracle.make_cfg(T, H, I, E, k, E_loc=El, off=off, add_shared=c["add_shared"],
+                          act_mode=c["act_mode"], inter_gs=INTER[name]["inter_global_scale"])
+    run = lambda: oracle.moe_forward(cfg, x, L, router_w=None if lg is not None else wr,
+                                     logit_bias=bias, logits_in=lg, tokens=tok)
+    return run, "first %d of the %d tokens of the batch (full routing + quantisation of "\
+        "all %d tokens, expert MLPs and combine for the sample)" % (n_tokens, T, T)
+
+
+ORACLE_SAMPLE = {"decode": 64, "prefill": 16, "shard": 16, "w4a16": 16, "tiny": 16}
+
+
+def cpu_baseline(name):
+    import oracle
+    run, what = oracle_setup(name, ORACLE_SAMPLE[name])
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    n = ORACLE_SAMPLE[name]
+    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": what, "seconds": round(dt, 2)}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", args.gpus if args.impl == "ours" else 1))
+    c = synth.CONFIGS[args.workload]
+    config = {"workload": "%s: T=%d, H=%d, I=%d, E=%d routed top-%d + 1 shared%s, %s" % (
+        args.workload, c["T"], c["H"], c["I"], c["E"], c["k"],
+        "" if c["E_loc"] == c["E"] else ", experts %d-%d" % (c["off"], c["off"] + c["E_loc"] - 1),
+        "W4A16" if c["act_mode"] == 2 else "W4A4 dynamic"),
+        "tokens_per_step_per_gpu": c["T"], "global_batch": c["T"] * max(1, args.gpus),
+        "parallelism": "replicas (dp%d)" % max(1, args.gpus),
+        "l2": "no flush: the weights streamed per step (>2 GB) exceed the 129 MB L2"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        run, what = oracle_setup(args.workload, max(1, ORACLE_SAMPLE[args.workload] // 8))
+        n = max(1, ORACLE_SAMPLE[args.workload] // 8)
+        for _ in range(max(0, args.warmup)):
+            run()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            run()
+        dt = (time.perf_counter() - t0) / args.steps
+        v = n / dt
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+                "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "sample": what,
+                                 "value": v, "unit": "tokens/s"},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    r = measure_ours(args, rank, world)
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 (e2m1 x e2m1, ue4m3 scales), fp32 accumulate" if c["act_mode"] != 2
+            else "bf16 x nvfp4, fp32 accumulate",
+            "data": "synthetic (seeded; N(0,1) activations, N(0,0.02) weights)",
+            "config": config, "clocks": r["clocks"],
+            "e2e": {"value": world * c["T"] / (r["ms_e2e"] / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": c["T"] * c["H"] * 2,
+                    "d2h_bytes_per_step": c["T"] * c["H"] * 2},
+            "gpu_launches": r["launches"], "roofline": r["roofline"]}
+    if "prefill" in r:
+        line["prefill"] = r["prefill"]
+    if world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -225,7 +225,8 @@ MOE_API moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int3
                                float** topk_w, int32_t** expert_counts,
                                int32_t** expert_offsets, int32_t** perm_src, int32_t** inv,
                                float** gs_a, uint8_t** a_codes, uint8_t** a_sf,
-                               uint8_t** inter_codes, uint8_t** inter_sf, float** y);
+                               void** a_bf16, uint8_t** inter_codes, uint8_t** inter_sf,
+                               void** inter_bf16, float** y);
 
 /* Reads the device status word of ws (synchronises the stream) into *bits (nullable) and
  * clears it.  Returns MOE_OK, MOE_ERR_TIMEOUT (MOE_DEV_WAIT_TIMEOUT set) or

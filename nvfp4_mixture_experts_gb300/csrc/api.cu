@@ -657,7 +657,8 @@ moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** to
                                float** topk_w, int32_t** expert_counts,
                                int32_t** expert_offsets, int32_t** perm_src, int32_t** inv,
                                float** gs_a, uint8_t** a_codes, uint8_t** a_sf,
-                               uint8_t** inter_codes, uint8_t** inter_sf, float** y)
+                               void** a_bf16, uint8_t** inter_codes, uint8_t** inter_sf,
+                               void** inter_bf16, float** y)
 {
     if (!h || !ws_d || !t_ok(h, T)) return MOE_ERR_INVALID;
     const Plan p = plan(h->cfg, T);
@@ -670,7 +671,9 @@ moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** to
     if (gs_a) *gs_a = at<float>(ws_d, p.gs_a);
     if (a_codes) *a_codes = at<uint8_t>(ws_d, p.a_codes);
     if (a_sf) *a_sf = at<uint8_t>(ws_d, p.a_sf);
+    if (a_bf16) *a_bf16 = at<void>(ws_d, p.a_bf16);
     if (inter_codes) *inter_codes = at<uint8_t>(ws_d, p.i_codes);
+    if (inter_bf16) *inter_bf16 = at<void>(ws_d, p.i_bf16);
     if (inter_sf) *inter_sf = at<uint8_t>(ws_d, p.i_sf);
     if (y) *y = at<float>(ws_d, p.y);
     return MOE_OK;
