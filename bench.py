@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-extra", action="store_true", help="skip the prefill side measurement")
+    ap.add_argument("--local-experts", type=int, default=0,
+                    help="hold only experts 0..N-1 (a shard; smaller case for profiling)")
+    ap.add_argument("--no-oracle", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--nvtx", action="store_true",
                     help="wrap the device-timed steps in an NVTX range named 'timed' (for ncu)")
     return ap.parse_args()
@@ -110,7 +113,7 @@ def summarise_clocks(rows):
 
 # ---------------------------------------------------------------- GPU layer setup
 
-def gpu_layer(name, seed=0, extra_handles=()):
+def gpu_layer(name, seed=0, extra_handles=(), local_experts=0):
     """Seeded weights (N(0, 0.02) masters rounded to bf16) quantised to NVFP4 by the
     library's own quantiser on the GPU, then handed to moe_create.  Returns the handles
     for name and for each config in extra_handles (same weights)."""
@@ -119,7 +122,7 @@ def gpu_layer(name, seed=0, extra_handles=()):
     import nvfp4_mixture_experts_gb300 as moe
     c = synth.CONFIGS[name]
     H, I, E, k = c["H"], c["I"], c["E"], c["k"]
-    experts = list(range(c["off"], c["off"] + c["E_loc"]))
+    experts = list(range(c["off"], c["off"] + (local_experts or c["E_loc"])))
     El = len(experts)
     dev = torch.device("cuda")
     w = dict(w13=torch.empty((El, 2 * I, H // 2), dtype=torch.uint8, device=dev),
@@ -230,8 +233,10 @@ def measure_ours(args, rank, world):
     name = args.workload
     c = synth.CONFIGS[name]
     T, H, k = c["T"], c["H"], c["k"]
-    extra = () if (args.no_extra or name != "decode") else ("prefill",)
-    handles = gpu_layer(name, extra_handles=extra)
+    extra = () if (args.no_extra or name != "decode" or args.local_experts) else ("prefill",)
+    handles = gpu_layer(name, extra_handles=extra, local_experts=args.local_experts)
+    if args.local_experts:
+        c = dict(c, E_loc=args.local_experts)
     layer = handles[name]
     x, lg, bias = inputs(name, seed=rank)
     dev = torch.device("cuda")
@@ -489,6 +494,8 @@ def main():
         "tokens_per_step_per_gpu": c["T"], "global_batch": c["T"] * max(1, args.gpus),
         "parallelism": "replicas (dp%d)" % max(1, args.gpus),
         "l2": "no flush: the weights streamed per step (>2 GB) exceed the 129 MB L2"}
+    if args.local_experts:
+        config["workload"] += " (shard: experts 0-%d only)" % (args.local_experts - 1)
     if args.impl == "reference":
         if rank != 0:
             return
@@ -532,7 +539,7 @@ def main():
             "gpu_launches": r["launches"], "roofline": r["roofline"]}
     if "prefill" in r:
         line["prefill"] = r["prefill"]
-    if world == 1:
+    if world == 1 and not args.no_oracle and not args.local_experts:
         line["cpu_baseline"] = cpu_baseline(args.workload)
     print(json.dumps(line), flush=True)
 

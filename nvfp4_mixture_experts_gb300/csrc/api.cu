@@ -99,7 +99,9 @@ Plan plan(const moe_config& c, int T)
     p.gs_a = take(4);
     p.ids = take((size_t)p.Tk * 4);
     p.w = take((size_t)p.Tk * 4);
-    p.logits = take((size_t)T * p.E * 4);
+    // router partial sums: one plane per k-split (the split count never exceeds the one
+    // for a 1024-SM device)
+    p.logits = take((size_t)router_splits(std::max(T, 1), p.E, p.H, 1024) * T * p.E * 4);
     p.hist = take((size_t)p.nblk * p.El * 4);
     p.blkoff = take((size_t)p.nblk * p.El * 4);
     p.counts = take((size_t)p.G * 4);
@@ -136,13 +138,23 @@ struct moe_layer {
     moe_config cfg;
     int device = 0, num_sms = 0;
     uint16_t* router_w = nullptr;              // [E][H] bf16
-    uint8_t *w13 = nullptr, *w13_sf = nullptr;  // tiled, G slots
-    uint8_t *w2 = nullptr, *w2_sf = nullptr;
+    uint8_t* w13 = nullptr;                    // weight blobs, G slots (repack_tiles_kernel)
+    uint8_t* w2 = nullptr;
     float *gs13 = nullptr, *gs2 = nullptr;     // [G]
     float* act_gs = nullptr;                   // static activation scale (device copy)
-    CUtensorMap tm_w13, tm_w2;                 // W4A4: 128 B x 128 rows, 128-byte swizzle
-    CUtensorMap tm_w13_raw, tm_w2_raw;         // W4A16: 32 B x 128 rows, no swizzle
+    CUtensorMap tm_router;                     // Wr [E][H] bf16, 64 x 64 boxes
 };
+
+namespace {
+
+// Bytes of the weight blobs of one expert slot for an N x K matrix.
+size_t blob_bytes(int N, int K, bool raw)
+{
+    const int kst = raw ? 64 : 256;
+    return (size_t)(N / 128) * ((K + kst - 1) / kst) * (raw ? kRawTileBytes : kNvf4TileBytes);
+}
+
+}  // namespace
 
 namespace {
 
@@ -198,19 +210,25 @@ int shared_rows(const moe_layer* h, int T)
 
 moe_status launch_route(const moe_layer* h, const void* x, const float* logits_in,
                         const float* bias, int T, int32_t* ids, float* w, float* logits_out,
-                        float* logits_scratch, cudaStream_t s)
+                        float* logits_scratch, uint32_t* status, cudaStream_t s)
 {
     const moe_config& c = h->cfg;
     const float* src = logits_in;
+    int nsplit = 1;
     if (!logits_in) {
-        dim3 grid(ceil_div(c.num_experts, 4), ceil_div(T, 64));
-        router_logits_kernel<<<grid, 128, 0, s>>>(static_cast<const uint16_t*>(x), h->router_w,
-                                                  nullptr, T, c.hidden, c.num_experts,
-                                                  logits_scratch);
+        nsplit = router_splits(T, c.num_experts, c.hidden, h->num_sms);
+        CUtensorMap tmX;
+        if (!make_tmap(&tmX, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.hidden, T,
+                       (uint64_t)c.hidden * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MOE_ERR_CUDA;
+        dim3 grid(ceil_div(T, 128), ceil_div(c.num_experts, 64), nsplit);
+        router_gemm_kernel<<<grid, 192, kRouterSmem, s>>>(tmX, h->tm_router, T, c.num_experts,
+                                                          c.hidden, c.hidden / nsplit,
+                                                          logits_scratch, status);
         src = logits_scratch;
     }
-    topk_kernel<<<grid_for((int64_t)T * 32, 256), 256, 0, s>>>(src, bias, T, c.num_experts,
-                                                               c.top_k, ids, w, logits_out);
+    topk_kernel<<<grid_for((int64_t)T * 32, 256), 256, 0, s>>>(
+        src, nsplit, bias, T, c.num_experts, c.top_k, ids, w, logits_out);
     return check_launch();
 }
 
@@ -273,7 +291,7 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     GemmArgs args;
     memset(&args, 0, sizeof(args));
     args.a_sf = a_sf;
-    args.b_sf = gateup ? h->w13_sf : h->w2_sf;
+    args.b_tiles = gateup ? h->w13 : h->w2;
     args.gs_a = gs_a;
     args.gs_w = gateup ? h->gs13 : h->gs2;
     args.counts = counts;
@@ -294,6 +312,10 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     args.status = at<uint32_t>(ws, p.status);
     CUtensorMap tmA, tmA16;
     const int grid = gemm_grid(h, p.T, N);
+    const int stage_bytes = a16 ? kBf16StageBytes : kNvf4StageBytes;
+    args.stages = gemm_stages(6, stage_bytes, p.G);
+    const int smem = gemm_smem_bytes(args.stages, stage_bytes, p.G);
+    if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
     if (!a16) {
         const int pitch = codes_pitch(K);
         if (!make_tmap(&tmA, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
@@ -301,16 +323,14 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
             !make_tmap(&tmA16, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
                        16, CU_TENSOR_MAP_SWIZZLE_128B))
             return MOE_ERR_CUDA;
-        gemm_nvf4_kernel<<<grid, kGemmThreads, kNvf4Smem, s>>>(
-            tmA, tmA16, gateup ? h->tm_w13 : h->tm_w2, args);
+        gemm_nvf4_kernel<<<grid, kNvf4Threads, smem, s>>>(tmA, tmA16, args);
     } else {
         if (!make_tmap(&tmA, a_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, p.cap, (uint64_t)K * 2,
                        64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !make_tmap(&tmA16, a_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, p.cap,
                        (uint64_t)K * 2, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B))
             return MOE_ERR_CUDA;
-        gemm_w4a16_kernel<<<grid, kBf16Threads, kBf16Smem, s>>>(
-            tmA, tmA16, gateup ? h->tm_w13_raw : h->tm_w2_raw, args);
+        gemm_w4a16_kernel<<<grid, kBf16Threads, smem, s>>>(tmA, tmA16, args);
     }
     return check_launch();
 }
@@ -353,9 +373,7 @@ void moe_destroy(moe_handle h)
     if (!h) return;
     cudaFree(h->router_w);
     cudaFree(h->w13);
-    cudaFree(h->w13_sf);
     cudaFree(h->w2);
-    cudaFree(h->w2_sf);
     cudaFree(h->gs13);
     cudaFree(h->gs2);
     cudaFree(h->act_gs);
@@ -389,67 +407,52 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
         return MOE_ERR_CUDA;
     }
     const int G = El + 1;
-    const size_t n13 = (size_t)G * 2 * I * codes_pitch(H), s13 = (size_t)G * 2 * I * (H / 16);
-    const size_t n2 = (size_t)G * H * codes_pitch(I), s2 = (size_t)G * H * (I / 16);
+    const bool raw = cfg->act_mode == MOE_W4A16;
+    const size_t b13 = blob_bytes(2 * I, H, raw), b2 = blob_bytes(H, I, raw);
     bool ok = cudaMalloc(&h->router_w, (size_t)cfg->num_experts * H * 2) == cudaSuccess &&
-              cudaMalloc(&h->w13, n13) == cudaSuccess &&
-              cudaMalloc(&h->w13_sf, s13) == cudaSuccess &&
-              cudaMalloc(&h->w2, n2) == cudaSuccess && cudaMalloc(&h->w2_sf, s2) == cudaSuccess &&
+              cudaMalloc(&h->w13, G * b13) == cudaSuccess &&
+              cudaMalloc(&h->w2, G * b2) == cudaSuccess &&
               cudaMalloc(&h->gs13, G * 4) == cudaSuccess &&
               cudaMalloc(&h->gs2, G * 4) == cudaSuccess &&
               cudaMalloc(&h->act_gs, 4) == cudaSuccess &&
               cudaMemcpy(h->act_gs, &cfg->act_global_scale, 4, cudaMemcpyHostToDevice) ==
                   cudaSuccess;
-    ok = ok && cudaMemsetAsync(h->w13, 0, n13, s) == cudaSuccess &&
-         cudaMemsetAsync(h->w13_sf, 0, s13, s) == cudaSuccess &&
-         cudaMemsetAsync(h->w2, 0, n2, s) == cudaSuccess &&
-         cudaMemsetAsync(h->w2_sf, 0, s2, s) == cudaSuccess &&
+    ok = ok && cudaMemsetAsync(h->w13, 0, G * b13, s) == cudaSuccess &&
+         cudaMemsetAsync(h->w2, 0, G * b2, s) == cudaSuccess &&
          cudaMemsetAsync(h->gs13, 0, G * 4, s) == cudaSuccess &&
          cudaMemsetAsync(h->gs2, 0, G * 4, s) == cudaSuccess;
     ok = ok && cudaMemcpyAsync(h->router_w, w->router_w_d, (size_t)cfg->num_experts * H * 2,
                                cudaMemcpyDeviceToDevice, s) == cudaSuccess;
     const int blocks = 8 * h->num_sms;
     if (ok && El > 0) {
-        repack_codes_kernel<<<blocks, 256, 0, s>>>(w->w13_d, El, 2 * I, H, 1, h->w13);
-        repack_sf_kernel<<<blocks, 256, 0, s>>>(w->w13_sf_d, El, 2 * I, H, 1, h->w13_sf);
-        repack_codes_kernel<<<blocks, 256, 0, s>>>(w->w2_d, El, H, I, 0, h->w2);
-        repack_sf_kernel<<<blocks, 256, 0, s>>>(w->w2_sf_d, El, H, I, 0, h->w2_sf);
+        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->w13_d, w->w13_sf_d, El, 2 * I, H, 1, raw,
+                                                   h->w13);
+        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->w2_d, w->w2_sf_d, El, H, I, 0, raw, h->w2);
         ok = cudaMemcpyAsync(h->gs13, w->w13_gs_d, El * 4, cudaMemcpyDeviceToDevice, s) ==
                  cudaSuccess &&
              cudaMemcpyAsync(h->gs2, w->w2_gs_d, El * 4, cudaMemcpyDeviceToDevice, s) ==
                  cudaSuccess;
     }
     if (ok && cfg->has_shared) {
-        repack_codes_kernel<<<blocks, 256, 0, s>>>(w->sh13_d, 1, 2 * I, H, 1,
-                                                   h->w13 + (size_t)El * 2 * I * codes_pitch(H));
-        repack_sf_kernel<<<blocks, 256, 0, s>>>(w->sh13_sf_d, 1, 2 * I, H, 1,
-                                                h->w13_sf + (size_t)El * 2 * I * (H / 16));
-        repack_codes_kernel<<<blocks, 256, 0, s>>>(w->sh2_d, 1, H, I, 0,
-                                                   h->w2 + (size_t)El * H * codes_pitch(I));
-        repack_sf_kernel<<<blocks, 256, 0, s>>>(w->sh2_sf_d, 1, H, I, 0,
-                                                h->w2_sf + (size_t)El * H * (I / 16));
+        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->sh13_d, w->sh13_sf_d, 1, 2 * I, H, 1, raw,
+                                                   h->w13 + (size_t)El * b13);
+        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->sh2_d, w->sh2_sf_d, 1, H, I, 0, raw,
+                                                   h->w2 + (size_t)El * b2);
         ok = cudaMemcpyAsync(h->gs13 + El, w->sh13_gs_d, 4, cudaMemcpyDeviceToDevice, s) ==
                  cudaSuccess &&
              cudaMemcpyAsync(h->gs2 + El, w->sh2_gs_d, 4, cudaMemcpyDeviceToDevice, s) ==
                  cudaSuccess;
     }
     ok = ok && cudaGetLastError() == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess;
-    // weight tensor maps (the buffers live as long as the handle)
-    const int p13 = codes_pitch(H), p2 = codes_pitch(I);
+    ok = ok && make_tmap(&h->tm_router, h->router_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H,
+                         cfg->num_experts, (uint64_t)H * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok &&
-         make_tmap(&h->tm_w13, h->w13, CU_TENSOR_MAP_DATA_TYPE_UINT8, p13, (uint64_t)G * 2 * I,
-                   p13, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         make_tmap(&h->tm_w2, h->w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, p2, (uint64_t)G * H, p2, 128,
-                   128, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         make_tmap(&h->tm_w13_raw, h->w13, CU_TENSOR_MAP_DATA_TYPE_UINT8, p13,
-                   (uint64_t)G * 2 * I, p13, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         make_tmap(&h->tm_w2_raw, h->w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, p2, (uint64_t)G * H, p2,
-                   32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
-    ok = ok &&
+         cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kRouterSmem) == cudaSuccess &&
          cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kNvf4Smem) == cudaSuccess &&
+                              kSmemLimit) == cudaSuccess &&
          cudaFuncSetAttribute(gemm_w4a16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kBf16Smem) == cudaSuccess;
+                              kSmemLimit) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
         moe_destroy(h);
@@ -468,13 +471,17 @@ moe_status moe_route_topk(moe_handle h, const void* x_bf16_d, const float* logit
     if (!logits_in_d && !x_bf16_d) return MOE_ERR_INVALID;
     if (T == 0) return MOE_OK;
     float* scratch = nullptr;
+    uint32_t* status = nullptr;
     if (!logits_in_d) {
+        if (reinterpret_cast<uintptr_t>(x_bf16_d) & 15) return MOE_ERR_INVALID;
         const moe_status st = check_ws(h, T, ws_d, ws_bytes);
         if (st != MOE_OK) return st;
-        scratch = at<float>(ws_d, plan(h->cfg, T).logits);
+        const Plan p = plan(h->cfg, T);
+        scratch = at<float>(ws_d, p.logits);
+        status = at<uint32_t>(ws_d, p.status);
     }
     return launch_route(h, x_bf16_d, logits_in_d, logit_bias_d, T, topk_ids_d, topk_w_d,
-                        logits_out_d, scratch, reinterpret_cast<cudaStream_t>(stream));
+                        logits_out_d, scratch, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_permute(moe_handle h, const int32_t* topk_ids_d, int32_t T,
@@ -617,6 +624,7 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
                        size_t ws_bytes, moe_stream_t stream)
 {
     if (!h || !t_ok(h, T) || !x_bf16_d || !out_bf16_d) return MOE_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(x_bf16_d) & 15) return MOE_ERR_INVALID;
     if (T == 0) return MOE_OK;  // nothing to do: no workspace needed
     const moe_status st = check_ws(h, T, ws_d, ws_bytes);
     if (st != MOE_OK) return st;
@@ -639,7 +647,7 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
     float* y = at<float>(ws, p.y);
     if (cudaMemsetAsync(at<uint32_t>(ws, p.status), 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
     moe_status r = launch_route(h, x_bf16_d, logits_in_d, logit_bias_d, T, ids, w, nullptr,
-                                at<float>(ws, p.logits), s);
+                                at<float>(ws, p.logits), at<uint32_t>(ws, p.status), s);
     if (r == MOE_OK) r = launch_permute(h, p, ids, T, counts, offsets, perm_src, inv, ws, s);
     if (r == MOE_OK)
         r = launch_gather(h, p, x_bf16_d, T, inv, offsets, a_codes, a_sf, a_bf16, gs_a, ws, s);

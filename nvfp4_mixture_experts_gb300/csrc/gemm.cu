@@ -6,12 +6,18 @@
 // consecutive tiles sharing the same weight tile so the second row block of an expert
 // reads the weights from L2.
 //
+// Weights are re-laid out at create time as one contiguous blob per (expert, 128-row
+// tile, k-stage): the codes exactly as the MMA reads them from shared memory, followed by
+// their scale atoms, so each stage's weights arrive with one sequential bulk copy.
+//
 // Warp roles (warp-specialised pipeline):
-//   warp 0   TMA producer: activation tile, weight tile, both scale tiles per k-stage
-//   warp 1   TMEM allocation; one thread issues tcgen05.cp (scales) and tcgen05.mma
+//   warp 0   TMA producer: activation tile (tensor map), weight blob, activation scales
+//   warp 1   TMEM allocation; one thread issues tcgen05.mma
 //   warps 2-5 epilogue: TMEM -> registers -> fused output (one TMEM lane quarter each)
-//   (W4A16 only) warps 6-9: FP4 -> bf16 dequantisation of the weight tile into the
-//   swizzled operand layout
+//   warps 6-9 W4A4: the stage's scale factors smem -> TMEM with tcgen05.st (keeping the
+//            copies out of the MMA thread's in-order tcgen05 queue, where they serialised
+//            with the MMAs); W4A16: FP4 -> bf16 dequantisation of the weight tile into
+//            the swizzled operand layout
 //
 // W4A4 (NVFP4 x NVFP4): kind::mxf4nvf4 block-scaled MMA, K = 64 per instruction, UE4M3
 // scales per 16 elements copied SMEM -> TMEM per k-step.  The global scales are applied in
@@ -35,27 +41,54 @@ struct TileInfo {
     int brow0;   // first weight row (slot * N + 128 * nb)
 };
 
+// Group tables staged in shared memory at kernel start (the tile decode runs once per tile
+// on the producer's critical path; global-memory latency there would stall the stream).
+struct Tables {
+    const int32_t* mb_start;  // [G+1]
+    const int32_t* counts;    // [G]
+    const int32_t* offsets;   // [G+1]
+};
+
 // Tile t of the list: groups in order; inside a group, weight tiles in order; inside a
 // weight tile, the group's row blocks (so row blocks sharing weights run back to back).
-__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int NB, int t)
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const Tables& tb, int NB,
+                                                int t)
 {
     int lo = 0, hi = a.G;  // largest g with mb_start[g] * NB <= t
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (a.mb_start[mid] * NB <= t) lo = mid;
+        if (tb.mb_start[mid] * NB <= t) lo = mid;
         else hi = mid;
     }
     const int g = lo;
-    const int nmb = a.mb_start[g + 1] - a.mb_start[g];
-    const int local = t - a.mb_start[g] * NB;
+    const int nmb = tb.mb_start[g + 1] - tb.mb_start[g];
+    const int local = t - tb.mb_start[g] * NB;
     const int nb = local / nmb, mb = local % nmb;
     TileInfo ti;
     ti.g = g;
     ti.nb = nb;
-    ti.rows = min(128, a.counts[g] - 128 * mb);
-    ti.arow0 = a.offsets[g] + 128 * mb;
+    ti.rows = min(128, tb.counts[g] - 128 * mb);
+    ti.arow0 = tb.offsets[g] + 128 * mb;
     ti.brow0 = g * a.N + 128 * nb;
     return ti;
+}
+
+// Copies the group tables into shared memory (all threads; a __syncthreads follows).
+__device__ __forceinline__ Tables load_tables(const GemmArgs& a, int32_t* smem)
+{
+    Tables tb;
+    int32_t* m = smem;
+    int32_t* c = m + (a.G + 1);
+    int32_t* o = c + a.G;
+    for (int i = threadIdx.x; i <= a.G; i += blockDim.x) {
+        m[i] = a.mb_start[i];
+        o[i] = a.offsets[i];
+        if (i < a.G) c[i] = a.counts[i];
+    }
+    tb.mb_start = m;
+    tb.counts = c;
+    tb.offsets = o;
+    return tb;
 }
 
 // Lane 0 waits, the warp follows (keeps .sync.aligned tcgen05 ops converged).
@@ -147,7 +180,8 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& 
         *reinterpret_cast<uint32_t*>(a.out_sf + sf_atom_offset(prow, 4 * ti.nb, I)) = sfword;
 }
 
-// Shared-memory carve-up: stages, then barriers, then the TMEM address slot and flags.
+// Shared-memory carve-up: stages, then barriers (room for kMaxStages), the TMEM address
+// slot and flags, then the group tables.
 struct Ctl {
     uint64_t* full;
     uint64_t* empty;
@@ -176,6 +210,11 @@ __device__ __forceinline__ Ctl carve(uint8_t* base, int stages)
     return c;
 }
 
+__device__ __forceinline__ int32_t* tables_smem(uint8_t* ctl_base)
+{
+    return reinterpret_cast<int32_t*>(ctl_base + kCtlBytes);
+}
+
 __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw)
 {
     const uint32_t u = smem_u32(raw);
@@ -184,22 +223,24 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw)
 
 // ============================================================== W4A4: NVFP4 x NVFP4
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kNvf4Threads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmA16,
-                     const __grid_constant__ CUtensorMap tmB, GemmArgs args)
+                     const __grid_constant__ CUtensorMap tmA16, GemmArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = aligned_smem(smem_raw);
-    Ctl ctl = carve(stages + kNvf4Stages * kNvf4StageBytes, kNvf4Stages);
+    const int NS = args.stages;
+    Ctl ctl = carve(stages + NS * kNvf4StageBytes, kMaxStages);
+    const Tables tb = load_tables(args, tables_smem(stages + NS * kNvf4StageBytes));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NB = args.N / 128;
     const int KB = (args.K + 255) / 256;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kNvf4Stages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&ctl.full[s], 1);
             mbar_init(&ctl.empty[s], 1);
+            mbar_init(&ctl.ready[s], 4);  // one arrival per scale warp
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl.acc_full[b], 1);
@@ -213,7 +254,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmA16);
-        prefetch_tmap(&tmB);
     }
     if (warp == 1) {
         tmem_alloc(ctl.tmem_slot, 512);
@@ -223,7 +263,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *ctl.tmem_slot;
-    const int ntiles = args.mb_start[args.G] * NB;
+    const int ntiles = tb.mb_start[args.G] * NB;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -232,12 +272,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t phase = 0, issued = 0, issued_par = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile(args, NB, t);
+                const TileInfo ti = decode_tile(args, tb, NB, t);
                 const int nbox = (ti.rows + 15) >> 4;
                 const bool big = nbox > 4;
                 const uint32_t a_bytes = big ? 16384u : (uint32_t)nbox * 2048u;
                 const uint8_t* sfa = args.a_sf + (size_t)(ti.arow0 >> 7) * (args.K / 64) * 512;
-                const uint8_t* sfb = args.b_sf + (size_t)(ti.brow0 >> 7) * (args.K / 64) * 512;
+                // this weight tile's k-stages: contiguous blobs of codes (SMEM image) + scales
+                const uint8_t* wt = args.b_tiles +
+                                    ((size_t)ti.g * NB + ti.nb) * KB * (size_t)kNvf4TileBytes;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, ctl.abort_flag)) {
                         ok = false;
@@ -245,10 +287,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     const int nk = min(4, (args.K - kb * 256) / 64);
                     uint8_t* sA = stages + stage * kNvf4StageBytes;
-                    uint8_t* sB = sA + 16384;
-                    uint8_t* sSFA = sB + 16384;
-                    uint8_t* sSFB = sSFA + 2048;
-                    mbar_arrive_expect_tx(&ctl.full[stage], a_bytes + 16384u + 1024u * nk);
+                    uint8_t* sB = sA + 16384;    // weight codes, then their scales (contiguous)
+                    uint8_t* sSFA = sB + kNvf4TileBytes;
+                    mbar_arrive_expect_tx(&ctl.full[stage],
+                                          a_bytes + (uint32_t)kNvf4TileBytes + 512u * nk);
                     if (big) {
                         tma_load_2d(sA, &tmA, &ctl.full[stage], kb * 128, ti.arow0, pol_a);
                     } else {
@@ -256,12 +298,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             tma_load_2d(sA + i * 2048, &tmA16, &ctl.full[stage], kb * 128,
                                         ti.arow0 + 16 * i, pol_a);
                     }
-                    tma_load_2d(sB, &tmB, &ctl.full[stage], kb * 128, ti.brow0, pol_w);
+                    bulk_load(sB, wt + (size_t)kb * kNvf4TileBytes, kNvf4TileBytes,
+                              &ctl.full[stage], pol_w);
                     bulk_load(sSFA, sfa + kb * 2048, 512u * nk, &ctl.full[stage], pol_a);
-                    bulk_load(sSFB, sfb + kb * 2048, 512u * nk, &ctl.full[stage], pol_w);
                     issued |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kNvf4Stages) {
+                    if (++stage == NS) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -271,7 +313,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
                 *ctl.abort_flag = 1;
             }
-            for (int s = 0; s < kNvf4Stages; ++s)  // copies in flight land before exit
+            for (int s = 0; s < NS; ++s)  // copies in flight land before exit
                 if ((issued >> s) & 1u) mbar_wait(&ctl.full[s], (issued_par >> s) & 1u, ctl.zero);
         }
     } else if (warp == 1) {
@@ -290,7 +332,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tc_fence_after();
                 const uint32_t d_t = tmem + buf * 128;
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&ctl.full[stage], phase, ctl.abort_flag)) {
+                    // operands in smem and the stage's scales in TMEM
+                    if (!mbar_wait(&ctl.ready[stage], phase, ctl.abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -298,19 +341,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const int nk = min(4, (args.K - kb * 256) / 64);
                     uint8_t* sA = stages + stage * kNvf4StageBytes;
                     uint8_t* sB = sA + 16384;
-                    uint8_t* sSFA = sB + 16384;
-                    uint8_t* sSFB = sSFA + 2048;
                     const uint32_t sfa_t = tmem + 256 + stage * 32, sfb_t = sfa_t + 16;
-                    for (int j = 0; j < nk; ++j) {
-                        tc_cp_sf(sfa_t + 4 * j, sdesc_sf(smem_u32(sSFA) + 512 * j));
-                        tc_cp_sf(sfb_t + 4 * j, sdesc_sf(smem_u32(sSFB) + 512 * j));
-                    }
                     const uint64_t ad = sdesc_sw128(smem_u32(sA)), bd = sdesc_sw128(smem_u32(sB));
                     for (int j = 0; j < nk; ++j)
                         tc_mma_nvf4(d_t, ad + 2 * j, bd + 2 * j, idesc, sfa_t + 4 * j,
                                     sfb_t + 4 * j, (kb | j) != 0);
                     tc_commit(&ctl.empty[stage]);
-                    if (++stage == kNvf4Stages) {
+                    if (++stage == NS) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -326,11 +363,57 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_wait(ctl.drain, 0, ctl.zero);
         }
         __syncwarp();
+    } else if (warp >= 6) {
+        // scale warps (one per TMEM lane quarter): each stage's activation and weight scale
+        // atoms, smem -> registers -> TMEM columns 256 + 32*stage (the layout tc_cp_sf
+        // describes: lane l, column c of a k-step = the 4 scales of row 32c + l)
+        const int q = warp & 3;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!warp_wait(&ctl.full[stage], phase, ctl.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* sB = stages + stage * kNvf4StageBytes + 16384;
+                const uint8_t* sSFB = sB + 16384;
+                const uint8_t* sSFA = sB + kNvf4TileBytes;
+                uint32_t r[32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(sSFA + 512 * j + 16 * lane);
+                    const uint4 b = *reinterpret_cast<const uint4*>(sSFB + 512 * j + 16 * lane);
+                    r[4 * j] = a.x;
+                    r[4 * j + 1] = a.y;
+                    r[4 * j + 2] = a.z;
+                    r[4 * j + 3] = a.w;
+                    r[16 + 4 * j] = b.x;
+                    r[16 + 4 * j + 1] = b.y;
+                    r[16 + 4 * j + 2] = b.z;
+                    r[16 + 4 * j + 3] = b.w;
+                }
+                tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + 256 + stage * 32, r);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl.ready[stage]);
+                if (++stage == NS) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+            *ctl.abort_flag = 1;
+        }
     } else {
         const int q = warp & 3;
         int it = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-            const TileInfo ti = decode_tile(args, NB, t);
+            const TileInfo ti = decode_tile(args, tb, NB, t);
             const int buf = it & 1;
             const uint32_t acc_par = (it >> 1) & 1;
             if (!warp_wait(&ctl.acc_full[buf], acc_par, ctl.abort_flag)) {
@@ -369,12 +452,13 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code)
 
 __global__ void __launch_bounds__(kBf16Threads, 1)
     gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmA16,
-                      const __grid_constant__ CUtensorMap tmB, GemmArgs args)
+                      const __grid_constant__ CUtensorMap tmA16, GemmArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = aligned_smem(smem_raw);
-    Ctl ctl = carve(stages + kBf16Stages * kBf16StageBytes, kBf16Stages);
+    const int NS = args.stages;
+    Ctl ctl = carve(stages + NS * kBf16StageBytes, kMaxStages);
+    const Tables tb = load_tables(args, tables_smem(stages + NS * kBf16StageBytes));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NB = args.N / 128;
     const int KB = args.K / 64;
@@ -382,7 +466,7 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
     constexpr int kOffB = 16384, kOffW = 32768, kOffSF = 36864;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kBf16Stages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&ctl.full[s], 1);
             mbar_init(&ctl.empty[s], 1);
             mbar_init(&ctl.ready[s], 128);
@@ -399,7 +483,6 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmA16);
-        prefetch_tmap(&tmB);
     }
     if (warp == 1) {
         tmem_alloc(ctl.tmem_slot, 256);
@@ -409,7 +492,7 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *ctl.tmem_slot;
-    const int ntiles = args.mb_start[args.G] * NB;
+    const int ntiles = tb.mb_start[args.G] * NB;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -418,18 +501,19 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
             uint32_t phase = 0, issued = 0, issued_par = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile(args, NB, t);
+                const TileInfo ti = decode_tile(args, tb, NB, t);
                 const int nbox = (ti.rows + 15) >> 4;
                 const bool big = nbox > 4;
                 const uint32_t a_bytes = big ? 16384u : (uint32_t)nbox * 2048u;
-                const uint8_t* sfb = args.b_sf + (size_t)(ti.brow0 >> 7) * (args.K / 64) * 512;
+                const uint8_t* wt = args.b_tiles +
+                                    ((size_t)ti.g * NB + ti.nb) * KB * (size_t)kRawTileBytes;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, ctl.abort_flag)) {
                         ok = false;
                         break;
                     }
                     uint8_t* st = stages + stage * kBf16StageBytes;
-                    mbar_arrive_expect_tx(&ctl.full[stage], a_bytes + 4096u + 512u);
+                    mbar_arrive_expect_tx(&ctl.full[stage], a_bytes + (uint32_t)kRawTileBytes);
                     if (big) {
                         tma_load_2d(st, &tmA, &ctl.full[stage], kb * 64, ti.arow0, pol_a);
                     } else {
@@ -437,11 +521,11 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
                             tma_load_2d(st + i * 2048, &tmA16, &ctl.full[stage], kb * 64,
                                         ti.arow0 + 16 * i, pol_a);
                     }
-                    tma_load_2d(st + kOffW, &tmB, &ctl.full[stage], kb * 32, ti.brow0, pol_w);
-                    bulk_load(st + kOffSF, sfb + kb * 512, 512u, &ctl.full[stage], pol_w);
+                    bulk_load(st + kOffW, wt + (size_t)kb * kRawTileBytes, kRawTileBytes,
+                              &ctl.full[stage], pol_w);
                     issued |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kBf16Stages) {
+                    if (++stage == NS) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -451,7 +535,7 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
                 set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
                 *ctl.abort_flag = 1;
             }
-            for (int s = 0; s < kBf16Stages; ++s)
+            for (int s = 0; s < NS; ++s)
                 if ((issued >> s) & 1u) mbar_wait(&ctl.full[s], (issued_par >> s) & 1u, ctl.zero);
         }
     } else if (warp == 1) {
@@ -481,7 +565,7 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
                     for (int j = 0; j < 4; ++j)
                         tc_mma_bf16(d_t, ad + 2 * j, bd + 2 * j, idesc, (kb | j) != 0);
                     tc_commit(&ctl.empty[stage]);
-                    if (++stage == kBf16Stages) {
+                    if (++stage == NS) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -501,7 +585,7 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
         const int q = warp & 3;
         int it = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-            const TileInfo ti = decode_tile(args, NB, t);
+            const TileInfo ti = decode_tile(args, tb, NB, t);
             const int buf = it & 1;
             const uint32_t acc_par = (it >> 1) & 1;
             if (!warp_wait(&ctl.acc_full[buf], acc_par, ctl.abort_flag)) {
@@ -551,7 +635,7 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive(&ctl.ready[stage]);
-                if (++stage == kBf16Stages) {
+                if (++stage == NS) {
                     stage = 0;
                     phase ^= 1u;
                 }

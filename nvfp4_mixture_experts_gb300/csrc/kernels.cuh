@@ -14,10 +14,13 @@ __device__ __forceinline__ float silu_mul(float g, float u)
 }
 
 // ---- route.cu
-__global__ void router_logits_kernel(const uint16_t* x, const uint16_t* wr, const float* bias,
-                                     int T, int H, int E, float* logits);
-__global__ void topk_kernel(const float* logits_src, const float* bias, int T, int E, int k,
-                            int32_t* ids, float* wts, float* logits_out);
+constexpr int kRouterSmem = 4 * (16384 + 8192) + 1024 + 256;
+__global__ void router_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
+                                   const __grid_constant__ CUtensorMap tmW, int T, int E, int H,
+                                   int k_per_split, float* part, uint32_t* status);
+int router_splits(int T, int E, int H, int num_sms);
+__global__ void topk_kernel(const float* logits_src, int nsplit, const float* bias, int T,
+                            int E, int k, int32_t* ids, float* wts, float* logits_out);
 __global__ void perm_hist_kernel(const int32_t* ids, int P, int E, int off, int El,
                                  int32_t* hist, uint32_t* status);
 __global__ void perm_scan_kernel(const int32_t* hist, int nblk, int El, int T, int k,
@@ -44,10 +47,8 @@ __global__ void swiglu_requant_kernel(const float* gu, int rows, int I, float gs
                                       uint8_t* codes, uint8_t* sf, int layout);
 __global__ void combine_kernel(const float* y, const int32_t* inv, int T, int H, int k,
                                int add_shared, uint16_t* out);
-__global__ void repack_codes_kernel(const uint8_t* src, int nexp, int N, int K,
-                                    int interleave, uint8_t* dst);
-__global__ void repack_sf_kernel(const uint8_t* src, int nexp, int N, int K, int interleave,
-                                 uint8_t* dst);
+__global__ void repack_tiles_kernel(const uint8_t* codes, const uint8_t* sf, int nexp, int N,
+                                    int K, int interleave, int raw, uint8_t* dst);
 
 // ---- gemm.cu
 enum GemmEpilogue : int {
@@ -58,7 +59,7 @@ enum GemmEpilogue : int {
 
 struct GemmArgs {
     const uint8_t* a_sf;      // W4A4: activation scale atoms (tiled, K-wide)
-    const uint8_t* b_sf;      // weight scale atoms [slots][N/128][K/64][512]
+    const uint8_t* b_tiles;   // weight blobs [slots][N/128][k-stages][tile bytes]
     const float* gs_a;        // W4A4: activation global scale (device scalar)
     const float* gs_w;        // [slots] weight global scales
     const int32_t* counts;    // [G] rows per group
@@ -76,23 +77,41 @@ struct GemmArgs {
     const int32_t* perm_src;  // kEpiDown
     const float* topk_w;      // kEpiDown
     int Tk;                   // kEpiDown: first pair index of the shared rows (T*k)
+    int stages;               // pipeline depth (<= kMaxStages; fits the shared memory)
     uint32_t* status;
 };
 
-constexpr int kGemmThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kNvf4Stages = 6;
+// warp 0 TMA, warp 1 MMA, warps 2..5 epilogue, warps 6..9 scale factors (W4A4) or
+// weight dequantisation (W4A16)
+constexpr int kNvf4Threads = 320;
+// Weight blob of one (expert, 128-row tile, k-stage):
+//   W4A4 : 128 rows x 128 bytes of codes (256 elements, 128-byte swizzled SMEM image)
+//          + 4 scale atoms of 512 bytes                                   = 18432 bytes
+//   W4A16: 128 rows x 32 bytes of codes (64 elements, row-major) + 1 atom =  4608 bytes
+constexpr int kNvf4TileBytes = 16384 + 2048;
+constexpr int kRawTileBytes = 4096 + 512;
+constexpr int kMaxStages = 8;
+constexpr int kCtlBytes = 256;          // barriers for kMaxStages + TMEM slot + flags
+constexpr int kSmemLimit = 232448;      // dynamic shared memory per block (227 KB)
 constexpr int kNvf4StageBytes = 16384 + 16384 + 2048 + 2048;
-constexpr int kNvf4Smem = kNvf4Stages * kNvf4StageBytes + 1024 + 256;
-constexpr int kBf16Stages = 6;
 constexpr int kBf16StageBytes = 37888;   // A 16K + B 16K + raw FP4 4K + scales 512, padded to 1 KB
-constexpr int kBf16Smem = kBf16Stages * kBf16StageBytes + 1024 + 256;
+// Shared memory of a GEMM launch: stages, 1 KB alignment slack, control block, and the
+// group tables (mb_start, counts, offsets).
+inline int gemm_smem_bytes(int stages, int stage_bytes, int G)
+{
+    return stages * stage_bytes + 1024 + kCtlBytes + 4 * (3 * G + 2);
+}
+inline int gemm_stages(int want, int stage_bytes, int G)
+{
+    int s = want;
+    while (s > 2 && gemm_smem_bytes(s, stage_bytes, G) > kSmemLimit) --s;
+    return s;
+}
 constexpr int kBf16Threads = 320;       // + 4 dequantisation warps
 
 __global__ void gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
-                                 const __grid_constant__ CUtensorMap tmA16,
-                                 const __grid_constant__ CUtensorMap tmB, GemmArgs args);
+                                 const __grid_constant__ CUtensorMap tmA16, GemmArgs args);
 __global__ void gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmA,
-                                  const __grid_constant__ CUtensorMap tmA16,
-                                  const __grid_constant__ CUtensorMap tmB, GemmArgs args);
+                                  const __grid_constant__ CUtensorMap tmA16, GemmArgs args);
 
 }  // namespace moe

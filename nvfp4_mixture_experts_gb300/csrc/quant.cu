@@ -229,11 +229,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 
 // ---------------------------------------------------------------- weight re-layout
 //
-// Canonical [N][K/2] codes and [N][K/16] scales of one expert -> tiled slot: codes
-// [N][pitch] and 512-byte scale atoms per (128-row tile, 64-element k-step).  With
-// interleave (gate/up of w13, N = 2I): destination row 128*nb + 32*c + 16*u + i holds
-// source row u*I + 64*nb + 16*c + i, so each 128-row tile has 4 pairs of 16 gate rows and
-// the 16 matching up rows -- the fused epilogue sees gate and up of the same features.
+// Canonical codes [nexp][N][K/2] and scales [nexp][N][K/16] -> one contiguous blob per
+// (expert, 128-row tile nb, k-stage kb), the bytes a GEMM stage copies into shared memory:
+//   raw == 0 (W4A4, k-stage of 256): 128 rows x 128 code bytes in the 128-byte swizzled
+//     layout (byte c of row r at r*128 + ((c/16) ^ (r%8))*16 + c%16), then the 4 scale atoms
+//     of k-steps 4kb..4kb+3;
+//   raw == 1 (W4A16, k-stage of 64): 128 rows x 32 code bytes row-major, then 1 atom.
+// Scale atom byte (m%32)*16 + (m/32)*4 + kk holds scale kk of the k-step for tile row m.
+// Bytes past K (a partial last stage) are zero.  With interleave (the gate/up matrix,
+// N = 2I), tile row 128*nb + 32*c + 16*u + i holds source row u*I + 64*nb + 16*c + i, so
+// each 128-row tile has 4 pairs of 16 gate rows and the 16 matching up rows -- the fused
+// epilogue sees gate and up of the same features.
 __device__ __forceinline__ int64_t src_row(int64_t r, int N, int interleave)
 {
     if (!interleave) return r;
@@ -243,33 +249,47 @@ __device__ __forceinline__ int64_t src_row(int64_t r, int N, int interleave)
     return (int64_t)u * I + 64 * nb + 16 * c + i;
 }
 
-__global__ void __launch_bounds__(256) repack_codes_kernel(const uint8_t* __restrict__ src,
+__global__ void __launch_bounds__(256) repack_tiles_kernel(const uint8_t* __restrict__ codes,
+                                                           const uint8_t* __restrict__ sf,
                                                            int nexp, int N, int K,
-                                                           int interleave,
+                                                           int interleave, int raw,
                                                            uint8_t* __restrict__ dst)
 {
-    const int pitch = codes_pitch(K);
-    const int64_t n = (int64_t)nexp * N * pitch;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+    const int kst = raw ? 64 : 256;  // elements per k-stage
+    const int cb = kst / 2;          // code bytes per row per stage
+    const int nat = kst / 64;        // scale atoms per blob
+    const int tile = 128 * cb + 512 * nat;
+    const int NB = N / 128, KB = (K + kst - 1) / kst;
+    const int64_t total = (int64_t)nexp * NB * KB * tile;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / pitch;  // destination row over all experts
-        const int c = (int)(i % pitch);
-        const int64_t e = r / N, rl = r % N;
-        dst[i] = c < K / 2 ? src[(e * N + src_row(rl, N, interleave)) * (K / 2) + c] : (uint8_t)0;
-    }
-}
-
-__global__ void __launch_bounds__(256) repack_sf_kernel(const uint8_t* __restrict__ src,
-                                                        int nexp, int N, int K, int interleave,
-                                                        uint8_t* __restrict__ dst)
-{
-    const int64_t n = (int64_t)nexp * N * (K / 16);
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / (K / 16);
-        const int b = (int)(i % (K / 16));
-        const int64_t e = r / N, rl = r % N;
-        dst[sf_atom_offset(r, b, K)] = src[(e * N + src_row(rl, N, interleave)) * (K / 16) + b];
+        const int64_t blob = i / tile;
+        const int o = (int)(i % tile);
+        const int kb = (int)(blob % KB);
+        const int64_t en = blob / KB;
+        const int nb = (int)(en % NB);
+        const int64_t e = en / NB;
+        uint8_t v = 0;
+        if (o < 128 * cb) {
+            int r, c;
+            if (raw) {
+                r = o / cb;
+                c = o % cb;
+            } else {
+                r = o >> 7;
+                c = ((((o >> 4) & 7) ^ (r & 7)) << 4) | (o & 15);
+            }
+            const int kbyte = kb * cb + c;
+            if (kbyte < K / 2)
+                v = codes[(e * N + src_row(nb * 128 + r, N, interleave)) * (K / 2) + kbyte];
+        } else {
+            const int a = (o - 128 * cb) / 512, w = (o - 128 * cb) % 512;
+            const int m = (w >> 4) + 32 * ((w & 15) >> 2), kk = w & 3;
+            const int step = kb * nat + a;
+            if (step < K / 64)
+                v = sf[(e * N + src_row(nb * 128 + m, N, interleave)) * (K / 16) + step * 4 + kk];
+        }
+        dst[i] = v;
     }
 }
 

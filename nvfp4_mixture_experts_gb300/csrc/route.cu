@@ -12,87 +12,147 @@ namespace moe {
 
 // ---------------------------------------------------------------- router logits
 //
-// logits[t][e] = sum_h x[t][h] * Wr[e][h] + bias[e], fp32 accumulation.
-// Block: 4 warps, one expert per warp, a chunk of 64 tokens.  The x chunk is staged in
-// shared memory 256 columns at a time; each lane accumulates all 64 tokens over its
-// 8-column slice, then the partial sums are reduced across the warp.
-constexpr int kRtTok = 64;
-constexpr int kRtCols = 256;
-constexpr int kRtExperts = 4;
+// logits = x . Wr^T on the tensor cores (kind::f16, bf16 operands, fp32 accumulation in
+// TMEM).  Tile: 128 tokens x 64 experts; grid (token tiles, expert tiles, k-splits).  Each
+// k-split writes its partial sums to part[split][T][E]; the top-k kernel adds the splits
+// in a fixed order (deterministic), then the bias.  Rows past T and experts past E are
+// zero-filled by the TMA and never stored.
+//   warp 0: TMA producer (x tile 128 x 64, Wr tile 64 x 64 per stage)
+//   warp 1: TMEM allocation, MMA issue (4 x K16 per stage)
+//   warps 2..5: epilogue, one TMEM lane quarter (32 tokens) each
+constexpr int kRgStages = 4;
+constexpr int kRgStageBytes = 16384 + 8192;
 
-__global__ void __launch_bounds__(128) router_logits_kernel(
-    const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
-    const float* __restrict__ bias, int T, int H, int E, float* __restrict__ logits)
+__global__ void __launch_bounds__(192, 1) router_gemm_kernel(
+    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, int T,
+    int E, int H, int k_per_split, float* __restrict__ part, uint32_t* status)
 {
-    __shared__ __align__(16) uint16_t xs[kRtTok][kRtCols];
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t u = smem_u32(smem_raw);
+    uint8_t* st = smem_raw + (((u + 1023u) & ~1023u) - u);
+    uint64_t* full = reinterpret_cast<uint64_t*>(st + kRgStages * kRgStageBytes);
+    uint64_t* empty = full + kRgStages;
+    uint64_t* acc = empty + kRgStages;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(acc + 1);
+    int* flags = reinterpret_cast<int*>(tslot + 1);  // [0] abort, [1] zero
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * kRtExperts + warp;
-    const int t0 = blockIdx.y * kRtTok;
-    const int nt = min(kRtTok, T - t0);
-    float acc[kRtTok];
+    const int m0 = blockIdx.x * 128, n0 = blockIdx.y * 64;
+    const int k0 = blockIdx.z * k_per_split;
+    const int KB = min(k_per_split, H - k0) / 64;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRgStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(acc, 1);
+        flags[0] = flags[1] = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 64);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    volatile int* abort = flags;
+    if (warp == 0 && lane == 0) {
+        const uint64_t pol = policy_evict_last();
+        uint32_t issued = 0, par = 0, phase = 0;
+        int stg = 0;
+        for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&empty[stg], phase ^ 1u, abort)) {
+                set_status(status, MOE_DEV_WAIT_TIMEOUT);
+                flags[0] = 1;
+                break;
+            }
+            uint8_t* sa = st + stg * kRgStageBytes;
+            mbar_arrive_expect_tx(&full[stg], kRgStageBytes);
+            tma_load_2d(sa, &tmX, &full[stg], k0 + kb * 64, m0, pol);
+            tma_load_2d(sa + 16384, &tmW, &full[stg], k0 + kb * 64, n0, pol);
+            issued |= 1u << stg;
+            par = (par & ~(1u << stg)) | (phase << stg);
+            if (++stg == kRgStages) {
+                stg = 0;
+                phase ^= 1u;
+            }
+        }
+        for (int i = 0; i < kRgStages; ++i)
+            if ((issued >> i) & 1u) mbar_wait(&full[i], (par >> i) & 1u, flags + 1);
+    } else if (warp == 1 && lane == 0) {
+        constexpr uint32_t idesc = idesc_bf16(128, 64);
+        uint32_t phase = 0;
+        int stg = 0;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&full[stg], phase, abort)) {
+                set_status(status, MOE_DEV_WAIT_TIMEOUT);
+                flags[0] = 1;
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint8_t* sa = st + stg * kRgStageBytes;
+            const uint64_t ad = sdesc_sw128(smem_u32(sa)), bd = sdesc_sw128(smem_u32(sa + 16384));
+            for (int j = 0; j < 4; ++j) tc_mma_bf16(tmem, ad + 2 * j, bd + 2 * j, idesc, (kb | j) != 0);
+            tc_commit(&empty[stg]);
+            if (++stg == kRgStages) {
+                stg = 0;
+                phase ^= 1u;
+            }
+        }
+        tc_commit(acc);  // also drains everything issued above
+        if (!ok) mbar_wait(acc, 0, flags + 1);
+    } else if (warp >= 2) {
+        const int q = warp & 3;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(acc, 0, abort) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok && !flags[0]) {
+            tc_fence_after();
+            const int t = m0 + q * 32 + lane;
+            float* dst = part + ((size_t)blockIdx.z * T + t) * E + n0;
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + 32 * c, r);
+                tmem_ld_wait();
+                if (t < T)
 #pragma unroll
-    for (int i = 0; i < kRtTok; ++i) acc[i] = 0.0f;
+                    for (int i = 0; i < 32; ++i)
+                        if (n0 + 32 * c + i < E) dst[32 * c + i] = __uint_as_float(r[i]);
+            }
+        } else if (lane == 0) {
+            set_status(status, MOE_DEV_WAIT_TIMEOUT);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 64);
+    }
+}
 
-    for (int h0 = 0; h0 < H; h0 += kRtCols) {
-        __syncthreads();
-        // stage x[t0 .. t0+nt)[h0 .. h0+512) (16-byte vectors)
-        for (int v = threadIdx.x; v < kRtTok * (kRtCols / 8); v += blockDim.x) {
-            const int r = v / (kRtCols / 8), c = (v % (kRtCols / 8)) * 8;
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (r < nt && h0 + c < H)
-                val = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + r) * H + h0 + c);
-            *reinterpret_cast<uint4*>(&xs[r][c]) = val;
-        }
-        __syncthreads();
-        if (e < E) {
-            // this lane's 8 weights
-            float w[8];
-            const int c = lane * 8;
-            if (h0 + c < H) {
-                const uint4 a = *reinterpret_cast<const uint4*>(wr + (size_t)e * H + h0 + c);
-                const uint32_t u[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    w[2 * i] = bf16_bits_to_f32(u[i] & 0xFFFFu);
-                    w[2 * i + 1] = bf16_bits_to_f32(u[i] >> 16);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = 0.0f;
-            }
-#pragma unroll
-            for (int t = 0; t < kRtTok; ++t) {
-                const uint4 a = *reinterpret_cast<const uint4*>(&xs[t][c]);
-                const uint32_t u[4] = {a.x, a.y, a.z, a.w};
-                float s = acc[t];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    s = fmaf(bf16_bits_to_f32(u[i] & 0xFFFFu), w[2 * i], s);
-                    s = fmaf(bf16_bits_to_f32(u[i] >> 16), w[2 * i + 1], s);
-                }
-                acc[t] = s;
-            }
-        }
-    }
-    if (e >= E) return;
-    const float b = bias ? bias[e] : 0.0f;
-#pragma unroll
-    for (int t = 0; t < kRtTok; ++t) {
-        float s = acc[t];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == (t & 31) && t < nt) logits[(size_t)(t0 + t) * E + e] = s + b;
-    }
+int router_splits(int T, int E, int H, int num_sms)
+{
+    const int tiles = ((T + 127) / 128) * ((E + 63) / 64);
+    int s = 1;
+    while (s * 2 * 256 <= H && tiles * s * 2 <= num_sms) s *= 2;
+    return s;
 }
 
 // ---------------------------------------------------------------- softmax top-k
 //
-// One warp per token.  k rounds of a warp arg-max over the remaining logits (larger value
-// first, equal values: lower id first), then w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0)
-// over the selected logits.
+// One warp per token.  The logits are the sum of nsplit partial-sum planes (added in
+// plane order) plus the bias.  k rounds of a warp arg-max over the remaining logits (larger
+// value first, equal values: lower id first), then w_j = exp(l_j - l_0) / sum_i
+// exp(l_i - l_0) over the selected logits.
 __global__ void __launch_bounds__(256) topk_kernel(
-    const float* __restrict__ logits_src, const float* __restrict__ bias, int T, int E, int k,
-    int32_t* __restrict__ ids, float* __restrict__ wts, float* __restrict__ logits_out)
+    const float* __restrict__ logits_src, int nsplit, const float* __restrict__ bias, int T,
+    int E, int k, int32_t* __restrict__ ids, float* __restrict__ wts,
+    float* __restrict__ logits_out)
 {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -106,7 +166,9 @@ __global__ void __launch_bounds__(256) topk_kernel(
         const int e = i * 32 + lane;
         float l = -INFINITY;
         if (e < E) {
-            l = logits_src[(size_t)t * E + e] + (bias ? bias[e] : 0.0f);
+            l = logits_src[(size_t)t * E + e];
+            for (int sp = 1; sp < nsplit; ++sp) l += logits_src[((size_t)sp * T + t) * E + e];
+            l += bias ? bias[e] : 0.0f;
             if (logits_out) logits_out[(size_t)t * E + e] = l;
         }
         v[i] = l;
