@@ -131,6 +131,27 @@ moe_status check_launch()
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Launches a kernel, with programmatic dependent launch when pdl is set (the forward's
+// chain: each kernel may start while its predecessor finishes; see pdl_wait()).
+template <typename... KArgs, typename... Args>
+moe_status launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                  bool pdl, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- the handle
@@ -210,7 +231,8 @@ int shared_rows(const moe_layer* h, int T)
 
 moe_status launch_route(const moe_layer* h, const void* x, const float* logits_in,
                         const float* bias, int T, int32_t* ids, float* w, float* logits_out,
-                        float* logits_scratch, uint32_t* status, cudaStream_t s)
+                        float* logits_scratch, uint32_t* status, uint32_t* clear0,
+                        uint32_t* clear1, bool pdl, cudaStream_t s)
 {
     const moe_config& c = h->cfg;
     const float* src = logits_in;
@@ -222,67 +244,73 @@ moe_status launch_route(const moe_layer* h, const void* x, const float* logits_i
                        (uint64_t)c.hidden * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
             return MOE_ERR_CUDA;
         dim3 grid(ceil_div(T, 128), ceil_div(c.num_experts, 64), nsplit);
-        router_gemm_kernel<<<grid, 192, kRouterSmem, s>>>(tmX, h->tm_router, T, c.num_experts,
-                                                          c.hidden, c.hidden / nsplit,
-                                                          logits_scratch, status);
+        const moe_status r = launch(router_gemm_kernel, grid, dim3(192), kRouterSmem, s, pdl,
+                                    tmX, h->tm_router, T, c.num_experts, c.hidden,
+                                    c.hidden / nsplit, logits_scratch, status, clear0, clear1);
+        if (r != MOE_OK) return r;
         src = logits_scratch;
+        clear0 = clear1 = nullptr;  // done by the router
     }
-    topk_kernel<<<grid_for((int64_t)T * 32, 256), 256, 0, s>>>(
-        src, nsplit, bias, T, c.num_experts, c.top_k, ids, w, logits_out);
-    return check_launch();
+    return launch(topk_kernel, dim3(grid_for((int64_t)T * 32, 256)), dim3(256), 0, s, pdl, src,
+                  nsplit, bias, T, c.num_experts, c.top_k, ids, w, logits_out, clear0, clear1);
 }
 
 moe_status launch_permute(const moe_layer* h, const Plan& p, const int32_t* ids, int T,
                           int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* inv,
-                          void* ws, cudaStream_t s)
+                          void* ws, bool pdl, cudaStream_t s)
 {
     const moe_config& c = h->cfg;
     uint32_t* status = at<uint32_t>(ws, p.status);
     int32_t* hist = at<int32_t>(ws, p.hist);
     int32_t* blkoff = at<int32_t>(ws, p.blkoff);
     int32_t* mb_start = at<int32_t>(ws, p.mb_start);
-    perm_hist_kernel<<<p.nblk, 256, 0, s>>>(ids, p.Tk, c.num_experts, c.local_expert_offset,
-                                            p.El, hist, status);
-    perm_scan_kernel<<<1, 1024, 0, s>>>(hist, p.nblk, p.El, T, c.top_k, shared_rows(h, T),
-                                        p.cap, blkoff, counts, offsets, mb_start, perm_src,
-                                        status);
-    perm_scatter_kernel<<<p.nblk, 32, 0, s>>>(ids, p.Tk, c.num_experts, c.local_expert_offset,
-                                              p.El, blkoff, offsets, p.cap, perm_src, inv);
-    return check_launch();
+    moe_status r = launch(perm_hist_kernel, dim3(p.nblk), dim3(256), 0, s, pdl, ids, p.Tk,
+                          c.num_experts, c.local_expert_offset, p.El, hist, status);
+    if (r == MOE_OK)
+        r = launch(perm_scan_kernel, dim3(1), dim3(1024), 0, s, pdl, (const int32_t*)hist,
+                   p.nblk, p.El, T, c.top_k, shared_rows(h, T), p.cap, blkoff, counts, offsets,
+                   mb_start, perm_src, status);
+    if (r == MOE_OK)
+        r = launch(perm_scatter_kernel, dim3(p.nblk), dim3(32), 0, s, pdl, ids, p.Tk,
+                   c.num_experts, c.local_expert_offset, p.El, (const int32_t*)blkoff,
+                   (const int32_t*)offsets, p.cap, perm_src, inv);
+    return r;
 }
 
 moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T,
                          const int32_t* inv, const int32_t* offsets, uint8_t* a_codes,
-                         uint8_t* a_sf, void* a_bf16, float* gs_out, void* ws, cudaStream_t s)
+                         uint8_t* a_sf, void* a_bf16, float* gs_out, void* ws, bool pdl,
+                         bool amax_zeroed, cudaStream_t s)
 {
     const moe_config& c = h->cfg;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     const int add = shared_rows(h, T) > 0 ? 1 : 0;
-    if (c.act_mode == MOE_W4A16) {
-        gather_bf16_kernel<<<grid_for((int64_t)T * 32, 256), 256, 0, s>>>(
-            xb, T, c.hidden, c.top_k, inv, offsets, p.El, add, static_cast<uint16_t*>(a_bf16));
-        return check_launch();
-    }
+    const dim3 grid(grid_for((int64_t)T * 32, 256));
+    if (c.act_mode == MOE_W4A16)
+        return launch(gather_bf16_kernel, grid, dim3(256), 0, s, pdl, xb, T, c.hidden, c.top_k,
+                      inv, offsets, p.El, add, static_cast<uint16_t*>(a_bf16));
     uint32_t* amax = at<uint32_t>(ws, p.amax);
     const float* gs_static = nullptr;
     if (c.act_mode == MOE_W4A4_DYNAMIC) {
-        if (cudaMemsetAsync(amax, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (!amax_zeroed && cudaMemsetAsync(amax, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
         const int64_t n = (int64_t)T * c.hidden;
         const int blocks = (int)std::min<int64_t>(2 * h->num_sms, std::max<int64_t>(1, n / 2048));
-        amax_bf16_kernel<<<blocks, 256, 0, s>>>(xb, n, amax);
+        const moe_status r = launch(amax_bf16_kernel, dim3(blocks), dim3(256), 0, s, pdl, xb, n,
+                                    amax);
+        if (r != MOE_OK) return r;
     } else {
         gs_static = h->act_gs;  // the handle's device copy of act_global_scale
     }
-    gather_quant_kernel<<<grid_for((int64_t)T * 32, 256), 256, 0, s>>>(
-        xb, T, c.hidden, c.top_k, inv, offsets, p.El, add, gs_static, amax, a_codes, a_sf, gs_out);
-    return check_launch();
+    return launch(gather_quant_kernel, grid, dim3(256), 0, s, pdl, xb, T, c.hidden, c.top_k, inv,
+                  offsets, p.El, add, gs_static, (const uint32_t*)amax, a_codes, a_sf, gs_out);
 }
 
 moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilogue,
                        const uint8_t* a_codes, const uint8_t* a_sf, const float* gs_a,
                        const void* a_bf16, const int32_t* counts, const int32_t* offsets,
                        float* out_f32, uint8_t* out_codes, uint8_t* out_sf, void* out_bf16,
-                       const int32_t* perm_src, const float* topk_w, void* ws, cudaStream_t s)
+                       const int32_t* perm_src, const float* topk_w, void* ws, bool pdl,
+                       cudaStream_t s)
 {
     const moe_config& c = h->cfg;
     const bool a16 = c.act_mode == MOE_W4A16;
@@ -323,16 +351,30 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
             !make_tmap(&tmA16, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
                        16, CU_TENSOR_MAP_SWIZZLE_128B))
             return MOE_ERR_CUDA;
-        gemm_nvf4_kernel<<<grid, kNvf4Threads, smem, s>>>(tmA, tmA16, args);
+        return launch(gemm_nvf4_kernel, dim3(grid), dim3(kNvf4Threads), smem, s, pdl, tmA, tmA16,
+                      args);
     } else {
         if (!make_tmap(&tmA, a_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, p.cap, (uint64_t)K * 2,
                        64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !make_tmap(&tmA16, a_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, p.cap,
                        (uint64_t)K * 2, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B))
             return MOE_ERR_CUDA;
-        gemm_w4a16_kernel<<<grid, kBf16Threads, smem, s>>>(tmA, tmA16, args);
+        return launch(gemm_w4a16_kernel, dim3(grid), dim3(kBf16Threads), smem, s, pdl, tmA,
+                      tmA16, args);
     }
-    return check_launch();
+}
+
+}  // namespace
+
+namespace {
+
+moe_status launch_combine(const moe_layer* h, const float* y, const int32_t* inv, int T,
+                          void* out, bool pdl, cudaStream_t s)
+{
+    const moe_config& c = h->cfg;
+    return launch(combine_kernel, dim3(grid_for((int64_t)T * (c.hidden / 8), 256)), dim3(256), 0,
+                  s, pdl, y, inv, T, c.hidden, c.top_k, shared_rows(h, T) > 0 ? 1 : 0,
+                  static_cast<uint16_t*>(out));
 }
 
 }  // namespace
@@ -481,7 +523,8 @@ moe_status moe_route_topk(moe_handle h, const void* x_bf16_d, const float* logit
         status = at<uint32_t>(ws_d, p.status);
     }
     return launch_route(h, x_bf16_d, logits_in_d, logit_bias_d, T, topk_ids_d, topk_w_d,
-                        logits_out_d, scratch, status, reinterpret_cast<cudaStream_t>(stream));
+                        logits_out_d, scratch, status, nullptr, nullptr, false,
+                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_permute(moe_handle h, const int32_t* topk_ids_d, int32_t T,
@@ -497,7 +540,7 @@ moe_status moe_permute(moe_handle h, const int32_t* topk_ids_d, int32_t T,
     if (st != MOE_OK) return st;
     const Plan p = plan(h->cfg, T);
     return launch_permute(h, p, topk_ids_d, T, expert_counts_d, expert_offsets_d, perm_src_d,
-                          inv_d, ws_d, reinterpret_cast<cudaStream_t>(stream));
+                          inv_d, ws_d, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_quant_nvfp4(const void* x_bf16_d, int32_t rows, int32_t cols,
@@ -541,7 +584,8 @@ moe_status moe_gather_activations(moe_handle h, const void* x_bf16_d, int32_t T,
     if (st != MOE_OK) return st;
     const Plan p = plan(h->cfg, T);
     return launch_gather(h, p, x_bf16_d, T, inv_d, expert_offsets_d, a_codes_d, a_sf_d,
-                         a_bf16_d, gs_out_d, ws_d, reinterpret_cast<cudaStream_t>(stream));
+                         a_bf16_d, gs_out_d, ws_d, false, false,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_grouped_gemm_gateup(moe_handle h, const uint8_t* a_codes_d,
@@ -567,7 +611,7 @@ moe_status moe_grouped_gemm_gateup(moe_handle h, const uint8_t* a_codes_d,
     return launch_gemm(h, p, true, fuse_epilogue ? kEpiGateUpSwiglu : kEpiGateUpF32, a_codes_d,
                        a_sf_d, gs_a_d, a_bf16_d, expert_counts_d, expert_offsets_d,
                        gateup_f32_d, inter_codes_d, inter_sf_d, inter_bf16_d, nullptr, nullptr,
-                       ws_d, reinterpret_cast<cudaStream_t>(stream));
+                       ws_d, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_swiglu_requant(const float* gateup_f32_d, int32_t rows, int32_t inter,
@@ -603,7 +647,7 @@ moe_status moe_grouped_gemm_down(moe_handle h, const uint8_t* inter_codes_d,
     const Plan p = plan(h->cfg, T);
     return launch_gemm(h, p, false, kEpiDown, inter_codes_d, inter_sf_d, nullptr, inter_bf16_d,
                        expert_counts_d, expert_offsets_d, y_d, nullptr, nullptr, nullptr,
-                       perm_src_d, topk_w_d, ws_d, reinterpret_cast<cudaStream_t>(stream));
+                       perm_src_d, topk_w_d, ws_d, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* inv_d, int32_t T,
@@ -611,12 +655,8 @@ moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* inv_d, int
 {
     if (!h || !t_ok(h, T) || !y_d || !inv_d || !out_bf16_d) return MOE_ERR_INVALID;
     if (T == 0) return MOE_OK;
-    const moe_config& c = h->cfg;
-    combine_kernel<<<grid_for((int64_t)T * (c.hidden / 8), 256), 256, 0,
-                     reinterpret_cast<cudaStream_t>(stream)>>>(
-        y_d, inv_d, T, c.hidden, c.top_k, shared_rows(h, T) > 0 ? 1 : 0,
-        static_cast<uint16_t*>(out_bf16_d));
-    return check_launch();
+    return launch_combine(h, y_d, inv_d, T, out_bf16_d, false,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_in_d,
@@ -645,19 +685,23 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
     uint8_t* i_sf = at<uint8_t>(ws, p.i_sf);
     void* i_bf16 = at<void>(ws, p.i_bf16);
     float* y = at<float>(ws, p.y);
-    if (cudaMemsetAsync(at<uint32_t>(ws, p.status), 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    // one chain of kernels with programmatic dependent launch; the first kernel clears the
+    // status word and the amax accumulator of this forward
+    uint32_t* status = at<uint32_t>(ws, p.status);
+    uint32_t* amax = at<uint32_t>(ws, p.amax);
     moe_status r = launch_route(h, x_bf16_d, logits_in_d, logit_bias_d, T, ids, w, nullptr,
-                                at<float>(ws, p.logits), at<uint32_t>(ws, p.status), s);
-    if (r == MOE_OK) r = launch_permute(h, p, ids, T, counts, offsets, perm_src, inv, ws, s);
+                                at<float>(ws, p.logits), status, status, amax, true, s);
+    if (r == MOE_OK) r = launch_permute(h, p, ids, T, counts, offsets, perm_src, inv, ws, true, s);
     if (r == MOE_OK)
-        r = launch_gather(h, p, x_bf16_d, T, inv, offsets, a_codes, a_sf, a_bf16, gs_a, ws, s);
+        r = launch_gather(h, p, x_bf16_d, T, inv, offsets, a_codes, a_sf, a_bf16, gs_a, ws, true,
+                          true, s);
     if (r == MOE_OK)
         r = launch_gemm(h, p, true, kEpiGateUpSwiglu, a_codes, a_sf, gs_a, a_bf16, counts,
-                        offsets, nullptr, i_codes, i_sf, i_bf16, nullptr, nullptr, ws, s);
+                        offsets, nullptr, i_codes, i_sf, i_bf16, nullptr, nullptr, ws, true, s);
     if (r == MOE_OK)
         r = launch_gemm(h, p, false, kEpiDown, i_codes, i_sf, nullptr, i_bf16, counts, offsets,
-                        y, nullptr, nullptr, nullptr, perm_src, w, ws, s);
-    if (r == MOE_OK) r = moe_combine(h, y, inv, T, out_bf16_d, stream);
+                        y, nullptr, nullptr, nullptr, perm_src, w, ws, true, s);
+    if (r == MOE_OK) r = launch_combine(h, y, inv, T, out_bf16_d, true, s);
     return r;
 }
 

@@ -36,6 +36,18 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits)
     if (status) atomicOr(status, bits);
 }
 
+// Programmatic dependent launch.  The forward's kernels are launched so that each may start
+// while its predecessor finishes.  pdl_wait() blocks the calling thread until the preceding
+// kernel has completed and its writes are visible (a no-op without the launch attribute);
+// pdl_trigger() lets the next kernel be scheduled.  Every kernel calls pdl_wait() before
+// pdl_trigger(), so when a kernel starts, all kernels before its predecessor are complete:
+// it may read their outputs (and constant data) before its own pdl_wait().
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)

@@ -100,25 +100,44 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return ok != 0;
 }
 
+// Per-row epilogue constants of one tile (global loads, issued before the accumulator
+// wait so their latency overlaps the tile's mainloop).
+struct EpiPrep {
+    int64_t prow;   // padded row of this thread
+    int64_t yrow;   // kEpiDown: output row (pair index)
+    float alpha;    // 1 / (global scales) (x routing weight for kEpiDown)
+    bool valid;
+};
+
+template <bool kW4A16>
+__device__ __forceinline__ EpiPrep epi_prep(const GemmArgs& a, const TileInfo& ti, int q,
+                                            int lane)
+{
+    EpiPrep e;
+    const int m = q * 32 + lane;
+    e.valid = m < ti.rows;
+    e.prow = (int64_t)ti.arow0 + m;
+    const float gw = a.gs_w[ti.g];
+    if (a.epilogue == kEpiDown) e.alpha = kW4A16 ? __frcp_rn(gw) : __frcp_rn(__fmul_rn(a.gs_i, gw));
+    else e.alpha = kW4A16 ? __frcp_rn(gw) : __frcp_rn(__fmul_rn(*a.gs_a, gw));
+    e.yrow = 0;
+    if (a.epilogue == kEpiDown && e.valid) {
+        e.yrow = a.perm_src[e.prow];
+        const float wgt = e.yrow < a.Tk ? a.topk_w[e.yrow] : 1.0f;
+        e.alpha = __fmul_rn(e.alpha, wgt);
+    }
+    return e;
+}
+
 // Epilogue of one tile for the 32 rows of TMEM lane quarter q (thread = row).
 template <bool kW4A16>
 __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& ti,
-                                             uint32_t tacc, int q, int lane)
+                                             const EpiPrep& ep, uint32_t tacc, int q, int lane)
 {
-    const int m = q * 32 + lane;
-    const bool valid = m < ti.rows;
-    const int64_t prow = (int64_t)ti.arow0 + m;
-    const float gw = a.gs_w[ti.g];
-    float alpha;
-    if (a.epilogue == kEpiDown) alpha = kW4A16 ? __frcp_rn(gw) : __frcp_rn(__fmul_rn(a.gs_i, gw));
-    else alpha = kW4A16 ? __frcp_rn(gw) : __frcp_rn(__fmul_rn(*a.gs_a, gw));
-    int64_t yrow = 0;
-    float wgt = 1.0f;
-    if (a.epilogue == kEpiDown && valid) {
-        yrow = a.perm_src[prow];
-        if (yrow < a.Tk) wgt = a.topk_w[yrow];
-        alpha = __fmul_rn(alpha, wgt);
-    }
+    const bool valid = ep.valid;
+    const int64_t prow = ep.prow;
+    const int64_t yrow = ep.yrow;
+    const float alpha = ep.alpha;
     const int I = a.N / 2;
     uint32_t sfword = 0;
 #pragma unroll 1
@@ -268,9 +287,29 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+            // the first NS stages' weights (constant) go out before the predecessor is done
+            int i = 0;
+            for (int t = blockIdx.x; t < ntiles && i < NS; t += gridDim.x) {
+                const TileInfo ti = decode_tile(args, tb, NB, t);
+                const int nbox = (ti.rows + 15) >> 4;
+                const uint32_t a_bytes = nbox > 4 ? 16384u : (uint32_t)nbox * 2048u;
+                const uint8_t* wt = args.b_tiles +
+                                    ((size_t)ti.g * NB + ti.nb) * KB * (size_t)kNvf4TileBytes;
+                for (int kb = 0; kb < KB && i < NS; ++kb, ++i) {
+                    const int nk = min(4, (args.K - kb * 256) / 64);
+                    mbar_arrive_expect_tx(&ctl.full[i],
+                                          a_bytes + (uint32_t)kNvf4TileBytes + 512u * nk);
+                    bulk_load(stages + i * kNvf4StageBytes + 16384,
+                              wt + (size_t)kb * kNvf4TileBytes, kNvf4TileBytes, &ctl.full[i],
+                              pol_w);
+                }
+            }
+            pdl_wait();
+            pdl_trigger();
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_par = 0;
             bool ok = true;
+            i = 0;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 const TileInfo ti = decode_tile(args, tb, NB, t);
                 const int nbox = (ti.rows + 15) >> 4;
@@ -280,26 +319,28 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
                 // this weight tile's k-stages: contiguous blobs of codes (SMEM image) + scales
                 const uint8_t* wt = args.b_tiles +
                                     ((size_t)ti.g * NB + ti.nb) * KB * (size_t)kNvf4TileBytes;
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, ctl.abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                for (int kb = 0; kb < KB; ++kb, ++i) {
                     const int nk = min(4, (args.K - kb * 256) / 64);
                     uint8_t* sA = stages + stage * kNvf4StageBytes;
                     uint8_t* sB = sA + 16384;    // weight codes, then their scales (contiguous)
                     uint8_t* sSFA = sB + kNvf4TileBytes;
-                    mbar_arrive_expect_tx(&ctl.full[stage],
-                                          a_bytes + (uint32_t)kNvf4TileBytes + 512u * nk);
+                    if (i >= NS) {  // (the first NS stages were armed above)
+                        if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, ctl.abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&ctl.full[stage],
+                                              a_bytes + (uint32_t)kNvf4TileBytes + 512u * nk);
+                        bulk_load(sB, wt + (size_t)kb * kNvf4TileBytes, kNvf4TileBytes,
+                                  &ctl.full[stage], pol_w);
+                    }
                     if (big) {
                         tma_load_2d(sA, &tmA, &ctl.full[stage], kb * 128, ti.arow0, pol_a);
                     } else {
-                        for (int i = 0; i < nbox; ++i)
-                            tma_load_2d(sA + i * 2048, &tmA16, &ctl.full[stage], kb * 128,
-                                        ti.arow0 + 16 * i, pol_a);
+                        for (int b = 0; b < nbox; ++b)
+                            tma_load_2d(sA + b * 2048, &tmA16, &ctl.full[stage], kb * 128,
+                                        ti.arow0 + 16 * b, pol_a);
                     }
-                    bulk_load(sB, wt + (size_t)kb * kNvf4TileBytes, kNvf4TileBytes,
-                              &ctl.full[stage], pol_w);
                     bulk_load(sSFA, sfa + kb * 2048, 512u * nk, &ctl.full[stage], pol_a);
                     issued |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -412,8 +453,10 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
     } else {
         const int q = warp & 3;
         int it = 0;
+        pdl_wait();
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
             const TileInfo ti = decode_tile(args, tb, NB, t);
+            const EpiPrep ep = epi_prep<false>(args, ti, q, lane);
             const int buf = it & 1;
             const uint32_t acc_par = (it >> 1) & 1;
             if (!warp_wait(&ctl.acc_full[buf], acc_par, ctl.abort_flag)) {
@@ -424,7 +467,7 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
                 break;
             }
             tc_fence_after();
-            run_epilogue<false>(args, ti, tmem + buf * 128, q, lane);
+            run_epilogue<false>(args, ti, ep, tmem + buf * 128, q, lane);
             tc_fence_before();
             mbar_arrive(&ctl.acc_empty[buf]);
         }
@@ -497,9 +540,26 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+            // the first NS stages' weights (constant) go out before the predecessor is done
+            int i = 0;
+            for (int t = blockIdx.x; t < ntiles && i < NS; t += gridDim.x) {
+                const TileInfo ti = decode_tile(args, tb, NB, t);
+                const int nbox = (ti.rows + 15) >> 4;
+                const uint32_t a_bytes = nbox > 4 ? 16384u : (uint32_t)nbox * 2048u;
+                const uint8_t* wt = args.b_tiles +
+                                    ((size_t)ti.g * NB + ti.nb) * KB * (size_t)kRawTileBytes;
+                for (int kb = 0; kb < KB && i < NS; ++kb, ++i) {
+                    mbar_arrive_expect_tx(&ctl.full[i], a_bytes + (uint32_t)kRawTileBytes);
+                    bulk_load(stages + i * kBf16StageBytes + kOffW,
+                              wt + (size_t)kb * kRawTileBytes, kRawTileBytes, &ctl.full[i], pol_w);
+                }
+            }
+            pdl_wait();
+            pdl_trigger();
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_par = 0;
             bool ok = true;
+            i = 0;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 const TileInfo ti = decode_tile(args, tb, NB, t);
                 const int nbox = (ti.rows + 15) >> 4;
@@ -507,22 +567,24 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
                 const uint32_t a_bytes = big ? 16384u : (uint32_t)nbox * 2048u;
                 const uint8_t* wt = args.b_tiles +
                                     ((size_t)ti.g * NB + ti.nb) * KB * (size_t)kRawTileBytes;
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, ctl.abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                for (int kb = 0; kb < KB; ++kb, ++i) {
                     uint8_t* st = stages + stage * kBf16StageBytes;
-                    mbar_arrive_expect_tx(&ctl.full[stage], a_bytes + (uint32_t)kRawTileBytes);
+                    if (i >= NS) {  // (the first NS stages were armed above)
+                        if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, ctl.abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&ctl.full[stage], a_bytes + (uint32_t)kRawTileBytes);
+                        bulk_load(st + kOffW, wt + (size_t)kb * kRawTileBytes, kRawTileBytes,
+                                  &ctl.full[stage], pol_w);
+                    }
                     if (big) {
                         tma_load_2d(st, &tmA, &ctl.full[stage], kb * 64, ti.arow0, pol_a);
                     } else {
-                        for (int i = 0; i < nbox; ++i)
-                            tma_load_2d(st + i * 2048, &tmA16, &ctl.full[stage], kb * 64,
-                                        ti.arow0 + 16 * i, pol_a);
+                        for (int b = 0; b < nbox; ++b)
+                            tma_load_2d(st + b * 2048, &tmA16, &ctl.full[stage], kb * 64,
+                                        ti.arow0 + 16 * b, pol_a);
                     }
-                    bulk_load(st + kOffW, wt + (size_t)kb * kRawTileBytes, kRawTileBytes,
-                              &ctl.full[stage], pol_w);
                     issued |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == NS) {
@@ -584,8 +646,10 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
     } else if (warp < 6) {
         const int q = warp & 3;
         int it = 0;
+        pdl_wait();
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
             const TileInfo ti = decode_tile(args, tb, NB, t);
+            const EpiPrep ep = epi_prep<true>(args, ti, q, lane);
             const int buf = it & 1;
             const uint32_t acc_par = (it >> 1) & 1;
             if (!warp_wait(&ctl.acc_full[buf], acc_par, ctl.abort_flag)) {
@@ -596,7 +660,7 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
                 break;
             }
             tc_fence_after();
-            run_epilogue<true>(args, ti, tmem + buf * 128, q, lane);
+            run_epilogue<true>(args, ti, ep, tmem + buf * 128, q, lane);
             tc_fence_before();
             mbar_arrive(&ctl.acc_empty[buf]);
         }

@@ -17,10 +17,12 @@ __device__ __forceinline__ float silu_mul(float g, float u)
 constexpr int kRouterSmem = 4 * (16384 + 8192) + 1024 + 256;
 __global__ void router_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                                    const __grid_constant__ CUtensorMap tmW, int T, int E, int H,
-                                   int k_per_split, float* part, uint32_t* status);
+                                   int k_per_split, float* part, uint32_t* status,
+                                   uint32_t* clear0, uint32_t* clear1);
 int router_splits(int T, int E, int H, int num_sms);
 __global__ void topk_kernel(const float* logits_src, int nsplit, const float* bias, int T,
-                            int E, int k, int32_t* ids, float* wts, float* logits_out);
+                            int E, int k, int32_t* ids, float* wts, float* logits_out,
+                            uint32_t* clear0, uint32_t* clear1);
 __global__ void perm_hist_kernel(const int32_t* ids, int P, int E, int off, int El,
                                  int32_t* hist, uint32_t* status);
 __global__ void perm_scan_kernel(const int32_t* hist, int nblk, int El, int T, int k,

@@ -16,6 +16,8 @@ namespace moe {
 __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t* __restrict__ x,
                                                         int64_t n, uint32_t* amax_bits)
 {
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
     float m = 0.0f;
     const int64_t n8 = n / 8;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
@@ -77,6 +79,8 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(
     const float* gs_static, const uint32_t* amax_bits, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ sf, float* gs_out)
 {
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= T) return;
@@ -123,6 +127,8 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(
     const int32_t* __restrict__ offsets, int shared_group, int add_shared,
     uint16_t* __restrict__ out)
 {
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= T) return;
@@ -200,6 +206,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       int H, int k, int add_shared,
                                                       uint16_t* __restrict__ out)
 {
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
     const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     const int per = H / 8;
     if (i >= (int64_t)T * per) return;

@@ -25,7 +25,8 @@ constexpr int kRgStageBytes = 16384 + 8192;
 
 __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
     const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, int T,
-    int E, int H, int k_per_split, float* __restrict__ part, uint32_t* status)
+    int E, int H, int k_per_split, float* __restrict__ part, uint32_t* status, uint32_t* clear0,
+    uint32_t* clear1)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t u = smem_u32(smem_raw);
@@ -57,6 +58,14 @@ __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
     tc_fence_after();
     const uint32_t tmem = *tslot;
     volatile int* abort = flags;
+    pdl_wait();
+    if (threadIdx.x == 0) {
+        pdl_trigger();
+        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {  // per-forward words
+            if (clear0) *clear0 = 0u;
+            if (clear1) *clear1 = 0u;
+        }
+    }
     if (warp == 0 && lane == 0) {
         const uint64_t pol = policy_evict_last();
         uint32_t issued = 0, par = 0, phase = 0;
@@ -152,8 +161,16 @@ int router_splits(int T, int E, int H, int num_sms)
 __global__ void __launch_bounds__(256) topk_kernel(
     const float* __restrict__ logits_src, int nsplit, const float* __restrict__ bias, int T,
     int E, int k, int32_t* __restrict__ ids, float* __restrict__ wts,
-    float* __restrict__ logits_out)
+    float* __restrict__ logits_out, uint32_t* clear0, uint32_t* clear1)
 {
+    pdl_wait();
+    if (threadIdx.x == 0) {
+        pdl_trigger();
+        if (blockIdx.x == 0) {  // per-forward words (when no router GEMM ran before)
+            if (clear0) *clear0 = 0u;
+            if (clear1) *clear1 = 0u;
+        }
+    }
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= T) return;
@@ -225,6 +242,8 @@ __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restric
                                                         int32_t* __restrict__ hist,
                                                         uint32_t* status)
 {
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
     __shared__ int32_t cnt[kMaxExperts];
     for (int e = threadIdx.x; e < El; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
@@ -251,6 +270,8 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(
     int32_t* __restrict__ offsets, int32_t* __restrict__ mb_start,
     int32_t* __restrict__ perm_src, uint32_t* status)
 {
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
     __shared__ int32_t s_cnt[kMaxExperts + 1];
     __shared__ int32_t s_pad[kMaxExperts + 2];
     __shared__ int32_t s_mb[kMaxExperts + 2];
@@ -306,6 +327,8 @@ __global__ void __launch_bounds__(32) perm_scatter_kernel(
     const int32_t* __restrict__ blkoff, const int32_t* __restrict__ offsets, int rows_cap,
     int32_t* __restrict__ perm_src, int32_t* __restrict__ inv)
 {
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
     __shared__ int32_t cursor[kMaxExperts];
     const int lane = threadIdx.x;
     for (int e = lane; e < El; e += 32)
