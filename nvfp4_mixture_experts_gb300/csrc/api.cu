@@ -251,7 +251,7 @@ moe_status launch_route(const moe_layer* h, const void* x, const float* logits_i
         src = logits_scratch;
         clear0 = clear1 = nullptr;  // done by the router
     }
-    return launch(topk_kernel, dim3(grid_for((int64_t)T * 32, 256)), dim3(256), 0, s, pdl, src,
+    return launch(topk_kernel, dim3(ceil_div(T, 8)), dim3(256), 0, s, pdl, src,
                   nsplit, bias, T, c.num_experts, c.top_k, ids, w, logits_out, clear0, clear1);
 }
 
@@ -271,7 +271,7 @@ moe_status launch_permute(const moe_layer* h, const Plan& p, const int32_t* ids,
                    p.nblk, p.El, T, c.top_k, shared_rows(h, T), p.cap, blkoff, counts, offsets,
                    mb_start, perm_src, status);
     if (r == MOE_OK)
-        r = launch(perm_scatter_kernel, dim3(p.nblk), dim3(32), 0, s, pdl, ids, p.Tk,
+        r = launch(perm_scatter_kernel, dim3(p.nblk), dim3(256), 0, s, pdl, ids, p.Tk,
                    c.num_experts, c.local_expert_offset, p.El, (const int32_t*)blkoff,
                    (const int32_t*)offsets, p.cap, perm_src, inv);
     return r;
@@ -285,10 +285,12 @@ moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T
     const moe_config& c = h->cfg;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     const int add = shared_rows(h, T) > 0 ? 1 : 0;
-    const dim3 grid(grid_for((int64_t)T * 32, 256));
     if (c.act_mode == MOE_W4A16)
-        return launch(gather_bf16_kernel, grid, dim3(256), 0, s, pdl, xb, T, c.hidden, c.top_k,
-                      inv, offsets, p.El, add, static_cast<uint16_t*>(a_bf16));
+        return launch(gather_bf16_kernel,
+                      dim3(grid_for((int64_t)T * ((c.hidden + 255) / 256) * 32, 256)), dim3(256),
+                      0, s, pdl, xb, T, c.hidden, c.top_k, inv, offsets, p.El, add,
+                      static_cast<uint16_t*>(a_bf16));
+    const dim3 grid(grid_for((int64_t)T * ((c.hidden / 16 + 31) / 32) * 32, 256));
     uint32_t* amax = at<uint32_t>(ws, p.amax);
     const float* gs_static = nullptr;
     if (c.act_mode == MOE_W4A4_DYNAMIC) {

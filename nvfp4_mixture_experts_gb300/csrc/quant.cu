@@ -69,10 +69,24 @@ __device__ __forceinline__ void load16_bf16(const uint16_t* p, float* v)
 
 // ---------------------------------------------------------------- gather-quantise
 //
-// One warp per token.  Lane l handles the 16-element blocks l, l+32, ... so code stores
-// from a warp are contiguous, and the 4 blocks of one 64-element k-step sit on 4
-// neighbouring lanes (their scale bytes are merged into one 32-bit atom word).
-// Destinations: the padded rows of the token's local pairs (inv) and its shared row.
+// Each warp handles 32 consecutive 16-element blocks (512 elements) of one token, so a
+// token is spread over H/512 warps.  Lane l handles block 32*chunk + l: code stores from a
+// warp are contiguous, and the 4 blocks of one 64-element k-step sit on 4 neighbouring
+// lanes (their scale bytes are merged into one 32-bit atom word).  Destinations: the padded
+// rows of the token's local pairs (inv) and its shared row.
+__device__ __forceinline__ int token_destinations(const int32_t* inv, const int32_t* offsets,
+                                                  int t, int k, int shared_group,
+                                                  int add_shared, int* dst)
+{
+    int nd = 0;
+    for (int j = 0; j < k; ++j) {
+        const int r = inv[(size_t)t * k + j];
+        if (r >= 0) dst[nd++] = r;
+    }
+    if (add_shared) dst[nd++] = offsets[shared_group] + t;
+    return nd;
+}
+
 __global__ void __launch_bounds__(256) gather_quant_kernel(
     const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, int shared_group, int add_shared,
@@ -81,47 +95,41 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(
 {
     pdl_wait();
     if (threadIdx.x == 0) pdl_trigger();
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (warp >= T) return;
-    const int t = warp;
+    const int nb = H / 16;
+    const int wpt = (nb + 31) / 32;  // warps per token
+    if (gw >= T * wpt) return;
+    const int t = gw / wpt, chunk = gw % wpt;
     const float gs = global_scale(gs_static, amax_bits);
-    if (t == 0 && lane == 0 && gs_out) *gs_out = gs;
+    if (gw == 0 && lane == 0 && gs_out) *gs_out = gs;
     int dst[kMaxTopK + 1];
-    int nd = 0;
-    for (int j = 0; j < k; ++j) {
-        const int r = inv[(size_t)t * k + j];
-        if (r >= 0) dst[nd++] = r;
-    }
-    if (add_shared) dst[nd++] = offsets[shared_group] + t;
+    const int nd = token_destinations(inv, offsets, t, k, shared_group, add_shared, dst);
     if (nd == 0) return;
     const int pitch = codes_pitch(H);
-    const int nb = H / 16;
-    for (int b0 = 0; b0 < nb; b0 += 32) {  // warp-uniform loop: every lane shuffles
-        const int b = b0 + lane;
-        const bool act = b < nb;               // nb % 4 == 0: k-step lanes agree
-        float v[16];
-        uint32_t c[2] = {0u, 0u}, s = 0u;
-        if (act) {
-            load16_bf16(x + (size_t)t * H + b * 16, v);
-            s = quant16(v, gs, c);
-        }
-        // merge the 4 scale bytes of this k-step into the lane with b % 4 == 0
-        const uint32_t s1 = __shfl_down_sync(0xffffffffu, s, 1);
-        const uint32_t s2 = __shfl_down_sync(0xffffffffu, s, 2);
-        const uint32_t s3 = __shfl_down_sync(0xffffffffu, s, 3);
-        const uint32_t word = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
-        if (!act) continue;
-        for (int d = 0; d < nd; ++d) {
-            const int64_t row = dst[d];
-            *reinterpret_cast<uint2*>(codes + row * pitch + b * 8) = make_uint2(c[0], c[1]);
-            if ((b & 3) == 0)
-                *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(row, b, H)) = word;
-        }
+    const int b = chunk * 32 + lane;
+    const bool act = b < nb;  // nb % 4 == 0: the lanes of one k-step agree
+    float v[16];
+    uint32_t c[2] = {0u, 0u}, sc = 0u;
+    if (act) {
+        load16_bf16(x + (size_t)t * H + b * 16, v);
+        sc = quant16(v, gs, c);
+    }
+    // merge the 4 scale bytes of this k-step into the lane with b % 4 == 0
+    const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
+    const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 2);
+    const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
+    const uint32_t word = sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    if (!act) return;
+    for (int d = 0; d < nd; ++d) {
+        const int64_t row = dst[d];
+        *reinterpret_cast<uint2*>(codes + row * pitch + b * 8) = make_uint2(c[0], c[1]);
+        if ((b & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(row, b, H)) = word;
     }
 }
 
-// W4A16: copy token rows (bf16) to the padded rows of their pairs and shared row.
+// W4A16: copy token rows (bf16) to the padded rows of their pairs and shared row; a warp
+// copies 256 elements of one token.
 __global__ void __launch_bounds__(256) gather_bf16_kernel(
     const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, int shared_group, int add_shared,
@@ -129,22 +137,16 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(
 {
     pdl_wait();
     if (threadIdx.x == 0) pdl_trigger();
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (warp >= T) return;
-    const int t = warp;
+    const int wpt = (H + 255) / 256;
+    if (gw >= T * wpt) return;
+    const int t = gw / wpt, c = (gw % wpt) * 256 + lane * 8;
     int dst[kMaxTopK + 1];
-    int nd = 0;
-    for (int j = 0; j < k; ++j) {
-        const int r = inv[(size_t)t * k + j];
-        if (r >= 0) dst[nd++] = r;
-    }
-    if (add_shared) dst[nd++] = offsets[shared_group] + t;
-    for (int c = lane * 8; c < H; c += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c);
-        for (int d = 0; d < nd; ++d)
-            *reinterpret_cast<uint4*>(out + (size_t)dst[d] * H + c) = v;
-    }
+    const int nd = token_destinations(inv, offsets, t, k, shared_group, add_shared, dst);
+    if (c >= H) return;
+    const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c);
+    for (int d = 0; d < nd; ++d) *reinterpret_cast<uint4*>(out + (size_t)dst[d] * H + c) = v;
 }
 
 // ---------------------------------------------------------------- standalone quantiser

@@ -146,23 +146,28 @@ __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
 
 int router_splits(int T, int E, int H, int num_sms)
 {
+    // at most 4 partial planes: more CTAs would make the top-k's plane sum the bottleneck
     const int tiles = ((T + 127) / 128) * ((E + 63) / 64);
     int s = 1;
-    while (s * 2 * 256 <= H && tiles * s * 2 <= num_sms) s *= 2;
+    while (s < 4 && s * 2 * 256 <= H && tiles * s * 2 <= num_sms) s *= 2;
     return s;
 }
 
 // ---------------------------------------------------------------- softmax top-k
 //
-// One warp per token.  The logits are the sum of nsplit partial-sum planes (added in
-// plane order) plus the bias.  k rounds of a warp arg-max over the remaining logits (larger
-// value first, equal values: lower id first), then w_j = exp(l_j - l_0) / sum_i
+// Block of 8 warps = 8 tokens.  The block first sums the nsplit partial-sum planes (in plane
+// order) and adds the bias into shared memory, with many loads in flight; then each warp
+// takes k rounds of an arg-max over its token's logits (larger value first, equal values:
+// lower id first).  Lane j keeps the j-th selection; w_j = exp(l_j - l_0) / sum_i
 // exp(l_i - l_0) over the selected logits.
+constexpr int kTopkTokens = 8;
+
 __global__ void __launch_bounds__(256) topk_kernel(
     const float* __restrict__ logits_src, int nsplit, const float* __restrict__ bias, int T,
     int E, int k, int32_t* __restrict__ ids, float* __restrict__ wts,
     float* __restrict__ logits_out, uint32_t* clear0, uint32_t* clear1)
 {
+    __shared__ float sl[kTopkTokens][kMaxExperts];
     pdl_wait();
     if (threadIdx.x == 0) {
         pdl_trigger();
@@ -171,36 +176,45 @@ __global__ void __launch_bounds__(256) topk_kernel(
             if (clear1) *clear1 = 0u;
         }
     }
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (warp >= T) return;
-    const int t = warp;
-    constexpr int kPer = kMaxExperts / 32;
-    float v[kPer];
-    uint32_t used = 0;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-        const int e = i * 32 + lane;
-        float l = -INFINITY;
-        if (e < E) {
-            l = logits_src[(size_t)t * E + e];
-            for (int sp = 1; sp < nsplit; ++sp) l += logits_src[((size_t)sp * T + t) * E + e];
-            l += bias ? bias[e] : 0.0f;
-            if (logits_out) logits_out[(size_t)t * E + e] = l;
+    const int t0 = blockIdx.x * kTopkTokens;
+    const int nt = min(kTopkTokens, T - t0);
+    const size_t plane = (size_t)T * E;
+    for (int idx = threadIdx.x; idx < nt * E; idx += blockDim.x) {
+        const size_t off = (size_t)t0 * E + idx;
+        float l = logits_src[off];
+        int sp = 1;
+        for (; sp + 3 < nsplit; sp += 4) {  // 4 loads in flight per element
+            const float a = logits_src[off + sp * plane], b = logits_src[off + (sp + 1) * plane];
+            const float c = logits_src[off + (sp + 2) * plane];
+            const float d = logits_src[off + (sp + 3) * plane];
+            l += a;
+            l += b;
+            l += c;
+            l += d;
         }
-        v[i] = l;
+        for (; sp < nsplit; ++sp) l += logits_src[off + sp * plane];
+        const int e = idx % E;
+        l += bias ? bias[e] : 0.0f;
+        sl[idx / E][e] = l;
+        if (logits_out) logits_out[off] = l;
     }
-    float sel_l[kMaxTopK];
-    int sel_e[kMaxTopK];
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= nt) return;
+    const int t = t0 + warp;
+    const float* v = sl[warp];
+    uint32_t used = 0;
+    float my_l = 0.0f;
+    int my_e = 0;
     for (int j = 0; j < k; ++j) {
         float best = -INFINITY;
         int be = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
+        for (int i = 0; i * 32 < E; ++i) {
             const int e = i * 32 + lane;
             if (e < E && !((used >> i) & 1u)) {
-                if (v[i] > best || (v[i] == best && e < be)) {
-                    best = v[i];
+                const float x = v[e];
+                if (x > best || (x == best && e < be)) {
+                    best = x;
                     be = e;
                 }
             }
@@ -215,16 +229,19 @@ __global__ void __launch_bounds__(256) topk_kernel(
             }
         }
         if ((be & 31) == lane) used |= 1u << (be >> 5);
-        sel_l[j] = best;
-        sel_e[j] = be;
-    }
-    if (lane == 0) {
-        float z = 0.0f;
-        for (int j = 0; j < k; ++j) z += expf(sel_l[j] - sel_l[0]);
-        for (int j = 0; j < k; ++j) {
-            ids[(size_t)t * k + j] = sel_e[j];
-            wts[(size_t)t * k + j] = expf(sel_l[j] - sel_l[0]) / z;
+        if (lane == j) {
+            my_l = best;
+            my_e = be;
         }
+    }
+    const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
+    const float ex = lane < k ? expf(my_l - l0) : 0.0f;
+    float z = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = my_e;
+        wts[(size_t)t * k + lane] = ex / z;
     }
 }
 
@@ -275,34 +292,79 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(
     __shared__ int32_t s_cnt[kMaxExperts + 1];
     __shared__ int32_t s_pad[kMaxExperts + 2];
     __shared__ int32_t s_mb[kMaxExperts + 2];
+    __shared__ int32_t s_wp[32], s_wm[32];
     const int G = El + 1;  // groups: routed experts, then the shared expert
-    for (int g = threadIdx.x; g < G; g += blockDim.x) {
-        int run = 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // per-group totals and per-block exclusive prefix: a warp per group, lanes over blocks
+    for (int g = warp; g < G; g += 32) {
+        int total = 0;
         if (g < El) {
-            for (int b = 0; b < nblk; ++b) {
-                blkoff[(size_t)b * El + g] = run;
-                run += hist[(size_t)b * El + g];
+            for (int b0 = 0; b0 < nblk; b0 += 32) {
+                const int b = b0 + lane;
+                const int v = b < nblk ? hist[(size_t)b * El + g] : 0;
+                int x = v;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                if (b < nblk) blkoff[(size_t)b * El + g] = total + x - v;
+                total += __shfl_sync(0xffffffffu, x, 31);
             }
         } else {
-            run = shared_rows;
+            total = shared_rows;
         }
-        s_cnt[g] = run;
-        counts[g] = run;
+        if (lane == 0) {
+            s_cnt[g] = total;
+            counts[g] = total;
+        }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {  // exclusive scans of padded sizes and 128-row blocks
-        int a = 0, m = 0;
-        for (int g = 0; g < G; ++g) {
-            s_pad[g] = a;
-            s_mb[g] = m;
-            a += round_up(s_cnt[g], kRowAlign);
-            m += (s_cnt[g] + kRowAlign - 1) / kRowAlign;
+    // exclusive scans over groups of padded rows and 128-row blocks (2 groups per thread)
+    const int g0 = 2 * threadIdx.x;
+    const int c0 = g0 < G ? s_cnt[g0] : 0, c1 = g0 + 1 < G ? s_cnt[g0 + 1] : 0;
+    const int p0 = round_up(c0, kRowAlign), p1 = round_up(c1, kRowAlign);
+    const int m0 = (c0 + kRowAlign - 1) / kRowAlign, m1 = (c1 + kRowAlign - 1) / kRowAlign;
+    int xp = p0 + p1, xm = m0 + m1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int yp = __shfl_up_sync(0xffffffffu, xp, o), ym = __shfl_up_sync(0xffffffffu, xm, o);
+        if (lane >= o) {
+            xp += yp;
+            xm += ym;
         }
-        s_pad[G] = a;
-        s_mb[G] = m;
-        if (a > rows_cap) set_status(status, MOE_DEV_ROWS_OVERFLOW);
+    }
+    if (lane == 31) {
+        s_wp[warp] = xp;
+        s_wm[warp] = xm;
     }
     __syncthreads();
+    if (warp == 0) {
+        int a = s_wp[lane], b = s_wm[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
+            if (lane >= o) {
+                a += ya;
+                b += yb;
+            }
+        }
+        s_wp[lane] = a;  // inclusive warp totals
+        s_wm[lane] = b;
+    }
+    __syncthreads();
+    const int bp = (warp ? s_wp[warp - 1] : 0) + xp - (p0 + p1);  // exclusive prefix
+    const int bm = (warp ? s_wm[warp - 1] : 0) + xm - (m0 + m1);
+    if (g0 <= G) {
+        s_pad[g0] = bp;
+        s_mb[g0] = bm;
+    }
+    if (g0 + 1 <= G) {
+        s_pad[g0 + 1] = bp + p0;
+        s_mb[g0 + 1] = bm + m0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && s_pad[G] > rows_cap) set_status(status, MOE_DEV_ROWS_OVERFLOW);
     for (int g = threadIdx.x; g <= G; g += blockDim.x) {
         offsets[g] = s_pad[g];
         mb_start[g] = s_mb[g];
@@ -322,7 +384,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(
     }
 }
 
-__global__ void __launch_bounds__(32) perm_scatter_kernel(
+__global__ void __launch_bounds__(256) perm_scatter_kernel(
     const int32_t* __restrict__ ids, int P, int E, int off, int El,
     const int32_t* __restrict__ blkoff, const int32_t* __restrict__ offsets, int rows_cap,
     int32_t* __restrict__ perm_src, int32_t* __restrict__ inv)
@@ -330,23 +392,29 @@ __global__ void __launch_bounds__(32) perm_scatter_kernel(
     pdl_wait();
     if (threadIdx.x == 0) pdl_trigger();
     __shared__ int32_t cursor[kMaxExperts];
-    const int lane = threadIdx.x;
-    for (int e = lane; e < El; e += 32)
-        cursor[e] = offsets[e] + blkoff[(size_t)blockIdx.x * El + e];
-    __syncwarp();
+    __shared__ int32_t le_s[kPairsPerBlock];
     const int p0 = blockIdx.x * kPairsPerBlock;
-    const int p1 = min(P, p0 + kPairsPerBlock);
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int base = p0; base < p1; base += 32) {
-        const int p = base + lane;
+    const int n = min(P, p0 + kPairsPerBlock) - p0;
+    for (int e = threadIdx.x; e < El; e += blockDim.x)
+        cursor[e] = offsets[e] + blkoff[(size_t)blockIdx.x * El + e];
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int id = ids[p0 + i];
         int le = -1;
-        if (p < p1) {
-            const int id = ids[p];
-            if (id >= 0 && id < E) {
-                le = id - off;
-                if (le < 0 || le >= El) le = -1;
-            }
+        if (id >= 0 && id < E) {
+            le = id - off;
+            if (le < 0 || le >= El) le = -1;
         }
+        le_s[i] = le;
+    }
+    __syncthreads();
+    if (threadIdx.x >= 32) return;
+    // one warp walks the block's pairs in order; equal experts in a 32-pair step are ranked
+    // with a match mask, so rows keep ascending pair order
+    const int lane = threadIdx.x;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int base = 0; base < n; base += 32) {
+        const int i = base + lane;
+        const int le = i < n ? le_s[i] : -1;
         const uint32_t grp = __match_any_sync(0xffffffffu, le);
         const int leader = __ffs(grp) - 1;
         int b = 0;
@@ -356,14 +424,14 @@ __global__ void __launch_bounds__(32) perm_scatter_kernel(
         }
         b = __shfl_sync(0xffffffffu, b, leader);
         __syncwarp();
-        if (p < p1) {
+        if (i < n) {
             int row = -1;
             if (le >= 0) {
                 row = b + __popc(grp & lt);
                 if (row >= rows_cap) row = -1;
-                else perm_src[row] = p;
+                else perm_src[row] = p0 + i;
             }
-            inv[p] = row;
+            inv[p0 + i] = row;
         }
     }
 }
