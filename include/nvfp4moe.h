@@ -197,9 +197,9 @@ MOE_API moe_status moe_swiglu_requant(const float* gateup_f32_d, int32_t rows, i
                               moe_stream_t stream);
 
 /* Grouped GEMM down: Y_g = Aq_g . W2_g^T / (gs_i * gs2_g) (W4A16: / gs2_g), each row
- * multiplied by its routing weight (1 for shared rows) and written to
- * y_d[perm_src[row]][H] fp32 -- i.e. y is indexed by pair p = t*k + j, shared rows at
- * T*k + t; rows of dropped pairs are left unwritten. */
+ * multiplied by its routing weight (1 for shared rows; the weight of padded row r is
+ * topk_w[perm_src[r]]), written to y_d[rows_capacity][H] fp32 at the same padded row.
+ * Padding rows of y may receive arbitrary values. */
 MOE_API moe_status moe_grouped_gemm_down(moe_handle h, const uint8_t* inter_codes_d,
                                  const uint8_t* inter_sf_d, const void* inter_bf16_d,
                                  const int32_t* expert_counts_d,
@@ -207,10 +207,13 @@ MOE_API moe_status moe_grouped_gemm_down(moe_handle h, const uint8_t* inter_code
                                  const float* topk_w_d, float* y_d, int32_t T, void* ws_d,
                                  size_t ws_bytes, moe_stream_t stream);
 
-/* Combine: out[t] = sum_{j: inv[t*k+j] >= 0} y[t*k+j] + (add_shared ? y[T*k+t] : 0),
- * summed in ascending j then the shared term in fp32, rounded to bf16. */
-MOE_API moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* inv_d, int32_t T,
-                       void* out_bf16_d, moe_stream_t stream);
+/* Combine: out[t] = sum_{j: inv[t*k+j] >= 0} y[inv[t*k+j]]
+ *                  + (add_shared ? y[expert_offsets[E_loc] + t] : 0),
+ * y indexed by padded row (moe_grouped_gemm_down), summed in ascending j then the shared
+ * term in fp32, rounded to bf16. */
+MOE_API moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* inv_d,
+                       const int32_t* expert_offsets_d, int32_t T, void* out_bf16_d,
+                       moe_stream_t stream);
 
 /* The whole layer: route, permute, gather-quantise, gate_up (fused SwiGLU+requant),
  * down, combine.  logits_in_d (nullable): given router logits [T][E] instead of x.Wr^T;

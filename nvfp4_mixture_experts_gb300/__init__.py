@@ -52,7 +52,7 @@ SIGNATURES = {
                                           _V, _SZ, _V]),
     "moe_swiglu_requant": (C.c_int, [_V, _I, _I, C.c_float, _V, _V, _I, _V]),
     "moe_grouped_gemm_down": (C.c_int, [_V, _V, _V, _V, _V, _V, _V, _V, _V, _I, _V, _SZ, _V]),
-    "moe_combine": (C.c_int, [_V, _V, _V, _I, _V, _V]),
+    "moe_combine": (C.c_int, [_V, _V, _V, _V, _I, _V, _V]),
     "moe_forward": (C.c_int, [_V, _V, _V, _V, _I, _V, _V, _SZ, _V]),
     "moe_forward_buffers": (C.c_int, [_V, _V, _I] + [C.POINTER(_V)] * 14),
     "moe_get_status": (C.c_int, [_V, _V, _V, C.POINTER(C.c_uint32)]),
@@ -175,8 +175,9 @@ def moe_grouped_gemm_down(h, inter_codes, inter_sf, inter_bf16, counts, offsets,
                                         _stream(stream)), "moe_grouped_gemm_down")
 
 
-def moe_combine(h, y, inv, T, out, stream=None):
-    _check(load().moe_combine(h, _p(y), _p(inv), T, _p(out), _stream(stream)), "moe_combine")
+def moe_combine(h, y, inv, offsets, T, out, stream=None):
+    _check(load().moe_combine(h, _p(y), _p(inv), _p(offsets), T, _p(out), _stream(stream)),
+           "moe_combine")
 
 
 def moe_forward(h, x, logits_in, logit_bias, T, out, ws, stream=None):

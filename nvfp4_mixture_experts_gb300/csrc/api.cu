@@ -115,7 +115,7 @@ Plan plan(const moe_config& c, int T)
     p.i_codes = take(a16 ? 0 : (size_t)p.cap * codes_pitch(p.I));
     p.i_sf = take(a16 ? 0 : (size_t)p.cap * (p.I / 16));
     p.i_bf16 = take(a16 ? (size_t)p.cap * p.I * 2 : 0);
-    p.y = take((size_t)(p.Tk + T) * p.H * 4);
+    p.y = take((size_t)p.cap * p.H * 4);
     p.total = o;
     return p;
 }
@@ -340,12 +340,18 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     args.topk_w = topk_w;
     args.Tk = p.Tk;
     args.status = at<uint32_t>(ws, p.status);
-    CUtensorMap tmA, tmA16;
+    CUtensorMap tmA, tmA16, tmY;
+    memset(&tmY, 0, sizeof(tmY));
     const int grid = gemm_grid(h, p.T, N);
     const int stage_bytes = a16 ? kBf16StageBytes : kNvf4StageBytes;
-    args.stages = gemm_stages(6, stage_bytes, p.G);
-    const int smem = gemm_smem_bytes(args.stages, stage_bytes, p.G);
+    args.staging = epilogue == kEpiDown ? kDownStaging : 0;
+    args.stages = gemm_stages(6, stage_bytes, args.staging, p.G);
+    const int smem = gemm_smem_bytes(args.stages, stage_bytes, args.staging, p.G);
     if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
+    if (epilogue == kEpiDown &&
+        !make_tmap(&tmY, out_f32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, p.cap, (uint64_t)N * 4, 32,
+                   32, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MOE_ERR_CUDA;
     if (!a16) {
         const int pitch = codes_pitch(K);
         if (!make_tmap(&tmA, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
@@ -354,7 +360,7 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
                        16, CU_TENSOR_MAP_SWIZZLE_128B))
             return MOE_ERR_CUDA;
         return launch(gemm_nvf4_kernel, dim3(grid), dim3(kNvf4Threads), smem, s, pdl, tmA, tmA16,
-                      args);
+                      tmY, args);
     } else {
         if (!make_tmap(&tmA, a_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, p.cap, (uint64_t)K * 2,
                        64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -362,7 +368,7 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
                        (uint64_t)K * 2, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B))
             return MOE_ERR_CUDA;
         return launch(gemm_w4a16_kernel, dim3(grid), dim3(kBf16Threads), smem, s, pdl, tmA,
-                      tmA16, args);
+                      tmA16, tmY, args);
     }
 }
 
@@ -370,13 +376,13 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
 
 namespace {
 
-moe_status launch_combine(const moe_layer* h, const float* y, const int32_t* inv, int T,
-                          void* out, bool pdl, cudaStream_t s)
+moe_status launch_combine(const moe_layer* h, const float* y, const int32_t* inv,
+                          const int32_t* offsets, int T, void* out, bool pdl, cudaStream_t s)
 {
     const moe_config& c = h->cfg;
     return launch(combine_kernel, dim3(grid_for((int64_t)T * (c.hidden / 8), 256)), dim3(256), 0,
-                  s, pdl, y, inv, T, c.hidden, c.top_k, shared_rows(h, T) > 0 ? 1 : 0,
-                  static_cast<uint16_t*>(out));
+                  s, pdl, y, inv, offsets, c.num_local_experts, T, c.hidden, c.top_k,
+                  shared_rows(h, T) > 0 ? 1 : 0, static_cast<uint16_t*>(out));
 }
 
 }  // namespace
@@ -652,12 +658,14 @@ moe_status moe_grouped_gemm_down(moe_handle h, const uint8_t* inter_codes_d,
                        perm_src_d, topk_w_d, ws_d, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
-moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* inv_d, int32_t T,
-                       void* out_bf16_d, moe_stream_t stream)
+moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* inv_d,
+                       const int32_t* expert_offsets_d, int32_t T, void* out_bf16_d,
+                       moe_stream_t stream)
 {
-    if (!h || !t_ok(h, T) || !y_d || !inv_d || !out_bf16_d) return MOE_ERR_INVALID;
+    if (!h || !t_ok(h, T) || !y_d || !inv_d || !expert_offsets_d || !out_bf16_d)
+        return MOE_ERR_INVALID;
     if (T == 0) return MOE_OK;
-    return launch_combine(h, y_d, inv_d, T, out_bf16_d, false,
+    return launch_combine(h, y_d, inv_d, expert_offsets_d, T, out_bf16_d, false,
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -703,7 +711,7 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
     if (r == MOE_OK)
         r = launch_gemm(h, p, false, kEpiDown, i_codes, i_sf, nullptr, i_bf16, counts, offsets,
                         y, nullptr, nullptr, nullptr, perm_src, w, ws, true, s);
-    if (r == MOE_OK) r = launch_combine(h, y, inv, T, out_bf16_d, true, s);
+    if (r == MOE_OK) r = launch_combine(h, y, inv, offsets, T, out_bf16_d, true, s);
     return r;
 }
 

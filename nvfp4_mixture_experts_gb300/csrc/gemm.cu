@@ -104,8 +104,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // wait so their latency overlaps the tile's mainloop).
 struct EpiPrep {
     int64_t prow;   // padded row of this thread
-    int64_t yrow;   // kEpiDown: output row (pair index)
     float alpha;    // 1 / (global scales) (x routing weight for kEpiDown)
+    int nvalid;     // valid rows in this warp's 32-row quarter (0..32)
     bool valid;
 };
 
@@ -120,24 +120,29 @@ __device__ __forceinline__ EpiPrep epi_prep(const GemmArgs& a, const TileInfo& t
     const float gw = a.gs_w[ti.g];
     if (a.epilogue == kEpiDown) e.alpha = kW4A16 ? __frcp_rn(gw) : __frcp_rn(__fmul_rn(a.gs_i, gw));
     else e.alpha = kW4A16 ? __frcp_rn(gw) : __frcp_rn(__fmul_rn(*a.gs_a, gw));
-    e.yrow = 0;
+    e.nvalid = max(0, min(32, ti.rows - q * 32));
     if (a.epilogue == kEpiDown && e.valid) {
-        e.yrow = a.perm_src[e.prow];
-        const float wgt = e.yrow < a.Tk ? a.topk_w[e.yrow] : 1.0f;
+        const int pair = a.perm_src[e.prow];
+        const float wgt = pair < a.Tk ? a.topk_w[pair] : 1.0f;
         e.alpha = __fmul_rn(e.alpha, wgt);
     }
     return e;
 }
 
-// Epilogue of one tile for the 32 rows of TMEM lane quarter q (thread = row).
+// Epilogue of one tile for the 32 rows of TMEM lane quarter q (thread = row).  A warp
+// whose quarter has no valid row does nothing.  kEpiDown with more than 8 valid rows
+// stages each 32 x 32 fp32 chunk in shared memory (128-byte swizzle, two buffers per warp)
+// and writes it with a TMA tensor store; sparse quarters store directly.
 template <bool kW4A16>
 __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& ti,
-                                             const EpiPrep& ep, uint32_t tacc, int q, int lane)
+                                             const EpiPrep& ep, uint32_t tacc, int q, int lane,
+                                             const CUtensorMap* tmY, uint8_t* stg, int& pp)
 {
+    if (ep.nvalid == 0) return;
     const bool valid = ep.valid;
     const int64_t prow = ep.prow;
-    const int64_t yrow = ep.yrow;
     const float alpha = ep.alpha;
+    const bool staged = a.epilogue == kEpiDown && a.staging && ep.nvalid > 8;
     const int I = a.N / 2;
     uint32_t sfword = 0;
 #pragma unroll 1
@@ -145,9 +150,29 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& 
         uint32_t r[32];
         tmem_ld32(tacc + ((uint32_t)(q * 32) << 16) + 32 * c, r);
         tmem_ld_wait();
+        if (staged) {
+            uint8_t* buf = stg + pp * 4096;
+            if (lane == 0) bulk_wait_read1();  // this buffer's previous store has read it
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<float4*>(buf + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+                    make_float4(__uint_as_float(r[4 * i]) * alpha,
+                                __uint_as_float(r[4 * i + 1]) * alpha,
+                                __uint_as_float(r[4 * i + 2]) * alpha,
+                                __uint_as_float(r[4 * i + 3]) * alpha);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(tmY, buf, 128 * ti.nb + 32 * c, ti.arow0 + 32 * q);
+                bulk_commit();
+            }
+            pp ^= 1;
+            continue;
+        }
         if (!valid) continue;
         if (a.epilogue == kEpiDown) {
-            float4* dst = reinterpret_cast<float4*>(a.out_f32 + yrow * a.N + 128 * ti.nb + 32 * c);
+            float4* dst = reinterpret_cast<float4*>(a.out_f32 + prow * a.N + 128 * ti.nb + 32 * c);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 dst[i] = make_float4(__uint_as_float(r[4 * i]) * alpha,
@@ -244,13 +269,15 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw)
 
 __global__ void __launch_bounds__(kNvf4Threads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmA16, GemmArgs args)
+                     const __grid_constant__ CUtensorMap tmA16,
+                     const __grid_constant__ CUtensorMap tmY, GemmArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = aligned_smem(smem_raw);
     const int NS = args.stages;
-    Ctl ctl = carve(stages + NS * kNvf4StageBytes, kMaxStages);
-    const Tables tb = load_tables(args, tables_smem(stages + NS * kNvf4StageBytes));
+    uint8_t* staging = stages + NS * kNvf4StageBytes;  // epilogue staging (kEpiDown)
+    Ctl ctl = carve(staging + args.staging, kMaxStages);
+    const Tables tb = load_tables(args, tables_smem(staging + args.staging));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NB = args.N / 128;
     const int KB = (args.K + 255) / 256;
@@ -452,7 +479,7 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
         }
     } else {
         const int q = warp & 3;
-        int it = 0;
+        int it = 0, pp = 0;
         pdl_wait();
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
             const TileInfo ti = decode_tile(args, tb, NB, t);
@@ -467,10 +494,12 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
                 break;
             }
             tc_fence_after();
-            run_epilogue<false>(args, ti, ep, tmem + buf * 128, q, lane);
+            run_epilogue<false>(args, ti, ep, tmem + buf * 128, q, lane, &tmY,
+                             staging + (warp - 2) * 8192, pp);
             tc_fence_before();
             mbar_arrive(&ctl.acc_empty[buf]);
         }
+        if (lane == 0) bulk_wait_all();  // staged stores complete before the CTA exits
     }
     tc_fence_before();
     __syncthreads();
@@ -495,13 +524,15 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code)
 
 __global__ void __launch_bounds__(kBf16Threads, 1)
     gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmA16, GemmArgs args)
+                      const __grid_constant__ CUtensorMap tmA16,
+                     const __grid_constant__ CUtensorMap tmY, GemmArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = aligned_smem(smem_raw);
     const int NS = args.stages;
-    Ctl ctl = carve(stages + NS * kBf16StageBytes, kMaxStages);
-    const Tables tb = load_tables(args, tables_smem(stages + NS * kBf16StageBytes));
+    uint8_t* staging = stages + NS * kBf16StageBytes;  // epilogue staging (kEpiDown)
+    Ctl ctl = carve(staging + args.staging, kMaxStages);
+    const Tables tb = load_tables(args, tables_smem(staging + args.staging));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NB = args.N / 128;
     const int KB = args.K / 64;
@@ -645,7 +676,7 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
         __syncwarp();
     } else if (warp < 6) {
         const int q = warp & 3;
-        int it = 0;
+        int it = 0, pp = 0;
         pdl_wait();
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
             const TileInfo ti = decode_tile(args, tb, NB, t);
@@ -660,10 +691,12 @@ __global__ void __launch_bounds__(kBf16Threads, 1)
                 break;
             }
             tc_fence_after();
-            run_epilogue<true>(args, ti, ep, tmem + buf * 128, q, lane);
+            run_epilogue<true>(args, ti, ep, tmem + buf * 128, q, lane, &tmY,
+                             staging + (warp - 2) * 8192, pp);
             tc_fence_before();
             mbar_arrive(&ctl.acc_empty[buf]);
         }
+        if (lane == 0) bulk_wait_all();  // staged stores complete before the CTA exits
     } else {
         // dequantisation: thread n converts weight row n of the stage (64 elements)
         const int n = (warp - 6) * 32 + lane;

@@ -47,8 +47,9 @@ __global__ void quant_rows_kernel(const uint16_t* x, int rows, int cols, const f
                                   int layout, float* gs_out);
 __global__ void swiglu_requant_kernel(const float* gu, int rows, int I, float gs_i,
                                       uint8_t* codes, uint8_t* sf, int layout);
-__global__ void combine_kernel(const float* y, const int32_t* inv, int T, int H, int k,
-                               int add_shared, uint16_t* out);
+__global__ void combine_kernel(const float* y, const int32_t* inv, const int32_t* offsets,
+                               int shared_group, int T, int H, int k, int add_shared,
+                               uint16_t* out);
 __global__ void repack_tiles_kernel(const uint8_t* codes, const uint8_t* sf, int nexp, int N,
                                     int K, int interleave, int raw, uint8_t* dst);
 
@@ -56,7 +57,7 @@ __global__ void repack_tiles_kernel(const uint8_t* codes, const uint8_t* sf, int
 enum GemmEpilogue : int {
     kEpiGateUpF32 = 0,     // G (alpha applied) -> fp32 rows, gate then up columns
     kEpiGateUpSwiglu = 1,  // silu(gate)*up -> NVFP4 (W4A4) or bf16 (W4A16)
-    kEpiDown = 2           // Y * routing weight -> fp32 rows indexed by pair
+    kEpiDown = 2           // Y * routing weight -> fp32 rows indexed by padded row
 };
 
 struct GemmArgs {
@@ -72,7 +73,7 @@ struct GemmArgs {
     int K;                    // contraction length (elements)
     int epilogue;             // GemmEpilogue
     float gs_i;               // intermediate global scale (W4A4)
-    float* out_f32;           // kEpiGateUpF32: [rows][2I]; kEpiDown: y [pairs][H]
+    float* out_f32;           // kEpiGateUpF32: [rows][2I]; kEpiDown: y [rows][H]
     uint8_t* out_codes;       // kEpiGateUpSwiglu W4A4: tiled codes [rows][pitch(I)]
     uint8_t* out_sf;          // kEpiGateUpSwiglu W4A4: scale atoms (K = I)
     uint16_t* out_bf16;       // kEpiGateUpSwiglu W4A16: [rows][I]
@@ -80,6 +81,7 @@ struct GemmArgs {
     const float* topk_w;      // kEpiDown
     int Tk;                   // kEpiDown: first pair index of the shared rows (T*k)
     int stages;               // pipeline depth (<= kMaxStages; fits the shared memory)
+    int staging;              // bytes of epilogue staging (kEpiDown: TMA stores of y), or 0
     uint32_t* status;
 };
 
@@ -97,23 +99,26 @@ constexpr int kCtlBytes = 256;          // barriers for kMaxStages + TMEM slot +
 constexpr int kSmemLimit = 232448;      // dynamic shared memory per block (227 KB)
 constexpr int kNvf4StageBytes = 16384 + 16384 + 2048 + 2048;
 constexpr int kBf16StageBytes = 37888;   // A 16K + B 16K + raw FP4 4K + scales 512, padded to 1 KB
-// Shared memory of a GEMM launch: stages, 1 KB alignment slack, control block, and the
-// group tables (mb_start, counts, offsets).
-inline int gemm_smem_bytes(int stages, int stage_bytes, int G)
+constexpr int kDownStaging = 4 * 2 * 4096;  // 4 epilogue warps x 2 buffers x 32x32 fp32
+// Shared memory of a GEMM launch: stages, epilogue staging, 1 KB alignment slack, control
+// block, and the group tables (mb_start, counts, offsets).
+inline int gemm_smem_bytes(int stages, int stage_bytes, int staging, int G)
 {
-    return stages * stage_bytes + 1024 + kCtlBytes + 4 * (3 * G + 2);
+    return stages * stage_bytes + staging + 1024 + kCtlBytes + 4 * (3 * G + 2);
 }
-inline int gemm_stages(int want, int stage_bytes, int G)
+inline int gemm_stages(int want, int stage_bytes, int staging, int G)
 {
     int s = want;
-    while (s > 2 && gemm_smem_bytes(s, stage_bytes, G) > kSmemLimit) --s;
+    while (s > 2 && gemm_smem_bytes(s, stage_bytes, staging, G) > kSmemLimit) --s;
     return s;
 }
 constexpr int kBf16Threads = 320;       // + 4 dequantisation warps
 
 __global__ void gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
-                                 const __grid_constant__ CUtensorMap tmA16, GemmArgs args);
+                                 const __grid_constant__ CUtensorMap tmA16,
+                                 const __grid_constant__ CUtensorMap tmY, GemmArgs args);
 __global__ void gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmA,
-                                  const __grid_constant__ CUtensorMap tmA16, GemmArgs args);
+                                  const __grid_constant__ CUtensorMap tmA16,
+                                  const __grid_constant__ CUtensorMap tmY, GemmArgs args);
 
 }  // namespace moe

@@ -201,12 +201,14 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(
 }
 
 // ---------------------------------------------------------------- combine
-// out[t][h] = sum_{j: inv >= 0} y[t*k+j][h] + (add_shared ? y[T*k+t][h] : 0) -> bf16.
-// One thread per 8 columns of one token.
+// out[t][h] = sum_{j: inv >= 0} y[inv[t*k+j]][h] + (add_shared ? y[offsets[G_s] + t][h] : 0)
+// in ascending j then the shared row, fp32, rounded to bf16.  y rows are padded rows (already
+// multiplied by their routing weight).  One thread per 8 columns of one token.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
-                                                      const int32_t* __restrict__ inv, int T,
-                                                      int H, int k, int add_shared,
-                                                      uint16_t* __restrict__ out)
+                                                      const int32_t* __restrict__ inv,
+                                                      const int32_t* __restrict__ offsets,
+                                                      int shared_group, int T, int H, int k,
+                                                      int add_shared, uint16_t* __restrict__ out)
 {
     pdl_wait();
     if (threadIdx.x == 0) pdl_trigger();
@@ -215,15 +217,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     if (i >= (int64_t)T * per) return;
     const int t = (int)(i / per), c = (int)(i % per) * 8;
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int j = 0; j < k; ++j) {
-        if (inv[(size_t)t * k + j] < 0) continue;
-        const float4* src = reinterpret_cast<const float4*>(y + ((size_t)t * k + j) * H + c);
-        const float4 a = src[0], b = src[1];
-        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-    }
-    if (add_shared) {
-        const float4* src = reinterpret_cast<const float4*>(y + ((size_t)T * k + t) * H + c);
+    for (int j = 0; j <= k; ++j) {
+        int64_t row;
+        if (j < k) {
+            row = inv[(size_t)t * k + j];
+            if (row < 0) continue;
+        } else {
+            if (!add_shared) break;
+            row = (int64_t)offsets[shared_group] + t;
+        }
+        const float4* src = reinterpret_cast<const float4*>(y + row * H + c);
         const float4 a = src[0], b = src[1];
         acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
         acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;

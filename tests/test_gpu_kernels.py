@@ -322,7 +322,7 @@ def test_grouped_gemm_fused_and_down_match_oracle(act_mode):
                                     np.uint16)
         dic = disf = None
         dib = bits16(full.reshape(-1))
-    y = torch.zeros(((T * k + T), H), dtype=torch.float32, device="cuda")
+    y = torch.zeros((st.cap, H), dtype=torch.float32, device="cuda")
     moe.moe_grouped_gemm_down(h.handle, dic, disf, dib, st.counts, st.offsets, st.perm, st.w,
                               y, T, st.ws)
     yg = host(y)
@@ -332,23 +332,28 @@ def test_grouped_gemm_fused_and_down_match_oracle(act_mode):
         pair = perm[r]
         wt = wts[pair] if pair < T * k else 1.0
         want = ref_Y[j] * wt
-        got = yg[pair]
+        got = yg[r]  # y is indexed by padded row
         assert np.max(np.abs(got - want)) <= 1e-4 * np.sqrt(np.mean(want ** 2)) * np.sqrt(I / 64) + 1e-9, (j, g)
 
 
 def test_combine_sums_pairs_and_shared():
-    T, k, H = 33, 8, 256
-    h, _ = _tiny_layer_handle(E=320, k=k, H=H)
+    T, k, H, El = 33, 8, 256, 320
+    h, _ = _tiny_layer_handle(E=El, k=k, H=H)
     rng = np.random.default_rng(1)
-    y = rng.standard_normal((T * k + T, H)).astype(np.float32)
-    inv = rng.integers(-1, 5, size=T * k).astype(np.int32)  # >= 0 means local
+    R = 600
+    y = rng.standard_normal((R, H)).astype(np.float32)
+    # pairs point at distinct padded rows (or -1: not local); shared rows start at 500
+    rows = rng.permutation(400)[:T * k].astype(np.int32)
+    inv = np.where(rng.random(T * k) < 0.7, rows, -1).astype(np.int32)
+    offsets = np.zeros(El + 2, np.int32)
+    offsets[El] = 500
     out = torch.zeros((T, H), dtype=torch.int16, device="cuda")
-    moe.moe_combine(h.handle, dev(y), dev(inv), T, out)
+    moe.moe_combine(h.handle, dev(y), dev(inv), dev(offsets), T, out)
     want = np.zeros((T, H), np.float64)
     for t in range(T):
         for j in range(k):
             if inv[t * k + j] >= 0:
-                want[t] += y[t * k + j]
-        want[t] += y[T * k + t]
+                want[t] += y[inv[t * k + j]]
+        want[t] += y[500 + t]
     got = synth.bf16_to_f32(host(out).view(np.uint16))
     assert np.max(np.abs(got - want) / (np.abs(want) + 1e-3)) < 2 ** -7
