@@ -344,7 +344,12 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     memset(&tmY, 0, sizeof(tmY));
     const int grid = gemm_grid(h, p.T, N);
     const int stage_bytes = a16 ? kBf16StageBytes : kNvf4StageBytes;
-    args.staging = epilogue == kEpiDown ? kDownStaging : 0;
+    // Kernel configuration from the expected LOCAL load (rows per local expert), as the
+    // pages' backend choice is re-tuned on the local rather than the global workload: with
+    // few rows per 128-row block the down epilogue stores directly and the shared memory
+    // goes to one more pipeline stage; with many it stages TMA stores.
+    const int64_t local_rows = (int64_t)p.T * c.top_k / std::max(1, c.num_local_experts);
+    args.staging = (epilogue == kEpiDown && local_rows >= 16) ? kDownStaging : 0;
     args.stages = gemm_stages(6, stage_bytes, args.staging, p.G);
     const int smem = gemm_smem_bytes(args.stages, stage_bytes, args.staging, p.G);
     if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
