@@ -140,6 +140,24 @@ MOE_API moe_status moe_route_topk(moe_handle h, const void* x_bf16_d, const floa
                           float* topk_w_d, float* logits_out_d, void* ws_d, size_t ws_bytes,
                           moe_stream_t stream);
 
+/* Routing that allocates nothing: the same result as moe_route_topk, for callers that
+ * cannot allocate device memory at call time and have no workspace to lend -- for example
+ * code running while another component owns every byte of device memory through its own
+ * pool, or a caller in a phase where a cudaMalloc (which may synchronise the device) is not
+ * allowed.  The pages have no counterpart; it is an addition of this library.
+ * The router's partial-sum planes live in one file-scope 8 MiB device array that every
+ * device loading the library keeps until exit; T * E (tokens x global experts) must not
+ * exceed 2,097,152, else MOE_ERR_WORKSPACE (with E = 320: T <= 6553).  The first call on a
+ * device looks the array's address up (cudaGetSymbolAddress, with the handle's device
+ * current) and should come before any stream capture.  All calls share the array: calls
+ * whose executions overlap on the GPU race (use one stream, or serialise them).  Nothing in
+ * the array needs to start at zero: each call writes every value it reads.  Given
+ * logits_in_d, no scratch is touched at all. */
+MOE_API moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
+                                          const float* logits_in_d, const float* logit_bias_d,
+                                          int32_t T, int32_t* topk_ids_d, float* topk_w_d,
+                                          float* logits_out_d, moe_stream_t stream);
+
 /* Local map + grouping (the "compact pre-pass").  Pair p = t*k + j with local expert
  * e' = topk_ids[p] - local_expert_offset is kept iff 0 <= e' < E_loc (a pair with an id
  * outside [0, E) is dropped and sets MOE_DEV_BAD_EXPERT_ID).  Outputs:

@@ -45,6 +45,7 @@ SIGNATURES = {
     "moe_workspace_size": (_SZ, [C.POINTER(moe_config), _I]),
     "moe_rows_capacity": (_I, [C.POINTER(moe_config), _I]),
     "moe_route_topk": (C.c_int, [_V, _V, _V, _V, _I, _V, _V, _V, _V, _SZ, _V]),
+    "moe_route_topk_noalloc": (C.c_int, [_V, _V, _V, _V, _I, _V, _V, _V, _V]),
     "moe_permute": (C.c_int, [_V, _V, _I, _V, _V, _V, _V, _V, _SZ, _V]),
     "moe_quant_nvfp4": (C.c_int, [_V, _I, _I, _V, _V, _V, _V, _I, _V, _SZ, _V]),
     "moe_gather_activations": (C.c_int, [_V, _V, _I, _V, _V, _V, _V, _V, _V, _V, _SZ, _V]),
@@ -129,6 +130,15 @@ def moe_route_topk(h, x, logits_in, logit_bias, T, topk_ids, topk_w, logits_out,
                                  _p(topk_w), _p(logits_out), _p(ws),
                                  0 if ws is None else ws.numel() * ws.element_size(),
                                  _stream(stream)), "moe_route_topk")
+
+
+def moe_route_topk_noalloc(h, x, logits_in, logit_bias, T, topk_ids, topk_w, logits_out,
+                           stream=None):
+    """moe_route_topk without a workspace: the scratch is a static device array of the
+    library (see include/nvfp4moe.h for its size limit and sharing rules)."""
+    _check(load().moe_route_topk_noalloc(h, _p(x), _p(logits_in), _p(logit_bias), T,
+                                         _p(topk_ids), _p(topk_w), _p(logits_out),
+                                         _stream(stream)), "moe_route_topk_noalloc")
 
 
 def moe_permute(h, topk_ids, T, counts, offsets, perm_src, inv, ws, stream=None):

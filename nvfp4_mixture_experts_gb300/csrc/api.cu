@@ -392,6 +392,42 @@ moe_status launch_combine(const moe_layer* h, const float* y, const int32_t* inv
 
 }  // namespace
 
+// ================================================================ routing without allocation
+//
+// Scratch for moe_route_topk_noalloc: the router's partial-sum logit planes live in this
+// file-scope device array instead of a caller workspace.  Every device that loads the
+// library holds it (8 MiB) until the process exits.  Host code may not pass the symbol
+// itself to a kernel (on the host it only names a stand-in); the device address is looked
+// up once per device with cudaGetSymbolAddress, with that device current.
+constexpr size_t kRouteScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) float g_route_scratch[kRouteScratchBytes / sizeof(float)];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_route_scratch_mu;
+float* g_route_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_route_scratch on the current device (looked up on first use).
+moe_status route_scratch_address(float** out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_route_scratch_mu);
+    if (!g_route_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        g_route_scratch_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_route_scratch_ptr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+
 // ================================================================ C ABI
 
 extern "C" {
@@ -744,6 +780,48 @@ moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** to
     if (inter_sf) *inter_sf = at<uint8_t>(ws_d, p.i_sf);
     if (y) *y = at<float>(ws_d, p.y);
     return MOE_OK;
+}
+
+moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
+                                  const float* logits_in_d, const float* logit_bias_d,
+                                  int32_t T, int32_t* topk_ids_d, float* topk_w_d,
+                                  float* logits_out_d, moe_stream_t stream)
+{
+    if (!h || !t_ok(h, T) || !topk_ids_d || !topk_w_d) return MOE_ERR_INVALID;
+    if (!logits_in_d && !x_bf16_d) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;
+    const moe_config& c = h->cfg;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const float* src = logits_in_d;
+    int nsplit = 1;
+    if (!logits_in_d) {
+        if (reinterpret_cast<uintptr_t>(x_bf16_d) & 15) return MOE_ERR_INVALID;
+        const size_t plane = (size_t)T * c.num_experts;          // floats per partial plane
+        const size_t capacity = kRouteScratchBytes / sizeof(float);
+        if (plane > capacity) return MOE_ERR_WORKSPACE;            // T * E beyond the scratch
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+        if (dev != h->device) return MOE_ERR_INVALID;
+        float* scratch = nullptr;
+        const moe_status st = route_scratch_address(&scratch);
+        if (st != MOE_OK) return st;
+        nsplit = router_splits(T, c.num_experts, c.hidden, h->num_sms);
+        while (nsplit > 1 && plane * nsplit > capacity) nsplit /= 2;
+        CUtensorMap tmX;
+        if (!make_tmap(&tmX, x_bf16_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.hidden, T,
+                       (uint64_t)c.hidden * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MOE_ERR_CUDA;
+        dim3 grid(ceil_div(T, 128), ceil_div(c.num_experts, 64), nsplit);
+        const moe_status r = launch(router_gemm_kernel, grid, dim3(192), kRouterSmem, s, false,
+                                    tmX, h->tm_router, (int)T, c.num_experts, c.hidden,
+                                    c.hidden / nsplit, scratch, (uint32_t*)nullptr,
+                                    (uint32_t*)nullptr, (uint32_t*)nullptr);
+        if (r != MOE_OK) return r;
+        src = scratch;
+    }
+    return launch(topk_kernel, dim3(ceil_div(T, 8)), dim3(256), 0, s, false, src, nsplit,
+                  logit_bias_d, (int)T, c.num_experts, c.top_k, topk_ids_d, topk_w_d,
+                  logits_out_d, (uint32_t*)nullptr, (uint32_t*)nullptr);
 }
 
 moe_status moe_get_status(moe_handle h, void* ws_d, moe_stream_t stream, uint32_t* bits)
