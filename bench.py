@@ -233,7 +233,8 @@ def measure_ours(args, rank, world):
     name = args.workload
     c = synth.CONFIGS[name]
     T, H, k = c["T"], c["H"], c["k"]
-    extra = () if (args.no_extra or name != "decode" or args.local_experts) else ("prefill",)
+    extra = () if (args.no_extra or name != "decode" or args.local_experts) else \
+        ("prefill", "w4a16")
     handles = gpu_layer(name, extra_handles=extra, local_experts=args.local_experts)
     if args.local_experts:
         c = dict(c, E_loc=args.local_experts)
@@ -329,6 +330,8 @@ def measure_ours(args, rank, world):
                launches=launches_per_forward(c) * args.steps)
     if "prefill" in extra and rank == 0:
         res["prefill"] = measure_prefill(handles["prefill"], stream, max(3, args.steps // 20))
+    if "w4a16" in extra and rank == 0:
+        res["w4a16"] = measure_w4a16(handles["w4a16"], stream, max(10, args.steps // 4))
     return res
 
 
@@ -428,6 +431,54 @@ def measure_prefill(layer, stream, steps):
     fl = gemm_flops(counts, c, True) + gemm_flops(counts, c, False)
     return {"workload": "prefill T=8192", "value": T / (ms / 1e3), "ms_per_step": ms,
             "roofline": roof, "expert_fp4_tflops": round(fl / (ms / 1e3) / 1e12, 2)}
+
+
+def measure_w4a16(layer, stream, steps):
+    """Side measurement of the W4A16 path (bf16 activations x NVFP4 weights, router logits
+    given ~ N(0,1)) over the decode sweep T in {1, 8, 32, 128, 256}: CUDA-graph replays."""
+    import torch
+
+    import nvfp4_mixture_experts_gb300 as moe
+    c = synth.CONFIGS["w4a16"]
+    H = c["H"]
+    out_rows = []
+    pk = peaks()
+    for T in c["sweep"]:
+        cc = dict(c, T=T)
+        x = synth.activations(0, T, H)
+        lg = synth.logits_normal(0, T, c["E"])
+        xd = torch.from_numpy(x.view(np.int16)).cuda()
+        lgd = torch.from_numpy(lg).cuda()
+        out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+        ws = layer.ensure_workspace(T)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                moe.moe_forward(layer.handle, xd, lgd, None, T, out, ws)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                moe.moe_forward(layer.handle, xd, lgd, None, T, out, ws)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        roof = roofline(layer, cc, xd, lgd, None, ws, stream, min(steps, 20), pk, "w4a16")
+        counts = staged_counts(layer, ws, T)
+        wbytes = gemm_bytes(cc, counts, True)[0] + gemm_bytes(cc, counts, False)[0]
+        out_rows.append({"T": T, "value": round(T / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
+                         "experts_touched": roof["experts_touched"],
+                         "gemm_bytes_per_step": int(wbytes),
+                         "step_hbm_frac": round(wbytes / (ms / 1e3) / 1e9 / pk["hbm"], 4),
+                         "gateup_us": roof["launch_us"], "gateup_frac": roof["frac"],
+                         "down_us": roof["down"]["launch_us"], "down_frac": roof["down"]["frac"]})
+    return {"workload": "w4a16 decode sweep (bf16 x NVFP4, logits given)", "unit": "tokens/s",
+            "sweep": out_rows}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -537,8 +588,9 @@ def main():
                     "h2d_bytes_per_step": c["T"] * c["H"] * 2,
                     "d2h_bytes_per_step": c["T"] * c["H"] * 2},
             "gpu_launches": r["launches"], "roofline": r["roofline"]}
-    if "prefill" in r:
-        line["prefill"] = r["prefill"]
+    for side in ("prefill", "w4a16"):
+        if side in r:
+            line[side] = r[side]
     if world == 1 and not args.no_oracle and not args.local_experts:
         line["cpu_baseline"] = cpu_baseline(args.workload)
     print(json.dumps(line), flush=True)

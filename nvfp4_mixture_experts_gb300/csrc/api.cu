@@ -164,6 +164,7 @@ struct moe_layer {
     float *gs13 = nullptr, *gs2 = nullptr;     // [G]
     float* act_gs = nullptr;                   // static activation scale (device copy)
     CUtensorMap tm_router;                     // Wr [E][H] bf16, 64 x 64 boxes
+    CUtensorMap tm_router160;                  // Wr [E][H] bf16, 64 x 160 boxes
 };
 
 namespace {
@@ -243,10 +244,12 @@ moe_status launch_route(const moe_layer* h, const void* x, const float* logits_i
         if (!make_tmap(&tmX, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.hidden, T,
                        (uint64_t)c.hidden * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
             return MOE_ERR_CUDA;
-        dim3 grid(ceil_div(T, 128), ceil_div(c.num_experts, 64), nsplit);
+        const int bn = router_bn(T, c.num_experts);
+        dim3 grid(ceil_div(T, 128), ceil_div(c.num_experts, bn), nsplit);
         const moe_status r = launch(router_gemm_kernel, grid, dim3(192), kRouterSmem, s, pdl,
-                                    tmX, h->tm_router, T, c.num_experts, c.hidden,
-                                    c.hidden / nsplit, logits_scratch, status, clear0, clear1);
+                                    tmX, bn == 160 ? h->tm_router160 : h->tm_router, T,
+                                    c.num_experts, c.hidden, c.hidden / nsplit, bn,
+                                    logits_scratch, status, clear0, clear1);
         if (r != MOE_OK) return r;
         src = logits_scratch;
         clear0 = clear1 = nullptr;  // done by the router
@@ -264,6 +267,10 @@ moe_status launch_permute(const moe_layer* h, const Plan& p, const int32_t* ids,
     int32_t* hist = at<int32_t>(ws, p.hist);
     int32_t* blkoff = at<int32_t>(ws, p.blkoff);
     int32_t* mb_start = at<int32_t>(ws, p.mb_start);
+    if (p.nblk == 1)  // every pair fits one block: the whole grouping in one CTA
+        return launch(perm_small_kernel, dim3(1), dim3(1024), 0, s, pdl, ids, p.Tk,
+                      c.num_experts, c.local_expert_offset, p.El, T, c.top_k,
+                      shared_rows(h, T), p.cap, counts, offsets, mb_start, perm_src, inv, status);
     moe_status r = launch(perm_hist_kernel, dim3(p.nblk), dim3(256), 0, s, pdl, ids, p.Tk,
                           c.num_experts, c.local_expert_offset, p.El, hist, status);
     if (r == MOE_OK)
@@ -536,7 +543,9 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     }
     ok = ok && cudaGetLastError() == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess;
     ok = ok && make_tmap(&h->tm_router, h->router_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H,
-                         cfg->num_experts, (uint64_t)H * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+                         cfg->num_experts, (uint64_t)H * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_tmap(&h->tm_router160, h->router_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H,
+                   cfg->num_experts, (uint64_t)H * 2, 64, 160, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok &&
          cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kRouterSmem) == cudaSuccess &&
@@ -811,11 +820,12 @@ moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
         if (!make_tmap(&tmX, x_bf16_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.hidden, T,
                        (uint64_t)c.hidden * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
             return MOE_ERR_CUDA;
-        dim3 grid(ceil_div(T, 128), ceil_div(c.num_experts, 64), nsplit);
+        const int bn = router_bn(T, c.num_experts);
+        dim3 grid(ceil_div(T, 128), ceil_div(c.num_experts, bn), nsplit);
         const moe_status r = launch(router_gemm_kernel, grid, dim3(192), kRouterSmem, s, false,
-                                    tmX, h->tm_router, (int)T, c.num_experts, c.hidden,
-                                    c.hidden / nsplit, scratch, (uint32_t*)nullptr,
-                                    (uint32_t*)nullptr, (uint32_t*)nullptr);
+                                    tmX, bn == 160 ? h->tm_router160 : h->tm_router, (int)T,
+                                    c.num_experts, c.hidden, c.hidden / nsplit, bn, scratch,
+                                    (uint32_t*)nullptr, (uint32_t*)nullptr, (uint32_t*)nullptr);
         if (r != MOE_OK) return r;
         src = scratch;
     }

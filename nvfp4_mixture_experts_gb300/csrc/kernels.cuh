@@ -14,12 +14,13 @@ __device__ __forceinline__ float silu_mul(float g, float u)
 }
 
 // ---- route.cu
-constexpr int kRouterSmem = 4 * (16384 + 8192) + 1024 + 256;
+constexpr int kRouterSmem = 4 * (16384 + 160 * 128) + 1024 + 256;
 __global__ void router_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                                    const __grid_constant__ CUtensorMap tmW, int T, int E, int H,
-                                   int k_per_split, float* part, uint32_t* status,
+                                   int k_per_split, int bn, float* part, uint32_t* status,
                                    uint32_t* clear0, uint32_t* clear1);
 int router_splits(int T, int E, int H, int num_sms);
+int router_bn(int T, int E);
 __global__ void topk_kernel(const float* logits_src, int nsplit, const float* bias, int T,
                             int E, int k, int32_t* ids, float* wts, float* logits_out,
                             uint32_t* clear0, uint32_t* clear1);
@@ -29,6 +30,10 @@ __global__ void perm_scan_kernel(const int32_t* hist, int nblk, int El, int T, i
                                  int shared_rows, int rows_cap, int32_t* blkoff,
                                  int32_t* counts, int32_t* offsets, int32_t* mb_start,
                                  int32_t* perm_src, uint32_t* status);
+__global__ void perm_small_kernel(const int32_t* ids, int P, int E, int off, int El, int T,
+                                  int k, int shared_rows, int rows_cap, int32_t* counts,
+                                  int32_t* offsets, int32_t* mb_start, int32_t* perm_src,
+                                  int32_t* inv, uint32_t* status);
 __global__ void perm_scatter_kernel(const int32_t* ids, int P, int E, int off, int El,
                                     const int32_t* blkoff, const int32_t* offsets,
                                     int rows_cap, int32_t* perm_src, int32_t* inv);

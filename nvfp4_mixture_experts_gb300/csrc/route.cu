@@ -13,20 +13,25 @@ namespace moe {
 // ---------------------------------------------------------------- router logits
 //
 // logits = x . Wr^T on the tensor cores (kind::f16, bf16 operands, fp32 accumulation in
-// TMEM).  Tile: 128 tokens x 64 experts; grid (token tiles, expert tiles, k-splits).  Each
+// TMEM).  Tile: 128 tokens x bn experts (64 or 160); grid (token tiles, expert tiles,
+// k-splits).  Each
 // k-split writes its partial sums to part[split][T][E]; the top-k kernel adds the splits
 // in a fixed order (deterministic), then the bias.  Rows past T and experts past E are
 // zero-filled by the TMA and never stored.
-//   warp 0: TMA producer (x tile 128 x 64, Wr tile 64 x 64 per stage)
+//   warp 0: TMA producer (x tile 128 x 64, Wr tile bn x 64 per stage)
 //   warp 1: TMEM allocation, MMA issue (4 x K16 per stage)
 //   warps 2..5: epilogue, one TMEM lane quarter (32 tokens) each
 constexpr int kRgStages = 4;
-constexpr int kRgStageBytes = 16384 + 8192;
+constexpr int kRgStageBytes = 16384 + 160 * 128;  // x tile + the widest expert tile
+
+// Expert-tile width: 64 experts for small T (more CTAs for the weight stream), 160 for
+// large T (fewer re-reads of the x tile, more work per MMA).
+int router_bn(int T, int E) { return (T >= 1024 && E > 64) ? 160 : 64; }
 
 __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
     const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, int T,
-    int E, int H, int k_per_split, float* __restrict__ part, uint32_t* status, uint32_t* clear0,
-    uint32_t* clear1)
+    int E, int H, int k_per_split, int bn, float* __restrict__ part, uint32_t* status,
+    uint32_t* clear0, uint32_t* clear1)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t u = smem_u32(smem_raw);
@@ -37,7 +42,7 @@ __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
     uint32_t* tslot = reinterpret_cast<uint32_t*>(acc + 1);
     int* flags = reinterpret_cast<int*>(tslot + 1);  // [0] abort, [1] zero
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * 128, n0 = blockIdx.y * 64;
+    const int m0 = blockIdx.x * 128, n0 = blockIdx.y * bn;
     const int k0 = blockIdx.z * k_per_split;
     const int KB = min(k_per_split, H - k0) / 64;
     if (threadIdx.x == 0) {
@@ -50,7 +55,7 @@ __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(tslot, 64);
+        tmem_alloc(tslot, 256);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -77,7 +82,7 @@ __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
                 break;
             }
             uint8_t* sa = st + stg * kRgStageBytes;
-            mbar_arrive_expect_tx(&full[stg], kRgStageBytes);
+            mbar_arrive_expect_tx(&full[stg], 16384u + (uint32_t)bn * 128u);
             tma_load_2d(sa, &tmX, &full[stg], k0 + kb * 64, m0, pol);
             tma_load_2d(sa + 16384, &tmW, &full[stg], k0 + kb * 64, n0, pol);
             issued |= 1u << stg;
@@ -90,7 +95,7 @@ __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
         for (int i = 0; i < kRgStages; ++i)
             if ((issued >> i) & 1u) mbar_wait(&full[i], (par >> i) & 1u, flags + 1);
     } else if (warp == 1 && lane == 0) {
-        constexpr uint32_t idesc = idesc_bf16(128, 64);
+        const uint32_t idesc = idesc_bf16(128, bn);
         uint32_t phase = 0;
         int stg = 0;
         bool ok = true;
@@ -123,7 +128,7 @@ __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
             const int t = m0 + q * 32 + lane;
             float* dst = part + ((size_t)blockIdx.z * T + t) * E + n0;
 #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < bn / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + 32 * c, r);
                 tmem_ld_wait();
@@ -140,14 +145,15 @@ __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 64);
+        tmem_dealloc(tmem, 256);
     }
 }
 
 int router_splits(int T, int E, int H, int num_sms)
 {
     // at most 4 partial planes: more CTAs would make the top-k's plane sum the bottleneck
-    const int tiles = ((T + 127) / 128) * ((E + 63) / 64);
+    const int bn = router_bn(T, E);
+    const int tiles = ((T + 127) / 128) * ((E + bn - 1) / bn);
     int s = 1;
     while (s < 4 && s * 2 * 256 <= H && tiles * s * 2 <= num_sms) s *= 2;
     return s;
@@ -181,18 +187,13 @@ __global__ void __launch_bounds__(256) topk_kernel(
     const size_t plane = (size_t)T * E;
     for (int idx = threadIdx.x; idx < nt * E; idx += blockDim.x) {
         const size_t off = (size_t)t0 * E + idx;
-        float l = logits_src[off];
-        int sp = 1;
-        for (; sp + 3 < nsplit; sp += 4) {  // 4 loads in flight per element
-            const float a = logits_src[off + sp * plane], b = logits_src[off + (sp + 1) * plane];
-            const float c = logits_src[off + (sp + 2) * plane];
-            const float d = logits_src[off + (sp + 3) * plane];
-            l += a;
-            l += b;
-            l += c;
-            l += d;
-        }
-        for (; sp < nsplit; ++sp) l += logits_src[off + sp * plane];
+        float pl[4];  // the router uses at most 4 planes; all loads issued before the sum
+#pragma unroll
+        for (int sp = 0; sp < 4; ++sp) pl[sp] = sp < nsplit ? logits_src[off + sp * plane] : 0.0f;
+        float l = pl[0];
+#pragma unroll
+        for (int sp = 1; sp < 4; ++sp)
+            if (sp < nsplit) l += pl[sp];
         const int e = idx % E;
         l += bias ? bias[e] : 0.0f;
         sl[idx / E][e] = l;
@@ -295,28 +296,70 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(
     __shared__ int32_t s_wp[32], s_wm[32];
     const int G = El + 1;  // groups: routed experts, then the shared expert
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // per-group totals and per-block exclusive prefix: a warp per group, lanes over blocks
-    for (int g = warp; g < G; g += 32) {
-        int total = 0;
-        if (g < El) {
-            for (int b0 = 0; b0 < nblk; b0 += 32) {
-                const int b = b0 + lane;
-                const int v = b < nblk ? hist[(size_t)b * El + g] : 0;
-                int x = v;
+    // per-group totals and per-block exclusive prefix: a warp per group, lanes over blocks;
+    // each lane first loads its blocks' counts of all its groups (independent loads)
+    constexpr int kMaxBlkPerLane = 2, kBatch = 8;  // loads in flight: kBatch x kMaxBlkPerLane
+    if (nblk <= 32 * kMaxBlkPerLane) {
+        for (int gb = warp; gb < G; gb += 32 * kBatch) {
+            int v[kBatch][kMaxBlkPerLane];
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, x, o);
-                    if (lane >= o) x += y;
+            for (int gi = 0; gi < kBatch; ++gi)
+#pragma unroll
+                for (int i = 0; i < kMaxBlkPerLane; ++i) {
+                    const int g = gb + 32 * gi, b = lane + 32 * i;
+                    v[gi][i] = (g < El && b < nblk) ? hist[(size_t)b * El + g] : 0;
                 }
-                if (b < nblk) blkoff[(size_t)b * El + g] = total + x - v;
-                total += __shfl_sync(0xffffffffu, x, 31);
+#pragma unroll
+            for (int gi = 0; gi < kBatch; ++gi) {
+                const int g = gb + 32 * gi;
+                if (g >= G) break;
+                int total = 0;
+                if (g < El) {
+#pragma unroll
+                    for (int i = 0; i < kMaxBlkPerLane; ++i) {
+                        if (32 * i >= nblk) break;
+                        int x = v[gi][i];
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const int y = __shfl_up_sync(0xffffffffu, x, o);
+                            if (lane >= o) x += y;
+                        }
+                        const int b = lane + 32 * i;
+                        if (b < nblk) blkoff[(size_t)b * El + g] = total + x - v[gi][i];
+                        total += __shfl_sync(0xffffffffu, x, 31);
+                    }
+                } else {
+                    total = shared_rows;
+                }
+                if (lane == 0) {
+                    s_cnt[g] = total;
+                    counts[g] = total;
+                }
             }
-        } else {
-            total = shared_rows;
         }
-        if (lane == 0) {
-            s_cnt[g] = total;
-            counts[g] = total;
+    } else {
+        for (int g = warp; g < G; g += 32) {
+            int total = 0;
+            if (g < El) {
+                for (int b0 = 0; b0 < nblk; b0 += 32) {
+                    const int b = b0 + lane;
+                    const int v = b < nblk ? hist[(size_t)b * El + g] : 0;
+                    int x = v;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, x, o);
+                        if (lane >= o) x += y;
+                    }
+                    if (b < nblk) blkoff[(size_t)b * El + g] = total + x - v;
+                    total += __shfl_sync(0xffffffffu, x, 31);
+                }
+            } else {
+                total = shared_rows;
+            }
+            if (lane == 0) {
+                s_cnt[g] = total;
+                counts[g] = total;
+            }
         }
     }
     __syncthreads();
@@ -369,18 +412,133 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(
         offsets[g] = s_pad[g];
         mb_start[g] = s_mb[g];
     }
-    // padding rows -> -1; shared rows -> T*k + t (routed rows are written by the scatter)
-    const int total = min(s_pad[G], rows_cap);
-    for (int r = threadIdx.x; r < total; r += blockDim.x) {
-        int lo = 0, hi = G;  // s_pad[lo] <= r < s_pad[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (s_pad[mid] <= r) lo = mid;
-            else hi = mid;
+    // padding rows -> -1; shared rows -> T*k + t (routed rows are written by the scatter);
+    // a warp per group
+    for (int g = warp; g < G; g += 32) {
+        const int start = s_pad[g], n = s_cnt[g], end = min(s_pad[g + 1], rows_cap);
+        for (int r = start + (g == El ? 0 : n) + lane; r < end; r += 32) {
+            const int i = r - start;
+            perm_src[r] = i < n ? T * k + i : -1;
         }
-        const int i = r - s_pad[lo];
-        if (i >= s_cnt[lo]) perm_src[r] = -1;
-        else if (lo == El) perm_src[r] = T * k + i;
+    }
+}
+
+// The whole grouping in one CTA when every pair fits one block (decode): per-expert counts,
+// the scans, the stable scatter and the padding markers.  Same outputs as hist + scan +
+// scatter.
+__global__ void __launch_bounds__(1024) perm_small_kernel(
+    const int32_t* __restrict__ ids, int P, int E, int off, int El, int T, int k,
+    int shared_rows, int rows_cap, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ mb_start, int32_t* __restrict__ perm_src, int32_t* __restrict__ inv,
+    uint32_t* status)
+{
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
+    __shared__ int32_t s_cnt[kMaxExperts + 1];
+    __shared__ int32_t s_pad[kMaxExperts + 2];
+    __shared__ int32_t s_mb[kMaxExperts + 2];
+    __shared__ int32_t le_s[kPairsPerBlock];
+    __shared__ int32_t s_wp[32], s_wm[32];
+    const int G = El + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = g < El ? 0 : shared_rows;
+    __syncthreads();
+    bool bad = false;
+    for (int i = threadIdx.x; i < P; i += blockDim.x) {
+        const int id = ids[i];
+        int le = -1;
+        if (id < 0 || id >= E) {
+            bad = true;
+        } else {
+            le = id - off;
+            if (le < 0 || le >= El) le = -1;
+            else atomicAdd(&s_cnt[le], 1);
+        }
+        le_s[i] = le;
+    }
+    if (bad) set_status(status, MOE_DEV_BAD_EXPERT_ID);
+    __syncthreads();
+    const int g0 = 2 * threadIdx.x;
+    const int c0 = g0 < G ? s_cnt[g0] : 0, c1 = g0 + 1 < G ? s_cnt[g0 + 1] : 0;
+    const int p0 = round_up(c0, kRowAlign), p1 = round_up(c1, kRowAlign);
+    const int m0 = (c0 + kRowAlign - 1) / kRowAlign, m1 = (c1 + kRowAlign - 1) / kRowAlign;
+    int xp = p0 + p1, xm = m0 + m1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int yp = __shfl_up_sync(0xffffffffu, xp, o), ym = __shfl_up_sync(0xffffffffu, xm, o);
+        if (lane >= o) {
+            xp += yp;
+            xm += ym;
+        }
+    }
+    if (lane == 31) {
+        s_wp[warp] = xp;
+        s_wm[warp] = xm;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int a = s_wp[lane], b = s_wm[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
+            if (lane >= o) {
+                a += ya;
+                b += yb;
+            }
+        }
+        s_wp[lane] = a;
+        s_wm[lane] = b;
+    }
+    __syncthreads();
+    const int bp = (warp ? s_wp[warp - 1] : 0) + xp - (p0 + p1);
+    const int bm = (warp ? s_wm[warp - 1] : 0) + xm - (m0 + m1);
+    if (g0 <= G) {
+        s_pad[g0] = bp;
+        s_mb[g0] = bm;
+    }
+    if (g0 + 1 <= G) {
+        s_pad[g0 + 1] = bp + p0;
+        s_mb[g0 + 1] = bm + m0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && s_pad[G] > rows_cap) set_status(status, MOE_DEV_ROWS_OVERFLOW);
+    for (int g = threadIdx.x; g <= G; g += blockDim.x) {
+        offsets[g] = s_pad[g];
+        mb_start[g] = s_mb[g];
+        if (g < G) counts[g] = s_cnt[g];
+    }
+    for (int g = warp; g < G; g += 32) {  // padding markers and shared rows
+        const int start = s_pad[g], n = s_cnt[g], end = min(s_pad[g + 1], rows_cap);
+        for (int r = start + (g == El ? 0 : n) + lane; r < end; r += 32) {
+            const int i = r - start;
+            perm_src[r] = i < n ? T * k + i : -1;
+        }
+    }
+    __syncthreads();  // every reader of s_pad is done before warp 0 advances it as a cursor
+    if (warp != 0) return;
+    // stable scatter: one warp walks the pairs in order (s_pad doubles as the cursor)
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int base = 0; base < P; base += 32) {
+        const int i = base + lane;
+        const int le = i < P ? le_s[i] : -1;
+        const uint32_t grp = __match_any_sync(0xffffffffu, le);
+        const int leader = __ffs(grp) - 1;
+        int b = 0;
+        if (le >= 0 && lane == leader) {
+            b = s_pad[le];
+            s_pad[le] = b + __popc(grp);
+        }
+        b = __shfl_sync(0xffffffffu, b, leader);
+        __syncwarp();
+        if (i < P) {
+            int row = -1;
+            if (le >= 0) {
+                row = b + __popc(grp & lt);
+                if (row >= rows_cap) row = -1;
+                else perm_src[row] = i;
+            }
+            inv[i] = row;
+        }
     }
 }
 

@@ -149,9 +149,16 @@ def test_permute_bit_exact(T, E_loc, off, add_shared):
     perm = torch.full((cap,), -7, dtype=torch.int32, device="cuda")
     inv = torch.zeros(T * k, dtype=torch.int32, device="cuda")
     ws = _ws(h.workspace_bytes(T))
-    moe.moe_permute(h.handle, dev(ids), T, counts, offsets, perm, inv, ws)
     rc, rp = oracle.permute(ids, E_loc, off)
-    c, o, p, iv = host(counts), host(offsets), host(perm), host(inv)
+    for rep in range(4):  # repeated: a race between the kernel's phases would show up here
+        perm.fill_(-7)
+        moe.moe_permute(h.handle, dev(ids), T, counts, offsets, perm, inv, ws)
+        _check_grouping(host(counts), host(offsets), host(perm), host(inv), rc, rp, T, k,
+                        E_loc, add_shared)
+    assert moe.moe_get_status(h.handle, ws) == (moe.MOE_OK, 0)
+
+
+def _check_grouping(c, o, p, iv, rc, rp, T, k, E_loc, add_shared):
     assert np.array_equal(c[:E_loc], rc)
     assert c[E_loc] == (T if add_shared else 0)
     pad = (c + 127) // 128 * 128
@@ -165,7 +172,6 @@ def test_permute_bit_exact(T, E_loc, off, add_shared):
     rows = np.concatenate([np.arange(o[e], o[e] + c[e]) for e in range(E_loc)]) if E_loc else []
     want_inv[rp] = rows
     assert np.array_equal(iv, want_inv)
-    assert moe.moe_get_status(h.handle, ws) == (moe.MOE_OK, 0)
 
 
 def test_permute_drops_and_flags_bad_ids():
