@@ -181,6 +181,22 @@ def inputs(name, seed=0):
     return x, lg, bias
 
 
+def max_over_ranks(value, world, device="cuda"):
+    """The slowest rank's time (the job is as fast as its slowest replica).  The process
+    group carries only this timing scalar and the barriers, never layer data."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_rank, ms_slowest):
+    """Whole-job throughput: every rank's tokens over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms_slowest / 1e3)
+
+
 def launches_per_forward(c):
     n = 1 + (0 if c["logits"] else 1)      # router logits (from x) + top-k
     n += 3                                 # grouping: histogram, scan, scatter
@@ -293,12 +309,8 @@ def measure_ours(args, rank, world):
                 g.replay()
             torch.cuda.synchronize()
     clocks = summarise_clocks(sampler.stop())
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * T / (ms / 1e3)
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    value = job_tokens_per_s(world, T, ms)
 
     # ---- end to end through the C ABI: pinned host x -> device, forward, out -> host
     xh = torch.from_numpy(x.view(np.int16)).pin_memory()
@@ -319,11 +331,7 @@ def measure_ours(args, rank, world):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
 
     roof = roofline(layer, c, xd, lgd, bd, ws, stream, args.steps, peaks(), name)
     res = dict(value=value, ms=ms, ms_e2e=ms_e2e, clocks=clocks, roofline=roof,
@@ -551,8 +559,15 @@ def main():
         if rank != 0:
             return
         import oracle
-        run, what = oracle_setup(args.workload, max(1, ORACLE_SAMPLE[args.workload] // 8))
-        n = max(1, ORACLE_SAMPLE[args.workload] // 8)
+        # size the per-step sample so the whole --steps/--warmup run stays near 150 s: probe
+        # one token, then take as many tokens per step as the budget allows (1..8)
+        probe, _ = oracle_setup(args.workload, 1)
+        t0 = time.perf_counter()
+        probe()
+        t1 = time.perf_counter() - t0
+        budget = 150.0 / max(1, args.steps + args.warmup)
+        n = int(max(1, min(8, budget / max(t1, 1e-3))))
+        run, what = oracle_setup(args.workload, n)
         for _ in range(max(0, args.warmup)):
             run()
         t0 = time.perf_counter()
@@ -584,7 +599,7 @@ def main():
             else "bf16 x nvfp4, fp32 accumulate",
             "data": "synthetic (seeded; N(0,1) activations, N(0,0.02) weights)",
             "config": config, "clocks": r["clocks"],
-            "e2e": {"value": world * c["T"] / (r["ms_e2e"] / 1e3), "unit": "tokens/s",
+            "e2e": {"value": job_tokens_per_s(world, c["T"], r["ms_e2e"]), "unit": "tokens/s",
                     "h2d_bytes_per_step": c["T"] * c["H"] * 2,
                     "d2h_bytes_per_step": c["T"] * c["H"] * 2},
             "gpu_launches": r["launches"], "roofline": r["roofline"]}
