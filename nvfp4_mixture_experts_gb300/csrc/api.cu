@@ -170,10 +170,9 @@ struct moe_layer {
 namespace {
 
 // Bytes of the weight blobs of one expert slot for an N x K matrix.
-size_t blob_bytes(int N, int K, bool raw)
+size_t blob_bytes(int N, int K)
 {
-    const int kst = raw ? 64 : 256;
-    return (size_t)(N / 128) * ((K + kst - 1) / kst) * (raw ? kRawTileBytes : kNvf4TileBytes);
+    return (size_t)(N / 128) * ((K + 255) / 256) * kNvf4TileBytes;
 }
 
 }  // namespace
@@ -213,12 +212,13 @@ bool t_ok(const moe_layer* h, int T) { return T >= 0 && T <= h->cfg.max_tokens; 
 
 int grid_for(int64_t threads, int block) { return (int)std::max<int64_t>(1, (threads + block - 1) / block); }
 
-// Upper bound on the GEMM tile count for T tokens (the exact count is on the device).
-int gemm_grid(const moe_layer* h, int T, int N)
+// Persistent grid: one CTA per SM, or fewer when the tile list (bounded above from the
+// pair count, with row blocks of `rows` rows) is shorter.
+int gemm_grid(const moe_layer* h, int T, int N, int rows)
 {
     const int64_t P = (int64_t)T * h->cfg.top_k;
-    int64_t mb = (P + 127) / 128 + std::min<int64_t>(h->cfg.num_local_experts, P);
-    if (h->cfg.has_shared && h->cfg.add_shared) mb += (T + 127) / 128;
+    int64_t mb = (P + rows - 1) / rows + std::min<int64_t>(h->cfg.num_local_experts, P);
+    if (h->cfg.has_shared && h->cfg.add_shared) mb += (T + rows - 1) / rows;
     const int64_t tiles = mb * (N / 128);
     return (int)std::max<int64_t>(1, std::min<int64_t>(tiles, h->num_sms));
 }
@@ -347,10 +347,29 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     args.topk_w = topk_w;
     args.Tk = p.Tk;
     args.status = at<uint32_t>(ws, p.status);
+    if (a16) {
+        // Token rows per tile from the expected rows per local expert: narrow tiles keep the
+        // token tile (re-read for every weight tile) small when experts see few tokens.
+        const int64_t local_rows = (int64_t)p.T * c.top_k / std::max(1, c.num_local_experts);
+        const int bn = local_rows <= 16 ? 16 : local_rows <= 32 ? 32 : 64;
+        args.stages = kW16MaxSlots;
+        args.raw_slots = kW16MaxSlots;
+        while (args.raw_slots > 2 &&
+               w4a16_smem_bytes(args.raw_slots, args.stages, bn, p.G) > kSmemLimit)
+            --args.raw_slots;
+        const int smem = w4a16_smem_bytes(args.raw_slots, args.stages, bn, p.G);
+        if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
+        CUtensorMap tmB;
+        if (!make_tmap(&tmB, a_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, p.cap, (uint64_t)K * 2,
+                       64, bn, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MOE_ERR_CUDA;
+        return launch(w4a16_kernel(bn), dim3(gemm_grid(h, p.T, N, bn)), dim3(kW16Threads), smem,
+                      s, pdl, tmB, args);
+    }
     CUtensorMap tmA, tmA16, tmY;
     memset(&tmY, 0, sizeof(tmY));
-    const int grid = gemm_grid(h, p.T, N);
-    const int stage_bytes = a16 ? kBf16StageBytes : kNvf4StageBytes;
+    const int grid = gemm_grid(h, p.T, N, 128);
+    const int stage_bytes = kNvf4StageBytes;
     // Kernel configuration from the expected LOCAL load (rows per local expert), as the
     // pages' backend choice is re-tuned on the local rather than the global workload: with
     // few rows per 128-row block the down epilogue stores directly and the shared memory
@@ -364,24 +383,14 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
         !make_tmap(&tmY, out_f32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, p.cap, (uint64_t)N * 4, 32,
                    32, CU_TENSOR_MAP_SWIZZLE_128B))
         return MOE_ERR_CUDA;
-    if (!a16) {
-        const int pitch = codes_pitch(K);
-        if (!make_tmap(&tmA, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
-                       128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_tmap(&tmA16, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
-                       16, CU_TENSOR_MAP_SWIZZLE_128B))
-            return MOE_ERR_CUDA;
-        return launch(gemm_nvf4_kernel, dim3(grid), dim3(kNvf4Threads), smem, s, pdl, tmA, tmA16,
-                      tmY, args);
-    } else {
-        if (!make_tmap(&tmA, a_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, p.cap, (uint64_t)K * 2,
-                       64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_tmap(&tmA16, a_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, p.cap,
-                       (uint64_t)K * 2, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B))
-            return MOE_ERR_CUDA;
-        return launch(gemm_w4a16_kernel, dim3(grid), dim3(kBf16Threads), smem, s, pdl, tmA,
-                      tmA16, tmY, args);
-    }
+    const int pitch = codes_pitch(K);
+    if (!make_tmap(&tmA, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap(&tmA16, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128, 16,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return MOE_ERR_CUDA;
+    return launch(gemm_nvf4_kernel, dim3(grid), dim3(kNvf4Threads), smem, s, pdl, tmA, tmA16,
+                  tmY, args);
 }
 
 }  // namespace
@@ -505,8 +514,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
         return MOE_ERR_CUDA;
     }
     const int G = El + 1;
-    const bool raw = cfg->act_mode == MOE_W4A16;
-    const size_t b13 = blob_bytes(2 * I, H, raw), b2 = blob_bytes(H, I, raw);
+    const int pairs = cfg->act_mode == MOE_W4A16 ? 1 : 0;  // W4A16 nibble order
+    const size_t b13 = blob_bytes(2 * I, H), b2 = blob_bytes(H, I);
     bool ok = cudaMalloc(&h->router_w, (size_t)cfg->num_experts * H * 2) == cudaSuccess &&
               cudaMalloc(&h->w13, G * b13) == cudaSuccess &&
               cudaMalloc(&h->w2, G * b2) == cudaSuccess &&
@@ -523,18 +532,18 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
                                cudaMemcpyDeviceToDevice, s) == cudaSuccess;
     const int blocks = 8 * h->num_sms;
     if (ok && El > 0) {
-        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->w13_d, w->w13_sf_d, El, 2 * I, H, 1, raw,
+        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->w13_d, w->w13_sf_d, El, 2 * I, H, 1, pairs,
                                                    h->w13);
-        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->w2_d, w->w2_sf_d, El, H, I, 0, raw, h->w2);
+        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->w2_d, w->w2_sf_d, El, H, I, 0, pairs, h->w2);
         ok = cudaMemcpyAsync(h->gs13, w->w13_gs_d, El * 4, cudaMemcpyDeviceToDevice, s) ==
                  cudaSuccess &&
              cudaMemcpyAsync(h->gs2, w->w2_gs_d, El * 4, cudaMemcpyDeviceToDevice, s) ==
                  cudaSuccess;
     }
     if (ok && cfg->has_shared) {
-        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->sh13_d, w->sh13_sf_d, 1, 2 * I, H, 1, raw,
+        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->sh13_d, w->sh13_sf_d, 1, 2 * I, H, 1, pairs,
                                                    h->w13 + (size_t)El * b13);
-        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->sh2_d, w->sh2_sf_d, 1, H, I, 0, raw,
+        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->sh2_d, w->sh2_sf_d, 1, H, I, 0, pairs,
                                                    h->w2 + (size_t)El * b2);
         ok = cudaMemcpyAsync(h->gs13 + El, w->sh13_gs_d, 4, cudaMemcpyDeviceToDevice, s) ==
                  cudaSuccess &&
@@ -551,7 +560,11 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
                               kRouterSmem) == cudaSuccess &&
          cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemLimit) == cudaSuccess &&
-         cudaFuncSetAttribute(gemm_w4a16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+         cudaFuncSetAttribute(w4a16_kernel(16), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemLimit) == cudaSuccess &&
+         cudaFuncSetAttribute(w4a16_kernel(32), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemLimit) == cudaSuccess &&
+         cudaFuncSetAttribute(w4a16_kernel(64), cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemLimit) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();

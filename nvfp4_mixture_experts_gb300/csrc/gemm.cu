@@ -1,4 +1,5 @@
-// Grouped GEMMs of the expert MLPs on the 5th-generation tensor cores (tcgen05).
+// NVFP4 x NVFP4 (W4A4) grouped GEMMs of the expert MLPs on the 5th-generation tensor cores
+// (tcgen05).  The W4A16 GEMMs are in gemm_w4a16.cu.
 //
 // Rows (M) are the padded rows of one expert group (tokens routed to that expert); columns
 // (N) are 128 rows of that expert's weight matrix; the accumulator lives in TMEM.  One
@@ -14,16 +15,12 @@
 //   warp 0   TMA producer: activation tile (tensor map), weight blob, activation scales
 //   warp 1   TMEM allocation; one thread issues tcgen05.mma
 //   warps 2-5 epilogue: TMEM -> registers -> fused output (one TMEM lane quarter each)
-//   warps 6-9 W4A4: the stage's scale factors smem -> TMEM with tcgen05.st (keeping the
-//            copies out of the MMA thread's in-order tcgen05 queue, where they serialised
-//            with the MMAs); W4A16: FP4 -> bf16 dequantisation of the weight tile into
-//            the swizzled operand layout
+//   warps 6-9 the stage's scale factors smem -> TMEM with tcgen05.st (keeping the copies
+//            out of the MMA thread's in-order tcgen05 queue, where they serialised with
+//            the MMAs)
 //
-// W4A4 (NVFP4 x NVFP4): kind::mxf4nvf4 block-scaled MMA, K = 64 per instruction, UE4M3
-// scales per 16 elements copied SMEM -> TMEM per k-step.  The global scales are applied in
-// the epilogue as alpha = 1 / (gs_a * gs_w).
-// W4A16: kind::f16 with bf16 operands; the weights are dequantised in the mainloop
-// (E2M1 * E4M3 is exact in bf16) and the global scale is applied in the epilogue.
+// kind::mxf4nvf4 block-scaled MMA, K = 64 per instruction, UE4M3 scales per 16 elements.
+// The global scales are applied in the epilogue as alpha = 1 / (gs_a * gs_w).
 //
 // Every pipeline wait is bounded: a wait that runs out sets MOE_DEV_WAIT_TIMEOUT in the
 // status word and makes all roles stop, drain their copies in flight, free TMEM and exit.
@@ -109,7 +106,6 @@ struct EpiPrep {
     bool valid;
 };
 
-template <bool kW4A16>
 __device__ __forceinline__ EpiPrep epi_prep(const GemmArgs& a, const TileInfo& ti, int q,
                                             int lane)
 {
@@ -118,8 +114,7 @@ __device__ __forceinline__ EpiPrep epi_prep(const GemmArgs& a, const TileInfo& t
     e.valid = m < ti.rows;
     e.prow = (int64_t)ti.arow0 + m;
     const float gw = a.gs_w[ti.g];
-    if (a.epilogue == kEpiDown) e.alpha = kW4A16 ? __frcp_rn(gw) : __frcp_rn(__fmul_rn(a.gs_i, gw));
-    else e.alpha = kW4A16 ? __frcp_rn(gw) : __frcp_rn(__fmul_rn(*a.gs_a, gw));
+    e.alpha = __frcp_rn(__fmul_rn(a.epilogue == kEpiDown ? a.gs_i : *a.gs_a, gw));
     e.nvalid = max(0, min(32, ti.rows - q * 32));
     if (a.epilogue == kEpiDown && e.valid) {
         const int pair = a.perm_src[e.prow];
@@ -133,7 +128,6 @@ __device__ __forceinline__ EpiPrep epi_prep(const GemmArgs& a, const TileInfo& t
 // whose quarter has no valid row does nothing.  kEpiDown with more than 8 valid rows
 // stages each 32 x 32 fp32 chunk in shared memory (128-byte swizzle, two buffers per warp)
 // and writes it with a TMA tensor store; sparse quarters store directly.
-template <bool kW4A16>
 __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& ti,
                                              const EpiPrep& ep, uint32_t tacc, int q, int lane,
                                              const CUtensorMap* tmY, uint8_t* stg, int& pp)
@@ -201,26 +195,14 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& 
             for (int i = 0; i < 16; ++i)
                 s[i] = silu_mul(__fmul_rn(__uint_as_float(r[i]), alpha),
                                 __fmul_rn(__uint_as_float(r[16 + i]), alpha));
-            if (kW4A16) {
-                uint32_t o[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const __nv_bfloat162 p = __floats2bfloat162_rn(s[2 * i], s[2 * i + 1]);
-                    o[i] = *reinterpret_cast<const uint32_t*>(&p);
-                }
-                uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + prow * I + f);
-                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-            } else {
-                uint32_t cw[2];
-                const uint32_t sb = quant16(s, a.gs_i, cw);
-                *reinterpret_cast<uint2*>(a.out_codes + prow * codes_pitch(I) + f / 2) =
-                    make_uint2(cw[0], cw[1]);
-                sfword |= sb << (8 * c);
-            }
+            uint32_t cw[2];
+            const uint32_t sb = quant16(s, a.gs_i, cw);
+            *reinterpret_cast<uint2*>(a.out_codes + prow * codes_pitch(I) + f / 2) =
+                make_uint2(cw[0], cw[1]);
+            sfword |= sb << (8 * c);
         }
     }
-    if (!kW4A16 && a.epilogue == kEpiGateUpSwiglu && valid)
+    if (a.epilogue == kEpiGateUpSwiglu && valid)
         *reinterpret_cast<uint32_t*>(a.out_sf + sf_atom_offset(prow, 4 * ti.nb, I)) = sfword;
 }
 
@@ -229,7 +211,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& 
 struct Ctl {
     uint64_t* full;
     uint64_t* empty;
-    uint64_t* ready;       // W4A16: weight tile dequantised
+    uint64_t* ready;       // the stage's scale factors are in TMEM
     uint64_t* acc_full;
     uint64_t* acc_empty;
     uint64_t* drain;
@@ -483,7 +465,7 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
         pdl_wait();
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
             const TileInfo ti = decode_tile(args, tb, NB, t);
-            const EpiPrep ep = epi_prep<false>(args, ti, q, lane);
+            const EpiPrep ep = epi_prep(args, ti, q, lane);
             const int buf = it & 1;
             const uint32_t acc_par = (it >> 1) & 1;
             if (!warp_wait(&ctl.acc_full[buf], acc_par, ctl.abort_flag)) {
@@ -494,7 +476,7 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
                 break;
             }
             tc_fence_after();
-            run_epilogue<false>(args, ti, ep, tmem + buf * 128, q, lane, &tmY,
+            run_epilogue(args, ti, ep, tmem + buf * 128, q, lane, &tmY,
                              staging + (warp - 2) * 8192, pp);
             tc_fence_before();
             mbar_arrive(&ctl.acc_empty[buf]);
@@ -506,248 +488,6 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
-    }
-}
-
-// ============================================================== W4A16: bf16 x NVFP4
-
-// E2M1 code (4 bits) -> fp32: magnitude 0, 0.5, 1, 1.5, 2, 3, 4, 6 from the exponent and
-// mantissa bits (exponent field e = c >> 1 with bias 1, mantissa m = c & 1).
-__device__ __forceinline__ float e2m1_to_f32(uint32_t code)
-{
-    const uint32_t c = code & 7u;
-    // e >= 1: fp32 exponent e + 126, mantissa bit m at bit 22  ==  (c + 252) << 22;
-    // c == 1 (subnormal 0.5): 0x3F000000 == 252 << 22;  c == 0: 0.
-    const uint32_t bits = c == 0 ? 0u : ((c + 252u - (c == 1u ? 1u : 0u)) << 22);
-    return __uint_as_float(bits | ((code & 8u) << 28));
-}
-
-__global__ void __launch_bounds__(kBf16Threads, 1)
-    gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmA16,
-                     const __grid_constant__ CUtensorMap tmY, GemmArgs args)
-{
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* stages = aligned_smem(smem_raw);
-    const int NS = args.stages;
-    uint8_t* staging = stages + NS * kBf16StageBytes;  // epilogue staging (kEpiDown)
-    Ctl ctl = carve(staging + args.staging, kMaxStages);
-    const Tables tb = load_tables(args, tables_smem(staging + args.staging));
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NB = args.N / 128;
-    const int KB = args.K / 64;
-    // stage layout: A bf16 [128][128 B] | B bf16 [128][128 B] | raw FP4 [128][32 B] | scales
-    constexpr int kOffB = 16384, kOffW = 32768, kOffSF = 36864;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&ctl.full[s], 1);
-            mbar_init(&ctl.empty[s], 1);
-            mbar_init(&ctl.ready[s], 128);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&ctl.acc_full[b], 1);
-            mbar_init(&ctl.acc_empty[b], 128);
-        }
-        mbar_init(ctl.drain, 1);
-        *ctl.abort_flag = 0;
-        *ctl.zero = 0;
-        fence_barrier_init();
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmA16);
-    }
-    if (warp == 1) {
-        tmem_alloc(ctl.tmem_slot, 256);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *ctl.tmem_slot;
-    const int ntiles = tb.mb_start[args.G] * NB;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
-            // the first NS stages' weights (constant) go out before the predecessor is done
-            int i = 0;
-            for (int t = blockIdx.x; t < ntiles && i < NS; t += gridDim.x) {
-                const TileInfo ti = decode_tile(args, tb, NB, t);
-                const int nbox = (ti.rows + 15) >> 4;
-                const uint32_t a_bytes = nbox > 4 ? 16384u : (uint32_t)nbox * 2048u;
-                const uint8_t* wt = args.b_tiles +
-                                    ((size_t)ti.g * NB + ti.nb) * KB * (size_t)kRawTileBytes;
-                for (int kb = 0; kb < KB && i < NS; ++kb, ++i) {
-                    mbar_arrive_expect_tx(&ctl.full[i], a_bytes + (uint32_t)kRawTileBytes);
-                    bulk_load(stages + i * kBf16StageBytes + kOffW,
-                              wt + (size_t)kb * kRawTileBytes, kRawTileBytes, &ctl.full[i], pol_w);
-                }
-            }
-            pdl_wait();
-            pdl_trigger();
-            int stage = 0;
-            uint32_t phase = 0, issued = 0, issued_par = 0;
-            bool ok = true;
-            i = 0;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile(args, tb, NB, t);
-                const int nbox = (ti.rows + 15) >> 4;
-                const bool big = nbox > 4;
-                const uint32_t a_bytes = big ? 16384u : (uint32_t)nbox * 2048u;
-                const uint8_t* wt = args.b_tiles +
-                                    ((size_t)ti.g * NB + ti.nb) * KB * (size_t)kRawTileBytes;
-                for (int kb = 0; kb < KB; ++kb, ++i) {
-                    uint8_t* st = stages + stage * kBf16StageBytes;
-                    if (i >= NS) {  // (the first NS stages were armed above)
-                        if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, ctl.abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&ctl.full[stage], a_bytes + (uint32_t)kRawTileBytes);
-                        bulk_load(st + kOffW, wt + (size_t)kb * kRawTileBytes, kRawTileBytes,
-                                  &ctl.full[stage], pol_w);
-                    }
-                    if (big) {
-                        tma_load_2d(st, &tmA, &ctl.full[stage], kb * 64, ti.arow0, pol_a);
-                    } else {
-                        for (int b = 0; b < nbox; ++b)
-                            tma_load_2d(st + b * 2048, &tmA16, &ctl.full[stage], kb * 64,
-                                        ti.arow0 + 16 * b, pol_a);
-                    }
-                    issued |= 1u << stage;
-                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == NS) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (!ok) {
-                set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
-                *ctl.abort_flag = 1;
-            }
-            for (int s = 0; s < NS; ++s)
-                if ((issued >> s) & 1u) mbar_wait(&ctl.full[s], (issued_par >> s) & 1u, ctl.zero);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(128, 128);
-            int stage = 0, it = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
-                const int buf = it & 1;
-                const uint32_t acc_par = (it >> 1) & 1;
-                if (!mbar_wait(&ctl.acc_empty[buf], acc_par ^ 1u, ctl.abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_t = tmem + buf * 128;
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&ctl.ready[stage], phase, ctl.abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    uint8_t* st = stages + stage * kBf16StageBytes;
-                    const uint64_t ad = sdesc_sw128(smem_u32(st));
-                    const uint64_t bd = sdesc_sw128(smem_u32(st + kOffB));
-                    for (int j = 0; j < 4; ++j)
-                        tc_mma_bf16(d_t, ad + 2 * j, bd + 2 * j, idesc, (kb | j) != 0);
-                    tc_commit(&ctl.empty[stage]);
-                    if (++stage == NS) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                tc_commit(&ctl.acc_full[buf]);
-            }
-            if (!ok) {
-                set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
-                *ctl.abort_flag = 1;
-            }
-            tc_commit(ctl.drain);
-            mbar_wait(ctl.drain, 0, ctl.zero);
-        }
-        __syncwarp();
-    } else if (warp < 6) {
-        const int q = warp & 3;
-        int it = 0, pp = 0;
-        pdl_wait();
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-            const TileInfo ti = decode_tile(args, tb, NB, t);
-            const EpiPrep ep = epi_prep<true>(args, ti, q, lane);
-            const int buf = it & 1;
-            const uint32_t acc_par = (it >> 1) & 1;
-            if (!warp_wait(&ctl.acc_full[buf], acc_par, ctl.abort_flag)) {
-                if (lane == 0) {
-                    set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
-                    *ctl.abort_flag = 1;
-                }
-                break;
-            }
-            tc_fence_after();
-            run_epilogue<true>(args, ti, ep, tmem + buf * 128, q, lane, &tmY,
-                             staging + (warp - 2) * 8192, pp);
-            tc_fence_before();
-            mbar_arrive(&ctl.acc_empty[buf]);
-        }
-        if (lane == 0) bulk_wait_all();  // staged stores complete before the CTA exits
-    } else {
-        // dequantisation: thread n converts weight row n of the stage (64 elements)
-        const int n = (warp - 6) * 32 + lane;
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-            for (int kb = 0; kb < KB; ++kb) {
-                if (!warp_wait(&ctl.full[stage], phase, ctl.abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* st = stages + stage * kBf16StageBytes;
-                const uint4 w0 = *reinterpret_cast<const uint4*>(st + kOffW + 32 * n);
-                const uint4 w1 = *reinterpret_cast<const uint4*>(st + kOffW + 32 * n + 16);
-                const uint32_t sw =
-                    *reinterpret_cast<const uint32_t*>(st + kOffSF + (n & 31) * 16 + (n >> 5) * 4);
-                const uint32_t by[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                uint8_t* dstrow = st + kOffB + n * 128;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {  // 8 elements (one 16-byte chunk) per step
-                    const float sv = e4m3_to_f32((sw >> (8 * (j >> 1))) & 0xFFu);
-                    uint32_t o[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float lo = e2m1_to_f32(by[j] >> (8 * i)) * sv;
-                        const float hi = e2m1_to_f32(by[j] >> (8 * i + 4)) * sv;
-                        const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
-                        o[i] = *reinterpret_cast<const uint32_t*>(&p);
-                    }
-                    *reinterpret_cast<uint4*>(dstrow + ((j ^ (n & 7)) << 4)) =
-                        make_uint4(o[0], o[1], o[2], o[3]);
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(&ctl.ready[stage]);
-                if (++stage == NS) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-        }
-        if (!ok && lane == 0) {
-            set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
-            *ctl.abort_flag = 1;
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, 256);
     }
 }
 

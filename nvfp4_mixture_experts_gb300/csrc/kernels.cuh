@@ -56,7 +56,7 @@ __global__ void combine_kernel(const float* y, const int32_t* inv, const int32_t
                                int shared_group, int T, int H, int k, int add_shared,
                                uint16_t* out);
 __global__ void repack_tiles_kernel(const uint8_t* codes, const uint8_t* sf, int nexp, int N,
-                                    int K, int interleave, int raw, uint8_t* dst);
+                                    int K, int interleave, int nibble_pairs, uint8_t* dst);
 
 // ---- gemm.cu
 enum GemmEpilogue : int {
@@ -87,23 +87,21 @@ struct GemmArgs {
     int Tk;                   // kEpiDown: first pair index of the shared rows (T*k)
     int stages;               // pipeline depth (<= kMaxStages; fits the shared memory)
     int staging;              // bytes of epilogue staging (kEpiDown: TMA stores of y), or 0
+    int raw_slots;            // W4A16: raw weight blobs in flight
     uint32_t* status;
 };
 
-// warp 0 TMA, warp 1 MMA, warps 2..5 epilogue, warps 6..9 scale factors (W4A4) or
-// weight dequantisation (W4A16)
+// W4A4: warp 0 TMA, warp 1 MMA, warps 2..5 epilogue, warps 6..9 scale factors
 constexpr int kNvf4Threads = 320;
-// Weight blob of one (expert, 128-row tile, k-stage):
-//   W4A4 : 128 rows x 128 bytes of codes (256 elements, 128-byte swizzled SMEM image)
-//          + 4 scale atoms of 512 bytes                                   = 18432 bytes
-//   W4A16: 128 rows x 32 bytes of codes (64 elements, row-major) + 1 atom =  4608 bytes
+// Weight blob of one (expert, 128-row tile, 256-element k-stage): 128 rows x 128 bytes of
+// codes (the 128-byte swizzled SMEM image) + 4 scale atoms of 512 bytes = 18432 bytes.
+// W4A16 blobs have the same image with the 8 codes of each 32-bit word in nibble order
+// 0,2,4,6,1,3,5,7 (the order its dequantisation unpacks in pairs).
 constexpr int kNvf4TileBytes = 16384 + 2048;
-constexpr int kRawTileBytes = 4096 + 512;
 constexpr int kMaxStages = 8;
 constexpr int kCtlBytes = 256;          // barriers for kMaxStages + TMEM slot + flags
 constexpr int kSmemLimit = 232448;      // dynamic shared memory per block (227 KB)
 constexpr int kNvf4StageBytes = 16384 + 16384 + 2048 + 2048;
-constexpr int kBf16StageBytes = 37888;   // A 16K + B 16K + raw FP4 4K + scales 512, padded to 1 KB
 constexpr int kDownStaging = 4 * 2 * 4096;  // 4 epilogue warps x 2 buffers x 32x32 fp32
 // Shared memory of a GEMM launch: stages, epilogue staging, 1 KB alignment slack, control
 // block, and the group tables (mb_start, counts, offsets).
@@ -117,13 +115,22 @@ inline int gemm_stages(int want, int stage_bytes, int staging, int G)
     while (s > 2 && gemm_smem_bytes(s, stage_bytes, staging, G) > kSmemLimit) --s;
     return s;
 }
-constexpr int kBf16Threads = 320;       // + 4 dequantisation warps
-
 __global__ void gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
                                  const __grid_constant__ CUtensorMap tmA16,
                                  const __grid_constant__ CUtensorMap tmY, GemmArgs args);
-__global__ void gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmA,
-                                  const __grid_constant__ CUtensorMap tmA16,
-                                  const __grid_constant__ CUtensorMap tmY, GemmArgs args);
+
+// ---- gemm_w4a16.cu: swap-AB weight stream, BN token rows per tile (16, 32 or 64)
+constexpr int kW16Threads = 480;        // 15 warps: see the kernel's role table
+constexpr int kW16MaxSlots = 8;         // raw blobs / work slots in flight at most
+// Shared memory: 1 KB alignment slack, raw blob ring, token tile ring, barriers and flags,
+// group tables (counts, offsets, first token block).
+inline int w4a16_smem_bytes(int raw_slots, int stages, int bn, int G)
+{
+    return 1024 + raw_slots * kNvf4TileBytes + stages * bn * 128 +
+           (2 * raw_slots + 3 * stages + 5) * 8 + 16 + 4 * (3 * G + 2);
+}
+// The kernel instantiated for BN = bn (16, 32 or 64).
+using W16Kernel = void (*)(CUtensorMap, GemmArgs);
+W16Kernel w4a16_kernel(int bn);
 
 }  // namespace moe

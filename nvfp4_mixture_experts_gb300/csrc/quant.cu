@@ -243,11 +243,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 // ---------------------------------------------------------------- weight re-layout
 //
 // Canonical codes [nexp][N][K/2] and scales [nexp][N][K/16] -> one contiguous blob per
-// (expert, 128-row tile nb, k-stage kb), the bytes a GEMM stage copies into shared memory:
-//   raw == 0 (W4A4, k-stage of 256): 128 rows x 128 code bytes in the 128-byte swizzled
-//     layout (byte c of row r at r*128 + ((c/16) ^ (r%8))*16 + c%16), then the 4 scale atoms
-//     of k-steps 4kb..4kb+3;
-//   raw == 1 (W4A16, k-stage of 64): 128 rows x 32 code bytes row-major, then 1 atom.
+// (expert, 128-row tile nb, 256-element k-stage kb), the bytes a GEMM stage copies into
+// shared memory: 128 rows x 128 code bytes in the 128-byte swizzled layout (byte c of row r
+// at r*128 + ((c/16) ^ (r%8))*16 + c%16), then the 4 scale atoms of k-steps 4kb..4kb+3.
+// With nibble_pairs (the W4A16 blobs) the 8 codes of each 32-bit word are stored in the
+// nibble order 0,2,4,6,1,3,5,7 instead of 0..7.
 // Scale atom byte (m%32)*16 + (m/32)*4 + kk holds scale kk of the k-step for tile row m.
 // Bytes past K (a partial last stage) are zero.  With interleave (the gate/up matrix,
 // N = 2I), tile row 128*nb + 32*c + 16*u + i holds source row u*I + 64*nb + 16*c + i, so
@@ -265,40 +265,43 @@ __device__ __forceinline__ int64_t src_row(int64_t r, int N, int interleave)
 __global__ void __launch_bounds__(256) repack_tiles_kernel(const uint8_t* __restrict__ codes,
                                                            const uint8_t* __restrict__ sf,
                                                            int nexp, int N, int K,
-                                                           int interleave, int raw,
+                                                           int interleave, int nibble_pairs,
                                                            uint8_t* __restrict__ dst)
 {
-    const int kst = raw ? 64 : 256;  // elements per k-stage
-    const int cb = kst / 2;          // code bytes per row per stage
-    const int nat = kst / 64;        // scale atoms per blob
-    const int tile = 128 * cb + 512 * nat;
-    const int NB = N / 128, KB = (K + kst - 1) / kst;
-    const int64_t total = (int64_t)nexp * NB * KB * tile;
+    const int KB = (K + 255) / 256, NB = N / 128;
+    const int64_t total = (int64_t)nexp * NB * KB * kNvf4TileBytes;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t blob = i / tile;
-        const int o = (int)(i % tile);
+        const int64_t blob = i / kNvf4TileBytes;
+        const int o = (int)(i % kNvf4TileBytes);
         const int kb = (int)(blob % KB);
         const int64_t en = blob / KB;
         const int nb = (int)(en % NB);
         const int64_t e = en / NB;
         uint8_t v = 0;
-        if (o < 128 * cb) {
-            int r, c;
-            if (raw) {
-                r = o / cb;
-                c = o % cb;
-            } else {
-                r = o >> 7;
-                c = ((((o >> 4) & 7) ^ (r & 7)) << 4) | (o & 15);
+        if (o < 16384) {
+            const int r = o >> 7;
+            const int c = ((((o >> 4) & 7) ^ (r & 7)) << 4) | (o & 15);  // byte of the row
+            const uint8_t* row =
+                codes + (e * N + src_row(nb * 128 + r, N, interleave)) * (int64_t)(K / 2);
+            const int kbyte = kb * 128 + c;
+            if (!nibble_pairs) {
+                if (kbyte < K / 2) v = row[kbyte];
+            } else if (kbyte < K / 2) {
+                // byte b of a word holds nibbles 2b, 2b + 1; nibble n holds element
+                // n < 4 ? 2n : 2(n - 4) + 1 of the word's eight
+                const int b = c & 3, w0 = kbyte - b;  // first byte of the word
+                const int n0 = 2 * b, n1 = 2 * b + 1;
+                const int e0 = n0 < 4 ? 2 * n0 : 2 * (n0 - 4) + 1;
+                const int e1 = n1 < 4 ? 2 * n1 : 2 * (n1 - 4) + 1;
+                const uint32_t lo = (row[w0 + (e0 >> 1)] >> (4 * (e0 & 1))) & 15u;
+                const uint32_t hi = (row[w0 + (e1 >> 1)] >> (4 * (e1 & 1))) & 15u;
+                v = (uint8_t)(lo | (hi << 4));
             }
-            const int kbyte = kb * cb + c;
-            if (kbyte < K / 2)
-                v = codes[(e * N + src_row(nb * 128 + r, N, interleave)) * (K / 2) + kbyte];
         } else {
-            const int a = (o - 128 * cb) / 512, w = (o - 128 * cb) % 512;
+            const int a = (o - 16384) / 512, w = (o - 16384) % 512;
             const int m = (w >> 4) + 32 * ((w & 15) >> 2), kk = w & 3;
-            const int step = kb * nat + a;
+            const int step = kb * 4 + a;
             if (step < K / 64)
                 v = sf[(e * N + src_row(nb * 128 + m, N, interleave)) * (K / 16) + step * 4 + kk];
         }
