@@ -184,8 +184,10 @@ MOE_API moe_status moe_quant_nvfp4(const void* x_bf16_d, int32_t rows, int32_t c
 
 /* Gather-quantise: NVFP4-quantise the T rows of x with gs (dynamic or static per the
  * handle's act_mode) and write row t to every padded row of its local pairs and to its
- * shared row, in the tiled layout (W4A4).  W4A16: copy the bf16 rows instead
- * (a_bf16_d [rows_capacity][H]).  gs_out_d receives the scale used (W4A4). */
+ * shared row, in the tiled layout (W4A4).  W4A16: write fp16(x * gs) instead
+ * (a_bf16_d [rows_capacity][H] fp16), gs = 2^(141 - e) for e the exponent field of
+ * amax|x| (clamped to 2^[-126, 127]), so |x * gs| <= 2^15 and every x above amax * 2^-29
+ * converts exactly.  gs_out_d receives the scale used (both modes). */
 MOE_API moe_status moe_gather_activations(moe_handle h, const void* x_bf16_d, int32_t T,
                                   const int32_t* inv_d, const int32_t* expert_offsets_d,
                                   uint8_t* a_codes_d, uint8_t* a_sf_d, void* a_bf16_d,
@@ -193,7 +195,8 @@ MOE_API moe_status moe_gather_activations(moe_handle h, const void* x_bf16_d, in
                                   moe_stream_t stream);
 
 /* Grouped GEMM gate_up over the padded rows: for group g with expert weights W13_g,
- * G = A_g . W13_g^T / (gs_a * gs13_g) (W4A4; W4A16: A_g . W13_g^T / gs13_g).
+ * G = A_g . W13_g^T / (gs_a * gs13_g), A_g the NVFP4 rows (W4A4) or the fp16 rows of
+ * moe_gather_activations (W4A16, gs_a its fp16 prescale).
  *   fuse_epilogue 0: gateup_f32_d [rows_capacity][2I] fp32 (gate cols 0..I-1, up I..2I-1)
  *   fuse_epilogue 1: s = silu(gate) * up, then
  *       W4A4 : NVFP4 with inter_global_scale -> inter_codes_d / inter_sf_d (tiled, K = I)

@@ -169,6 +169,17 @@ struct moe_layer {
 
 namespace {
 
+bool set_w4a16_smem_limits()
+{
+    for (int bn : {16, 32, 64})
+        for (bool f16 : {false, true})
+            if (cudaFuncSetAttribute(w4a16_kernel(bn, f16),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemLimit) != cudaSuccess)
+                return false;
+    return true;
+}
+
 // Bytes of the weight blobs of one expert slot for an N x K matrix.
 size_t blob_bytes(int N, int K)
 {
@@ -292,15 +303,10 @@ moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T
     const moe_config& c = h->cfg;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     const int add = shared_rows(h, T) > 0 ? 1 : 0;
-    if (c.act_mode == MOE_W4A16)
-        return launch(gather_bf16_kernel,
-                      dim3(grid_for((int64_t)T * ((c.hidden + 255) / 256) * 32, 256)), dim3(256),
-                      0, s, pdl, xb, T, c.hidden, c.top_k, inv, offsets, p.El, add,
-                      static_cast<uint16_t*>(a_bf16));
     const dim3 grid(grid_for((int64_t)T * ((c.hidden / 16 + 31) / 32) * 32, 256));
     uint32_t* amax = at<uint32_t>(ws, p.amax);
     const float* gs_static = nullptr;
-    if (c.act_mode == MOE_W4A4_DYNAMIC) {
+    if (c.act_mode != MOE_W4A4_STATIC) {
         if (!amax_zeroed && cudaMemsetAsync(amax, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
         const int64_t n = (int64_t)T * c.hidden;
         const int blocks = (int)std::min<int64_t>(2 * h->num_sms, std::max<int64_t>(1, n / 2048));
@@ -310,6 +316,11 @@ moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T
     } else {
         gs_static = h->act_gs;  // the handle's device copy of act_global_scale
     }
+    if (c.act_mode == MOE_W4A16)
+        return launch(gather_f16_kernel,
+                      dim3(grid_for((int64_t)T * ((c.hidden + 255) / 256) * 32, 256)), dim3(256),
+                      0, s, pdl, xb, T, c.hidden, c.top_k, inv, offsets, p.El, add,
+                      (const uint32_t*)amax, static_cast<uint16_t*>(a_bf16), gs_out);
     return launch(gather_quant_kernel, grid, dim3(256), 0, s, pdl, xb, T, c.hidden, c.top_k, inv,
                   offsets, p.El, add, gs_static, (const uint32_t*)amax, a_codes, a_sf, gs_out);
 }
@@ -352,19 +363,29 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
         // token tile (re-read for every weight tile) small when experts see few tokens.
         const int64_t local_rows = (int64_t)p.T * c.top_k / std::max(1, c.num_local_experts);
         const int bn = local_rows <= 16 ? 16 : local_rows <= 32 ? 32 : 64;
-        args.stages = kW16MaxSlots;
-        args.raw_slots = kW16MaxSlots;
-        while (args.raw_slots > 2 &&
-               w4a16_smem_bytes(args.raw_slots, args.stages, bn, p.G) > kSmemLimit)
-            --args.raw_slots;
+        // shared memory split between raw weight blobs and token tiles, both rings kept
+        // at least 4 blobs deep
+        args.raw_slots = kW16MaxRaw;
+        args.stages = kW16MaxB;
+        while (w4a16_smem_bytes(args.raw_slots, args.stages, bn, p.G) > kSmemLimit &&
+               (args.raw_slots > 4 || args.stages > 4)) {
+            if (args.stages * 4 * bn * 128 >= args.raw_slots * kNvf4TileBytes && args.stages > 4)
+                --args.stages;
+            else if (args.raw_slots > 4)
+                --args.raw_slots;
+            else
+                --args.stages;
+        }
         const int smem = w4a16_smem_bytes(args.raw_slots, args.stages, bn, p.G);
         if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
+        // gate_up reads the fp16 activation rows (x * gs_a), down the bf16 intermediate
         CUtensorMap tmB;
-        if (!make_tmap(&tmB, a_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, p.cap, (uint64_t)K * 2,
-                       64, bn, CU_TENSOR_MAP_SWIZZLE_128B))
+        if (!make_tmap(&tmB, a_bf16,
+                       gateup ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                       K, p.cap, (uint64_t)K * 2, 64, bn, CU_TENSOR_MAP_SWIZZLE_128B))
             return MOE_ERR_CUDA;
-        return launch(w4a16_kernel(bn), dim3(gemm_grid(h, p.T, N, bn)), dim3(kW16Threads), smem,
-                      s, pdl, tmB, args);
+        return launch(w4a16_kernel(bn, gateup), dim3(gemm_grid(h, p.T, N, bn)),
+                      dim3(kW16Threads), smem, s, pdl, tmB, args);
     }
     CUtensorMap tmA, tmA16, tmY;
     memset(&tmY, 0, sizeof(tmY));
@@ -514,7 +535,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
         return MOE_ERR_CUDA;
     }
     const int G = El + 1;
-    const int pairs = cfg->act_mode == MOE_W4A16 ? 1 : 0;  // W4A16 nibble order
+    const int pairs = cfg->act_mode == MOE_W4A16 ? 1 : 0;  // W4A16 down: nibble order
     const size_t b13 = blob_bytes(2 * I, H), b2 = blob_bytes(H, I);
     bool ok = cudaMalloc(&h->router_w, (size_t)cfg->num_experts * H * 2) == cudaSuccess &&
               cudaMalloc(&h->w13, G * b13) == cudaSuccess &&
@@ -532,7 +553,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
                                cudaMemcpyDeviceToDevice, s) == cudaSuccess;
     const int blocks = 8 * h->num_sms;
     if (ok && El > 0) {
-        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->w13_d, w->w13_sf_d, El, 2 * I, H, 1, pairs,
+        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->w13_d, w->w13_sf_d, El, 2 * I, H, 1, 0,
                                                    h->w13);
         repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->w2_d, w->w2_sf_d, El, H, I, 0, pairs, h->w2);
         ok = cudaMemcpyAsync(h->gs13, w->w13_gs_d, El * 4, cudaMemcpyDeviceToDevice, s) ==
@@ -541,7 +562,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
                  cudaSuccess;
     }
     if (ok && cfg->has_shared) {
-        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->sh13_d, w->sh13_sf_d, 1, 2 * I, H, 1, pairs,
+        repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->sh13_d, w->sh13_sf_d, 1, 2 * I, H, 1, 0,
                                                    h->w13 + (size_t)El * b13);
         repack_tiles_kernel<<<blocks, 256, 0, s>>>(w->sh2_d, w->sh2_sf_d, 1, H, I, 0, pairs,
                                                    h->w2 + (size_t)El * b2);
@@ -560,12 +581,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
                               kRouterSmem) == cudaSuccess &&
          cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemLimit) == cudaSuccess &&
-         cudaFuncSetAttribute(w4a16_kernel(16), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemLimit) == cudaSuccess &&
-         cudaFuncSetAttribute(w4a16_kernel(32), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemLimit) == cudaSuccess &&
-         cudaFuncSetAttribute(w4a16_kernel(64), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemLimit) == cudaSuccess;
+         set_w4a16_smem_limits();
     if (!ok) {
         cudaGetLastError();
         moe_destroy(h);

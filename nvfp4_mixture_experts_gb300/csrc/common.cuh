@@ -86,18 +86,49 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may stay suspended up to kSuspendHintNs while the phase
+// is incomplete (it resumes as soon as the phase completes), so a waiting warp takes no
+// issue slots from the warps doing the work.
+constexpr uint32_t kSuspendHintNs = 1000000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false if the wait ran
 // longer than kWaitLimitNs or if *abort became nonzero (another warp gave up).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    for (uint32_t i = 0;; ++i) {
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// mbar_wait for a waiter off the critical path (a producer far ahead, an epilogue waiting
+// for a whole tile): between polls the thread sleeps sleep_ns, leaving the issue slots to
+// the warps doing the work.
+__device__ __forceinline__ bool mbar_wait_lazy(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort, uint32_t sleep_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        __nanosleep(sleep_ns);
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255) == 255) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) return false;
-        }
+        if (*abort) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
     }
 }
 

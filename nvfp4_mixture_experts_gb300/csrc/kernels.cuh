@@ -44,9 +44,9 @@ __global__ void gather_quant_kernel(const uint16_t* x, int T, int H, int k, cons
                                     const int32_t* offsets, int shared_group, int add_shared,
                                     const float* gs_static, const uint32_t* amax_bits,
                                     uint8_t* codes, uint8_t* sf, float* gs_out);
-__global__ void gather_bf16_kernel(const uint16_t* x, int T, int H, int k, const int32_t* inv,
-                                   const int32_t* offsets, int shared_group, int add_shared,
-                                   uint16_t* out);
+__global__ void gather_f16_kernel(const uint16_t* x, int T, int H, int k, const int32_t* inv,
+                                  const int32_t* offsets, int shared_group, int add_shared,
+                                  const uint32_t* amax_bits, uint16_t* out, float* gs_out);
 __global__ void quant_rows_kernel(const uint16_t* x, int rows, int cols, const float* gs_static,
                                   const uint32_t* amax_bits, uint8_t* codes, uint8_t* sf,
                                   int layout, float* gs_out);
@@ -121,16 +121,18 @@ __global__ void gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
 
 // ---- gemm_w4a16.cu: swap-AB weight stream, BN token rows per tile (16, 32 or 64)
 constexpr int kW16Threads = 480;        // 15 warps: see the kernel's role table
-constexpr int kW16MaxSlots = 8;         // raw blobs / work slots in flight at most
-// Shared memory: 1 KB alignment slack, raw blob ring, token tile ring, barriers and flags,
+constexpr int kW16MaxRaw = 8;           // raw blobs in flight at most
+constexpr int kW16MaxB = 8;             // token-tile slots (one blob's k-range each) at most
+// Shared memory: 1 KB alignment slack, raw blob ring, token-tile ring, barriers and flags,
 // group tables (counts, offsets, first token block).
-inline int w4a16_smem_bytes(int raw_slots, int stages, int bn, int G)
+inline int w4a16_smem_bytes(int raw_slots, int b_slots, int bn, int G)
 {
-    return 1024 + raw_slots * kNvf4TileBytes + stages * bn * 128 +
-           (2 * raw_slots + 3 * stages + 5) * 8 + 16 + 4 * (3 * G + 2);
+    return 1024 + raw_slots * kNvf4TileBytes + b_slots * 4 * bn * 128 +
+           (2 * raw_slots + 2 * b_slots + 2 * 3 + 5) * 8 + 16 + 4 * (3 * G + 2);
 }
-// The kernel instantiated for BN = bn (16, 32 or 64).
+// The kernel instantiated for BN = bn (16, 32 or 64) token rows per tile, with fp16 operands
+// (gate_up: prescaled fp16 activations) or bf16 operands (down: the bf16 intermediate).
 using W16Kernel = void (*)(CUtensorMap, GemmArgs);
-W16Kernel w4a16_kernel(int bn);
+W16Kernel w4a16_kernel(int bn, bool f16);
 
 }  // namespace moe

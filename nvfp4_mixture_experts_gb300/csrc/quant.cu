@@ -6,6 +6,8 @@
 // E2M1 codes, one E4M3 scale per 16 consecutive elements, value = code * scale / gs.
 #include <cuda_bf16.h>
 
+#include <cuda_fp16.h>
+
 #include "kernels.cuh"
 
 namespace moe {
@@ -130,13 +132,27 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(
 
 // W4A16: copy token rows (bf16) to the padded rows of their pairs and shared row; a warp
 // copies 256 elements of one token.
-__global__ void __launch_bounds__(256) gather_bf16_kernel(
+// W4A16 activation rows: x (bf16) times the power of two gs = 2^(141 - exponent field of
+// amax(x)), clamped to 2^[-126, 127], rounded to fp16.  amax <= 2^(e - 126) for exponent
+// field e, so |x * gs| <= 2^15 < 65504 and every bf16 value x with |x * gs| >= 2^-14 (all but
+// values below amax * 2^-29) converts exactly; the GEMM divides by gs in its epilogue.
+__device__ __forceinline__ float f16_prescale(const uint32_t* amax_bits)
+{
+    const int e = (int)((*amax_bits >> 23) & 0xFFu);
+    if (*amax_bits == 0u) return 1.0f;
+    const int p = min(127, max(-126, 141 - e));
+    return __uint_as_float((uint32_t)(p + 127) << 23);
+}
+
+__global__ void __launch_bounds__(256) gather_f16_kernel(
     const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, int shared_group, int add_shared,
-    uint16_t* __restrict__ out)
+    const uint32_t* amax_bits, uint16_t* __restrict__ out, float* gs_out)
 {
     pdl_wait();
     if (threadIdx.x == 0) pdl_trigger();
+    const float gs = f16_prescale(amax_bits);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && gs_out) *gs_out = gs;
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int wpt = (H + 255) / 256;
@@ -146,7 +162,16 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(
     const int nd = token_destinations(inv, offsets, t, k, shared_group, add_shared, dst);
     if (c >= H) return;
     const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c);
-    for (int d = 0; d < nd; ++d) *reinterpret_cast<uint4*>(out + (size_t)dst[d] * H + c) = v;
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(__fmul_rn(bf16_bits_to_f32(in[i] & 0xFFFFu), gs),
+                                            __fmul_rn(bf16_bits_to_f32(in[i] >> 16), gs));
+        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    for (int d = 0; d < nd; ++d)
+        *reinterpret_cast<uint4*>(out + (size_t)dst[d] * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // ---------------------------------------------------------------- standalone quantiser

@@ -249,6 +249,30 @@ def _mid_problem(act_mode, T=200):
     return layer, wr, x, lg, h, (H, I, E, k, T)
 
 
+def _f16_prescale(x_bits):
+    """The W4A16 activation prescale as the header states it: 2^(141 - e) for e the fp32
+    exponent field of amax|x|, clamped to 2^[-126, 127] (1 for an all-zero x)."""
+    amax = np.max(np.abs(synth.bf16_to_f32(x_bits).astype(np.float32)))
+    if amax == 0:
+        return np.float32(1.0)
+    e = int(np.float32(amax).view(np.uint32) >> 23) & 0xFF
+    return np.float32(2.0) ** np.float32(min(127, max(-126, 141 - e)))
+
+
+@pytest.mark.parametrize("scale", [1.0, 3e-6, 5e4])
+def test_gather_w4a16_rows_are_exact_fp16_copies(scale):
+    layer, wr, x, lg, h, (H, I, E, k, T) = _mid_problem(2, 60)
+    xs = synth.bf16_bits(synth.bf16_to_f32(x).astype(np.float64) * scale)
+    st = Staged(h, bits16(xs), T, k, lg)
+    gs = _f16_prescale(xs)
+    assert host(st.gs)[0] == gs
+    rows = st.rows()
+    got = host(st.a_bf16).view(np.uint16).reshape(st.cap, H)[rows[:, 0]]
+    want = (synth.bf16_to_f32(xs)[rows[:, 1]].astype(np.float32) * gs).astype(np.float16)
+    assert np.array_equal(got, want.view(np.uint16))
+    assert np.max(np.abs(want.astype(np.float32))) <= 2.0 ** 15
+
+
 # W4A16 picks 16, 32 or 64 token rows per tile from T * k / E (here 15, 25 and 50 rows)
 @pytest.mark.parametrize("act_mode,T", [(0, 200), (2, 60), (2, 100), (2, 200)])
 def test_grouped_gemm_gateup_unfused_matches_oracle(act_mode, T):
