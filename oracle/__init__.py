@@ -64,8 +64,8 @@ def load():
                                         C.c_void_p, C.POINTER(Expert), C.c_void_p, C.c_long,
                                         C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                         C.c_void_p, C.POINTER(C.c_long), C.c_void_p,
-                                        C.c_void_p, C.POINTER(C.c_float), C.c_void_p,
-                                        C.c_void_p]
+                                        C.c_void_p, C.POINTER(C.c_float),
+                                        C.POINTER(C.c_float), C.c_void_p, C.c_void_p]
         lib.orc_num_threads.restype = C.c_int
         lib.orc_set_num_threads.argtypes = [C.c_int]
         _lib = lib
@@ -289,6 +289,7 @@ def moe_forward(cfg, x_bf16, layer, router_w=None, logit_bias=None, logits_in=No
     else:
         r.x_codes = r.x_sf = None
     gs = C.c_float(0.0)
+    gs_i = C.c_float(0.0)
     r.out = np.empty((nt, H), np.float64)
     r.out_bf16 = np.empty((nt, H), np.uint16)
     experts = layer.experts()
@@ -296,8 +297,9 @@ def moe_forward(cfg, x_bf16, layer, router_w=None, logit_bias=None, logits_in=No
                            _p(_c(logit_bias, np.float32)), _p(_c(logits_in, np.float32)),
                            experts, _p(tok), nt, _p(r.logits), _p(r.ids), _p(r.w),
                            _p(r.counts), _p(pairs), C.byref(n_local), _p(r.x_codes),
-                           _p(r.x_sf), C.byref(gs), _p(r.out), _p(r.out_bf16))
+                           _p(r.x_sf), C.byref(gs), C.byref(gs_i), _p(r.out), _p(r.out_bf16))
     r.pairs = pairs[:n_local.value].copy()
     r.gs_a = gs.value
+    r.gs_i = gs_i.value
     r.tokens = np.arange(T, dtype=np.int32) if tok is None else tok
     return r

@@ -27,7 +27,9 @@
  *   - the shared expert has weight 1 and is added by the shard that sets add_shared;
  *   - dynamic activation scale: one FP32 scale for the whole [T,H] input,
  *     gs = 2688 / amax (2688 = 448 * 6);
- *   - the intermediate (post-SwiGLU) tensor is requantised with a static global scale;
+ *   - the intermediate (post-SwiGLU) tensor is requantised with a static global scale,
+ *     or, when the configured scale is <= 0, with the dynamic one 2688 / amax over every
+ *     intermediate row the shard computes (two passes);
  *   - the permutation groups pairs by local expert and keeps ascending pair index
  *     p = t*k + j inside an expert.
  *
@@ -323,7 +325,8 @@ typedef struct {
     int has_shared, add_shared;
     int act_mode;        /* 0: W4A4 dynamic activation scale, 1: W4A4 static, 2: W4A16 */
     float act_gs;        /* static activation global scale (act_mode 1) */
-    float inter_gs;      /* static intermediate global scale (W4A4) */
+    float inter_gs;      /* intermediate global scale (W4A4): static if > 0, else computed
+                            per call from the intermediate's amax (dynamic) */
 } orc_cfg;
 
 /* One expert's weights, canonical layout (rows of the output dimension, K packed):
@@ -370,9 +373,9 @@ static void row_gateup(const orc_cfg* c, const double* a, double a_div, const or
 
 /* Intermediate activation of one row from its gate/up values and its down-projection
  * input (fp64 values without global scale plus the divisor that restores it):
- *   W4A4 : s = silu(g)*u rounded to fp32, NVFP4-quantised with the static scale gs_i
+ *   W4A4 : s = silu(g)*u rounded to fp32, NVFP4-quantised with the global scale gs_i
  *   W4A16: s rounded to bf16 */
-static double row_inter(const orc_cfg* c, const double* G, double* s64, float* s32,
+static double row_inter(const orc_cfg* c, const double* G, float gs_i, double* s64, float* s32,
                         uint8_t* qc, uint8_t* qsf, double* aq)
 {
     int i;
@@ -382,12 +385,9 @@ static double row_inter(const orc_cfg* c, const double* G, double* s64, float* s
         return 1.0;
     }
     for (i = 0; i < c->I; i++) s32[i] = (float)s64[i];
-    {
-        float gs_i = c->inter_gs;
-        orc_quant_nvfp4(s32, 1, c->I, 0, &gs_i, qc, qsf);
-    }
+    orc_quant_nvfp4(s32, 1, c->I, 0, &gs_i, qc, qsf);
     for (i = 0; i < c->I; i++) aq[i] = nvfp4_elem(qc, qsf, c->I, 0, i);
-    return (double)c->inter_gs;
+    return (double)gs_i;
 }
 
 /* Down projection: Y[h] = (sum_i aq[i] * w2[h][i]) / (inter_div * gs2). */
@@ -444,7 +444,7 @@ void orc_expert_rows(const orc_cfg* c, const orc_expert* ex, const uint16_t* x,
         input_row(c, x, xc, xsf, tok[r], a);
         row_gateup(c, a, a_div, ex, &d, G);
         if (G_out) memcpy(G_out + r * 2L * c->I, G, sizeof(double) * 2 * c->I);
-        i_div = row_inter(c, G, s64, s32, qc, qsf, aq);
+        i_div = row_inter(c, G, c->inter_gs, s64, s32, qc, qsf, aq);
         if (inter_codes && c->act_mode != 2) {
             memcpy(inter_codes + r * (long)(c->I / 2), qc, c->I / 2);
             memcpy(inter_sf + r * (long)(c->I / 16), qsf, c->I / 16);
@@ -483,6 +483,52 @@ void orc_swiglu_requant(const float* gu, long R, int I, float gs_i,
 /* Whole layer                                                                */
 /* ------------------------------------------------------------------------- */
 
+/* Dynamic intermediate global scale (W4A4 with inter_gs <= 0): 2688 / amax of the fp32
+ * intermediate s = silu(g)*u over every row the shard computes -- its local pairs of all
+ * T tokens and, with add_shared, every token's shared-expert row -- by the same formula as
+ * the dynamic activation scale (1 if that amax is 0).  A first pass over the gate/up
+ * projections; the forward then quantises each row's s with this scale. */
+static float dynamic_inter_scale(const orc_cfg* c, const uint16_t* x, const uint8_t* xc,
+                                 const uint8_t* xsf, float gs_a, const int32_t* ids,
+                                 const orc_expert* ex)
+{
+    const long T = c->T;
+    const int El = c->E_loc, k = c->k;
+    float amax = 0.0f;
+    int e;
+#pragma omp parallel for schedule(dynamic, 1) reduction(max : amax)
+    for (e = 0; e <= El; e++) {
+        orc_expert_f64 d;
+        double *a, *G;
+        long p, n_rows = (e == El) ? T : T * k;
+        int used = 0, i;
+        if (e == El && !(c->has_shared && c->add_shared)) continue;
+        if (e == El) used = T > 0;
+        for (p = 0; p < T * k && !used; p++)
+            if (ids[p] - c->off == e) used = 1;
+        if (!used) continue;
+        d.w13 = (double*)malloc(sizeof(double) * 2L * c->I * c->H);
+        d.w2 = (double*)malloc(sizeof(double) * (long)c->H * c->I);
+        expert_dequant(c, &ex[e], &d);
+        a = (double*)malloc(sizeof(double) * c->H);
+        G = (double*)malloc(sizeof(double) * 2 * c->I);
+        for (p = 0; p < n_rows; p++) {
+            const long tt = (e == El) ? p : p / k;
+            if (e != El && ids[p] - c->off != e) continue;
+            input_row(c, x, xc, xsf, tt, a);
+            row_gateup(c, a, (double)gs_a, &ex[e], &d, G);
+            for (i = 0; i < c->I; i++) {
+                const float v = fabsf((float)swiglu(G[i], G[c->I + i]));
+                if (v > amax) amax = v;
+            }
+        }
+        free(a); free(G);
+        free(d.w13);
+        free(d.w2);
+    }
+    return orc_dynamic_global_scale(&amax, 1);
+}
+
 /* Forward of the layer (or of one expert shard of it).
  *
  * Inputs: x bf16 [T][H]; the router either from x (router_w bf16 [E][H]) or from given
@@ -490,7 +536,8 @@ void orc_swiglu_requant(const float* gu, long R, int I, float gs_i,
  * weights ex[0..E_loc-1] (ex[E_loc] is the shared expert when has_shared).
  * Outputs for every token: logits (fp64, may be NULL), top-k ids and weights, the local
  * counts and grouped pair list (may be NULL), the activation codes/sf/gs (W4A4, may be
- * NULL).  Outputs for the tokens listed in tok[0..n_tok-1] (all tokens when tok is
+ * NULL), the intermediate global scale used (W4A4; the static one, or the dynamic one of
+ * dynamic_inter_scale when cfg.inter_gs <= 0; may be NULL).  Outputs for the tokens listed in tok[0..n_tok-1] (all tokens when tok is
  * NULL): out[n_tok][H] in fp64 and out_bf16 (may be NULL), the final values rounded to
  * bf16.
  *
@@ -502,7 +549,7 @@ int orc_moe_forward(const orc_cfg* c, const uint16_t* x, const uint16_t* router_
                     const int32_t* tok, long n_tok,
                     double* logits_out, int32_t* topk_ids, double* topk_w,
                     int32_t* counts, int32_t* sorted_pairs, long* n_local,
-                    uint8_t* x_codes, uint8_t* x_sf, float* gs_a_out,
+                    uint8_t* x_codes, uint8_t* x_sf, float* gs_a_out, float* gs_i_out,
                     double* out, uint16_t* out_bf16)
 {
     const long T = c->T;
@@ -513,6 +560,7 @@ int orc_moe_forward(const orc_cfg* c, const uint16_t* x, const uint16_t* router_
     uint8_t* xc = NULL;
     uint8_t* xsf = NULL;
     float gs_a = 1.0f;
+    float gs_i = c->inter_gs;
     long t, i, nt = tok ? n_tok : T;
     int* row_of_tok = (int*)malloc(sizeof(int) * T);
     double* Yr;   /* [nt][k][H] routed outputs (unweighted) */
@@ -547,7 +595,9 @@ int orc_moe_forward(const orc_cfg* c, const uint16_t* x, const uint16_t* router_
         orc_quant_nvfp4(xf, T, H, c->act_mode == 0, &gs_a, xc, xsf);
         if (gs_a_out) *gs_a_out = gs_a;
         free(xf);
+        if (!(c->inter_gs > 0.0f)) gs_i = dynamic_inter_scale(c, x, xc, xsf, gs_a, ids, ex);
     }
+    if (gs_i_out) *gs_i_out = gs_i;
 
     /* a5..a8: expert MLPs for the requested tokens */
     for (t = 0; t < T; t++) row_of_tok[t] = -1;
@@ -589,7 +639,7 @@ int orc_moe_forward(const orc_cfg* c, const uint16_t* x, const uint16_t* router_
             if (e != El && ids[p] - c->off != e) continue;
             input_row(c, x, xc, xsf, tt, a);
             row_gateup(c, a, c->act_mode == 2 ? 1.0 : (double)gs_a, &ex[e], &d, G);
-            i_div = row_inter(c, G, s64, s32, qc, qsf, aq);
+            i_div = row_inter(c, G, gs_i, s64, s32, qc, qsf, aq);
             Y = (e == El) ? Ys + r * (long)H : Yr + (r * k + p % k) * (long)H;
             row_down(c, aq, i_div, &ex[e], &d, Y);
             if (e != El) have[r * k + p % k] = 1;

@@ -230,3 +230,65 @@ def test_layer_facts_of_the_pages():
         assert c["E"] == facts["routed_experts"] and c["k"] == facts["top_k"]
     lo, hi = facts["shards"][1]
     assert synth.CONFIGS["shard"]["off"] == lo and synth.CONFIGS["shard"]["E_loc"] == hi - lo + 1
+
+
+def _numpy_dynamic_inter_scale(cfg, x, wr, layer):
+    """2688 / amax|fp32(s)| over every row a shard computes (its local pairs of all tokens,
+    plus the shared rows when it adds the shared expert), from numpy matmuls over
+    independently dequantised weights; 1 when there is no such row (or amax is 0)."""
+    T, I, k = cfg.T, cfg.I, cfg.k
+    lg = synth.bf16_to_f32(x).astype(np.float64) @ synth.bf16_to_f32(wr).astype(np.float64).T
+    ids = _lexsort_topk(lg, k)
+    xc, xsf, gs_a = oracle.quant_nvfp4(synth.bf16_to_f32(x))
+    a = dequant_independent(xc, xsf, 1.0)
+    amax = np.float32(0.0)
+    for le in range(cfg.E_loc):
+        rows = [t for t in range(T) for j in range(k) if ids[t, j] - cfg.off == le]
+        if not rows:
+            continue
+        w13d = dequant_independent(layer.w13[le], layer.w13_sf[le], layer.w13_gs[le])
+        G = (a[rows] @ w13d.T) / gs_a
+        s = (G[:, :I] * expit(G[:, :I]) * G[:, I:]).astype(np.float32)
+        amax = max(amax, np.abs(s).max())
+    if cfg.has_shared and cfg.add_shared:
+        w13d = dequant_independent(layer.sh13, layer.sh13_sf, layer.sh13_gs)
+        G = (a @ w13d.T) / gs_a
+        s = (G[:, :I] * expit(G[:, :I]) * G[:, I:]).astype(np.float32)
+        amax = max(amax, np.abs(s).max())
+    return np.float32(1.0) if amax == 0 else np.float32(2688.0) / np.float32(amax)
+
+
+@pytest.mark.parametrize("E_loc,off,add_shared", [(6, 0, 1), (3, 3, 0), (3, 0, 1)])
+def test_dynamic_intermediate_scale_is_the_amax_of_the_shards_rows(E_loc, off, add_shared):
+    """inter_gs <= 0 (dynamic): the scale is 2688 / amax of the fp32 intermediate over the
+    shard's own rows, and the forward equals the static forward at that scale."""
+    H, I, E, k, T = 128, 64, 6, 2, 10
+    full = build_layer(31, H, I, E)
+    layer = slice_layer(full, off, off + E_loc)
+    wr = synth.router_weight(31, E, H)
+    x = synth.activations(31, T, H)
+    cfg = oracle.make_cfg(T, H, I, E, k, E_loc=E_loc, off=off, add_shared=add_shared,
+                          inter_gs=0.0)
+    dyn = oracle.moe_forward(cfg, x, layer, router_w=wr)
+    want = _numpy_dynamic_inter_scale(cfg, x, wr, layer)
+    assert abs(dyn.gs_i - float(want)) <= 1e-6 * float(want)
+    cfg_s = oracle.make_cfg(T, H, I, E, k, E_loc=E_loc, off=off, add_shared=add_shared,
+                            inter_gs=dyn.gs_i)
+    sta = oracle.moe_forward(cfg_s, x, layer, router_w=wr)
+    assert sta.gs_i == dyn.gs_i
+    assert np.array_equal(sta.out, dyn.out)
+
+
+def test_dynamic_intermediate_scale_matches_dense_mixture():
+    """Whole layer with the dynamic intermediate scale against the dense all-experts
+    mixture (numpy) quantising the intermediate with the numpy-derived scale."""
+    H, I, E, k, T = 128, 64, 4, 2, 8
+    layer = build_layer(32, H, I, E)
+    wr = synth.router_weight(32, E, H)
+    x = synth.activations(32, T, H)
+    cfg = oracle.make_cfg(T, H, I, E, k, inter_gs=0.0)
+    got = oracle.moe_forward(cfg, x, layer, router_w=wr)
+    gs_i = float(_numpy_dynamic_inter_scale(cfg, x, wr, layer))
+    ref, ids = _dense_mixture(cfg, x, wr, layer, gs_i)
+    assert np.array_equal(np.sort(got.ids, 1), np.sort(ids, 1))
+    np.testing.assert_allclose(got.out, ref, rtol=1e-9, atol=1e-9 * np.abs(ref).max())
