@@ -164,6 +164,7 @@ def gpu_layer(name, seed=0, extra_handles=(), local_experts=0):
         cc = synth.CONFIGS[nm]
         cfg = moe.make_config(H, I, E, k, E_loc=El, off=c["off"], has_shared=1,
                               add_shared=cc["add_shared"], act_mode=cc["act_mode"],
+                              act_gs=INTER[nm].get("act_global_scale", 0.0),
                               inter_gs=INTER[nm]["inter_global_scale"],
                               max_tokens=cc["T"])
         handles[nm] = moe.MoELayer(cfg, w)
@@ -207,7 +208,8 @@ def launches_per_forward(c):
 
 def gemm_bytes(c, counts, gateup):
     """Algorithmic bytes of one grouped-GEMM launch: the weights of every expert that has
-    rows, the activation rows it reads and the rows it writes, each once."""
+    rows, the activation rows it reads and the rows it writes, each once (with the dynamic
+    intermediate scale gate_up also writes and re-reads the fp32 intermediate)."""
     H, I, El = c["H"], c["I"], c["E_loc"]
     touched = int((counts[:El] > 0).sum()) + int(counts[El] > 0)
     rows = int(counts.sum())
@@ -216,6 +218,8 @@ def gemm_bytes(c, counts, gateup):
         wbytes = touched * 2 * I * H * NVFP4_BYTES
         a_in = rows * H * (2 if w4a16 else NVFP4_BYTES)
         a_out = rows * I * (2 if w4a16 else NVFP4_BYTES)
+        if c.get("inter") == "dynamic":
+            a_out += 2 * rows * I * 4
     else:
         wbytes = touched * H * I * NVFP4_BYTES
         a_in = rows * I * (2 if w4a16 else NVFP4_BYTES)
@@ -250,7 +254,7 @@ def measure_ours(args, rank, world):
     c = synth.CONFIGS[name]
     T, H, k = c["T"], c["H"], c["k"]
     extra = () if (args.no_extra or name != "decode" or args.local_experts) else \
-        ("prefill", "w4a16")
+        ("prefill", "w4a16", "decode_static", "decode_dyninter")
     handles = gpu_layer(name, extra_handles=extra, local_experts=args.local_experts)
     if args.local_experts:
         c = dict(c, E_loc=args.local_experts)
@@ -340,6 +344,9 @@ def measure_ours(args, rank, world):
         res["prefill"] = measure_prefill(handles["prefill"], stream, max(3, args.steps // 20))
     if "w4a16" in extra and rank == 0:
         res["w4a16"] = measure_w4a16(handles["w4a16"], stream, max(10, args.steps // 4))
+    for nm in ("decode_static", "decode_dyninter"):
+        if nm in extra and rank == 0:
+            res[nm] = measure_variant(handles[nm], nm, stream, max(10, args.steps // 4))
     return res
 
 
@@ -439,6 +446,51 @@ def measure_prefill(layer, stream, steps):
     fl = gemm_flops(counts, c, True) + gemm_flops(counts, c, False)
     return {"workload": "prefill T=8192", "value": T / (ms / 1e3), "ms_per_step": ms,
             "roofline": roof, "expert_fp4_tflops": round(fl / (ms / 1e3) / 1e12, 2)}
+
+
+VARIANTS = {
+    "decode_static": "decode T=64, W4A4 with the calibrated static activation scale",
+    "decode_dyninter": "decode T=64, W4A4 with the dynamic intermediate scale (two passes)",
+}
+
+
+def measure_variant(layer, name, stream, steps):
+    """Side measurement of a decode-layer variant (same weights and input as the headline
+    line): CUDA-graph replays, plus the gate_up / down launches timed on their own."""
+    import torch
+
+    import nvfp4_mixture_experts_gb300 as moe
+    c = synth.CONFIGS[name]
+    T, H = c["T"], c["H"]
+    x, _, _ = inputs(name)
+    xd = torch.from_numpy(x.view(np.int16)).cuda()
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    ws = layer.ensure_workspace(T)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            moe.moe_forward(layer.handle, xd, None, None, T, out, ws)
+        torch.cuda.synchronize()
+        st, bits = moe.moe_get_status(layer.handle, ws)
+        if st != moe.MOE_OK:
+            raise RuntimeError("device status %#x" % bits)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            moe.moe_forward(layer.handle, xd, None, None, T, out, ws)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    roof = roofline(layer, c, xd, None, None, ws, stream, min(steps, 20), peaks(), name)
+    return {"workload": VARIANTS[name], "value": round(T / (ms / 1e3), 1),
+            "ms_per_step": round(ms, 4), "gateup_us": roof["launch_us"],
+            "gateup_frac": roof["frac"], "down_us": roof["down"]["launch_us"],
+            "down_frac": roof["down"]["frac"]}
 
 
 def measure_w4a16(layer, stream, steps):
@@ -603,7 +655,7 @@ def main():
                     "h2d_bytes_per_step": c["T"] * c["H"] * 2,
                     "d2h_bytes_per_step": c["T"] * c["H"] * 2},
             "gpu_launches": r["launches"], "roofline": r["roofline"]}
-    for side in ("prefill", "w4a16"):
+    for side in ("prefill", "w4a16", "decode_static", "decode_dyninter"):
         if side in r:
             line[side] = r[side]
     if world == 1 and not args.no_oracle and not args.local_experts:

@@ -92,7 +92,10 @@ typedef struct {
     int32_t add_shared;           /* 1: add the shared expert into THIS partial sum */
     int32_t act_mode;             /* moe_act_mode */
     float act_global_scale;       /* MOE_W4A4_STATIC only */
-    float inter_global_scale;     /* static global scale of the intermediate (W4A4) */
+    float inter_global_scale;     /* global scale of the intermediate (W4A4): > 0 static;
+                                     0 dynamic -- 2688 / amax of the fp32 intermediate over
+                                     every row the call computes, in two passes (gate_up
+                                     writes fp32 s and its amax, then s is quantised) */
     int32_t max_tokens;           /* largest T a call may pass */
 } moe_config;
 
@@ -199,7 +202,10 @@ MOE_API moe_status moe_gather_activations(moe_handle h, const void* x_bf16_d, in
  * moe_gather_activations (W4A16, gs_a its fp16 prescale).
  *   fuse_epilogue 0: gateup_f32_d [rows_capacity][2I] fp32 (gate cols 0..I-1, up I..2I-1)
  *   fuse_epilogue 1: s = silu(gate) * up, then
- *       W4A4 : NVFP4 with inter_global_scale -> inter_codes_d / inter_sf_d (tiled, K = I)
+ *       W4A4 : NVFP4 with inter_global_scale -> inter_codes_d / inter_sf_d (tiled, K = I);
+ *              with the dynamic scale (inter_global_scale 0) the call runs both passes,
+ *              using the workspace for the fp32 intermediate, and leaves gs_i there for
+ *              moe_grouped_gemm_down on the same workspace
  *       W4A16: bf16 -> inter_bf16_d [rows_capacity][I]
  * Padding rows of the outputs are left unwritten. */
 MOE_API moe_status moe_grouped_gemm_gateup(moe_handle h, const uint8_t* a_codes_d,
@@ -217,7 +223,8 @@ MOE_API moe_status moe_swiglu_requant(const float* gateup_f32_d, int32_t rows, i
                               float gs_i, uint8_t* codes_d, uint8_t* sf_d, int32_t sf_layout,
                               moe_stream_t stream);
 
-/* Grouped GEMM down: Y_g = Aq_g . W2_g^T / (gs_i * gs2_g) (W4A16: / gs2_g), each row
+/* Grouped GEMM down: Y_g = Aq_g . W2_g^T / (gs_i * gs2_g) (W4A16: / gs2_g; dynamic
+ * intermediate scale: gs_i is the one moe_grouped_gemm_gateup left in ws_d), each row
  * multiplied by its routing weight (1 for shared rows; the weight of padded row r is
  * topk_w[perm_src[r]]), written to y_d[rows_capacity][H] fp32 at the same padded row.
  * Padding rows of y may receive arbitrary values. */
@@ -244,13 +251,14 @@ MOE_API moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* 
                        size_t ws_bytes, moe_stream_t stream);
 
 /* Where moe_forward keeps its intermediates inside the workspace (device pointers into
- * ws_d), so callers can inspect them after a forward.  Any pointer may be NULL. */
+ * ws_d), so callers can inspect them after a forward.  Any pointer may be NULL.  inter_gs:
+ * the dynamic intermediate scale of the last forward (set only in that mode). */
 MOE_API moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** topk_ids,
                                float** topk_w, int32_t** expert_counts,
                                int32_t** expert_offsets, int32_t** perm_src, int32_t** inv,
                                float** gs_a, uint8_t** a_codes, uint8_t** a_sf,
                                void** a_bf16, uint8_t** inter_codes, uint8_t** inter_sf,
-                               void** inter_bf16, float** y);
+                               void** inter_bf16, float** y, float** inter_gs);
 
 /* Reads the device status word of ws (synchronises the stream) into *bits (nullable) and
  * clears it.  Returns MOE_OK, MOE_ERR_TIMEOUT (MOE_DEV_WAIT_TIMEOUT set) or

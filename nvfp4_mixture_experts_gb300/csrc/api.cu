@@ -59,9 +59,16 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // ---------------------------------------------------------------- workspace plan
 struct Plan {
     int T, k, E, El, G, H, I, cap, nblk, Tk;
-    size_t status, amax, gs_a, ids, w, logits, hist, blkoff, counts, offsets, mb_start,
-        perm_src, inv, a_codes, a_sf, a_bf16, i_codes, i_sf, i_bf16, y, total;
+    size_t status, amax, gs_a, gs_i, ids, w, logits, hist, blkoff, counts, offsets, mb_start,
+        perm_src, inv, a_codes, a_sf, a_bf16, i_codes, i_sf, i_bf16, s_f32, y, total;
+    // amax holds two words: the activation amax, then the intermediate amax (dynamic gs_i)
 };
+
+// W4A4 with inter_global_scale == 0: the intermediate scale is computed per call.
+bool dynamic_inter(const moe_config& c)
+{
+    return c.act_mode != MOE_W4A16 && c.inter_global_scale == 0.0f;
+}
 
 int rows_cap(const moe_config& c, int T)
 {
@@ -95,8 +102,9 @@ Plan plan(const moe_config& c, int T)
         return at;
     };
     p.status = take(4);
-    p.amax = take(4);
+    p.amax = take(8);
     p.gs_a = take(4);
+    p.gs_i = take(4);
     p.ids = take((size_t)p.Tk * 4);
     p.w = take((size_t)p.Tk * 4);
     // router partial sums: one plane per k-split (the split count never exceeds the one
@@ -115,6 +123,7 @@ Plan plan(const moe_config& c, int T)
     p.i_codes = take(a16 ? 0 : (size_t)p.cap * codes_pitch(p.I));
     p.i_sf = take(a16 ? 0 : (size_t)p.cap * (p.I / 16));
     p.i_bf16 = take(a16 ? (size_t)p.cap * p.I * 2 : 0);
+    p.s_f32 = take(dynamic_inter(c) ? (size_t)p.cap * p.I * 4 : 0);
     p.y = take((size_t)p.cap * p.H * 4);
     p.total = o;
     return p;
@@ -201,7 +210,7 @@ bool valid_cfg(const moe_config* c, moe_status* why)
     if (c->max_tokens < 0) return false;
     if (c->act_mode < 0 || c->act_mode > 2) return false;
     if (c->act_mode == MOE_W4A4_STATIC && !(c->act_global_scale > 0.0f)) return false;
-    if (c->act_mode != MOE_W4A16 && !(c->inter_global_scale > 0.0f)) return false;
+    if (c->act_mode != MOE_W4A16 && !(c->inter_global_scale >= 0.0f)) return false;
     *why = MOE_ERR_UNSUPPORTED;
     if (c->hidden % 128 || c->inter % 64) return false;
     if (c->num_experts > kMaxExperts || c->top_k > kMaxTopK) return false;
@@ -357,6 +366,8 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     args.perm_src = perm_src;
     args.topk_w = topk_w;
     args.Tk = p.Tk;
+    args.inter_amax = at<uint32_t>(ws, p.amax) + 1;
+    args.gs_i_dev = (epilogue == kEpiDown && dynamic_inter(c)) ? at<float>(ws, p.gs_i) : nullptr;
     args.status = at<uint32_t>(ws, p.status);
     if (a16) {
         // Token rows per tile from the expected rows per local expert: narrow tiles keep the
@@ -417,6 +428,34 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
 }  // namespace
 
 namespace {
+
+// gate_up with the fused SwiGLU epilogue.  Static intermediate scale: one pass that writes
+// the NVFP4 intermediate.  Dynamic: the epilogue writes the fp32 intermediate and folds
+// amax |s| into the workspace (the caller zeroed it), then quant_inter_kernel quantises it
+// with 2688 / amax and stores gs_i for the down GEMM.
+moe_status launch_gateup_fused(const moe_layer* h, const Plan& p, const uint8_t* a_codes,
+                               const uint8_t* a_sf, const float* gs_a, const void* a_bf16,
+                               const int32_t* counts, const int32_t* offsets, uint8_t* i_codes,
+                               uint8_t* i_sf, void* i_bf16, void* ws, bool pdl, cudaStream_t s)
+{
+    if (!dynamic_inter(h->cfg))
+        return launch_gemm(h, p, true, kEpiGateUpSwiglu, a_codes, a_sf, gs_a, a_bf16, counts,
+                           offsets, nullptr, i_codes, i_sf, i_bf16, nullptr, nullptr, ws, pdl, s);
+    float* sbuf = at<float>(ws, p.s_f32);
+    const moe_status r = launch_gemm(h, p, true, kEpiGateUpSwigluF32, a_codes, a_sf, gs_a,
+                                     a_bf16, counts, offsets, sbuf, nullptr, nullptr, nullptr,
+                                     nullptr, nullptr, ws, pdl, s);
+    if (r != MOE_OK) return r;
+    // upper bound on the 128-row blocks (the exact count is on the device)
+    const int64_t P = (int64_t)p.T * p.k;
+    const int64_t blocks = (P + 127) / 128 + std::min<int64_t>(p.El, P) +
+                           ((int64_t)shared_rows(h, p.T) + 127) / 128;
+    return launch(quant_inter_kernel, dim3((unsigned)std::max<int64_t>(1, blocks)), dim3(256), 0,
+                  s, pdl, (const float*)sbuf, counts, offsets,
+                  (const int32_t*)at<int32_t>(ws, p.mb_start), p.G, p.I,
+                  (const uint32_t*)(at<uint32_t>(ws, p.amax) + 1), i_codes, i_sf,
+                  at<float>(ws, p.gs_i));
+}
 
 moe_status launch_combine(const moe_layer* h, const float* y, const int32_t* inv,
                           const int32_t* offsets, int T, void* out, bool pdl, cudaStream_t s)
@@ -695,10 +734,17 @@ moe_status moe_grouped_gemm_gateup(moe_handle h, const uint8_t* a_codes_d,
     const moe_status st = check_ws(h, T, ws_d, ws_bytes);
     if (st != MOE_OK) return st;
     const Plan p = plan(h->cfg, T);
-    return launch_gemm(h, p, true, fuse_epilogue ? kEpiGateUpSwiglu : kEpiGateUpF32, a_codes_d,
-                       a_sf_d, gs_a_d, a_bf16_d, expert_counts_d, expert_offsets_d,
-                       gateup_f32_d, inter_codes_d, inter_sf_d, inter_bf16_d, nullptr, nullptr,
-                       ws_d, false, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!fuse_epilogue)
+        return launch_gemm(h, p, true, kEpiGateUpF32, a_codes_d, a_sf_d, gs_a_d, a_bf16_d,
+                           expert_counts_d, expert_offsets_d, gateup_f32_d, nullptr, nullptr,
+                           nullptr, nullptr, nullptr, ws_d, false, s);
+    if (dynamic_inter(h->cfg) &&
+        cudaMemsetAsync(at<uint32_t>(ws_d, p.amax) + 1, 0, 4, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return launch_gateup_fused(h, p, a_codes_d, a_sf_d, gs_a_d, a_bf16_d, expert_counts_d,
+                               expert_offsets_d, inter_codes_d, inter_sf_d, inter_bf16_d, ws_d,
+                               false, s);
 }
 
 moe_status moe_swiglu_requant(const float* gateup_f32_d, int32_t rows, int32_t inter,
@@ -775,7 +821,7 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
     void* i_bf16 = at<void>(ws, p.i_bf16);
     float* y = at<float>(ws, p.y);
     // one chain of kernels with programmatic dependent launch; the first kernel clears the
-    // status word and the amax accumulator of this forward
+    // status word and the two amax accumulators of this forward
     uint32_t* status = at<uint32_t>(ws, p.status);
     uint32_t* amax = at<uint32_t>(ws, p.amax);
     moe_status r = launch_route(h, x_bf16_d, logits_in_d, logit_bias_d, T, ids, w, nullptr,
@@ -785,8 +831,8 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
         r = launch_gather(h, p, x_bf16_d, T, inv, offsets, a_codes, a_sf, a_bf16, gs_a, ws, true,
                           true, s);
     if (r == MOE_OK)
-        r = launch_gemm(h, p, true, kEpiGateUpSwiglu, a_codes, a_sf, gs_a, a_bf16, counts,
-                        offsets, nullptr, i_codes, i_sf, i_bf16, nullptr, nullptr, ws, true, s);
+        r = launch_gateup_fused(h, p, a_codes, a_sf, gs_a, a_bf16, counts, offsets, i_codes,
+                                i_sf, i_bf16, ws, true, s);
     if (r == MOE_OK)
         r = launch_gemm(h, p, false, kEpiDown, i_codes, i_sf, nullptr, i_bf16, counts, offsets,
                         y, nullptr, nullptr, nullptr, perm_src, w, ws, true, s);
@@ -799,7 +845,7 @@ moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** to
                                int32_t** expert_offsets, int32_t** perm_src, int32_t** inv,
                                float** gs_a, uint8_t** a_codes, uint8_t** a_sf,
                                void** a_bf16, uint8_t** inter_codes, uint8_t** inter_sf,
-                               void** inter_bf16, float** y)
+                               void** inter_bf16, float** y, float** inter_gs)
 {
     if (!h || !ws_d || !t_ok(h, T)) return MOE_ERR_INVALID;
     const Plan p = plan(h->cfg, T);
@@ -817,6 +863,7 @@ moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** to
     if (inter_bf16) *inter_bf16 = at<void>(ws_d, p.i_bf16);
     if (inter_sf) *inter_sf = at<uint8_t>(ws_d, p.i_sf);
     if (y) *y = at<float>(ws_d, p.y);
+    if (inter_gs) *inter_gs = at<float>(ws_d, p.gs_i);
     return MOE_OK;
 }
 

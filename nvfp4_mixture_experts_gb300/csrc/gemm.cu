@@ -114,7 +114,8 @@ __device__ __forceinline__ EpiPrep epi_prep(const GemmArgs& a, const TileInfo& t
     e.valid = m < ti.rows;
     e.prow = (int64_t)ti.arow0 + m;
     const float gw = a.gs_w[ti.g];
-    e.alpha = __frcp_rn(__fmul_rn(a.epilogue == kEpiDown ? a.gs_i : *a.gs_a, gw));
+    const float gs_in = a.epilogue != kEpiDown ? *a.gs_a : a.gs_i_dev ? *a.gs_i_dev : a.gs_i;
+    e.alpha = __frcp_rn(__fmul_rn(gs_in, gw));
     e.nvalid = max(0, min(32, ti.rows - q * 32));
     if (a.epilogue == kEpiDown && e.valid) {
         const int pair = a.perm_src[e.prow];
@@ -139,6 +140,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& 
     const bool staged = a.epilogue == kEpiDown && a.staging && ep.nvalid > 8;
     const int I = a.N / 2;
     uint32_t sfword = 0;
+    float smax = 0.0f;  // kEpiGateUpSwigluF32: this lane's amax |s|
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
@@ -195,6 +197,16 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& 
             for (int i = 0; i < 16; ++i)
                 s[i] = silu_mul(__fmul_rn(__uint_as_float(r[i]), alpha),
                                 __fmul_rn(__uint_as_float(r[16 + i]), alpha));
+            if (a.epilogue == kEpiGateUpSwigluF32) {
+                float4* dst = reinterpret_cast<float4*>(a.out_f32 + prow * I + f);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    dst[i] = make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
+                    smax = fmaxf(smax, fmaxf(fmaxf(fabsf(s[4 * i]), fabsf(s[4 * i + 1])),
+                                             fmaxf(fabsf(s[4 * i + 2]), fabsf(s[4 * i + 3]))));
+                }
+                continue;
+            }
             uint32_t cw[2];
             const uint32_t sb = quant16(s, a.gs_i, cw);
             *reinterpret_cast<uint2*>(a.out_codes + prow * codes_pitch(I) + f / 2) =
@@ -204,6 +216,12 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& 
     }
     if (a.epilogue == kEpiGateUpSwiglu && valid)
         *reinterpret_cast<uint32_t*>(a.out_sf + sf_atom_offset(prow, 4 * ti.nb, I)) = sfword;
+    if (a.epilogue == kEpiGateUpSwigluF32) {
+        // one atomic per warp; |s| >= 0, so its fp32 bits order like the values
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+        if (lane == 0) atomicMax(a.inter_amax, __float_as_uint(smax));
+    }
 }
 
 // Shared-memory carve-up: stages, then barriers (room for kMaxStages), the TMEM address

@@ -52,6 +52,10 @@ __global__ void quant_rows_kernel(const uint16_t* x, int rows, int cols, const f
                                   int layout, float* gs_out);
 __global__ void swiglu_requant_kernel(const float* gu, int rows, int I, float gs_i,
                                       uint8_t* codes, uint8_t* sf, int layout);
+__global__ void quant_inter_kernel(const float* s, const int32_t* counts, const int32_t* offsets,
+                                   const int32_t* mb_start, int G, int I,
+                                   const uint32_t* amax_bits, uint8_t* codes, uint8_t* sf,
+                                   float* gs_out);
 __global__ void combine_kernel(const float* y, const int32_t* inv, const int32_t* offsets,
                                int shared_group, int T, int H, int k, int add_shared,
                                uint16_t* out);
@@ -62,7 +66,9 @@ __global__ void repack_tiles_kernel(const uint8_t* codes, const uint8_t* sf, int
 enum GemmEpilogue : int {
     kEpiGateUpF32 = 0,     // G (alpha applied) -> fp32 rows, gate then up columns
     kEpiGateUpSwiglu = 1,  // silu(gate)*up -> NVFP4 (W4A4) or bf16 (W4A16)
-    kEpiDown = 2           // Y * routing weight -> fp32 rows indexed by padded row
+    kEpiDown = 2,          // Y * routing weight -> fp32 rows indexed by padded row
+    kEpiGateUpSwigluF32 = 3  // silu(gate)*up -> fp32 rows [rows][I], and amax |s| into
+                             // inter_amax (first pass of the dynamic intermediate scale)
 };
 
 struct GemmArgs {
@@ -88,6 +94,8 @@ struct GemmArgs {
     int stages;               // pipeline depth (<= kMaxStages; fits the shared memory)
     int staging;              // bytes of epilogue staging (kEpiDown: TMA stores of y), or 0
     int raw_slots;            // W4A16: raw weight blobs in flight
+    uint32_t* inter_amax;     // kEpiGateUpSwigluF32: fp32 bits of amax |s| (atomic max)
+    const float* gs_i_dev;    // kEpiDown: device intermediate scale (dynamic), else gs_i
     uint32_t* status;
 };
 

@@ -225,6 +225,54 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(
     }
 }
 
+// ---------------------------------------------------------------- dynamic intermediate scale
+// Second pass of the dynamic intermediate scale: the fp32 intermediate s [rows][I] of the
+// gate_up epilogue (padded rows), NVFP4-quantised with gs_i = 2688 / amax |s| (amax from
+// the first pass; 1 if 0) into the tiled codes / scale atoms the down GEMM reads.  Block b
+// takes 128-row block b of the padded layout (mb_start maps it to its group); only the
+// group's valid rows are written.  Block 0 stores gs_i.
+__global__ void __launch_bounds__(256) quant_inter_kernel(
+    const float* __restrict__ s, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ mb_start, int G, int I,
+    const uint32_t* amax_bits, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+    float* gs_out)
+{
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
+    const float gs = global_scale(nullptr, amax_bits);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *gs_out = gs;
+    const int b = blockIdx.x;
+    if (b >= mb_start[G]) return;
+    int lo = 0, hi = G;  // group of block b: last g with mb_start[g] <= b
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (mb_start[mid] <= b) lo = mid;
+        else hi = mid;
+    }
+    const int blk = b - mb_start[lo];
+    const int nrows = min(128, counts[lo] - 128 * blk);
+    const int64_t row0 = offsets[lo] + 128 * blk;
+    const int nb = I / 16, pitch = codes_pitch(I);
+    for (int i = threadIdx.x; i < nrows * nb; i += blockDim.x) {
+        const int64_t r = row0 + i / nb;
+        const int q = i % nb;
+        const float4* src = reinterpret_cast<const float4*>(s + r * I + q * 16);
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 f = src[j];
+            v[4 * j] = f.x;
+            v[4 * j + 1] = f.y;
+            v[4 * j + 2] = f.z;
+            v[4 * j + 3] = f.w;
+        }
+        uint32_t c[2];
+        const uint32_t sb = quant16(v, gs, c);
+        *reinterpret_cast<uint2*>(codes + r * pitch + q * 8) = make_uint2(c[0], c[1]);
+        sf[sf_atom_offset(r, q, I)] = (uint8_t)sb;
+    }
+}
+
 // ---------------------------------------------------------------- combine
 // out[t][h] = sum_{j: inv >= 0} y[inv[t*k+j]][h] + (add_shared ? y[offsets[G_s] + t][h] : 0)
 // in ascending j then the shared row, fp32, rounded to bf16.  y rows are padded rows (already

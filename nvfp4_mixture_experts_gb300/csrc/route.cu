@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
         pdl_trigger();
         if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {  // per-forward words
             if (clear0) *clear0 = 0u;
-            if (clear1) *clear1 = 0u;
+            if (clear1) clear1[0] = clear1[1] = 0u;  // both amax accumulators
         }
     }
     if (warp == 0 && lane == 0) {
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(256) topk_kernel(
         pdl_trigger();
         if (blockIdx.x == 0) {  // per-forward words (when no router GEMM ran before)
             if (clear0) *clear0 = 0u;
-            if (clear1) *clear1 = 0u;
+            if (clear1) clear1[0] = clear1[1] = 0u;  // both amax accumulators
         }
     }
     const int t0 = blockIdx.x * kTopkTokens;

@@ -99,6 +99,13 @@ CONFIGS = {
     # expert shard 160..319 of the decode layer, Zipf(1.1) popularity, 2048 tokens
     "shard": dict(T=2048, H=4096, I=1280, E=320, k=8, E_loc=160, off=160, add_shared=0,
                   act_mode=0, outlier_frac=0.0, bias=True, logits=False),
+    # the decode layer with a static activation scale (calibrated once, power of two)
+    "decode_static": dict(T=64, H=4096, I=1280, E=320, k=8, E_loc=320, off=0, add_shared=1,
+                          act_mode=1, outlier_frac=0.0, bias=False, logits=False),
+    # the decode layer with the dynamic (per-call, two-pass) intermediate scale
+    "decode_dyninter": dict(T=64, H=4096, I=1280, E=320, k=8, E_loc=320, off=0, add_shared=1,
+                            act_mode=0, outlier_frac=0.0, bias=False, logits=False,
+                            inter="dynamic"),
     # W4A16: bf16 activations x NVFP4 weights, router logits ~ N(0,1), decode sweep
     "w4a16": dict(T=256, H=4096, I=1280, E=320, k=8, E_loc=320, off=0, add_shared=1,
                   act_mode=2, outlier_frac=0.0, bias=False, logits=True,

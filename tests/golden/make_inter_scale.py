@@ -5,7 +5,9 @@ Rule: run a calibration batch (activations from seed 1, the layer's weights from
 through routing and the experts' gate/up projections, take amax of silu(gate) * up over
 every routed and shared pair, and set gs_i = 2^floor(log2(2688 / (2 * amax))): a power
 of two (so the scale itself introduces no rounding) with at least 2x headroom before the
-E4M3 block scale saturates at 448.
+E4M3 block scale saturates at 448.  A workload with the dynamic intermediate scale gets 0.
+A workload with a static activation scale gets act_global_scale by the same rule from
+amax |x| of the calibration batch.
 
 Usage: python tests/golden/make_inter_scale.py
 """
@@ -52,11 +54,17 @@ def calibrate(name):
         s = g / (1.0 + np.exp(-g)) * u
         amax = max(amax, float(np.abs(s).max()))
     gs = float(2.0 ** np.floor(np.log2(2688.0 / (2.0 * amax))))
-    return dict(inter_global_scale=gs, amax=amax, cal_tokens=T)
+    out = dict(inter_global_scale=0.0 if c.get("inter") == "dynamic" else gs, amax=amax,
+               cal_tokens=T)
+    if c["act_mode"] == 1:
+        xa = float(np.abs(synth.bf16_to_f32(x)).max())
+        out["act_global_scale"] = float(2.0 ** np.floor(np.log2(2688.0 / (2.0 * xa))))
+        out["act_amax"] = xa
+    return out
 
 
 def main():
-    out = {"_rule": __doc__.strip().splitlines()[2:8]}
+    out = {"_rule": __doc__.strip().splitlines()[2:11]}
     for name in synth.CONFIGS:
         out[name] = calibrate(name)
         print(name, out[name], flush=True)

@@ -60,6 +60,9 @@ def test_workspace_and_capacity_host_logic(lib):
     assert moe.moe_workspace_size(cfg, T) > cap * (256 // 2)
     assert moe.moe_rows_capacity(cfg, 0) == 0
     assert moe.moe_rows_capacity(_cfg(add_shared=0), 4) == 128 * (1 + 8)
+    # the dynamic intermediate scale keeps the fp32 intermediate [rows][I] in the workspace
+    dyn = _cfg(max_tokens=64, inter_gs=0.0)
+    assert moe.moe_workspace_size(dyn, T) >= moe.moe_workspace_size(cfg, T) + cap * dyn.inter * 4
 
 
 def test_invalid_configs_are_rejected_before_any_launch(lib):
@@ -68,7 +71,7 @@ def test_invalid_configs_are_rejected_before_any_launch(lib):
         _cfg(I=96),                    # I % 64
         _cfg(k=17),                    # k > E
         _cfg(E_loc=10, off=8),         # shard past E
-        _cfg(inter_gs=0.0),            # W4A4 needs the intermediate scale
+        _cfg(inter_gs=-1.0),           # W4A4: a static scale > 0, or 0 for the dynamic one
         _cfg(act_mode=moe.MOE_W4A4_STATIC, act_gs=0.0),
     ]
     for cfg in bad:

@@ -220,3 +220,59 @@ def test_prefill_chunk_sampled_parity(big_layer):
     _same_routing(ids, ora.ids, x, wr, None, k)
     counts = np.bincount(ora.ids.ravel(), minlength=E)
     assert 150 < counts.mean() < 260  # ~205 tokens per expert
+
+
+def _dyn_scale_check(h, T, ora):
+    gs = _read_ws(h, moe.moe_forward_buffers(h.handle, h.ws, T)["inter_gs"], 1, np.float32)[0]
+    # fp32 tensor-core gate/up vs the oracle's fp64: the amax element agrees to ~1e-6
+    assert abs(float(gs) - ora.gs_i) <= 1e-5 * ora.gs_i, (gs, ora.gs_i)
+
+
+def test_tiny_layer_dynamic_intermediate_scale():
+    c = synth.CONFIGS["tiny"]
+    T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+    layer = build_layer(0, H, I, E)
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(0, T, H)
+    h = make_layer(layer, wr, H, I, E, k, inter_gs=0.0, max_tokens=T)
+    got = _forward(h, x, T)
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, inter_gs=0.0), x, layer, router_w=wr)
+    _dyn_scale_check(h, T, ora)
+    _check(got, ora.out, "tiny dynamic intermediate scale")
+    # twice in a row: the forward clears its amax accumulators itself
+    got2 = _forward(h, x, T)
+    assert np.array_equal(got, got2)
+
+
+def test_decode_layer_dynamic_intermediate_scale(big_layer):
+    c = synth.CONFIGS["decode"]
+    T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(0, T, H)
+    h = make_layer(big_layer, wr, H, I, E, k, inter_gs=0.0, max_tokens=T)
+    got = _forward(h, x, T)
+    clear, _ = _routing_clear(x, wr, None, k)
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, inter_gs=0.0), x, big_layer,
+                             router_w=wr)
+    _dyn_scale_check(h, T, ora)
+    _check(got[clear], ora.out[clear], "decode dynamic intermediate scale")
+
+
+def test_decode_layer_static_activation_scale(big_layer):
+    """W4A4 with the calibrated static activation scale: activation codes bit-exact with
+    the oracle's (same scale), the layer within the bar."""
+    c = synth.CONFIGS["decode_static"]
+    T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+    gs_i = INTER["decode_static"]["inter_global_scale"]
+    gs_a = INTER["decode_static"]["act_global_scale"]
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(0, T, H)
+    h = make_layer(big_layer, wr, H, I, E, k, act_mode=moe.MOE_W4A4_STATIC, act_gs=gs_a,
+                   inter_gs=gs_i, max_tokens=T)
+    got = _forward(h, x, T)
+    clear, _ = _routing_clear(x, wr, None, k)
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, act_mode=1, act_gs=gs_a,
+                                             inter_gs=gs_i), x, big_layer, router_w=wr)
+    assert ora.gs_a == np.float32(gs_a)
+    _check(got[clear], ora.out[clear], "decode static activation scale")
+    _forward_buffers_check(h, T, ora, clear, x, wr)

@@ -10,7 +10,7 @@ import oracle
 import synth
 from gpu_util import (bits16, canonical_to_tiled, dev, host, make_layer,
                       quant_decisions_near_boundary, tiled_to_canonical)
-from helpers import build_layer
+from helpers import build_layer, within_layer_tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -389,3 +389,44 @@ def test_combine_sums_pairs_and_shared():
         want[t] += y[500 + t]
     got = synth.bf16_to_f32(host(out).view(np.uint16))
     assert np.max(np.abs(got - want) / (np.abs(want) + 1e-3)) < 2 ** -7
+
+
+def test_grouped_gemms_with_the_dynamic_intermediate_scale():
+    """Staged gate_up (both passes) and down with inter_global_scale 0: gs_i is 2688 / amax
+    of the fp32 intermediate of the computed rows, and the down output matches the oracle's
+    expert MLP quantising the intermediate with that scale."""
+    H, I, E, k, T = 512, 256, 8, 2, 200
+    layer = build_layer(12, H, I, E)
+    wr = synth.router_weight(12, E, H)
+    x = synth.activations(12, T, H, outlier_frac=0.01)
+    lg = synth.logits_normal(12, T, E)
+    h = make_layer(layer, wr, H, I, E, k, act_mode=0, inter_gs=0.0)
+    st = Staged(h, bits16(x), T, k, lg)
+    rows = st.rows()
+    ic = torch.zeros(st.cap * ((I // 2 + 127) // 128 * 128), dtype=torch.uint8, device="cuda")
+    isf = torch.zeros(st.cap * I // 16, dtype=torch.uint8, device="cuda")
+    moe.moe_grouped_gemm_gateup(h.handle, st.a_codes, st.a_sf, st.gs, st.a_bf16, st.counts,
+                                st.offsets, 1, None, ic, isf, None, T, st.ws)
+    y = torch.zeros((st.cap, H), dtype=torch.float32, device="cuda")
+    moe.moe_grouped_gemm_down(h.handle, ic, isf, None, st.counts, st.offsets, st.perm, st.w,
+                              y, T, st.ws)
+    torch.cuda.synchronize()
+    ptr = moe.moe_forward_buffers(h.handle, st.ws, T)["inter_gs"]
+    gs_gpu = float(st.ws[ptr - st.ws.data_ptr():][:4].cpu().numpy().view(np.float32)[0])
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, act_mode=0, inter_gs=0.0), x, layer,
+                             logits_in=lg, tokens=np.zeros(0, np.int32))
+    assert abs(gs_gpu - ora.gs_i) <= 1e-5 * ora.gs_i, (gs_gpu, ora.gs_i)
+    cfg = oracle.make_cfg(T, H, I, E, k, act_mode=0, inter_gs=gs_gpu)
+    xc, xsf, gs_a = oracle.quant_nvfp4(synth.bf16_to_f32(x))
+    wts = host(st.w).reshape(-1)
+    Yg = host(y)
+    for g in range(E + 1):
+        sel = rows[rows[:, 2] == g]
+        if len(sel) == 0:
+            continue
+        e = "shared" if g == E else g
+        Y = oracle.expert_rows(cfg, layer, e, x, xc, xsf, gs_a, sel[:, 1].astype(np.int32))[3]
+        pair = host(st.perm)[sel[:, 0]]
+        w = np.where(pair < T * k, wts[np.minimum(pair, T * k - 1)], 1.0)
+        rel, mx = within_layer_tolerance(Yg[sel[:, 0]], Y * w[:, None])
+        assert rel <= 1e-2 and mx <= 5e-2, (g, rel, mx)
