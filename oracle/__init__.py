@@ -66,6 +66,10 @@ def load():
                                         C.c_void_p, C.POINTER(C.c_long), C.c_void_p,
                                         C.c_void_p, C.POINTER(C.c_float),
                                         C.POINTER(C.c_float), C.c_void_p, C.c_void_p]
+        lib.orc_prepare_weights.restype = None
+        lib.orc_prepare_weights.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int,
+                                            C.c_int, C.c_int, C.c_float, C.c_int, C.c_int,
+                                            C.c_int, C.c_void_p, C.c_void_p, C.c_void_p]
         lib.orc_num_threads.restype = C.c_int
         lib.orc_set_num_threads.argtypes = [C.c_int]
         _lib = lib
@@ -303,3 +307,25 @@ def moe_forward(cfg, x_bf16, layer, router_w=None, logit_bias=None, logits_in=No
     r.gs_i = gs_i.value
     r.tokens = np.arange(T, dtype=np.int32) if tok is None else tok
     return r
+
+
+GS_ENCODE, GS_DEQUANT = 0, 1   # global-scale conventions of a checkpoint
+
+
+def prepare_weights(codes, sf, glob, convention=GS_ENCODE, fold_target=0.0, swap_halves=False,
+                    off=0, count=None):
+    """Checkpoint-convention weights [E][N][K/2] codes, [E][N][K/16] E4M3 scales, [E]
+    globals -> the library's codes / scales / encode scales for experts off..off+count-1
+    (see orc_prepare_weights)."""
+    codes = _c(codes, np.uint8)
+    sf = _c(sf, np.uint8)
+    glob = _c(glob, np.float32)
+    E, N, K2 = codes.shape
+    K = 2 * K2
+    count = E - off if count is None else count
+    co = np.empty((count, N, K // 2), np.uint8)
+    so = np.empty((count, N, K // 16), np.uint8)
+    go = np.empty(count, np.float32)
+    load().orc_prepare_weights(_p(codes), _p(sf), _p(glob), N, K, convention, fold_target,
+                               int(bool(swap_halves)), off, count, _p(co), _p(so), _p(go))
+    return co, so, go

@@ -675,6 +675,57 @@ int orc_moe_forward(const orc_cfg* c, const uint16_t* x, const uint16_t* router_
     return 0;
 }
 
+/* ------------------------------------------------------------------------- */
+/* Checkpoint-convention weight preparation                                   */
+/* ------------------------------------------------------------------------- */
+
+/* One weight matrix type of a checkpoint (E_total experts of N x K NVFP4, canonical:
+ * codes [E][N][K/2], E4M3 block scales [E][N][K/16], one global value per expert) ->
+ * the library's convention for the experts off..off+count-1:
+ *   - global: convention 0 gives the encode scale gs (dequantised value = code*sf/gs,
+ *     the reciprocal form), convention 1 the dequantisation multiplier m (value =
+ *     code*sf*m), turned into gs = 1/m in fp32;
+ *   - fold_target > 0: the expert's global is folded into its block scales relative to
+ *     the common scale gs_t = fold_target: r = gs_t / gs (fp32), sf' = E4M3(sf * r)
+ *     rounded to nearest even and saturated at 448 (re-rounding), and gs' = gs_t for every
+ *     expert (gs_t = 1 folds the global away completely);
+ *   - swap_halves: rows N/2..N-1 come first (a fused gate/up matrix stored up-then-gate
+ *     becomes gate-then-up).
+ * Codes are copied unchanged. */
+void orc_prepare_weights(const uint8_t* codes, const uint8_t* sf, const float* glob,
+                         int N, int K, int convention, float fold_target, int swap_halves,
+                         int off, int count, uint8_t* codes_out, uint8_t* sf_out,
+                         float* gs_out)
+{
+    long e;
+    for (e = 0; e < count; e++) {
+        const long src_e = off + e;
+        float gs = convention == 1 ? 1.0f / glob[src_e] : glob[src_e];
+        float r = 1.0f;
+        long n;
+        if (fold_target > 0.0f) {
+            r = fold_target / gs;
+            gs = fold_target;
+        }
+        gs_out[e] = gs;
+        for (n = 0; n < N; n++) {
+            const long src_n = swap_halves ? (n + N / 2) % N : n;
+            const long src_row = src_e * N + src_n, dst_row = e * N + n;
+            int b;
+            memcpy(codes_out + dst_row * (K / 2), codes + src_row * (K / 2), K / 2);
+            for (b = 0; b < K / 16; b++) {
+                const uint8_t v = sf[src_row * (K / 16) + b];
+                if (fold_target > 0.0f) {
+                    const float x = (float)orc_e4m3_value(v) * r;
+                    sf_out[dst_row * (K / 16) + b] = (uint8_t)orc_e4m3_encode(x);
+                } else {
+                    sf_out[dst_row * (K / 16) + b] = v;
+                }
+            }
+        }
+    }
+}
+
 /* Threads the parallel loops use. */
 int orc_num_threads(void)
 {
