@@ -347,6 +347,8 @@ def measure_ours(args, rank, world):
     for nm in ("decode_static", "decode_dyninter"):
         if nm in extra and rank == 0:
             res[nm] = measure_variant(handles[nm], nm, stream, max(10, args.steps // 4))
+    if extra and rank == 0:
+        res["weight_prep"] = measure_weight_prep(c, stream, 10)
     return res
 
 
@@ -491,6 +493,40 @@ def measure_variant(layer, name, stream, steps):
             "ms_per_step": round(ms, 4), "gateup_us": roof["launch_us"],
             "gateup_frac": roof["frac"], "down_us": roof["down"]["launch_us"],
             "down_frac": roof["down"]["frac"]}
+
+
+def measure_weight_prep(c, stream, steps):
+    """Checkpoint-convention preparation of the layer's w13 (all E experts, N = 2I, K = H):
+    the global scales folded into the block scales and the gate/up halves swapped.  An HBM
+    stream: every code and scale byte read and written once."""
+    import torch
+
+    import nvfp4_mixture_experts_gb300 as moe
+    E, N, K = c["E"], 2 * c["I"], c["H"]
+    g = torch.Generator(device="cuda").manual_seed(0)
+    codes = torch.randint(0, 256, (E, N, K // 2), dtype=torch.uint8, device="cuda", generator=g)
+    sf = torch.randint(0, 127, (E, N, K // 16), dtype=torch.uint8, device="cuda", generator=g)
+    glob = torch.rand(E, device="cuda", generator=g) * 3000 + 100
+    co, so, go = torch.empty_like(codes), torch.empty_like(sf), torch.empty_like(glob)
+    run = lambda: moe.moe_prepare_weights(codes, sf, glob, N, K, moe.MOE_GS_ENCODE, 1024.0,
+                                          True, 0, E, co, so, go, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    s = e0.elapsed_time(e1) / steps / 1e3
+    nbytes = 2 * (codes.numel() + sf.numel()) + 8 * E
+    gbs = nbytes / s / 1e9
+    return {"workload": "checkpoint weight prep: w13 of %d experts (N=%d, K=%d), globals "
+                        "folded into the E4M3 scales, gate/up swapped" % (E, N, K),
+            "launch_us": round(s * 1e6, 2), "bytes": nbytes, "achieved_gbs": round(gbs, 1),
+            "frac": round(gbs / peaks()["hbm"], 4)}
 
 
 def measure_w4a16(layer, stream, steps):
@@ -655,7 +691,7 @@ def main():
                     "h2d_bytes_per_step": c["T"] * c["H"] * 2,
                     "d2h_bytes_per_step": c["T"] * c["H"] * 2},
             "gpu_launches": r["launches"], "roofline": r["roofline"]}
-    for side in ("prefill", "w4a16", "decode_static", "decode_dyninter"):
+    for side in ("prefill", "w4a16", "decode_static", "decode_dyninter", "weight_prep"):
         if side in r:
             line[side] = r[side]
     if world == 1 and not args.no_oracle and not args.local_experts:

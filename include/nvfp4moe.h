@@ -75,6 +75,12 @@ typedef enum {
     MOE_W4A16 = 2           /* bf16 activations x NVFP4 weights */
 } moe_act_mode;
 
+/* How a checkpoint gives an expert's global scale (moe_prepare_weights). */
+typedef enum {
+    MOE_GS_ENCODE = 0,      /* the encode scale gs: value = code * sf / gs (reciprocal form) */
+    MOE_GS_DEQUANT = 1      /* a dequantisation multiplier m: value = code * sf * m */
+} moe_gs_convention;
+
 /* Device status bits (moe_get_status's *bits). */
 #define MOE_DEV_BAD_EXPERT_ID  0x1u   /* a top-k id outside [0, num_experts): pair dropped */
 #define MOE_DEV_WAIT_TIMEOUT   0x2u   /* a pipeline wait ran out: that tile was abandoned */
@@ -215,6 +221,32 @@ MOE_API moe_status moe_grouped_gemm_gateup(moe_handle h, const uint8_t* a_codes_
                                    float* gateup_f32_d, uint8_t* inter_codes_d,
                                    uint8_t* inter_sf_d, void* inter_bf16_d, int32_t T,
                                    void* ws_d, size_t ws_bytes, moe_stream_t stream);
+
+/* Checkpoint-convention weight preparation ("Serving Solar Open 2 (NVFP4) on DGX Spark",
+ * section on reading real NVFP4 checkpoints: packed FP4 weights, FP8 block scales and a
+ * per-expert global scale in either convention; the reciprocal global scale inverted and
+ * folded into the FP8 block scales with re-rounding, clamped at 448; the fused gate/up row
+ * order; per-shard scale slicing).  One weight matrix type of num_experts experts, each
+ * N x K NVFP4 in the canonical layout -- codes_d [E][N][K/2] (element 2i in the low
+ * nibble), sf_d [E][N][K/16] E4M3, glob_d [E] fp32 -- becomes the moe_weights form of
+ * experts off .. off+count-1:
+ *   codes_out_d [count][N][K/2]: the codes (rows reordered by swap_halves);
+ *   gs_out_d [count]: the encode scale gs (convention MOE_GS_DEQUANT: gs = 1/m in fp32);
+ *   sf_out_d [count][N][K/16]: the scales, or with fold_target > 0 each expert's global
+ *     folded in relative to the common scale gs_t = fold_target: r = gs_t / gs (fp32),
+ *     sf' = E4M3(sf * r) rounded to nearest even and saturated at 448, and gs_out = gs_t
+ *     for every expert (gs_t = 1 removes the global scale altogether);
+ *   swap_halves != 0: output rows 0..N/2-1 are input rows N/2..N-1 and vice versa (a fused
+ *     gate/up matrix stored up-then-gate becomes gate-then-up).
+ * Scale bytes must not be the NaN pattern.  Device pointers, caller-owned; codes_d and
+ * codes_out_d 16-byte aligned; K a multiple of 64; count 0 is a no-op (pointers unused).
+ * Stream-ordered; argument errors return before any launch. */
+MOE_API moe_status moe_prepare_weights(const uint8_t* codes_d, const uint8_t* sf_d,
+                                       const float* glob_d, int32_t num_experts, int32_t N,
+                                       int32_t K, int32_t convention, float fold_target,
+                                       int32_t swap_halves, int32_t off, int32_t count,
+                                       uint8_t* codes_out_d, uint8_t* sf_out_d,
+                                       float* gs_out_d, moe_stream_t stream);
 
 /* SwiGLU + NVFP4 requantisation of fp32 gate/up rows [rows][2I] (gate cols 0..I-1):
  * s = silu(g) * u in fp32, quantised with the static scale gs_i.  sf_layout as for

@@ -16,6 +16,7 @@ LIB_PATH = _build.LIB
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE, \
     MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_STATUS = range(7)
 MOE_W4A4_DYNAMIC, MOE_W4A4_STATIC, MOE_W4A16 = 0, 1, 2
+MOE_GS_ENCODE, MOE_GS_DEQUANT = 0, 1
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_WAIT_TIMEOUT, MOE_DEV_ROWS_OVERFLOW = 1, 2, 4
 
 
@@ -52,6 +53,8 @@ SIGNATURES = {
     "moe_grouped_gemm_gateup": (C.c_int, [_V, _V, _V, _V, _V, _V, _V, _I, _V, _V, _V, _V, _I,
                                           _V, _SZ, _V]),
     "moe_swiglu_requant": (C.c_int, [_V, _I, _I, C.c_float, _V, _V, _I, _V]),
+    "moe_prepare_weights": (C.c_int, [_V, _V, _V, _I, _I, _I, _I, C.c_float, _I, _I, _I, _V,
+                                      _V, _V, _V]),
     "moe_grouped_gemm_down": (C.c_int, [_V, _V, _V, _V, _V, _V, _V, _V, _V, _I, _V, _SZ, _V]),
     "moe_combine": (C.c_int, [_V, _V, _V, _V, _I, _V, _V]),
     "moe_forward": (C.c_int, [_V, _V, _V, _V, _I, _V, _V, _SZ, _V]),
@@ -175,6 +178,14 @@ def moe_grouped_gemm_gateup(h, a_codes, a_sf, gs_a, a_bf16, counts, offsets, fus
 def moe_swiglu_requant(gateup_f32, rows, inter, gs_i, codes, sf, sf_layout, stream=None):
     _check(load().moe_swiglu_requant(_p(gateup_f32), rows, inter, float(gs_i), _p(codes),
                                      _p(sf), sf_layout, _stream(stream)), "moe_swiglu_requant")
+
+
+def moe_prepare_weights(codes, sf, glob, N, K, convention, fold_target, swap_halves, off, count,
+                        codes_out, sf_out, gs_out, stream=None):
+    _check(load().moe_prepare_weights(_p(codes), _p(sf), _p(glob), int(glob.numel()), N, K,
+                                      convention, float(fold_target), int(bool(swap_halves)),
+                                      off, count, _p(codes_out), _p(sf_out), _p(gs_out),
+                                      _stream(stream)), "moe_prepare_weights")
 
 
 def moe_grouped_gemm_down(h, inter_codes, inter_sf, inter_bf16, counts, offsets, perm_src,

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -745,6 +746,33 @@ moe_status moe_grouped_gemm_gateup(moe_handle h, const uint8_t* a_codes_d,
     return launch_gateup_fused(h, p, a_codes_d, a_sf_d, gs_a_d, a_bf16_d, expert_counts_d,
                                expert_offsets_d, inter_codes_d, inter_sf_d, inter_bf16_d, ws_d,
                                false, s);
+}
+
+moe_status moe_prepare_weights(const uint8_t* codes_d, const uint8_t* sf_d, const float* glob_d,
+                               int32_t num_experts, int32_t N, int32_t K, int32_t convention,
+                               float fold_target, int32_t swap_halves, int32_t off,
+                               int32_t count, uint8_t* codes_out_d, uint8_t* sf_out_d,
+                               float* gs_out_d, moe_stream_t stream)
+{
+    if (N <= 0 || K <= 0 || num_experts < 0 || off < 0 || count < 0 ||
+        (int64_t)off + count > num_experts)
+        return MOE_ERR_INVALID;
+    if ((convention != MOE_GS_ENCODE && convention != MOE_GS_DEQUANT) ||
+        !(fold_target >= 0.0f) || isinf(fold_target) || (swap_halves && (N & 1)))
+        return MOE_ERR_INVALID;
+    if (K % 64) return MOE_ERR_UNSUPPORTED;
+    if (count == 0) return MOE_OK;  // an empty slice: nothing to read or write
+    if (!codes_d || !sf_d || !glob_d || !codes_out_d || !sf_out_d || !gs_out_d)
+        return MOE_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(codes_d) | reinterpret_cast<uintptr_t>(codes_out_d)) & 15)
+        return MOE_ERR_INVALID;
+    // a warp per output row, 8 rows per block, up to 16 blocks per SM (grid-stride)
+    const int64_t blocks = ((int64_t)count * N + 7) / 8;
+    prepare_weights_kernel<<<(unsigned)std::min<int64_t>(blocks, 152 * 16), 256, 0,
+                             reinterpret_cast<cudaStream_t>(stream)>>>(
+        codes_d, sf_d, glob_d, N, K, convention, fold_target, swap_halves ? 1 : 0, off, count,
+        codes_out_d, sf_out_d, gs_out_d);
+    return check_launch();
 }
 
 moe_status moe_swiglu_requant(const float* gateup_f32_d, int32_t rows, int32_t inter,

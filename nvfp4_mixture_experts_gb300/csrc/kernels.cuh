@@ -59,6 +59,10 @@ __global__ void quant_inter_kernel(const float* s, const int32_t* counts, const 
 __global__ void combine_kernel(const float* y, const int32_t* inv, const int32_t* offsets,
                                int shared_group, int T, int H, int k, int add_shared,
                                uint16_t* out);
+__global__ void prepare_weights_kernel(const uint8_t* codes, const uint8_t* sf,
+                                       const float* glob, int N, int K, int convention,
+                                       float fold_target, int swap_halves, int off, int count,
+                                       uint8_t* codes_out, uint8_t* sf_out, float* gs_out);
 __global__ void repack_tiles_kernel(const uint8_t* codes, const uint8_t* sf, int nexp, int N,
                                     int K, int interleave, int nibble_pairs, uint8_t* dst);
 

@@ -313,6 +313,58 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     *reinterpret_cast<uint4*>(out + (size_t)t * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// ---------------------------------------------------------------- checkpoint weights
+// One matrix type of a checkpoint (codes [E][N][K/2], E4M3 scales [E][N][K/16], a global
+// value per expert) -> the library's convention for experts off..off+count-1: global given
+// as the encode scale (convention 0) or as a dequantisation multiplier m (1: gs = 1/m);
+// fold_target > 0 folds each expert's global into its block scales relative to that
+// common scale (r = gs_t / gs, sf' = E4M3(sf * r), nearest even, saturating at 448) and
+// gives every expert gs_t; swap_halves puts rows N/2..N-1 first.  Codes are copied.
+// A warp per output row: the row's codes in 16-byte pieces, its scales 4 bytes a lane.
+__device__ __forceinline__ uint32_t fold_scale_byte(uint32_t v, float r)
+{
+    const float sv = e4m3_to_f32(v & 0x7Fu);  // the sign bit, if set, is kept
+    return f32_to_e4m3(__fmul_rn((v & 0x80u) ? -sv : sv, r));
+}
+
+__global__ void __launch_bounds__(256) prepare_weights_kernel(
+    const uint8_t* __restrict__ codes, const uint8_t* __restrict__ sf,
+    const float* __restrict__ glob, int N, int K, int convention, float fold_target,
+    int swap_halves, int off, int count, uint8_t* __restrict__ codes_out,
+    uint8_t* __restrict__ sf_out, float* __restrict__ gs_out)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = (int64_t)count * N;
+    const int cpr = K / 32, spr = K / 64;  // 16-byte code pieces, 4-byte scale words per row
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; row < rows;
+         row += nwarps) {
+        const int64_t e = row / N;
+        const int n = (int)(row - e * N);
+        const int sn = swap_halves ? (n + N / 2) % N : n;
+        const int64_t src = (off + e) * N + sn;
+        const uint4* cs = reinterpret_cast<const uint4*>(codes) + src * cpr;
+        uint4* cd = reinterpret_cast<uint4*>(codes_out) + row * cpr;
+        for (int i = lane; i < cpr; i += 32) cd[i] = cs[i];
+        const float g = glob[off + e];
+        const float gs = convention == 1 ? __fdiv_rn(1.0f, g) : g;
+        const uint32_t* ss = reinterpret_cast<const uint32_t*>(sf + src * (K / 16));
+        uint32_t* sd = reinterpret_cast<uint32_t*>(sf_out + row * (K / 16));
+        if (fold_target > 0.0f) {
+            const float r = __fdiv_rn(fold_target, gs);
+            for (int i = lane; i < spr; i += 32) {
+                const uint32_t w = ss[i];
+                sd[i] = fold_scale_byte(w & 0xFFu, r) | (fold_scale_byte((w >> 8) & 0xFFu, r) << 8) |
+                        (fold_scale_byte((w >> 16) & 0xFFu, r) << 16) |
+                        (fold_scale_byte(w >> 24, r) << 24);
+            }
+        } else {
+            for (int i = lane; i < spr; i += 32) sd[i] = ss[i];
+        }
+        if (n == 0 && lane == 0) gs_out[e] = fold_target > 0.0f ? fold_target : gs;
+    }
+}
+
 // ---------------------------------------------------------------- weight re-layout
 //
 // Canonical codes [nexp][N][K/2] and scales [nexp][N][K/16] -> one contiguous blob per
