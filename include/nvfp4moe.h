@@ -283,7 +283,8 @@ MOE_API moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* 
                        size_t ws_bytes, moe_stream_t stream);
 
 /* Where moe_forward keeps its intermediates inside the workspace (device pointers into
- * ws_d), so callers can inspect them after a forward.  Any pointer may be NULL.  inter_gs:
+ * ws_d), so callers can inspect them after a forward.  Any pointer may be NULL.  Unlike
+ * moe_permute's, the forward's perm_src leaves padding rows unmarked (stale).  inter_gs:
  * the dynamic intermediate scale of the last forward (set only in that mode). */
 MOE_API moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** topk_ids,
                                float** topk_w, int32_t** expert_counts,

@@ -275,13 +275,15 @@ moe_status launch_route(const moe_layer* h, const void* x, const float* logits_i
         src = logits_scratch;
         clear0 = clear1 = nullptr;  // done by the router
     }
-    return launch(topk_kernel, dim3(ceil_div(T, 8)), dim3(256), 0, s, pdl, src,
+    return launch(topk_kernel, dim3(ceil_div(T, 4)), dim3(128), 0, s, pdl, src,
                   nsplit, bias, T, c.num_experts, c.top_k, ids, w, logits_out, clear0, clear1);
 }
 
+// write_padding: mark padding rows of perm_src with -1 (the staged call's contract; the
+// forward's own kernels never read them, so it skips the writes where it can).
 moe_status launch_permute(const moe_layer* h, const Plan& p, const int32_t* ids, int T,
                           int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* inv,
-                          void* ws, bool pdl, cudaStream_t s)
+                          void* ws, bool pdl, cudaStream_t s, bool write_padding = true)
 {
     const moe_config& c = h->cfg;
     uint32_t* status = at<uint32_t>(ws, p.status);
@@ -289,9 +291,10 @@ moe_status launch_permute(const moe_layer* h, const Plan& p, const int32_t* ids,
     int32_t* blkoff = at<int32_t>(ws, p.blkoff);
     int32_t* mb_start = at<int32_t>(ws, p.mb_start);
     if (p.nblk == 1)  // every pair fits one block: the whole grouping in one CTA
-        return launch(perm_small_kernel, dim3(1), dim3(1024), 0, s, pdl, ids, p.Tk,
-                      c.num_experts, c.local_expert_offset, p.El, T, c.top_k,
-                      shared_rows(h, T), p.cap, counts, offsets, mb_start, perm_src, inv, status);
+        return launch(perm_small_kernel, dim3(1), dim3(1024), perm_small_smem(p.G), s, pdl, ids,
+                      p.Tk, c.num_experts, c.local_expert_offset, p.El, T, c.top_k,
+                      shared_rows(h, T), p.cap, write_padding ? 1 : 0, counts, offsets,
+                      mb_start, perm_src, inv, status);
     moe_status r = launch(perm_hist_kernel, dim3(p.nblk), dim3(256), 0, s, pdl, ids, p.Tk,
                           c.num_experts, c.local_expert_offset, p.El, hist, status);
     if (r == MOE_OK)
@@ -619,6 +622,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     ok = ok &&
          cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kRouterSmem) == cudaSuccess &&
+         cudaFuncSetAttribute(perm_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              perm_small_smem(kMaxExperts + 1)) == cudaSuccess &&
          cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemLimit) == cudaSuccess &&
          set_w4a16_smem_limits();
@@ -854,7 +859,8 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
     uint32_t* amax = at<uint32_t>(ws, p.amax);
     moe_status r = launch_route(h, x_bf16_d, logits_in_d, logit_bias_d, T, ids, w, nullptr,
                                 at<float>(ws, p.logits), status, status, amax, true, s);
-    if (r == MOE_OK) r = launch_permute(h, p, ids, T, counts, offsets, perm_src, inv, ws, true, s);
+    if (r == MOE_OK)
+        r = launch_permute(h, p, ids, T, counts, offsets, perm_src, inv, ws, true, s, false);
     if (r == MOE_OK)
         r = launch_gather(h, p, x_bf16_d, T, inv, offsets, a_codes, a_sf, a_bf16, gs_a, ws, true,
                           true, s);
@@ -933,7 +939,7 @@ moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
         if (r != MOE_OK) return r;
         src = scratch;
     }
-    return launch(topk_kernel, dim3(ceil_div(T, 8)), dim3(256), 0, s, false, src, nsplit,
+    return launch(topk_kernel, dim3(ceil_div(T, 4)), dim3(128), 0, s, false, src, nsplit,
                   logit_bias_d, (int)T, c.num_experts, c.top_k, topk_ids_d, topk_w_d,
                   logits_out_d, (uint32_t*)nullptr, (uint32_t*)nullptr);
 }

@@ -30,10 +30,12 @@ __global__ void perm_scan_kernel(const int32_t* hist, int nblk, int El, int T, i
                                  int shared_rows, int rows_cap, int32_t* blkoff,
                                  int32_t* counts, int32_t* offsets, int32_t* mb_start,
                                  int32_t* perm_src, uint32_t* status);
+// dynamic shared memory of perm_small_kernel: the per-warp count table [32][G] uint16
+inline int perm_small_smem(int G) { return 32 * G * 2; }
 __global__ void perm_small_kernel(const int32_t* ids, int P, int E, int off, int El, int T,
-                                  int k, int shared_rows, int rows_cap, int32_t* counts,
-                                  int32_t* offsets, int32_t* mb_start, int32_t* perm_src,
-                                  int32_t* inv, uint32_t* status);
+                                  int k, int shared_rows, int rows_cap, int write_padding,
+                                  int32_t* counts, int32_t* offsets, int32_t* mb_start,
+                                  int32_t* perm_src, int32_t* inv, uint32_t* status);
 __global__ void perm_scatter_kernel(const int32_t* ids, int P, int E, int off, int El,
                                     const int32_t* blkoff, const int32_t* offsets,
                                     int rows_cap, int32_t* perm_src, int32_t* inv);

@@ -151,29 +151,34 @@ __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
 
 int router_splits(int T, int E, int H, int num_sms)
 {
-    // at most 4 partial planes: more CTAs would make the top-k's plane sum the bottleneck
+    // Split K over more CTAs while the grid fills the GPU: up to 16 partial planes for small
+    // batches (a weight stream, and the top-k's plane sum is small), 4 for large ones (where
+    // that sum would dominate).  Each split is a whole number of 64-element k-steps, >= 256.
     const int bn = router_bn(T, E);
     const int tiles = ((T + 127) / 128) * ((E + bn - 1) / bn);
+    const int cap = T <= 256 ? 16 : 4;
     int s = 1;
-    while (s < 4 && s * 2 * 256 <= H && tiles * s * 2 <= num_sms) s *= 2;
+    while (s < cap && H % (2 * s * 64) == 0 && H / (2 * s) >= 256 && tiles * s * 2 <= num_sms)
+        s *= 2;
     return s;
 }
 
 // ---------------------------------------------------------------- softmax top-k
 //
-// Block of 8 warps = 8 tokens.  The block first sums the nsplit partial-sum planes (in plane
-// order) and adds the bias into shared memory, with many loads in flight; then each warp
-// takes k rounds of an arg-max over its token's logits (larger value first, equal values:
-// lower id first).  Lane j keeps the j-th selection; w_j = exp(l_j - l_0) / sum_i
-// exp(l_i - l_0) over the selected logits.
-constexpr int kTopkTokens = 8;
+// A warp per token (4 per block).  Lane l holds the logits of experts l, l+32, ... in
+// registers: each is the sum of the nsplit partial-sum planes in plane order plus the bias,
+// the planes read four at a time with every load in flight.  Then k rounds of a warp
+// arg-max (larger value first, equal values: lower id first); only the lane whose element
+// was taken rescans its registers.  Lane j keeps the j-th selection; w_j = exp(l_j - l_0) /
+// sum_i exp(l_i - l_0) over the selected logits.
+constexpr int kTopkTokens = 4;
+constexpr int kTopkPerLane = kMaxExperts / 32;
 
-__global__ void __launch_bounds__(256) topk_kernel(
+__global__ void __launch_bounds__(32 * kTopkTokens) topk_kernel(
     const float* __restrict__ logits_src, int nsplit, const float* __restrict__ bias, int T,
     int E, int k, int32_t* __restrict__ ids, float* __restrict__ wts,
     float* __restrict__ logits_out, uint32_t* clear0, uint32_t* clear1)
 {
-    __shared__ float sl[kTopkTokens][kMaxExperts];
     pdl_wait();
     if (threadIdx.x == 0) {
         pdl_trigger();
@@ -182,44 +187,65 @@ __global__ void __launch_bounds__(256) topk_kernel(
             if (clear1) clear1[0] = clear1[1] = 0u;  // both amax accumulators
         }
     }
-    const int t0 = blockIdx.x * kTopkTokens;
-    const int nt = min(kTopkTokens, T - t0);
-    const size_t plane = (size_t)T * E;
-    for (int idx = threadIdx.x; idx < nt * E; idx += blockDim.x) {
-        const size_t off = (size_t)t0 * E + idx;
-        float pl[4];  // the router uses at most 4 planes; all loads issued before the sum
-#pragma unroll
-        for (int sp = 0; sp < 4; ++sp) pl[sp] = sp < nsplit ? logits_src[off + sp * plane] : 0.0f;
-        float l = pl[0];
-#pragma unroll
-        for (int sp = 1; sp < 4; ++sp)
-            if (sp < nsplit) l += pl[sp];
-        const int e = idx % E;
-        l += bias ? bias[e] : 0.0f;
-        sl[idx / E][e] = l;
-        if (logits_out) logits_out[off] = l;
-    }
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp >= nt) return;
-    const int t = t0 + warp;
-    const float* v = sl[warp];
-    uint32_t used = 0;
+    const int t = blockIdx.x * kTopkTokens + warp;
+    if (t >= T) return;
+    const int ne = (E + 31) / 32;
+    const size_t plane = (size_t)T * E;
+    const float* row = logits_src + (size_t)t * E;
+    float v[kTopkPerLane];
+#pragma unroll
+    for (int i = 0; i < kTopkPerLane; ++i) {
+        const int e = i * 32 + lane;
+        v[i] = (i < ne && e < E) ? row[e] : 0.0f;
+    }
+    for (int sp0 = 1; sp0 < nsplit; sp0 += 4) {  // planes 1.. in order, four at a time
+        float p[4][kTopkPerLane];
+#pragma unroll
+        for (int d = 0; d < 4; ++d)
+#pragma unroll
+            for (int i = 0; i < kTopkPerLane; ++i) {
+                const int e = i * 32 + lane;
+                p[d][i] = (sp0 + d < nsplit && i < ne && e < E)
+                              ? row[(size_t)(sp0 + d) * plane + e] : 0.0f;
+            }
+#pragma unroll
+        for (int d = 0; d < 4; ++d)
+#pragma unroll
+            for (int i = 0; i < kTopkPerLane; ++i)
+                if (sp0 + d < nsplit) v[i] += p[d][i];
+    }
+    uint32_t live = 0;  // bit i: element i of this lane is a valid, unselected expert
+#pragma unroll
+    for (int i = 0; i < kTopkPerLane; ++i) {
+        const int e = i * 32 + lane;
+        if (i < ne && e < E) {
+            v[i] += bias ? bias[e] : 0.0f;
+            if (logits_out) logits_out[(size_t)t * E + e] = v[i];
+            live |= 1u << i;
+        }
+    }
+    // this lane's best remaining element
+    auto lane_best = [&](float& best, int& be) {
+        best = -INFINITY;
+        be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < kTopkPerLane; ++i) {
+            const int e = i * 32 + lane;
+            if (((live >> i) & 1u) && (v[i] > best || (v[i] == best && e < be))) {
+                best = v[i];
+                be = e;
+            }
+        }
+    };
+    float lb;
+    int le;
+    lane_best(lb, le);
     float my_l = 0.0f;
     int my_e = 0;
     for (int j = 0; j < k; ++j) {
-        float best = -INFINITY;
-        int be = 0x7fffffff;
-        for (int i = 0; i * 32 < E; ++i) {
-            const int e = i * 32 + lane;
-            if (e < E && !((used >> i) & 1u)) {
-                const float x = v[e];
-                if (x > best || (x == best && e < be)) {
-                    best = x;
-                    be = e;
-                }
-            }
-        }
+        float best = lb;
+        int be = le;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float ob = __shfl_xor_sync(0xffffffffu, best, o);
@@ -229,10 +255,13 @@ __global__ void __launch_bounds__(256) topk_kernel(
                 be = oe;
             }
         }
-        if ((be & 31) == lane) used |= 1u << (be >> 5);
         if (lane == j) {
             my_l = best;
             my_e = be;
+        }
+        if (be == le) {  // this lane's element was taken: drop it, rescan
+            live &= ~(1u << (le >> 5));
+            lane_best(lb, le);
         }
     }
     const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
@@ -424,39 +453,45 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(
 }
 
 // The whole grouping in one CTA when every pair fits one block (decode): per-expert counts,
-// the scans, the stable scatter and the padding markers.  Same outputs as hist + scan +
-// scatter.
+// the scans, the stable scatter and (write_padding) the padding markers.  Same outputs as
+// hist + scan + scatter.  Thread i takes pair i (P <= 1024 = 32 warps x 32 lanes): its rank
+// inside its group is (pairs of that group in earlier warps) + (earlier lanes of its warp),
+// the first from a per-warp count table (dynamic shared memory, [32][G] uint16) turned into
+// an exclusive prefix over warps by one thread per group.
 __global__ void __launch_bounds__(1024) perm_small_kernel(
     const int32_t* __restrict__ ids, int P, int E, int off, int El, int T, int k,
-    int shared_rows, int rows_cap, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ mb_start, int32_t* __restrict__ perm_src, int32_t* __restrict__ inv,
-    uint32_t* status)
+    int shared_rows, int rows_cap, int write_padding, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ mb_start, int32_t* __restrict__ perm_src,
+    int32_t* __restrict__ inv, uint32_t* status)
 {
     pdl_wait();
     if (threadIdx.x == 0) pdl_trigger();
     __shared__ int32_t s_cnt[kMaxExperts + 1];
     __shared__ int32_t s_pad[kMaxExperts + 2];
     __shared__ int32_t s_mb[kMaxExperts + 2];
-    __shared__ int32_t le_s[kPairsPerBlock];
     __shared__ int32_t s_wp[32], s_wm[32];
+    extern __shared__ uint16_t s_wtab[];  // [32][G]: pairs of group g in warp w, then prefix
     const int G = El + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = g < El ? 0 : shared_rows;
+    for (int x = threadIdx.x; x < 32 * G; x += blockDim.x) s_wtab[x] = 0;
     __syncthreads();
-    bool bad = false;
-    for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    // local expert of pair i (-1: dropped), per-expert counts, per-warp counts and ranks
+    const int i = threadIdx.x;
+    int le = -1;
+    if (i < P) {
         const int id = ids[i];
-        int le = -1;
         if (id < 0 || id >= E) {
-            bad = true;
+            set_status(status, MOE_DEV_BAD_EXPERT_ID);
         } else {
             le = id - off;
             if (le < 0 || le >= El) le = -1;
             else atomicAdd(&s_cnt[le], 1);
         }
-        le_s[i] = le;
     }
-    if (bad) set_status(status, MOE_DEV_BAD_EXPERT_ID);
+    const uint32_t grp = __match_any_sync(0xffffffffu, le);
+    const int rank = __popc(grp & ((1u << lane) - 1u));
+    if (le >= 0 && rank == 0) s_wtab[warp * G + le] = (uint16_t)__popc(grp);
     __syncthreads();
     const int g0 = 2 * threadIdx.x;
     const int c0 = g0 < G ? s_cnt[g0] : 0, c1 = g0 + 1 < G ? s_cnt[g0 + 1] : 0;
@@ -474,6 +509,15 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(
     if (lane == 31) {
         s_wp[warp] = xp;
         s_wm[warp] = xm;
+    }
+    // per group: exclusive prefix of its per-warp counts over the warps
+    if (threadIdx.x < G) {
+        int run = 0;
+        for (int w = 0; w < 32; ++w) {
+            const int c = s_wtab[w * G + threadIdx.x];
+            s_wtab[w * G + threadIdx.x] = (uint16_t)run;
+            run += c;
+        }
     }
     __syncthreads();
     if (warp == 0) {
@@ -507,37 +551,23 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(
         mb_start[g] = s_mb[g];
         if (g < G) counts[g] = s_cnt[g];
     }
-    for (int g = warp; g < G; g += 32) {  // padding markers and shared rows
-        const int start = s_pad[g], n = s_cnt[g], end = min(s_pad[g + 1], rows_cap);
-        for (int r = start + (g == El ? 0 : n) + lane; r < end; r += 32) {
-            const int i = r - start;
-            perm_src[r] = i < n ? T * k + i : -1;
+    // the stable scatter: the pair's row, and its inverse
+    if (i < P) {
+        int row = -1;
+        if (le >= 0) {
+            row = s_pad[le] + s_wtab[warp * G + le] + rank;
+            if (row >= rows_cap) row = -1;
+            else perm_src[row] = i;
         }
+        inv[i] = row;
     }
-    __syncthreads();  // every reader of s_pad is done before warp 0 advances it as a cursor
-    if (warp != 0) return;
-    // stable scatter: one warp walks the pairs in order (s_pad doubles as the cursor)
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int base = 0; base < P; base += 32) {
-        const int i = base + lane;
-        const int le = i < P ? le_s[i] : -1;
-        const uint32_t grp = __match_any_sync(0xffffffffu, le);
-        const int leader = __ffs(grp) - 1;
-        int b = 0;
-        if (le >= 0 && lane == leader) {
-            b = s_pad[le];
-            s_pad[le] = b + __popc(grp);
-        }
-        b = __shfl_sync(0xffffffffu, b, leader);
-        __syncwarp();
-        if (i < P) {
-            int row = -1;
-            if (le >= 0) {
-                row = b + __popc(grp & lt);
-                if (row >= rows_cap) row = -1;
-                else perm_src[row] = i;
-            }
-            inv[i] = row;
+    // shared rows, and the padding markers when asked for
+    for (int g = warp; g < G; g += 32) {
+        const int start = s_pad[g], n = s_cnt[g], end = min(s_pad[g + 1], rows_cap);
+        const int r_end = (write_padding || g == El) ? end : start;
+        for (int r = start + (g == El ? 0 : n) + lane; r < r_end; r += 32) {
+            const int q = r - start;
+            perm_src[r] = q < n ? T * k + q : -1;
         }
     }
 }

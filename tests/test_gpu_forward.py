@@ -102,7 +102,9 @@ def _forward_buffers_check(h, T, ora, clear, x, wr, bias=None):
         ac = _read_ws(h, b["a_codes"], rows * pitch, np.uint8)
         asf = _read_ws(h, b["a_sf"], rows * H // 16, np.uint8)
         c, s = tiled_to_canonical(ac, asf, rows, H)
-        valid = np.nonzero(perm >= 0)[0]
+        # the forward's padding rows are not marked: valid rows from counts and offsets
+        valid = np.concatenate([np.arange(offsets[g], offsets[g] + counts[g])
+                                for g in range(El + 1)]).astype(np.int64)
         tok = np.where(perm[valid] < T * k, perm[valid] // k, perm[valid] - T * k)
         assert np.array_equal(c[valid], ora.x_codes[tok])
         assert np.array_equal(s[valid], ora.x_sf[tok])
