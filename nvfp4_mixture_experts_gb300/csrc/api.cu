@@ -275,8 +275,9 @@ moe_status launch_route(const moe_layer* h, const void* x, const float* logits_i
         src = logits_scratch;
         clear0 = clear1 = nullptr;  // done by the router
     }
-    return launch(topk_kernel, dim3(ceil_div(T, 4)), dim3(128), 0, s, pdl, src,
-                  nsplit, bias, T, c.num_experts, c.top_k, ids, w, logits_out, clear0, clear1);
+    return launch(topk_kernel, dim3(ceil_div(T, topk_tokens_per_block(nsplit))),
+                  dim3(kTopkThreads), topk_smem(nsplit, c.num_experts), s, pdl, src, nsplit,
+                  bias, T, c.num_experts, c.top_k, ids, w, logits_out, clear0, clear1);
 }
 
 // write_padding: mark padding rows of perm_src with -1 (the staged call's contract; the
@@ -624,6 +625,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
                               kRouterSmem) == cudaSuccess &&
          cudaFuncSetAttribute(perm_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               perm_small_smem(kMaxExperts + 1)) == cudaSuccess &&
+         cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)topk_smem(1, kMaxExperts)) == cudaSuccess &&
          cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemLimit) == cudaSuccess &&
          set_w4a16_smem_limits();
@@ -939,7 +942,8 @@ moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
         if (r != MOE_OK) return r;
         src = scratch;
     }
-    return launch(topk_kernel, dim3(ceil_div(T, 4)), dim3(128), 0, s, false, src, nsplit,
+    return launch(topk_kernel, dim3(ceil_div(T, topk_tokens_per_block(nsplit))),
+                  dim3(kTopkThreads), topk_smem(nsplit, c.num_experts), s, false, src, nsplit,
                   logit_bias_d, (int)T, c.num_experts, c.top_k, topk_ids_d, topk_w_d,
                   logits_out_d, (uint32_t*)nullptr, (uint32_t*)nullptr);
 }

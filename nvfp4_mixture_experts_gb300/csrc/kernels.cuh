@@ -21,6 +21,11 @@ __global__ void router_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                                    uint32_t* clear0, uint32_t* clear1);
 int router_splits(int T, int E, int H, int num_sms);
 int router_bn(int T, int E);
+// top-k launch shape: 512 threads per block of topk_tokens_per_block(nsplit) tokens,
+// topk_smem(nsplit, E) bytes of dynamic shared memory (at most 16 * E floats)
+__host__ __device__ int topk_tokens_per_block(int nsplit);
+size_t topk_smem(int nsplit, int E);
+constexpr int kTopkThreads = 512;
 __global__ void topk_kernel(const float* logits_src, int nsplit, const float* bias, int T,
                             int E, int k, int32_t* ids, float* wts, float* logits_out,
                             uint32_t* clear0, uint32_t* clear1);

@@ -165,20 +165,46 @@ int router_splits(int T, int E, int H, int num_sms)
 
 // ---------------------------------------------------------------- softmax top-k
 //
-// A warp per token (4 per block).  Lane l holds the logits of experts l, l+32, ... in
-// registers: each is the sum of the nsplit partial-sum planes in plane order plus the bias,
-// the planes read four at a time with every load in flight.  Then k rounds of a warp
-// arg-max (larger value first, equal values: lower id first); only the lane whose element
-// was taken rescans its registers.  Lane j keeps the j-th selection; w_j = exp(l_j - l_0) /
+// A block of 16 warps per topk_tokens_per_block(nsplit) consecutive tokens, so that the
+// block holds 16 partial-sum rows (nsplit planes x tokens).  All threads first copy those
+// rows, contiguous within each plane, into shared memory with every load in flight at once;
+// then each logit is the sum of its nsplit partials in plane order plus the bias.  Warp j
+// selects for token j: lane l holds experts l, l+32, ... as order-preserving integer keys,
+// and each of the k rounds is a warp max over the keys, then a warp min over the ids that
+// hold it (larger value first; equal values: lower id first); only the lane whose element
+// was taken rescans.  Lane j keeps the j-th selection; w_j = exp(l_j - l_0) /
 // sum_i exp(l_i - l_0) over the selected logits.
-constexpr int kTopkTokens = 4;
+constexpr int kTopkWarps = 16;
 constexpr int kTopkPerLane = kMaxExperts / 32;
 
-__global__ void __launch_bounds__(32 * kTopkTokens) topk_kernel(
+__host__ __device__ int topk_tokens_per_block(int nsplit)
+{
+    return nsplit >= kTopkWarps ? 1 : kTopkWarps / nsplit;
+}
+
+size_t topk_smem(int nsplit, int E)
+{
+    return (size_t)nsplit * topk_tokens_per_block(nsplit) * E * sizeof(float);
+}
+
+// Unsigned keys in the order of the floats (no NaNs); -0 ranks with +0.
+__device__ __forceinline__ uint32_t order_key(float f)
+{
+    const uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+__global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(
     const float* __restrict__ logits_src, int nsplit, const float* __restrict__ bias, int T,
     int E, int k, int32_t* __restrict__ ids, float* __restrict__ wts,
     float* __restrict__ logits_out, uint32_t* clear0, uint32_t* clear1)
 {
+    extern __shared__ float s_part[];  // [nsplit][tokens of this block][E]
     pdl_wait();
     if (threadIdx.x == 0) {
         pdl_trigger();
@@ -187,90 +213,109 @@ __global__ void __launch_bounds__(32 * kTopkTokens) topk_kernel(
             if (clear1) clear1[0] = clear1[1] = 0u;  // both amax accumulators
         }
     }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kTopkTokens + warp;
-    if (t >= T) return;
-    const int ne = (E + 31) / 32;
+    const int tpb = topk_tokens_per_block(nsplit);
+    const int t0 = blockIdx.x * tpb;
+    const int nt = min(tpb, T - t0);
+    const int per = nt * E;  // floats of this block in one plane
+    uint32_t dyn_smem;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_smem));
+    if (blockDim.x != 32 * kTopkWarps || dyn_smem < (uint32_t)(nsplit * per) * 4u) return;
     const size_t plane = (size_t)T * E;
-    const float* row = logits_src + (size_t)t * E;
-    float v[kTopkPerLane];
+    const float* src = logits_src + (size_t)t0 * E;
+    const int nthr = blockDim.x;
+    if ((E & 3) == 0 && (reinterpret_cast<uintptr_t>(logits_src) & 15) == 0) {  // 16-byte rows
+        const int per4 = per >> 2, n4 = nsplit * per4;
+        const size_t plane4 = plane >> 2;
+        const float4* src4 = reinterpret_cast<const float4*>(src);
+        float4* dst4 = reinterpret_cast<float4*>(s_part);
+        for (int q0 = threadIdx.x; q0 < n4; q0 += 4 * nthr) {
+            float4 r[4];
 #pragma unroll
-    for (int i = 0; i < kTopkPerLane; ++i) {
-        const int e = i * 32 + lane;
-        v[i] = (i < ne && e < E) ? row[e] : 0.0f;
-    }
-    for (int sp0 = 1; sp0 < nsplit; sp0 += 4) {  // planes 1.. in order, four at a time
-        float p[4][kTopkPerLane];
-#pragma unroll
-        for (int d = 0; d < 4; ++d)
-#pragma unroll
-            for (int i = 0; i < kTopkPerLane; ++i) {
-                const int e = i * 32 + lane;
-                p[d][i] = (sp0 + d < nsplit && i < ne && e < E)
-                              ? row[(size_t)(sp0 + d) * plane + e] : 0.0f;
+            for (int u = 0; u < 4; ++u) {
+                const int q = q0 + u * nthr;
+                if (q < n4) {
+                    const int sp = q / per4;
+                    r[u] = src4[sp * plane4 + (q - sp * per4)];
+                }
             }
 #pragma unroll
-        for (int d = 0; d < 4; ++d)
+            for (int u = 0; u < 4; ++u)
+                if (q0 + u * nthr < n4) dst4[q0 + u * nthr] = r[u];
+        }
+    } else {
+        const int n = nsplit * per;
+        for (int q0 = threadIdx.x; q0 < n; q0 += 8 * nthr) {
+            float r[8];
 #pragma unroll
-            for (int i = 0; i < kTopkPerLane; ++i)
-                if (sp0 + d < nsplit) v[i] += p[d][i];
+            for (int u = 0; u < 8; ++u) {
+                const int q = q0 + u * nthr;
+                if (q < n) {
+                    const int sp = q / per;
+                    r[u] = src[sp * plane + (q - sp * per)];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (q0 + u * nthr < n) s_part[q0 + u * nthr] = r[u];
+        }
     }
+    __syncthreads();
+    for (int j = threadIdx.x; j < per; j += nthr) {
+        float v = s_part[j];
+        for (int sp = 1; sp < nsplit; ++sp) v += s_part[sp * per + j];
+        if (bias) v += bias[j % E];
+        if (logits_out) logits_out[(size_t)t0 * E + j] = v;
+        s_part[j] = v;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= nt) return;
+    const float* lg = s_part + warp * E;
+    const int ne = (E + 31) / 32;
+    uint32_t key[kTopkPerLane];
     uint32_t live = 0;  // bit i: element i of this lane is a valid, unselected expert
 #pragma unroll
     for (int i = 0; i < kTopkPerLane; ++i) {
         const int e = i * 32 + lane;
-        if (i < ne && e < E) {
-            v[i] += bias ? bias[e] : 0.0f;
-            if (logits_out) logits_out[(size_t)t * E + e] = v[i];
-            live |= 1u << i;
-        }
+        const bool ok = i < ne && e < E;
+        key[i] = ok ? order_key(lg[e]) : 0u;
+        live |= (uint32_t)ok << i;
     }
-    // this lane's best remaining element
-    auto lane_best = [&](float& best, int& be) {
-        best = -INFINITY;
-        be = 0x7fffffff;
+    // this lane's best remaining element: the first (lowest id) of its largest key
+    auto lane_best = [&](uint32_t& best, uint32_t& be) {
+        best = 0u;
+        be = 0xffffffffu;
 #pragma unroll
-        for (int i = 0; i < kTopkPerLane; ++i) {
-            const int e = i * 32 + lane;
-            if (((live >> i) & 1u) && (v[i] > best || (v[i] == best && e < be))) {
-                best = v[i];
-                be = e;
+        for (int i = 0; i < kTopkPerLane; ++i)
+            if (((live >> i) & 1u) && key[i] > best) {
+                best = key[i];
+                be = (uint32_t)(i * 32 + lane);
             }
-        }
     };
-    float lb;
-    int le;
-    lane_best(lb, le);
-    float my_l = 0.0f;
-    int my_e = 0;
+    uint32_t lk, le;
+    lane_best(lk, le);
+    uint32_t my_key = 0u, my_e = 0u;
     for (int j = 0; j < k; ++j) {
-        float best = lb;
-        int be = le;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (ob > best || (ob == best && oe < be)) {
-                best = ob;
-                be = oe;
-            }
-        }
+        const uint32_t m = __reduce_max_sync(0xffffffffu, lk);
+        const uint32_t be = __reduce_min_sync(0xffffffffu, lk == m ? le : 0xffffffffu);
         if (lane == j) {
-            my_l = best;
+            my_key = m;
             my_e = be;
         }
-        if (be == le) {  // this lane's element was taken: drop it, rescan
-            live &= ~(1u << (le >> 5));
-            lane_best(lb, le);
+        if (le == be) {  // this lane's element was taken: drop it, rescan
+            live &= ~(1u << (be >> 5));
+            lane_best(lk, le);
         }
     }
+    const float my_l = key_value(my_key);
     const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
     const float ex = lane < k ? expf(my_l - l0) : 0.0f;
     float z = ex;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
     if (lane < k) {
-        ids[(size_t)t * k + lane] = my_e;
+        const int t = t0 + warp;
+        ids[(size_t)t * k + lane] = (int32_t)my_e;
         wts[(size_t)t * k + lane] = ex / z;
     }
 }

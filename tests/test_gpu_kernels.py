@@ -273,8 +273,10 @@ def test_gather_w4a16_rows_are_exact_fp16_copies(scale):
     assert np.max(np.abs(want.astype(np.float32))) <= 2.0 ** 15
 
 
-# W4A16 picks 16, 32 or 64 token rows per tile from T * k / E (here 15, 25 and 50 rows)
-@pytest.mark.parametrize("act_mode,T", [(0, 200), (2, 60), (2, 100), (2, 200)])
+# W4A16 picks 16, 32 or 64 token rows per tile from T * k / E (here 15, 25 and 50 rows);
+# W4A4 sizes its activation slots from T (32 rows at T=30, 64 at T=60, 128 at T=200)
+@pytest.mark.parametrize("act_mode,T", [(0, 30), (0, 60), (0, 200), (2, 60), (2, 100),
+                                        (2, 200)])
 def test_grouped_gemm_gateup_unfused_matches_oracle(act_mode, T):
     layer, wr, x, lg, h, (H, I, E, k, T) = _mid_problem(act_mode, T)
     st = Staged(h, bits16(x), T, k, lg)
