@@ -413,8 +413,9 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     // goes to one more pipeline stage; with many it stages TMA stores.
     const int64_t local_rows = (int64_t)p.T * c.top_k / std::max(1, c.num_local_experts);
     args.staging = (epilogue == kEpiDown && local_rows >= 16) ? kDownStaging : 0;
-    args.stages = gemm_stages(6, stage_bytes, args.staging, p.G);
-    const int smem = gemm_smem_bytes(args.stages, stage_bytes, args.staging, p.G);
+    args.rb_cap = p.cap / 128;
+    args.stages = gemm_stages(6, stage_bytes, args.staging, p.G, args.rb_cap);
+    const int smem = gemm_smem_bytes(args.stages, stage_bytes, args.staging, p.G, args.rb_cap);
     if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
     if (epilogue == kEpiDown &&
         !make_tmap(&tmY, out_f32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, p.cap, (uint64_t)N * 4, 32,

@@ -44,23 +44,20 @@ struct Tables {
     const int32_t* mb_start;  // [G+1]
     const int32_t* counts;    // [G]
     const int32_t* offsets;   // [G+1]
+    const int32_t* rb_group;  // [rb_cap] group of each 128-row block
 };
 
 // Tile t of the list: groups in order; inside a group, weight tiles in order; inside a
 // weight tile, the group's row blocks (so row blocks sharing weights run back to back).
+// Group g owns tiles [mb_start[g] * NB, mb_start[g+1] * NB), so t / NB is one of its row
+// blocks and the row-block table gives g directly.
 __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, const Tables& tb, int NB,
                                                 int t)
 {
-    int lo = 0, hi = a.G;  // largest g with mb_start[g] * NB <= t
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (tb.mb_start[mid] * NB <= t) lo = mid;
-        else hi = mid;
-    }
-    const int g = lo;
+    const int g = tb.rb_group[t / NB];
     const int nmb = tb.mb_start[g + 1] - tb.mb_start[g];
     const int local = t - tb.mb_start[g] * NB;
-    const int nb = local / nmb, mb = local % nmb;
+    const int nb = nmb == 1 ? local : local / nmb, mb = nmb == 1 ? 0 : local % nmb;
     TileInfo ti;
     ti.g = g;
     ti.nb = nb;
@@ -77,14 +74,21 @@ __device__ __forceinline__ Tables load_tables(const GemmArgs& a, int32_t* smem)
     int32_t* m = smem;
     int32_t* c = m + (a.G + 1);
     int32_t* o = c + a.G;
+    int32_t* r = o + (a.G + 1);
     for (int i = threadIdx.x; i <= a.G; i += blockDim.x) {
-        m[i] = a.mb_start[i];
+        const int m0 = a.mb_start[i];
+        m[i] = m0;
         o[i] = a.offsets[i];
-        if (i < a.G) c[i] = a.counts[i];
+        if (i < a.G) {
+            c[i] = a.counts[i];
+            const int m1 = min(a.mb_start[i + 1], a.rb_cap);
+            for (int b = max(m0, 0); b < m1; ++b) r[b] = i;
+        }
     }
     tb.mb_start = m;
     tb.counts = c;
     tb.offsets = o;
+    tb.rb_group = r;
     return tb;
 }
 
@@ -309,7 +313,8 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *ctl.tmem_slot;
-    const int ntiles = tb.mb_start[args.G] * NB;
+    // (row blocks beyond the capacity were flagged by the grouping and are not run)
+    const int ntiles = min(tb.mb_start[args.G], args.rb_cap) * NB;
 
     if (warp == 0) {
         if (lane == 0) {

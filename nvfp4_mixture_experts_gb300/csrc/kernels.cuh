@@ -104,6 +104,7 @@ struct GemmArgs {
     int Tk;                   // kEpiDown: first pair index of the shared rows (T*k)
     int stages;               // pipeline depth (<= kMaxStages; fits the shared memory)
     int staging;              // bytes of epilogue staging (kEpiDown: TMA stores of y), or 0
+    int rb_cap;               // W4A4: 128-row blocks the padded rows hold (capacity / 128)
     int raw_slots;            // W4A16: raw weight blobs in flight
     uint32_t* inter_amax;     // kEpiGateUpSwigluF32: fp32 bits of amax |s| (atomic max)
     const float* gs_i_dev;    // kEpiDown: device intermediate scale (dynamic), else gs_i
@@ -123,15 +124,15 @@ constexpr int kSmemLimit = 232448;      // dynamic shared memory per block (227 
 constexpr int kNvf4StageBytes = 16384 + 16384 + 2048 + 2048;
 constexpr int kDownStaging = 4 * 2 * 4096;  // 4 epilogue warps x 2 buffers x 32x32 fp32
 // Shared memory of a GEMM launch: stages, epilogue staging, 1 KB alignment slack, control
-// block, and the group tables (mb_start, counts, offsets).
-inline int gemm_smem_bytes(int stages, int stage_bytes, int staging, int G)
+// block, the group tables (mb_start, counts, offsets) and the group of each row block.
+inline int gemm_smem_bytes(int stages, int stage_bytes, int staging, int G, int rb_cap)
 {
-    return stages * stage_bytes + staging + 1024 + kCtlBytes + 4 * (3 * G + 2);
+    return stages * stage_bytes + staging + 1024 + kCtlBytes + 4 * (3 * G + 2) + 4 * rb_cap;
 }
-inline int gemm_stages(int want, int stage_bytes, int staging, int G)
+inline int gemm_stages(int want, int stage_bytes, int staging, int G, int rb_cap)
 {
     int s = want;
-    while (s > 2 && gemm_smem_bytes(s, stage_bytes, staging, G) > kSmemLimit) --s;
+    while (s > 2 && gemm_smem_bytes(s, stage_bytes, staging, G, rb_cap) > kSmemLimit) --s;
     return s;
 }
 __global__ void gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
