@@ -251,10 +251,13 @@ int shared_rows(const moe_layer* h, int T)
 
 // ---- launch pieces (no argument checks; callers validated)
 
+// amax_out: with the router GEMM (no logits_in), the top-k kernel also folds max |x| into
+// *amax_out (cleared by the router); returns in *amax_done whether it did.
 moe_status launch_route(const moe_layer* h, const void* x, const float* logits_in,
                         const float* bias, int T, int32_t* ids, float* w, float* logits_out,
                         float* logits_scratch, uint32_t* status, uint32_t* clear0,
-                        uint32_t* clear1, bool pdl, cudaStream_t s)
+                        uint32_t* clear1, bool pdl, cudaStream_t s, uint32_t* amax_out = nullptr,
+                        bool* amax_done = nullptr)
 {
     const moe_config& c = h->cfg;
     const float* src = logits_in;
@@ -274,10 +277,14 @@ moe_status launch_route(const moe_layer* h, const void* x, const float* logits_i
         if (r != MOE_OK) return r;
         src = logits_scratch;
         clear0 = clear1 = nullptr;  // done by the router
+    } else {
+        amax_out = nullptr;  // nothing clears it before the top-k blocks would fold into it
     }
+    if (amax_done) *amax_done = amax_out != nullptr;
     return launch(topk_kernel, dim3(ceil_div(T, topk_tokens_per_block(nsplit))),
                   dim3(kTopkThreads), topk_smem(nsplit, c.num_experts), s, pdl, src, nsplit,
-                  bias, T, c.num_experts, c.top_k, ids, w, logits_out, clear0, clear1);
+                  bias, T, c.num_experts, c.top_k, ids, w, logits_out, clear0, clear1,
+                  static_cast<const uint16_t*>(x), c.hidden, amax_out);
 }
 
 // write_padding: mark padding rows of perm_src with -1 (the staged call's contract; the
@@ -309,10 +316,12 @@ moe_status launch_permute(const moe_layer* h, const Plan& p, const int32_t* ids,
     return r;
 }
 
+// amax_zeroed: the amax word is zero (no memset); amax_ready: it already holds max |x|
+// (folded by the top-k kernel), so no amax pass runs.
 moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T,
                          const int32_t* inv, const int32_t* offsets, uint8_t* a_codes,
                          uint8_t* a_sf, void* a_bf16, float* gs_out, void* ws, bool pdl,
-                         bool amax_zeroed, cudaStream_t s)
+                         bool amax_zeroed, cudaStream_t s, bool amax_ready = false)
 {
     const moe_config& c = h->cfg;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
@@ -320,14 +329,14 @@ moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T
     const dim3 grid(grid_for((int64_t)T * ((c.hidden / 16 + 31) / 32) * 32, 256));
     uint32_t* amax = at<uint32_t>(ws, p.amax);
     const float* gs_static = nullptr;
-    if (c.act_mode != MOE_W4A4_STATIC) {
+    if (c.act_mode != MOE_W4A4_STATIC && !amax_ready) {
         if (!amax_zeroed && cudaMemsetAsync(amax, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
         const int64_t n = (int64_t)T * c.hidden;
         const int blocks = (int)std::min<int64_t>(2 * h->num_sms, std::max<int64_t>(1, n / 2048));
         const moe_status r = launch(amax_bf16_kernel, dim3(blocks), dim3(256), 0, s, pdl, xb, n,
                                     amax);
         if (r != MOE_OK) return r;
-    } else {
+    } else if (c.act_mode == MOE_W4A4_STATIC) {
         gs_static = h->act_gs;  // the handle's device copy of act_global_scale
     }
     if (c.act_mode == MOE_W4A16)
@@ -861,13 +870,16 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
     // status word and the two amax accumulators of this forward
     uint32_t* status = at<uint32_t>(ws, p.status);
     uint32_t* amax = at<uint32_t>(ws, p.amax);
+    const bool need_amax = h->cfg.act_mode != MOE_W4A4_STATIC;
+    bool amax_done = false;
     moe_status r = launch_route(h, x_bf16_d, logits_in_d, logit_bias_d, T, ids, w, nullptr,
-                                at<float>(ws, p.logits), status, status, amax, true, s);
+                                at<float>(ws, p.logits), status, status, amax, true, s,
+                                need_amax ? amax : nullptr, &amax_done);
     if (r == MOE_OK)
         r = launch_permute(h, p, ids, T, counts, offsets, perm_src, inv, ws, true, s, false);
     if (r == MOE_OK)
         r = launch_gather(h, p, x_bf16_d, T, inv, offsets, a_codes, a_sf, a_bf16, gs_a, ws, true,
-                          true, s);
+                          true, s, amax_done);
     if (r == MOE_OK)
         r = launch_gateup_fused(h, p, a_codes, a_sf, gs_a, a_bf16, counts, offsets, i_codes,
                                 i_sf, i_bf16, ws, true, s);
@@ -946,7 +958,8 @@ moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
     return launch(topk_kernel, dim3(ceil_div(T, topk_tokens_per_block(nsplit))),
                   dim3(kTopkThreads), topk_smem(nsplit, c.num_experts), s, false, src, nsplit,
                   logit_bias_d, (int)T, c.num_experts, c.top_k, topk_ids_d, topk_w_d,
-                  logits_out_d, (uint32_t*)nullptr, (uint32_t*)nullptr);
+                  logits_out_d, (uint32_t*)nullptr, (uint32_t*)nullptr,
+                  (const uint16_t*)nullptr, 0, (uint32_t*)nullptr);
 }
 
 moe_status moe_get_status(moe_handle h, void* ws_d, moe_stream_t stream, uint32_t* bits)

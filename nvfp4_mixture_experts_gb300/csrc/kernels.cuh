@@ -28,7 +28,8 @@ size_t topk_smem(int nsplit, int E);
 constexpr int kTopkThreads = 512;
 __global__ void topk_kernel(const float* logits_src, int nsplit, const float* bias, int T,
                             int E, int k, int32_t* ids, float* wts, float* logits_out,
-                            uint32_t* clear0, uint32_t* clear1);
+                            uint32_t* clear0, uint32_t* clear1, const uint16_t* x_amax, int H,
+                            uint32_t* amax_out);
 __global__ void perm_hist_kernel(const int32_t* ids, int P, int E, int off, int El,
                                  int32_t* hist, uint32_t* status);
 __global__ void perm_scan_kernel(const int32_t* hist, int nblk, int El, int T, int k,

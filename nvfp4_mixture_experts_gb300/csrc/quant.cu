@@ -95,38 +95,54 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(
     const float* gs_static, const uint32_t* amax_bits, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ sf, float* gs_out)
 {
-    pdl_wait();
-    if (threadIdx.x == 0) pdl_trigger();
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int nb = H / 16;
     const int wpt = (nb + 31) / 32;  // warps per token
-    if (gw >= T * wpt) return;
-    const int t = gw / wpt, chunk = gw % wpt;
+    const bool live = gw < T * wpt;
+    const int t = live ? gw / wpt : 0, chunk = live ? gw % wpt : 0;
+    const int b = chunk * 32 + lane;
+    const bool act = live && b < nb;  // nb % 4 == 0: the lanes of one k-step agree
+    const int nrows = k + (add_shared ? 1 : 0);  // pairs in top-k order, then the shared row
+    // destinations eight at a time (-1: a pair outside this shard)
+    auto rows_of = [&](int j0, int64_t* row) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = j0 + u;
+            row[u] = !act || j >= nrows ? -1
+                     : j < k            ? (int64_t)inv[(size_t)t * k + j]
+                                        : (int64_t)offsets[shared_group] + t;
+        }
+    };
+    // the layer input is complete before the forward starts: its load goes out before the
+    // wait; the destinations and the activation scale come from the preceding launches
+    float v[16];
+    if (act) load16_bf16(x + (size_t)t * H + b * 16, v);
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
+    if (!live) return;
+    int64_t row[8];
+    rows_of(0, row);
     const float gs = global_scale(gs_static, amax_bits);
     if (gw == 0 && lane == 0 && gs_out) *gs_out = gs;
-    int dst[kMaxTopK + 1];
-    const int nd = token_destinations(inv, offsets, t, k, shared_group, add_shared, dst);
-    if (nd == 0) return;
     const int pitch = codes_pitch(H);
-    const int b = chunk * 32 + lane;
-    const bool act = b < nb;  // nb % 4 == 0: the lanes of one k-step agree
-    float v[16];
     uint32_t c[2] = {0u, 0u}, sc = 0u;
-    if (act) {
-        load16_bf16(x + (size_t)t * H + b * 16, v);
-        sc = quant16(v, gs, c);
-    }
+    if (act) sc = quant16(v, gs, c);
     // merge the 4 scale bytes of this k-step into the lane with b % 4 == 0
     const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
     const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 2);
     const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
     const uint32_t word = sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
     if (!act) return;
-    for (int d = 0; d < nd; ++d) {
-        const int64_t row = dst[d];
-        *reinterpret_cast<uint2*>(codes + row * pitch + b * 8) = make_uint2(c[0], c[1]);
-        if ((b & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(row, b, H)) = word;
+    for (int j0 = 0; j0 < nrows; j0 += 8) {
+        if (j0) rows_of(j0, row);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (row[u] < 0) continue;
+            *reinterpret_cast<uint2*>(codes + row[u] * pitch + b * 8) = make_uint2(c[0], c[1]);
+            if ((b & 3) == 0)
+                *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(row[u], b, H)) = word;
+        }
     }
 }
 
@@ -283,26 +299,44 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       int shared_group, int T, int H, int k,
                                                       int add_shared, uint16_t* __restrict__ out)
 {
-    pdl_wait();
-    if (threadIdx.x == 0) pdl_trigger();
     const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     const int per = H / 8;
-    if (i >= (int64_t)T * per) return;
-    const int t = (int)(i / per), c = (int)(i % per) * 8;
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int j = 0; j <= k; ++j) {
-        int64_t row;
-        if (j < k) {
-            row = inv[(size_t)t * k + j];
-            if (row < 0) continue;
-        } else {
-            if (!add_shared) break;
-            row = (int64_t)offsets[shared_group] + t;
+    const bool live = i < (int64_t)T * per;
+    const int t = live ? (int)(i / per) : 0, c = live ? (int)(i % per) * 8 : 0;
+    const int nrows = k + (add_shared ? 1 : 0);  // pairs in top-k order, then the shared row
+    // rows of eight pairs at a time: their indices, then all their y loads, then the sums
+    // in order (row -1: a pair outside this shard)
+    auto rows_of = [&](int j0, int64_t* row) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = j0 + u;
+            row[u] = !live || j >= nrows ? -1
+                     : j < k             ? (int64_t)inv[(size_t)t * k + j]
+                                         : (int64_t)offsets[shared_group] + t;
         }
-        const float4* src = reinterpret_cast<const float4*>(y + row * H + c);
-        const float4 a = src[0], b = src[1];
-        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    };
+    int64_t row[8];
+    rows_of(0, row);  // inv and offsets were complete before the predecessor started
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
+    if (!live) return;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j0 = 0; j0 < nrows; j0 += 8) {
+        if (j0) rows_of(j0, row);
+        float4 v[8][2];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (row[u] >= 0) {
+                const float4* src = reinterpret_cast<const float4*>(y + row[u] * H + c);
+                v[u][0] = src[0];
+                v[u][1] = src[1];
+            }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (row[u] >= 0) {
+                acc[0] += v[u][0].x; acc[1] += v[u][0].y; acc[2] += v[u][0].z; acc[3] += v[u][0].w;
+                acc[4] += v[u][1].x; acc[5] += v[u][1].y; acc[6] += v[u][1].z; acc[7] += v[u][1].w;
+            }
     }
     uint32_t o[4];
 #pragma unroll

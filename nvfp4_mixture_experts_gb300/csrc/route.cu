@@ -173,7 +173,9 @@ int router_splits(int T, int E, int H, int num_sms)
 // and each of the k rounds is a warp max over the keys, then a warp min over the ids that
 // hold it (larger value first; equal values: lower id first); only the lane whose element
 // was taken rescans.  Lane j keeps the j-th selection; w_j = exp(l_j - l_0) /
-// sum_i exp(l_i - l_0) over the selected logits.
+// sum_i exp(l_i - l_0) over the selected logits.  With amax_out, each block also folds
+// max |x| over its tokens' rows of the layer input into *amax_out (fp32 bits, integer max;
+// the router cleared it), so the forward needs no separate amax pass.
 constexpr int kTopkWarps = 16;
 constexpr int kTopkPerLane = kMaxExperts / 32;
 
@@ -202,9 +204,31 @@ __device__ __forceinline__ float key_value(uint32_t key)
 __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(
     const float* __restrict__ logits_src, int nsplit, const float* __restrict__ bias, int T,
     int E, int k, int32_t* __restrict__ ids, float* __restrict__ wts,
-    float* __restrict__ logits_out, uint32_t* clear0, uint32_t* clear1)
+    float* __restrict__ logits_out, uint32_t* clear0, uint32_t* clear1,
+    const uint16_t* __restrict__ x_amax, int H, uint32_t* amax_out)
 {
     extern __shared__ float s_part[];  // [nsplit][tokens of this block][E]
+    __shared__ float s_xm[kTopkWarps];
+    const int tpb = topk_tokens_per_block(nsplit);
+    const int t0 = blockIdx.x * tpb;
+    const int nt = min(tpb, T - t0);
+    // max |x| over this block's token rows (the layer input is complete before the forward)
+    float xm = 0.0f;
+    if (amax_out) {
+        const int64_t n8 = (int64_t)nt * H / 8;
+        const uint4* xr = reinterpret_cast<const uint4*>(x_amax + (size_t)t0 * H);
+        for (int64_t q = threadIdx.x; q < n8; q += blockDim.x) {
+            const uint4 v = xr[q];
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                xm = fmaxf(xm, fmaxf(fabsf(bf16_bits_to_f32(u[j] & 0xFFFFu)),
+                                     fabsf(bf16_bits_to_f32(u[j] >> 16))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) xm = fmaxf(xm, __shfl_xor_sync(0xffffffffu, xm, o));
+        if ((threadIdx.x & 31) == 0) s_xm[threadIdx.x >> 5] = xm;
+    }
     pdl_wait();
     if (threadIdx.x == 0) {
         pdl_trigger();
@@ -213,9 +237,6 @@ __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(
             if (clear1) clear1[0] = clear1[1] = 0u;  // both amax accumulators
         }
     }
-    const int tpb = topk_tokens_per_block(nsplit);
-    const int t0 = blockIdx.x * tpb;
-    const int nt = min(tpb, T - t0);
     const int per = nt * E;  // floats of this block in one plane
     uint32_t dyn_smem;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_smem));
@@ -260,6 +281,11 @@ __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(
         }
     }
     __syncthreads();
+    if (amax_out && threadIdx.x == 0) {
+        float m = 0.0f;
+        for (int w = 0; w < kTopkWarps; ++w) m = fmaxf(m, s_xm[w]);
+        atomicMax(amax_out, __float_as_uint(m));  // non-negative: bits order like values
+    }
     for (int j = threadIdx.x; j < per; j += nthr) {
         float v = s_part[j];
         for (int sp = 1; sp < nsplit; ++sp) v += s_part[sp * per + j];

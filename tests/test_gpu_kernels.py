@@ -107,6 +107,28 @@ def test_topk_from_given_logits_bit_exact():
     assert np.array_equal(host(ids), rid)
 
 
+@pytest.mark.parametrize("E,k,T,offset", [(37, 5, 70, 0), (320, 32, 33, 1), (1023, 32, 17, 0),
+                                          (64, 1, 129, 1)])
+def test_topk_edge_shapes_signed_zeros_and_unaligned_logits(E, k, T, offset):
+    """E not a multiple of 4 and logits 4 bytes off a 16-byte boundary take the scalar load
+    path; k up to 32; +0 and -0 rank as equal values (lower id first); blocks of 16 tokens
+    with a ragged last block."""
+    h, _ = _tiny_layer_handle(E=E, k=k)
+    rng = np.random.default_rng(E + k)
+    lg = np.round(rng.standard_normal((T, E)) * 2).astype(np.float32) / 2
+    lg[:, ::5] = 0.0
+    lg[:, 1::7] = -0.0
+    lg[T // 2:, :] = np.abs(lg[T // 2:, :]) * -1.0  # all-negative rows (with -0 maxima)
+    buf = torch.zeros(T * E + 4, dtype=torch.float32, device="cuda")
+    buf[offset:offset + T * E] = torch.from_numpy(lg.reshape(-1)).cuda()
+    ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(h.handle, None, buf[offset:], None, T, ids, w, None, None)
+    rid, rw = oracle.topk(lg.astype(np.float64), k)
+    assert np.array_equal(host(ids), rid)
+    assert np.max(np.abs(host(w) - rw)) <= 1e-6
+
+
 def test_router_logits_and_topk_from_x():
     T, E, H, k = 200, 320, 4096, 8
     h, wr = _tiny_layer_handle(E=E, H=H, k=k)
