@@ -326,7 +326,10 @@ moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T
     const moe_config& c = h->cfg;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     const int add = shared_rows(h, T) > 0 ? 1 : 0;
-    const dim3 grid(grid_for((int64_t)T * ((c.hidden / 16 + 31) / 32) * 32, 256));
+    // a lane per 64-element k-step for large batches (1 KB pieces per destination row), per
+    // 16-element block for small ones (more threads on a latency-bound step)
+    const int bpl = T >= 1024 ? 4 : 1;
+    const dim3 grid(grid_for((int64_t)T * ((c.hidden / 16 + 32 * bpl - 1) / (32 * bpl)) * 32, 256));
     uint32_t* amax = at<uint32_t>(ws, p.amax);
     const float* gs_static = nullptr;
     if (c.act_mode != MOE_W4A4_STATIC && !amax_ready) {
@@ -344,8 +347,9 @@ moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T
                       dim3(grid_for((int64_t)T * ((c.hidden + 255) / 256) * 32, 256)), dim3(256),
                       0, s, pdl, xb, T, c.hidden, c.top_k, inv, offsets, p.El, add,
                       (const uint32_t*)amax, static_cast<uint16_t*>(a_bf16), gs_out);
-    return launch(gather_quant_kernel, grid, dim3(256), 0, s, pdl, xb, T, c.hidden, c.top_k, inv,
-                  offsets, p.El, add, gs_static, (const uint32_t*)amax, a_codes, a_sf, gs_out);
+    return launch(gather_quant_kernel_for(bpl), grid, dim3(256), 0, s, pdl, xb, T, c.hidden,
+                  c.top_k, inv, offsets, p.El, add, gs_static, (const uint32_t*)amax, a_codes,
+                  a_sf, gs_out);
 }
 
 moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilogue,

@@ -48,10 +48,13 @@ __global__ void perm_scatter_kernel(const int32_t* ids, int P, int E, int off, i
 
 // ---- quant.cu
 __global__ void amax_bf16_kernel(const uint16_t* x, int64_t n, uint32_t* amax_bits);
-__global__ void gather_quant_kernel(const uint16_t* x, int T, int H, int k, const int32_t* inv,
-                                    const int32_t* offsets, int shared_group, int add_shared,
-                                    const float* gs_static, const uint32_t* amax_bits,
-                                    uint8_t* codes, uint8_t* sf, float* gs_out);
+// NVFP4 gather-quantise of the activation rows; blocks_per_lane 1 (a lane per 16-element
+// block: more threads, for small batches) or 4 (a lane per 64-element k-step: 1 KB pieces
+// per destination row, for large batches).
+using GatherKernel = void (*)(const uint16_t*, int, int, int, const int32_t*, const int32_t*,
+                              int, int, const float*, const uint32_t*, uint8_t*, uint8_t*,
+                              float*);
+GatherKernel gather_quant_kernel_for(int blocks_per_lane);
 __global__ void gather_f16_kernel(const uint16_t* x, int T, int H, int k, const int32_t* inv,
                                   const int32_t* offsets, int shared_group, int add_shared,
                                   const uint32_t* amax_bits, uint16_t* out, float* gs_out);

@@ -89,6 +89,7 @@ __device__ __forceinline__ int token_destinations(const int32_t* inv, const int3
     return nd;
 }
 
+template <int BPL>
 __global__ void __launch_bounds__(256) gather_quant_kernel(
     const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, int shared_group, int add_shared,
@@ -98,10 +99,10 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int nb = H / 16;
-    const int wpt = (nb + 31) / 32;  // warps per token
+    const int wpt = (nb + 32 * BPL - 1) / (32 * BPL);  // warps per token
     const bool live = gw < T * wpt;
     const int t = live ? gw / wpt : 0, chunk = live ? gw % wpt : 0;
-    const int b = chunk * 32 + lane;
+    const int b = (chunk * 32 + lane) * BPL;  // this lane's first 16-element block
     const bool act = live && b < nb;  // nb % 4 == 0: the lanes of one k-step agree
     const int nrows = k + (add_shared ? 1 : 0);  // pairs in top-k order, then the shared row
     // destinations eight at a time (-1: a pair outside this shard)
@@ -116,8 +117,10 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(
     };
     // the layer input is complete before the forward starts: its load goes out before the
     // wait; the destinations and the activation scale come from the preceding launches
-    float v[16];
-    if (act) load16_bf16(x + (size_t)t * H + b * 16, v);
+    float v[16 * BPL];
+    if (act)
+#pragma unroll
+        for (int i = 0; i < BPL; ++i) load16_bf16(x + (size_t)t * H + (b + i) * 16, v + 16 * i);
     pdl_wait();
     if (threadIdx.x == 0) pdl_trigger();
     if (!live) return;
@@ -126,24 +129,42 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(
     const float gs = global_scale(gs_static, amax_bits);
     if (gw == 0 && lane == 0 && gs_out) *gs_out = gs;
     const int pitch = codes_pitch(H);
-    uint32_t c[2] = {0u, 0u}, sc = 0u;
-    if (act) sc = quant16(v, gs, c);
-    // merge the 4 scale bytes of this k-step into the lane with b % 4 == 0
-    const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
-    const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 2);
-    const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
-    const uint32_t word = sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    uint32_t c[2 * BPL], word = 0u;
+    if (BPL == 4) {  // a whole 64-element k-step per lane: its own scale word
+        if (act)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) word |= quant16(v + 16 * i, gs, c + 2 * i) << (8 * i);
+    } else {  // merge the 4 scale bytes of a k-step into the lane with b % 4 == 0
+        uint32_t sc = 0u;
+        c[0] = c[1] = 0u;
+        if (act) sc = quant16(v, gs, c);
+        const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
+        const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 2);
+        const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
+        word = sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    }
     if (!act) return;
     for (int j0 = 0; j0 < nrows; j0 += 8) {
         if (j0) rows_of(j0, row);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             if (row[u] < 0) continue;
-            *reinterpret_cast<uint2*>(codes + row[u] * pitch + b * 8) = make_uint2(c[0], c[1]);
+            uint8_t* dst = codes + row[u] * pitch + b * 8;
+            if (BPL == 4) {
+                reinterpret_cast<uint4*>(dst)[0] = make_uint4(c[0], c[1], c[2], c[3]);
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(c[4], c[5], c[6], c[7]);
+            } else {
+                *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
+            }
             if ((b & 3) == 0)
                 *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(row[u], b, H)) = word;
         }
     }
+}
+
+GatherKernel gather_quant_kernel_for(int blocks_per_lane)
+{
+    return blocks_per_lane == 4 ? gather_quant_kernel<4> : gather_quant_kernel<1>;
 }
 
 // W4A16: copy token rows (bf16) to the padded rows of their pairs and shared row; a warp
