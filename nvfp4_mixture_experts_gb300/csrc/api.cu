@@ -190,6 +190,16 @@ bool set_w4a16_smem_limits()
     return true;
 }
 
+// Every top-k instantiation may take up to 16 rows of kMaxExperts floats of shared memory.
+bool set_topk_smem_limits()
+{
+    for (int E : {128, 256, 384, 512, kMaxExperts})
+        if (cudaFuncSetAttribute(topk_kernel_for(E), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)topk_smem(1, kMaxExperts)) != cudaSuccess)
+            return false;
+    return true;
+}
+
 // Bytes of the weight blobs of one expert slot for an N x K matrix.
 size_t blob_bytes(int N, int K)
 {
@@ -281,7 +291,7 @@ moe_status launch_route(const moe_layer* h, const void* x, const float* logits_i
         amax_out = nullptr;  // nothing clears it before the top-k blocks would fold into it
     }
     if (amax_done) *amax_done = amax_out != nullptr;
-    return launch(topk_kernel, dim3(ceil_div(T, topk_tokens_per_block(nsplit))),
+    return launch(topk_kernel_for(c.num_experts), dim3(ceil_div(T, topk_tokens_per_block(nsplit))),
                   dim3(kTopkThreads), topk_smem(nsplit, c.num_experts), s, pdl, src, nsplit,
                   bias, T, c.num_experts, c.top_k, ids, w, logits_out, clear0, clear1,
                   static_cast<const uint16_t*>(x), c.hidden, amax_out);
@@ -310,7 +320,8 @@ moe_status launch_permute(const moe_layer* h, const Plan& p, const int32_t* ids,
                    p.nblk, p.El, T, c.top_k, shared_rows(h, T), p.cap, blkoff, counts, offsets,
                    mb_start, perm_src, status);
     if (r == MOE_OK)
-        r = launch(perm_scatter_kernel, dim3(p.nblk), dim3(256), 0, s, pdl, ids, p.Tk,
+        r = launch(perm_scatter_kernel, dim3(p.nblk), dim3(kPairsPerBlock),
+                   perm_small_smem(p.El), s, pdl, ids, p.Tk,
                    c.num_experts, c.local_expert_offset, p.El, (const int32_t*)blkoff,
                    (const int32_t*)offsets, p.cap, perm_src, inv);
     return r;
@@ -639,8 +650,9 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
                               kRouterSmem) == cudaSuccess &&
          cudaFuncSetAttribute(perm_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               perm_small_smem(kMaxExperts + 1)) == cudaSuccess &&
-         cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)topk_smem(1, kMaxExperts)) == cudaSuccess &&
+         cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              perm_small_smem(kMaxExperts)) == cudaSuccess &&
+         set_topk_smem_limits() &&
          cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemLimit) == cudaSuccess &&
          set_w4a16_smem_limits();
@@ -959,7 +971,7 @@ moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
         if (r != MOE_OK) return r;
         src = scratch;
     }
-    return launch(topk_kernel, dim3(ceil_div(T, topk_tokens_per_block(nsplit))),
+    return launch(topk_kernel_for(c.num_experts), dim3(ceil_div(T, topk_tokens_per_block(nsplit))),
                   dim3(kTopkThreads), topk_smem(nsplit, c.num_experts), s, false, src, nsplit,
                   logit_bias_d, (int)T, c.num_experts, c.top_k, topk_ids_d, topk_w_d,
                   logits_out_d, (uint32_t*)nullptr, (uint32_t*)nullptr,

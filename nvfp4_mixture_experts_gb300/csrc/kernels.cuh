@@ -26,17 +26,18 @@ int router_bn(int T, int E);
 __host__ __device__ int topk_tokens_per_block(int nsplit);
 size_t topk_smem(int nsplit, int E);
 constexpr int kTopkThreads = 512;
-__global__ void topk_kernel(const float* logits_src, int nsplit, const float* bias, int T,
-                            int E, int k, int32_t* ids, float* wts, float* logits_out,
-                            uint32_t* clear0, uint32_t* clear1, const uint16_t* x_amax, int H,
-                            uint32_t* amax_out);
+using TopkKernel = void (*)(const float*, int, const float*, int, int, int, int32_t*, float*,
+                            float*, uint32_t*, uint32_t*, const uint16_t*, int, uint32_t*);
+// the top-k kernel instantiated for E experts (E <= kMaxExperts)
+TopkKernel topk_kernel_for(int E);
 __global__ void perm_hist_kernel(const int32_t* ids, int P, int E, int off, int El,
                                  int32_t* hist, uint32_t* status);
 __global__ void perm_scan_kernel(const int32_t* hist, int nblk, int El, int T, int k,
                                  int shared_rows, int rows_cap, int32_t* blkoff,
                                  int32_t* counts, int32_t* offsets, int32_t* mb_start,
                                  int32_t* perm_src, uint32_t* status);
-// dynamic shared memory of perm_small_kernel: the per-warp count table [32][G] uint16
+// dynamic shared memory of perm_small_kernel (G groups) and perm_scatter_kernel (El
+// experts): the per-warp count table [32][G] uint16
 inline int perm_small_smem(int G) { return 32 * G * 2; }
 __global__ void perm_small_kernel(const int32_t* ids, int P, int E, int off, int El, int T,
                                   int k, int shared_rows, int rows_cap, int write_padding,

@@ -177,7 +177,6 @@ int router_splits(int T, int E, int H, int num_sms)
 // max |x| over its tokens' rows of the layer input into *amax_out (fp32 bits, integer max;
 // the router cleared it), so the forward needs no separate amax pass.
 constexpr int kTopkWarps = 16;
-constexpr int kTopkPerLane = kMaxExperts / 32;
 
 __host__ __device__ int topk_tokens_per_block(int nsplit)
 {
@@ -201,6 +200,8 @@ __device__ __forceinline__ float key_value(uint32_t key)
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
+// PL: expert slots per lane (E <= 32 * PL), so the selection scans no more than it holds.
+template <int PL>
 __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(
     const float* __restrict__ logits_src, int nsplit, const float* __restrict__ bias, int T,
     int E, int k, int32_t* __restrict__ ids, float* __restrict__ wts,
@@ -217,13 +218,20 @@ __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(
     if (amax_out) {
         const int64_t n8 = (int64_t)nt * H / 8;
         const uint4* xr = reinterpret_cast<const uint4*>(x_amax + (size_t)t0 * H);
-        for (int64_t q = threadIdx.x; q < n8; q += blockDim.x) {
-            const uint4 v = xr[q];
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        const int nthr = blockDim.x;
+        for (int64_t q0 = threadIdx.x; q0 < n8; q0 += 4 * nthr) {  // four loads in flight
+            uint4 v[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                xm = fmaxf(xm, fmaxf(fabsf(bf16_bits_to_f32(u[j] & 0xFFFFu)),
-                                     fabsf(bf16_bits_to_f32(u[j] >> 16))));
+            for (int d = 0; d < 4; ++d)
+                v[d] = q0 + d * nthr < n8 ? xr[q0 + d * nthr] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int d = 0; d < 4; ++d) {
+                const uint32_t u[4] = {v[d].x, v[d].y, v[d].z, v[d].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    xm = fmaxf(xm, fmaxf(fabsf(bf16_bits_to_f32(u[j] & 0xFFFFu)),
+                                         fabsf(bf16_bits_to_f32(u[j] >> 16))));
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) xm = fmaxf(xm, __shfl_xor_sync(0xffffffffu, xm, o));
@@ -298,10 +306,10 @@ __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(
     if (warp >= nt) return;
     const float* lg = s_part + warp * E;
     const int ne = (E + 31) / 32;
-    uint32_t key[kTopkPerLane];
+    uint32_t key[PL];
     uint32_t live = 0;  // bit i: element i of this lane is a valid, unselected expert
 #pragma unroll
-    for (int i = 0; i < kTopkPerLane; ++i) {
+    for (int i = 0; i < PL; ++i) {
         const int e = i * 32 + lane;
         const bool ok = i < ne && e < E;
         key[i] = ok ? order_key(lg[e]) : 0u;
@@ -312,7 +320,7 @@ __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(
         best = 0u;
         be = 0xffffffffu;
 #pragma unroll
-        for (int i = 0; i < kTopkPerLane; ++i)
+        for (int i = 0; i < PL; ++i)
             if (((live >> i) & 1u) && key[i] > best) {
                 best = key[i];
                 be = (uint32_t)(i * 32 + lane);
@@ -346,14 +354,22 @@ __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(
     }
 }
 
+TopkKernel topk_kernel_for(int E)
+{
+    return E <= 128 ? topk_kernel<4> : E <= 256 ? topk_kernel<8> : E <= 384 ? topk_kernel<12>
+         : E <= 512 ? topk_kernel<16> : topk_kernel<32>;
+}
+
 // ---------------------------------------------------------------- grouping
 //
 // Stable counting sort of the local pairs by local expert, in three launches:
-//   hist    per block of kPairsPerBlock pairs: count of each local expert
+//   hist    per block of kPairsPerBlock pairs: count of each local expert, stored
+//           expert-major (hist[e][block]) so the scan reads each expert's counts in one piece
 //   scan    per expert: prefix over blocks; per group: padded offsets, tile table,
 //           shared-expert rows and padding markers
-//   scatter per block: one warp walks its pairs in order; pairs of the same expert in a
-//           32-pair step are ranked with a match mask, so rows keep ascending pair order.
+//   scatter a thread per pair: its rank among the pairs of its expert in its warp (match
+//           mask), plus the counts of the earlier warps, plus the block's base, so rows keep
+//           ascending pair order.
 
 __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restrict__ ids, int P,
                                                         int E, int off, int El,
@@ -379,7 +395,7 @@ __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restric
     }
     if (bad) set_status(status, MOE_DEV_BAD_EXPERT_ID);
     __syncthreads();
-    for (int e = threadIdx.x; e < El; e += blockDim.x) hist[(size_t)blockIdx.x * El + e] = cnt[e];
+    for (int e = threadIdx.x; e < El; e += blockDim.x) hist[(size_t)e * gridDim.x + blockIdx.x] = cnt[e];
 }
 
 __global__ void __launch_bounds__(1024) perm_scan_kernel(
@@ -407,7 +423,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(
 #pragma unroll
                 for (int i = 0; i < kMaxBlkPerLane; ++i) {
                     const int g = gb + 32 * gi, b = lane + 32 * i;
-                    v[gi][i] = (g < El && b < nblk) ? hist[(size_t)b * El + g] : 0;
+                    v[gi][i] = (g < El && b < nblk) ? hist[(size_t)g * nblk + b] : 0;
                 }
 #pragma unroll
             for (int gi = 0; gi < kBatch; ++gi) {
@@ -425,7 +441,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(
                             if (lane >= o) x += y;
                         }
                         const int b = lane + 32 * i;
-                        if (b < nblk) blkoff[(size_t)b * El + g] = total + x - v[gi][i];
+                        if (b < nblk) blkoff[(size_t)g * nblk + b] = total + x - v[gi][i];
                         total += __shfl_sync(0xffffffffu, x, 31);
                     }
                 } else {
@@ -443,14 +459,14 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(
             if (g < El) {
                 for (int b0 = 0; b0 < nblk; b0 += 32) {
                     const int b = b0 + lane;
-                    const int v = b < nblk ? hist[(size_t)b * El + g] : 0;
+                    const int v = b < nblk ? hist[(size_t)g * nblk + b] : 0;
                     int x = v;
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) {
                         const int y = __shfl_up_sync(0xffffffffu, x, o);
                         if (lane >= o) x += y;
                     }
-                    if (b < nblk) blkoff[(size_t)b * El + g] = total + x - v;
+                    if (b < nblk) blkoff[(size_t)g * nblk + b] = total + x - v;
                     total += __shfl_sync(0xffffffffu, x, 31);
                 }
             } else {
@@ -643,7 +659,7 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(
     }
 }
 
-__global__ void __launch_bounds__(256) perm_scatter_kernel(
+__global__ void __launch_bounds__(kPairsPerBlock) perm_scatter_kernel(
     const int32_t* __restrict__ ids, int P, int E, int off, int El,
     const int32_t* __restrict__ blkoff, const int32_t* __restrict__ offsets, int rows_cap,
     int32_t* __restrict__ perm_src, int32_t* __restrict__ inv)
@@ -651,47 +667,45 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(
     pdl_wait();
     if (threadIdx.x == 0) pdl_trigger();
     __shared__ int32_t cursor[kMaxExperts];
-    __shared__ int32_t le_s[kPairsPerBlock];
-    const int p0 = blockIdx.x * kPairsPerBlock;
-    const int n = min(P, p0 + kPairsPerBlock) - p0;
+    extern __shared__ uint16_t s_wtab[];  // [32][El]: pairs of expert e in warp w, then prefix
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int e = threadIdx.x; e < El; e += blockDim.x)
-        cursor[e] = offsets[e] + blkoff[(size_t)blockIdx.x * El + e];
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const int id = ids[p0 + i];
-        int le = -1;
+        cursor[e] = offsets[e] + blkoff[(size_t)e * gridDim.x + blockIdx.x];
+    for (int x = threadIdx.x; x < 32 * El; x += blockDim.x) s_wtab[x] = 0;
+    __syncthreads();
+    // a thread per pair: local expert (-1: dropped), rank among the warp's pairs of that
+    // expert, per-warp counts
+    const int i = blockIdx.x * kPairsPerBlock + threadIdx.x;
+    int le = -1;
+    if (i < P) {
+        const int id = ids[i];
         if (id >= 0 && id < E) {
             le = id - off;
             if (le < 0 || le >= El) le = -1;
         }
-        le_s[i] = le;
+    }
+    const uint32_t grp = __match_any_sync(0xffffffffu, le);
+    const int rank = __popc(grp & ((1u << lane) - 1u));
+    if (le >= 0 && rank == 0) s_wtab[warp * El + le] = (uint16_t)__popc(grp);
+    __syncthreads();
+    for (int e = threadIdx.x; e < El; e += blockDim.x) {  // exclusive prefix over the warps
+        int run = 0;
+        for (int w = 0; w < 32; ++w) {
+            const int c = s_wtab[w * El + e];
+            s_wtab[w * El + e] = (uint16_t)run;
+            run += c;
+        }
     }
     __syncthreads();
-    if (threadIdx.x >= 32) return;
-    // one warp walks the block's pairs in order; equal experts in a 32-pair step are ranked
-    // with a match mask, so rows keep ascending pair order
-    const int lane = threadIdx.x;
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int base = 0; base < n; base += 32) {
-        const int i = base + lane;
-        const int le = i < n ? le_s[i] : -1;
-        const uint32_t grp = __match_any_sync(0xffffffffu, le);
-        const int leader = __ffs(grp) - 1;
-        int b = 0;
-        if (le >= 0 && lane == leader) {
-            b = cursor[le];
-            cursor[le] = b + __popc(grp);
+    // rows in ascending pair order within each expert: block base, warp prefix, rank
+    if (i < P) {
+        int row = -1;
+        if (le >= 0) {
+            row = cursor[le] + s_wtab[warp * El + le] + rank;
+            if (row >= rows_cap) row = -1;
+            else perm_src[row] = i;
         }
-        b = __shfl_sync(0xffffffffu, b, leader);
-        __syncwarp();
-        if (i < n) {
-            int row = -1;
-            if (le >= 0) {
-                row = b + __popc(grp & lt);
-                if (row >= rows_cap) row = -1;
-                else perm_src[row] = p0 + i;
-            }
-            inv[p0 + i] = row;
-        }
+        inv[i] = row;
     }
 }
 

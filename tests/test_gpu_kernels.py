@@ -159,10 +159,11 @@ def test_router_logits_and_topk_from_x():
 
 @pytest.mark.parametrize("T,E_loc,off,add_shared", [(1, 320, 0, 1), (64, 320, 0, 1),
                                                     (300, 160, 160, 0), (2000, 160, 0, 1),
-                                                    (2000, 37, 100, 0)])
+                                                    (2000, 37, 100, 0), (9000, 320, 0, 1)])
 def test_permute_bit_exact(T, E_loc, off, add_shared):
     E, k = 320, 8
-    h, _ = _tiny_layer_handle(E=E, k=k, E_loc=E_loc, off=off, add_shared=add_shared)
+    h, _ = _tiny_layer_handle(E=E, k=k, E_loc=E_loc, off=off, add_shared=add_shared,
+                              max_tokens=max(T, 8192))
     rng = np.random.default_rng(T + E_loc)
     ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
     cap = h.rows_capacity(T)
