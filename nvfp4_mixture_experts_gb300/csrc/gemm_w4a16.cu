@@ -247,13 +247,22 @@ __global__ void __launch_bounds__(kW16Threads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (threadIdx.x == 0) {
-        int acc = 0;
-        for (int g = 0; g < args.G; ++g) {
+    if (warp == 0) {  // token-block starts: exclusive prefix over the groups, one warp
+        const int per = (args.G + 31) / 32, g0 = lane * per, g1 = min(args.G, g0 + per);
+        int sum = 0;
+        for (int g = g0; g < g1; ++g) sum += (c.counts[g] + BN - 1) / BN;
+        int x = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        int acc = x - sum;
+        for (int g = g0; g < g1; ++g) {
             c.tb_start[g] = acc;
             acc += (c.counts[g] + BN - 1) / BN;
         }
-        c.tb_start[args.G] = acc;
+        if (lane == 31) c.tb_start[args.G] = x;
     }
     __syncthreads();
     const uint32_t tmem = *c.tmem_slot;
