@@ -108,7 +108,7 @@ def test_topk_from_given_logits_bit_exact():
 
 
 @pytest.mark.parametrize("E,k,T,offset", [(37, 5, 70, 0), (320, 32, 33, 1), (1023, 32, 17, 0),
-                                          (64, 1, 129, 1)])
+                                          (64, 1, 129, 1), (200, 8, 40, 0), (500, 8, 20, 1)])
 def test_topk_edge_shapes_signed_zeros_and_unaligned_logits(E, k, T, offset):
     """E not a multiple of 4 and logits 4 bytes off a 16-byte boundary take the scalar load
     path; k up to 32; +0 and -0 rank as equal values (lower id first); blocks of 16 tokens
@@ -280,6 +280,24 @@ def _f16_prescale(x_bits):
         return np.float32(1.0)
     e = int(np.float32(amax).view(np.uint32) >> 23) & 0xFF
     return np.float32(2.0) ** np.float32(min(127, max(-126, 141 - e)))
+
+
+@pytest.mark.parametrize("T,H", [(60, 512), (1100, 512), (1030, 1280)])
+def test_gather_w4a4_rows_bit_exact(T, H):
+    """Every valid padded row holds its token's NVFP4 codes and scales, bit for bit: a lane
+    per 16-element block below 1024 tokens, a lane per 64-element k-step from 1024 on
+    (H = 1280: 20 k-steps, a partly idle warp per token)."""
+    E, k = 8, 2
+    h, _ = _tiny_layer_handle(E=E, H=H, I=64, k=k, max_tokens=max(T, 8192))
+    x = synth.activations(21, T, H, outlier_frac=0.01)
+    st = Staged(h, bits16(x), T, k, synth.logits_normal(21, T, E))
+    rc, rs, rg = oracle.quant_nvfp4(synth.bf16_to_f32(x))
+    assert float(host(st.gs)[0]) == rg
+    c, s = tiled_to_canonical(host(st.a_codes), host(st.a_sf), st.cap, H)
+    rows = st.rows()
+    assert len(rows) == T * (k + 1)
+    assert np.array_equal(c[rows[:, 0]], rc[rows[:, 1]])
+    assert np.array_equal(s[rows[:, 0]], rs[rows[:, 1]])
 
 
 @pytest.mark.parametrize("scale", [1.0, 3e-6, 5e4])
