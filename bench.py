@@ -12,7 +12,9 @@ device time of K CUDA-graph replays (CUDA events).  e2e: the same through the C 
 the batch copied host->device and the output device->host inside the timed region.
 roofline: the gate_up grouped GEMM (the dominant kernel), algorithmic bytes per launch /
 its CUDA-event duration measured here, against the measured HBM copy bandwidth.
-Weights (2.3-2.8 GB per step) exceed the 129 MB L2, so no L2 flush is needed between steps.
+The decode and prefill steps stream 2.3-2.8 GB of weights, far more than the 129 MB L2, so
+their steps run back to back; W4A16 sweep points that stream less than twice the L2 (T=1)
+flush it before every timed step and time the steps alone.
 """
 import argparse
 import hashlib
@@ -379,9 +381,14 @@ def roofline(layer, c, xd, lgd, bd, ws, stream, steps, pk, workload):
     a16 = c["act_mode"] == 2
     P = lambda n: C.c_void_p(b[n])
     times = {"gateup": [], "down": []}
+    # steps whose weights fit twice in L2 get an L2 flush before each timed launch
+    small = gemm_bytes(c, counts, True)[0] + gemm_bytes(c, counts, False)[0] < L2_FLUSH_BELOW
+    flush = torch.empty(L2_FLUSH_BELOW // 4, dtype=torch.float32, device="cuda") if small else None
     with torch.cuda.stream(stream):
         for i in range(steps + 3):
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            if small:
+                flush.fill_(float(i))
             e[0].record(stream)
             st = lib.moe_grouped_gemm_gateup(h, P("a_codes"), P("a_sf"), P("gs_a"),
                                              P("a_bf16"), P("expert_counts"),
@@ -389,19 +396,22 @@ def roofline(layer, c, xd, lgd, bd, ws, stream, steps, pk, workload):
                                              P("inter_sf"), P("inter_bf16"),
                                              T, C.c_void_p(ws.data_ptr()), nbytes, strm)
             e[1].record(stream)
+            if small:
+                flush.fill_(float(-i))
+            e[2].record(stream)
             st |= lib.moe_grouped_gemm_down(h, P("inter_codes"), P("inter_sf"),
                                             P("inter_bf16"),
                                             P("expert_counts"), P("expert_offsets"),
                                             P("perm_src"), P("topk_w"), P("y"), T,
                                             C.c_void_p(ws.data_ptr()), nbytes, strm)
-            e[2].record(stream)
+            e[3].record(stream)
             if st:
                 raise RuntimeError("staged GEMM call failed: %d" % st)
             if i >= 3:
                 times["gateup"].append(e)
         torch.cuda.synchronize()
     gu = statistics.mean(x[0].elapsed_time(x[1]) for x in times["gateup"]) / 1e3
-    dn = statistics.mean(x[1].elapsed_time(x[2]) for x in times["gateup"]) / 1e3
+    dn = statistics.mean(x[2].elapsed_time(x[3]) for x in times["gateup"]) / 1e3
     bytes_gu, touched, rows = gemm_bytes(c, counts, True)
     bytes_dn, _, _ = gemm_bytes(c, counts, False)
     ach = bytes_gu / gu / 1e9
@@ -529,6 +539,30 @@ def measure_weight_prep(c, stream, steps):
             "frac": round(gbs / peaks()["hbm"], 4)}
 
 
+L2_BYTES = 129 * 2 ** 20
+L2_FLUSH_BELOW = 2 * L2_BYTES
+
+
+def flushed_replays(g, stream, steps):
+    """Mean device time (ms) of `steps` graph replays, each after an L2 flush (a write of
+    twice the L2 size); only the replays are timed."""
+    import torch
+    flush = torch.empty(L2_FLUSH_BELOW // 4, dtype=torch.float32, device="cuda")
+    total = 0.0
+    with torch.cuda.stream(stream):
+        evs = []
+        for i in range(steps):
+            flush.fill_(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        total = sum(a.elapsed_time(b) for a, b in evs)
+    return total / steps
+
+
 def measure_w4a16(layer, stream, steps):
     """Side measurement of the W4A16 path (bf16 activations x NVFP4 weights, router logits
     given ~ N(0,1)) over the decode sweep T in {1, 8, 32, 128, 256}: CUDA-graph replays."""
@@ -567,12 +601,19 @@ def measure_w4a16(layer, stream, steps):
         roof = roofline(layer, cc, xd, lgd, None, ws, stream, min(steps, 20), pk, "w4a16")
         counts = staged_counts(layer, ws, T)
         wbytes = gemm_bytes(cc, counts, True)[0] + gemm_bytes(cc, counts, False)[0]
+        l2 = "no flush: the step streams %.0f MB, over twice the 129 MB L2" % (wbytes / 1e6)
+        if wbytes < L2_FLUSH_BELOW:
+            # the touched weights could stay in L2 from one step to the next: flush it before
+            # every timed step (a write larger than L2) and time only the steps
+            ms = flushed_replays(g, stream, steps)
+            l2 = "flushed before every step (the step streams %.0f MB)" % (wbytes / 1e6)
         out_rows.append({"T": T, "value": round(T / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
                          "experts_touched": roof["experts_touched"],
                          "gemm_bytes_per_step": int(wbytes),
                          "step_hbm_frac": round(wbytes / (ms / 1e3) / 1e9 / pk["hbm"], 4),
                          "gateup_us": roof["launch_us"], "gateup_frac": roof["frac"],
-                         "down_us": roof["down"]["launch_us"], "down_frac": roof["down"]["frac"]})
+                         "down_us": roof["down"]["launch_us"], "down_frac": roof["down"]["frac"],
+                         "l2": l2})
     return {"workload": "w4a16 decode sweep (bf16 x NVFP4, logits given)", "unit": "tokens/s",
             "sweep": out_rows}
 
