@@ -456,8 +456,22 @@ def measure_prefill(layer, stream, steps):
     roof = roofline(layer, c, xd, None, None, ws, stream, steps, pk, "prefill")
     counts = staged_counts(layer, ws, T)
     fl = gemm_flops(counts, c, True) + gemm_flops(counts, c, False)
+    # the layer against the combined roofline t = max(bytes / HBM, flops / FP4 peak): the
+    # two grouped GEMMs' FP4 flops and algorithmic bytes (touched weights + activation rows);
+    # FP4 peak = the measured bf16 peak x the nominal FP4 / bf16 ratio (13.5 / 2.25)
+    by = gemm_bytes(c, counts, True)[0] + gemm_bytes(c, counts, False)[0]
+    fp4_peak = pk["bf16"] * 6.0
+    t = ms / 1e3
+    t_roof = max(by / (pk["hbm"] * 1e9), fl / (fp4_peak * 1e12))
+    layer_roof = {"fp4_tflop": round(fl / 1e12, 3), "bytes": int(by),
+                  "fp4_peak_tflops": round(fp4_peak, 1), "fp4_peak_src": pk["src"] + " bf16 x 6",
+                  "hbm_frac": round(by / t / 1e9 / pk["hbm"], 4),
+                  "fp4_frac": round(fl / t / 1e12 / fp4_peak, 4),
+                  "bound": "hbm" if by / (pk["hbm"] * 1e9) >= fl / (fp4_peak * 1e12) else "tensor",
+                  "roof_us": round(t_roof * 1e6, 1), "roof_frac": round(t_roof / t, 4)}
     return {"workload": "prefill T=8192", "value": T / (ms / 1e3), "ms_per_step": ms,
-            "roofline": roof, "expert_fp4_tflops": round(fl / (ms / 1e3) / 1e12, 2)}
+            "roofline": roof, "expert_fp4_tflops": round(fl / (ms / 1e3) / 1e12, 2),
+            "layer": layer_roof}
 
 
 VARIANTS = {

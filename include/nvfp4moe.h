@@ -141,7 +141,8 @@ MOE_API int32_t moe_rows_capacity(const moe_config* cfg, int32_t T);
 
 /* Router (steps: logits, softmax + top-k).  logits = x . Wr^T (+ logit_bias) in fp32, or
  * logits_in (+ logit_bias) when given.  topk_ids_d[T][k]: the k largest logits,
- * descending, ties to the lower id; topk_w_d[T][k]: softmax over the selected logits.
+ * descending, ties to the lower id (-0 equals +0; a NaN ranks below every number);
+ * topk_w_d[T][k]: softmax over the selected logits.
  * logits_out_d (nullable): fp32 [T][E] including the bias.  x_bf16_d may be NULL when
  * logits_in_d is set.  ws: scratch for the logits when they are computed from x. */
 MOE_API moe_status moe_route_topk(moe_handle h, const void* x_bf16_d, const float* logits_in_d,

@@ -71,23 +71,11 @@ __device__ __forceinline__ void load16_bf16(const uint16_t* p, float* v)
 
 // ---------------------------------------------------------------- gather-quantise
 //
-// Each warp handles 32 consecutive 16-element blocks (512 elements) of one token, so a
-// token is spread over H/512 warps.  Lane l handles block 32*chunk + l: code stores from a
-// warp are contiguous, and the 4 blocks of one 64-element k-step sit on 4 neighbouring
-// lanes (their scale bytes are merged into one 32-bit atom word).  Destinations: the padded
-// rows of the token's local pairs (inv) and its shared row.
-__device__ __forceinline__ int token_destinations(const int32_t* inv, const int32_t* offsets,
-                                                  int t, int k, int shared_group,
-                                                  int add_shared, int* dst)
-{
-    int nd = 0;
-    for (int j = 0; j < k; ++j) {
-        const int r = inv[(size_t)t * k + j];
-        if (r >= 0) dst[nd++] = r;
-    }
-    if (add_shared) dst[nd++] = offsets[shared_group] + t;
-    return nd;
-}
+// Each warp handles 32 consecutive lanes' worth of one token: with BPL = 1 a lane per
+// 16-element block (the 4 blocks of one 64-element k-step sit on 4 neighbouring lanes and
+// their scale bytes are merged into one 32-bit atom word), with BPL = 4 a lane per k-step
+// (its own scale word).  Code stores from a warp are contiguous.  Destinations: the padded
+// rows of the token's local pairs (inv), then its shared row, read eight at a time.
 
 template <int BPL>
 __global__ void __launch_bounds__(256) gather_quant_kernel(
@@ -186,19 +174,21 @@ __global__ void __launch_bounds__(256) gather_f16_kernel(
     const int32_t* __restrict__ offsets, int shared_group, int add_shared,
     const uint32_t* amax_bits, uint16_t* __restrict__ out, float* gs_out)
 {
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int wpt = (H + 255) / 256;
+    const bool live = gw < T * wpt;
+    const int t = live ? gw / wpt : 0, c = live ? (gw % wpt) * 256 + lane * 8 : 0;
+    const bool act = live && c < H;
+    // the layer input is complete before the forward starts: its load goes out before the
+    // wait; the destinations and the prescale come from the preceding launches
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (act) v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c);
     pdl_wait();
     if (threadIdx.x == 0) pdl_trigger();
     const float gs = f16_prescale(amax_bits);
     if (blockIdx.x == 0 && threadIdx.x == 0 && gs_out) *gs_out = gs;
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    const int wpt = (H + 255) / 256;
-    if (gw >= T * wpt) return;
-    const int t = gw / wpt, c = (gw % wpt) * 256 + lane * 8;
-    int dst[kMaxTopK + 1];
-    const int nd = token_destinations(inv, offsets, t, k, shared_group, add_shared, dst);
-    if (c >= H) return;
-    const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c);
+    if (!act) return;
     const uint32_t in[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
 #pragma unroll
@@ -207,8 +197,21 @@ __global__ void __launch_bounds__(256) gather_f16_kernel(
                                             __fmul_rn(bf16_bits_to_f32(in[i] >> 16), gs));
         o[i] = *reinterpret_cast<const uint32_t*>(&h);
     }
-    for (int d = 0; d < nd; ++d)
-        *reinterpret_cast<uint4*>(out + (size_t)dst[d] * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    const int nrows = k + (add_shared ? 1 : 0);  // pairs in top-k order, then the shared row
+    for (int j0 = 0; j0 < nrows; j0 += 8) {
+        int64_t row[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = j0 + u;
+            row[u] = j >= nrows ? -1
+                     : j < k    ? (int64_t)inv[(size_t)t * k + j]
+                                : (int64_t)offsets[shared_group] + t;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (row[u] >= 0)
+                *reinterpret_cast<uint4*>(out + row[u] * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
 }
 
 // ---------------------------------------------------------------- standalone quantiser

@@ -188,9 +188,11 @@ size_t topk_smem(int nsplit, int E)
     return (size_t)nsplit * topk_tokens_per_block(nsplit) * E * sizeof(float);
 }
 
-// Unsigned keys in the order of the floats (no NaNs); -0 ranks with +0.
+// Unsigned keys in the order of the floats; -0 ranks with +0, and a NaN below -inf (key 1:
+// key 0 marks an empty slot).
 __device__ __forceinline__ uint32_t order_key(float f)
 {
+    if (f != f) return 1u;
     const uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }

@@ -129,6 +129,19 @@ def test_topk_edge_shapes_signed_zeros_and_unaligned_logits(E, k, T, offset):
     assert np.max(np.abs(host(w) - rw)) <= 1e-6
 
 
+def test_topk_nan_logits_rank_below_every_number():
+    T, E, k = 20, 64, 8
+    h, _ = _tiny_layer_handle(E=E, k=k)
+    lg = synth.logits_normal(9, T, E)
+    lg[::2, ::3] = np.nan
+    ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(h.handle, None, dev(lg), None, T, ids, w, None, None)
+    rid, rw = oracle.topk(np.where(np.isnan(lg), -np.inf, lg).astype(np.float64), k)
+    assert np.array_equal(host(ids), rid)
+    assert np.max(np.abs(host(w) - rw)) <= 1e-6
+
+
 def test_router_logits_and_topk_from_x():
     T, E, H, k = 200, 320, 4096, 8
     h, wr = _tiny_layer_handle(E=E, H=H, k=k)
