@@ -487,10 +487,39 @@ moe_status launch_gateup_fused(const moe_layer* h, const Plan& p, const uint8_t*
                   at<float>(ws, p.gs_i));
 }
 
+// Large batches move the y rows with bulk copies (combine_tma_kernel): pieces of cw columns,
+// the widest of 2048 / 1024 / 512 that divides H and lets two ring slots fit (wide pieces
+// stream better than deep rings of narrow ones: 8 KB pieces in 2 slots took 290 us for the
+// prefill combine, 4 KB pieces in 5 slots 411 us); the sums are the same as combine_kernel's.
+constexpr int kCombineTmaMinTokens = 1024;
+constexpr size_t kCombineSmemBudget = 220 * 1024;
+
 moe_status launch_combine(const moe_layer* h, const float* y, const int32_t* inv,
-                          const int32_t* offsets, int T, void* out, bool pdl, cudaStream_t s)
+                          const int32_t* offsets, int T, void* out, bool pdl, cudaStream_t s,
+                          uint32_t* status = nullptr)
 {
     const moe_config& c = h->cfg;
+    const int add = shared_rows(h, T) > 0 ? 1 : 0;
+    const int nrows = c.top_k + add;
+    if (T >= kCombineTmaMinTokens && nrows > 0 &&
+        (reinterpret_cast<uintptr_t>(y) & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 7) == 0) {
+        int cw = 0;
+        for (int w : {2048, 1024, 512})
+            if (c.hidden % w == 0 && 2 * (size_t)nrows * w * 4 <= kCombineSmemBudget) {
+                cw = w;
+                break;
+            }
+        if (cw) {
+            const int nslots = (int)std::min<size_t>(
+                kCombineMaxSlots, kCombineSmemBudget / ((size_t)nrows * cw * 4));
+            const int64_t units = (int64_t)T * (c.hidden / cw);
+            return launch(combine_tma_kernel,
+                          dim3((unsigned)std::min<int64_t>(units, h->num_sms)),
+                          dim3(kCombineTmaThreads), combine_tma_smem(nrows, cw, nslots), s, pdl,
+                          y, inv, offsets, c.num_local_experts, T, c.hidden, c.top_k, add, cw,
+                          nslots, static_cast<uint16_t*>(out), status);
+        }
+    }
     return launch(combine_kernel, dim3(grid_for((int64_t)T * (c.hidden / 8), 256)), dim3(256), 0,
                   s, pdl, y, inv, offsets, c.num_local_experts, T, c.hidden, c.top_k,
                   shared_rows(h, T) > 0 ? 1 : 0, static_cast<uint16_t*>(out));
@@ -652,6 +681,9 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
                               perm_small_smem(kMaxExperts + 1)) == cudaSuccess &&
          cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               perm_small_smem(kMaxExperts)) == cudaSuccess &&
+         cudaFuncSetAttribute(combine_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)combine_tma_smem(1, (int)(kCombineSmemBudget / 4), 1)) ==
+             cudaSuccess &&
          set_topk_smem_limits() &&
          cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemLimit) == cudaSuccess &&
@@ -902,7 +934,7 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
     if (r == MOE_OK)
         r = launch_gemm(h, p, false, kEpiDown, i_codes, i_sf, nullptr, i_bf16, counts, offsets,
                         y, nullptr, nullptr, nullptr, perm_src, w, ws, true, s);
-    if (r == MOE_OK) r = launch_combine(h, y, inv, offsets, T, out_bf16_d, true, s);
+    if (r == MOE_OK) r = launch_combine(h, y, inv, offsets, T, out_bf16_d, true, s, status);
     return r;
 }
 

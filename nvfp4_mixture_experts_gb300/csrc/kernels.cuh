@@ -71,6 +71,17 @@ __global__ void quant_inter_kernel(const float* s, const int32_t* counts, const 
 __global__ void combine_kernel(const float* y, const int32_t* inv, const int32_t* offsets,
                                int shared_group, int T, int H, int k, int add_shared,
                                uint16_t* out);
+// Bulk-copy combine for large batches: 160 threads (a copy thread, four adding warps), a
+// ring of nslots slots of (k + add_shared) row pieces of cw fp32 columns each.
+constexpr int kCombineTmaThreads = 160;
+constexpr int kCombineMaxSlots = 6;
+inline size_t combine_tma_smem(int nrows, int cw, int nslots)
+{
+    return (size_t)nslots * nrows * cw * 4 + 3 * kCombineMaxSlots * 8 + 16;
+}
+__global__ void combine_tma_kernel(const float* y, const int32_t* inv, const int32_t* offsets,
+                                   int shared_group, int T, int H, int k, int add_shared, int cw,
+                                   int nslots, uint16_t* out, uint32_t* status);
 __global__ void prepare_weights_kernel(const uint8_t* codes, const uint8_t* sf,
                                        const float* glob, int N, int K, int convention,
                                        float fold_target, int swap_halves, int off, int count,

@@ -371,6 +371,134 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     *reinterpret_cast<uint4*>(out + (size_t)t * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// The same combine for large batches, with the y rows moved by bulk copies: a work unit is
+// one token and one cw-column piece; thread 0 of warp 0 copies the piece of each of the
+// token's rows (pairs in top-k order, then its shared row; a pair outside the shard has none)
+// into a ring slot of shared memory, and warps 1-4 add them in that order (the sums of
+// combine_kernel, bit for bit), round to bf16 and store.  Every wait is bounded; a wait that
+// runs out sets MOE_DEV_WAIT_TIMEOUT (when a status word is given) and ends the CTA's work.
+__device__ __forceinline__ bool cmb_warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort)
+{
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__global__ void __launch_bounds__(kCombineTmaThreads, 1) combine_tma_kernel(
+    const float* __restrict__ y, const int32_t* __restrict__ inv,
+    const int32_t* __restrict__ offsets, int shared_group, int T, int H, int k, int add_shared,
+    int cw, int nslots, uint16_t* __restrict__ out, uint32_t* status)
+{
+    extern __shared__ __align__(128) uint8_t smem_cmb[];
+    const int nrows = k + (add_shared ? 1 : 0);
+    const size_t slot_bytes = (size_t)nrows * cw * 4;
+    float* slots = reinterpret_cast<float*>(smem_cmb);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_cmb + nslots * slot_bytes);
+    uint64_t* empty = full + kCombineMaxSlots;
+    uint64_t* masks = empty + kCombineMaxSlots;  // valid rows of each slot's unit
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(masks + kCombineMaxSlots);
+    int* zero = const_cast<int*>(reinterpret_cast<volatile int*>(abort_flag + 1));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < nslots; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kCombineTmaThreads / 32 - 1);  // one arrival per consumer warp
+        }
+        *abort_flag = 0;
+        *zero = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int nchunk = H / cw;
+    const int64_t nunits = (int64_t)T * nchunk;
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            pdl_wait();  // y is the predecessor's output
+            pdl_trigger();
+            uint32_t issued = 0, issued_par = 0;
+            bool ok = true;
+            int i = 0;
+            // a unit's rows are read one unit ahead, so their latency hides behind the wait
+            int64_t row[kMaxTopK + 1];
+            auto rows_of = [&](int64_t uu) {
+                const int tt = (int)(uu / nchunk);
+                for (int j = 0; j < nrows; ++j)
+                    row[j] = j < k ? (int64_t)inv[(size_t)tt * k + j]
+                                   : (int64_t)offsets[shared_group] + tt;
+            };
+            if (blockIdx.x < nunits) rows_of(blockIdx.x);
+            for (int64_t u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++i) {
+                const int sl = i % nslots;
+                const uint32_t ph = (uint32_t)(i / nslots) & 1u;
+                if (!mbar_wait(&empty[sl], ph ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int c0 = (int)(u % nchunk) * cw;
+                uint64_t mask = 0;
+                uint32_t nbytes = 0;
+                for (int j = 0; j < nrows; ++j)
+                    if (row[j] >= 0) {
+                        mask |= 1ull << j;
+                        nbytes += (uint32_t)cw * 4u;
+                    }
+                masks[sl] = mask;
+                mbar_arrive_expect_tx(&full[sl], nbytes);
+                float* dst = slots + (size_t)sl * nrows * cw;
+                for (int j = 0; j < nrows; ++j)
+                    if (row[j] >= 0)
+                        bulk_load(dst + (size_t)j * cw, y + row[j] * H + c0, (uint32_t)cw * 4u,
+                                  &full[sl], pol);
+                issued |= 1u << sl;
+                issued_par = (issued_par & ~(1u << sl)) | (ph << sl);
+                if (u + gridDim.x < nunits) rows_of(u + gridDim.x);
+            }
+            if (!ok) {
+                set_status(status, MOE_DEV_WAIT_TIMEOUT);
+                *abort_flag = 1;
+            }
+            for (int sl = 0; sl < nslots; ++sl)  // copies in flight land before the CTA exits
+                if ((issued >> sl) & 1u) mbar_wait(&full[sl], (issued_par >> sl) & 1u, zero);
+        }
+    } else {
+        const int tid = threadIdx.x - 32;  // 0..127: four columns per 512-column segment
+        int i = 0;
+        for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x, ++i) {
+            const int sl = i % nslots;
+            const uint32_t ph = (uint32_t)(i / nslots) & 1u;
+            if (!cmb_warp_wait(&full[sl], ph, abort_flag)) {
+                if (lane == 0) {
+                    set_status(status, MOE_DEV_WAIT_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            const uint64_t mask = masks[sl];
+            const int t = (int)(u / nchunk), c0 = (int)(u % nchunk) * cw;
+            const float* src = slots + (size_t)sl * nrows * cw;
+            for (int col = 4 * tid; col < cw; col += 512) {
+                float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+                for (int j = 0; j < nrows; ++j)
+                    if ((mask >> j) & 1ull) {
+                        const float4 v = *reinterpret_cast<const float4*>(src + (size_t)j * cw + col);
+                        a0 += v.x;
+                        a1 += v.y;
+                        a2 += v.z;
+                        a3 += v.w;
+                    }
+                const __nv_bfloat162 p0 = __floats2bfloat162_rn(a0, a1);
+                const __nv_bfloat162 p1 = __floats2bfloat162_rn(a2, a3);
+                *reinterpret_cast<uint2*>(out + (size_t)t * H + c0 + col) =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&p0),
+                               *reinterpret_cast<const uint32_t*>(&p1));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[sl]);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- checkpoint weights
 // One matrix type of a checkpoint (codes [E][N][K/2], E4M3 scales [E][N][K/16], a global
 // value per expert) -> the library's convention for experts off..off+count-1: global given

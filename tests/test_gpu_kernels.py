@@ -424,27 +424,35 @@ def test_grouped_gemm_fused_and_down_match_oracle(act_mode, T):
         assert np.max(np.abs(got - want)) <= 1e-4 * np.sqrt(np.mean(want ** 2)) * np.sqrt(I / 64) + 1e-9, (j, g)
 
 
-def test_combine_sums_pairs_and_shared():
-    T, k, H, El = 33, 8, 256, 320
-    h, _ = _tiny_layer_handle(E=El, k=k, H=H)
-    rng = np.random.default_rng(1)
-    R = 600
+@pytest.mark.parametrize("T,H,k", [(33, 256, 8), (1500, 4096, 8), (1100, 1536, 8),
+                                   (1200, 4096, 2)])
+def test_combine_sums_pairs_and_shared(T, H, k):
+    """out[t] = bf16(fp32 sum of the token's pair rows in top-k order, then its shared row),
+    bit for bit, for the load-based combine (small T) and the bulk-copy combine (T >= 1024;
+    2048-column pieces in 3 or 6 slots, 512-column pieces)."""
+    El = 320
+    h, _ = _tiny_layer_handle(E=El, k=k, H=H, max_tokens=max(T, 8192))
+    rng = np.random.default_rng(T)
+    n_pair_rows = T * k + 17
+    shared0 = n_pair_rows + 5
+    R = shared0 + T
     y = rng.standard_normal((R, H)).astype(np.float32)
-    # pairs point at distinct padded rows (or -1: not local); shared rows start at 500
-    rows = rng.permutation(400)[:T * k].astype(np.int32)
+    # pairs point at distinct padded rows (or -1: not local); shared rows start at shared0
+    rows = rng.permutation(n_pair_rows)[:T * k].astype(np.int32)
     inv = np.where(rng.random(T * k) < 0.7, rows, -1).astype(np.int32)
+    inv[:k] = -1  # a token with no local pair: its shared row alone
     offsets = np.zeros(El + 2, np.int32)
-    offsets[El] = 500
+    offsets[El] = shared0
     out = torch.zeros((T, H), dtype=torch.int16, device="cuda")
     moe.moe_combine(h.handle, dev(y), dev(inv), dev(offsets), T, out)
-    want = np.zeros((T, H), np.float64)
-    for t in range(T):
-        for j in range(k):
-            if inv[t * k + j] >= 0:
-                want[t] += y[inv[t * k + j]]
-        want[t] += y[500 + t]
-    got = synth.bf16_to_f32(host(out).view(np.uint16))
-    assert np.max(np.abs(got - want) / (np.abs(want) + 1e-3)) < 2 ** -7
+    want = np.zeros((T, H), np.float32)
+    for j in range(k):
+        r = inv[j::k]
+        sel = r >= 0
+        want[sel] = want[sel] + y[r[sel]]
+    want = want + y[shared0:shared0 + T]
+    want_bits = torch.from_numpy(want).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(host(out), want_bits)
 
 
 def test_grouped_gemms_with_the_dynamic_intermediate_scale():
