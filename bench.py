@@ -51,7 +51,12 @@ def parse():
     ap.add_argument("--no-oracle", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--nvtx", action="store_true",
                     help="wrap the device-timed steps in an NVTX range named 'timed' (for ncu)")
-    return ap.parse_args()
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count (a smaller case for profiling)")
+    args = ap.parse_args()
+    if args.tokens:
+        synth.CONFIGS[args.workload] = dict(synth.CONFIGS[args.workload], T=args.tokens)
+    return args
 
 
 def peaks():

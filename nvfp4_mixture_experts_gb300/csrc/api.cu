@@ -181,6 +181,11 @@ namespace {
 
 bool set_w4a16_smem_limits()
 {
+    for (bool gateup : {false, true})
+        if (cudaFuncSetAttribute(gemv_w4a16_kernel_for(gateup),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemLimit) != cudaSuccess)
+            return false;
     for (int bn : {16, 32, 64})
         for (bool f16 : {false, true})
             if (cudaFuncSetAttribute(w4a16_kernel(bn, f16),
@@ -243,8 +248,14 @@ bool t_ok(const moe_layer* h, int T) { return T >= 0 && T <= h->cfg.max_tokens; 
 
 int grid_for(int64_t threads, int block) { return (int)std::max<int64_t>(1, (threads + block - 1) / block); }
 
+// W4A16 batches of at most this many tokens take the grouped GEMV (gemv_w4a16.cu), which
+// reads each weight once per chunk of 8 rows of a group instead of padding every group to
+// the tensor-core kernel's 128-row MMA.
+constexpr int kGemvMaxTokens = 256;
+
 // Persistent grid: one CTA per SM, or fewer when the tile list (bounded above from the
 // pair count, with row blocks of `rows` rows) is shorter.
+
 int gemm_grid(const moe_layer* h, int T, int N, int rows)
 {
     const int64_t P = (int64_t)T * h->cfg.top_k;
@@ -399,6 +410,18 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     args.gs_i_dev = (epilogue == kEpiDown && dynamic_inter(c)) ? at<float>(ws, p.gs_i) : nullptr;
     args.status = at<uint32_t>(ws, p.status);
     if (a16) {
+        // Few token rows per group: the CUDA-core GEMV reads each weight once per chunk of
+        // kGvChunk rows, where a 128-row MMA per 16 k would be mostly padding.
+        const int64_t rows = (int64_t)p.T * c.top_k + shared_rows(h, p.T);
+        const int list_cap = (int)(p.G + (rows + kGvChunk - 1) / kGvChunk);
+        const int slots = gemv_w4a16_slots(K, list_cap);
+        if (p.T <= kGemvMaxTokens && epilogue != kEpiGateUpSwigluF32 && slots >= 4) {
+            const size_t gsm = gemv_w4a16_smem(K, slots, list_cap);
+            const int64_t items = (int64_t)list_cap * (N / 128);
+            const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(h->num_sms, items));
+            return launch(gemv_w4a16_kernel_for(gateup), dim3(grid), dim3(kGvThreads), gsm, s,
+                          pdl, args, static_cast<const uint16_t*>(a_bf16), list_cap, slots);
+        }
         // Token rows per tile from the expected rows per local expert: narrow tiles keep the
         // token tile (re-read for every weight tile) small when experts see few tokens.
         const int64_t local_rows = (int64_t)p.T * c.top_k / std::max(1, c.num_local_experts);

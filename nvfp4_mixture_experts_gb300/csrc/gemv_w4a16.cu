@@ -1,0 +1,504 @@
+// W4A16 grouped GEMV: 16-bit activation rows x NVFP4 weights for batches in which each
+// expert sees a few tokens (up to 8 rows per pass over the weights).
+//
+// Solar Open 2 on DGX Spark, "b12x에서의 Expert Parallelism 구현 추가": the W4A16 backend
+// (bf16 activations, NVFP4 weights dequantised in the main loop) among the fused-MoE
+// backends, chosen by the local workload.  With one or two tokens per expert the layer is a
+// weight stream, and what bounds it is how many weight elements per clock the SM can
+// dequantise and feed to a multiplier.  Measured on this GPU: the tcgen05 kind::f16 MMA
+// (M128 x K16) takes 46 cycles whatever N is up to 64, i.e. 44 weight elements per clock per
+// SM; the warp-level mma.sync m16n8k16 (f16 in, f32 accumulate) issues 0.8 per clock per SM,
+// i.e. 205 weight elements per clock, with its A operand straight from registers -- where the
+// dequantised codes already are.  So this kernel decodes each weight fragment in registers
+// (cvt.rn.f16x2.e2m1x2, then one exact f16x2 multiply by the block scale: E2M1 x E4M3 has at
+// most 6 significant bits and lies in [2^-10, 2688]) and runs mma.sync with the token rows
+// as the 8 columns of B: the instructions per weight element do not depend on the number of
+// tokens up to 8.
+//
+// Data flow.  A copy warp streams the weight blobs of the block's work (one per (expert,
+// 128-row tile, 256-element k-block): 128 rows x 128 bytes of swizzled codes and 4 scale
+// atoms, 18 KB) by 1-D bulk copies into a ring of shared-memory slots; bytes in flight, not
+// registers, carry the HBM stream.  Sixteen consumer warps read every blob: warp (u, a)
+// takes rows 32u .. 32u + 31 of the tile and k-step a (64 elements) of the k-block, so each
+// warp waits on every phase of every ring barrier in order.
+//
+// Fragment layout.  The dot product does not care in which order k is summed, so each
+// lane's k positions are chosen to match the blob: lane (g = lane / 4, c = lane % 4) owns
+// elements 16c .. 16c + 15 of its k-step (8 code bytes, one 16-element block: one scale) for
+// rows g and g + 8 of each 16-row MMA block; MMA m (0..3) takes elements 16c + 4m ..
+// 16c + 4m + 3 (code bytes 2m, 2m + 1: fragment registers a0/a1 and a2/a3), and the B
+// fragment of token g holds the same four positions, read from shared memory in one
+// 8-byte load.  The W4A16 down blobs store each 32-bit word's codes in nibble order
+// 0,2,4,6,1,3,5,7, so there the staged activations of every 8-element group are permuted
+// the same way.
+//
+// Activations in shared memory are fp16.  gate_up's rows are already fp16 copies of
+// x * gs_a.  down's bf16 intermediate rows are staged as fp16 x * 2^k_t with k_t chosen per
+// token so that the row's largest magnitude lands in [2^14, 2^15): every value above 2^-28
+// of the row's largest converts exactly, and the epilogue multiplies by 2^-k_t.
+//
+// Work: an item is a chunk of up to 8 token rows of one group (local expert or the shared
+// slot) and one 128-row weight tile; a block takes a contiguous run of items, chunk-major,
+// so it restages activations (and the chunk's output scales: routing weights, global
+// scales) only when its chunk changes.  The four k-step warps of a unit meet in shared
+// memory and the epilogue is the tensor-core kernel's: gate_up times 1 / (gs_a * gs_w),
+// SwiGLU, bf16 (or fp32 gate / up when unfused); down times 2^-k_t, 1 / gs_w and the pair's
+// routing weight into y.  Every wait is bounded; one that runs out sets
+// MOE_DEV_WAIT_TIMEOUT and every role stops.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kGvTok = kGvChunk;  // token rows per pass over the weights (the MMA's N)
+
+// Bytes of one staged activation row of KB k-blocks (2 bytes per element), the pitch 8
+// modulo 128: the B-fragment loads of a half-warp (lanes g = 0..3, c = 0..3 at byte
+// g pitch + 2 (64 a + 16 c + 4 m) + const) then fall on 16 distinct 8-byte slots.
+__host__ __device__ __forceinline__ int gv_row_pitch(int KB) { return 512 * KB + 8; }
+
+// Two E4M3 bytes (low first) -> f16x2, exact.
+__device__ __forceinline__ uint32_t gv_e4m3x2(uint32_t two)
+{
+    uint32_t d;
+    asm("{\n\t.reg .b16 s;\n\tcvt.u16.u32 s, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, s;\n\t}"
+        : "=r"(d)
+        : "r"(two));
+    return d;
+}
+
+// Bytes 2h and 2h + 1 of w, each two E2M1 codes (low nibble -> low half), as f16x2.
+template <int H>
+__device__ __forceinline__ void gv_e2m1_pair(uint32_t w, uint32_t& lo, uint32_t& hi)
+{
+    if constexpr (H == 0)
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %2;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
+    else
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %2;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %0, b2;\n\tcvt.rn.f16x2.e2m1x2 %1, b3;\n\t}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t gv_hmul2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// D += A B for one m16n8k16 tile, f16 operands, f32 accumulators.
+__device__ __forceinline__ void gv_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                       uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One lane's share of one k-step (64 elements) of a blob for a warp's 32 weight rows: rows
+// rbase + 16 mb + 8 hh + g (index 2 mb + hh), code bytes 8c .. 8c + 7 of the k-step
+// (elements 16c .. 16c + 15) and the scale word of the k-step (its byte c is the lane's).
+struct GvFrag {
+    uint2 code[4];
+    uint32_t sw[4];
+};
+
+__device__ __forceinline__ void gv_load(GvFrag& f, const uint8_t* blob, int rbase, int ks, int lane)
+{
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = rbase + 16 * (i >> 1) + 8 * (i & 1) + g;
+        f.code[i] = *reinterpret_cast<const uint2*>(
+            blob + r * 128 + ((((2 * ks + (c >> 1)) ^ (r & 7)) << 4) | (8 * (c & 1))));
+        f.sw[i] = *reinterpret_cast<const uint32_t*>(blob + 16384 + 512 * ks + (r & 31) * 16 +
+                                                     (r >> 5) * 4);
+    }
+}
+
+// The 8 MMAs of one k-step: xs = this lane's B base (token g, elements 16c .. of the
+// k-step).  MMA m takes elements 16c + 4m .. 16c + 4m + 3: code bytes 2m, 2m + 1.  Four
+// accumulator chains, d[m & 1][mb], summed by the caller.
+__device__ __forceinline__ void gv_kstep(const GvFrag& f, const uint8_t* xs, int lane,
+                                         float (&d)[2][2][4])
+{
+    // the lane's block scale of each row, in both halves: byte c twice -> one cvt
+    const uint32_t sel = (uint32_t)(lane & 3) * 0x11u;
+    uint32_t sc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[i] = gv_e4m3x2(__byte_perm(f.sw[i], 0, sel));
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const uint2 b = *reinterpret_cast<const uint2*>(xs + 8 * m);
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb) {
+            uint32_t a[4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = 2 * mb + hh;
+                const uint32_t w = m < 2 ? f.code[i].x : f.code[i].y;
+                uint32_t lo, hi;
+                if (m & 1)
+                    gv_e2m1_pair<1>(w, lo, hi);
+                else
+                    gv_e2m1_pair<0>(w, lo, hi);
+                a[hh] = gv_hmul2(lo, sc[i]);
+                a[2 + hh] = gv_hmul2(hi, sc[i]);
+            }
+            gv_mma(d[m & 1][mb], a, b.x, b.y);
+        }
+    }
+}
+
+}  // namespace
+
+namespace {
+
+constexpr int kGvConsumers = kGvThreads / 32 - 1;  // 16 consumer warps, then the copy warp
+constexpr int kGvUnits = 4;                        // 32-row units per 128-row tile
+constexpr int kGvKsteps = 4;                       // 64-element k-steps per blob
+constexpr int kGvScales = 32;                      // per-chunk output scales (floats)
+
+// Consumer-warp wait on a full barrier: every lane polls; the vote keeps the outcome
+// warp-uniform should the lanes' time limits run out at different polls.
+__device__ __forceinline__ bool gv_all_wait(uint64_t* bar, uint32_t parity, volatile int* abort)
+{
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
+__device__ __forceinline__ void gv_consumer_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kGvConsumers * 32) : "memory");
+}
+
+struct GvSmem {
+    uint8_t* ring;
+    uint8_t* sx;
+    float* red;
+    float* tscale;  // [kGvScales]: 2^-k_t per token, then (down) rcp(gs_w) x routing weight
+                    // per token, then (gate_up) 1 / (gs_a gs_w)
+    uint64_t* full;
+    uint64_t* empty;
+    volatile int* abort_flag;
+    int* zero;
+    int* n;
+    int* list;
+};
+
+__host__ __device__ __forceinline__ size_t gv_fixed_bytes(int K)
+{
+    return (size_t)kGvTok * gv_row_pitch((K + 255) / 256) + kGvConsumers * 32 * kGvTok * 4 +
+           kGvScales * 4 + 2 * kGvMaxSlots * 8 + 16;
+}
+
+__device__ __forceinline__ GvSmem gv_carve(uint8_t* base, int K, int slots)
+{
+    GvSmem m;
+    m.ring = base;
+    m.sx = m.ring + (size_t)slots * kNvf4TileBytes;
+    m.red = reinterpret_cast<float*>(m.sx + (size_t)kGvTok * gv_row_pitch((K + 255) / 256));
+    m.tscale = m.red + kGvConsumers * 32 * kGvTok;
+    m.full = reinterpret_cast<uint64_t*>(m.tscale + kGvScales);
+    m.empty = m.full + kGvMaxSlots;
+    m.abort_flag = reinterpret_cast<volatile int*>(m.empty + kGvMaxSlots);
+    m.zero = const_cast<int*>(m.abort_flag + 1);
+    m.n = m.zero + 1;
+    m.list = m.n + 2;
+    return m;
+}
+
+// Token row src (K 16-bit values) -> dst as fp16, zeros past K; one warp.
+// down: bf16 -> fp16 x * 2^k_t (k_t from the row's largest magnitude), 2^-k_t -> *tscale, and
+// each 8-element group stored in the blobs' nibble order 0,2,4,6,1,3,5,7.
+template <bool kGateUp>
+__device__ __forceinline__ void gv_stage(const uint16_t* src, int K, int KB, uint8_t* dst,
+                                         float* tscale, int lane)
+{
+    float up = 1.0f;  // down: 2^k_t
+    if constexpr (!kGateUp) {
+        uint32_t mx = 0;
+        for (int e8 = 8 * lane; e8 < K; e8 += 256) {
+            const uint4 q = *reinterpret_cast<const uint4*>(src + e8);
+            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) mx = max(mx, max(u[j] & 0x7FFFu, (u[j] >> 16) & 0x7FFFu));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        // bf16 exponent field of the largest magnitude -> k_t in [-113, 113]
+        const int ex = (int)(mx >> 7) - 127;
+        const int kt = mx ? max(-113, min(113, 14 - ex)) : 0;
+        up = __uint_as_float((uint32_t)(127 + kt) << 23);
+        if (lane == 0) *tscale = __uint_as_float((uint32_t)(127 - kt) << 23);
+    }
+    for (int e8 = 8 * lane; e8 < KB * 256; e8 += 256) {
+        uint4 q = make_uint4(0, 0, 0, 0);
+        if (e8 < K) q = *reinterpret_cast<const uint4*>(src + e8);
+        uint2 lo, hi;  // elements (0..3, 4..7), or (0,2,4,6), (1,3,5,7) for down
+        if constexpr (kGateUp) {
+            lo = make_uint2(q.x, q.y);
+            hi = make_uint2(q.z, q.w);
+        } else {
+            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+            uint32_t h[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __half2 v = __floats2half2_rn(__uint_as_float(u[j] << 16) * up,
+                                                    __uint_as_float(u[j] & 0xFFFF0000u) * up);
+                h[j] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+            // h[j] = (x_2j, x_2j+1) -> (x0, x2), (x4, x6) | (x1, x3), (x5, x7)
+            lo = make_uint2(__byte_perm(h[0], h[1], 0x5410), __byte_perm(h[2], h[3], 0x5410));
+            hi = make_uint2(__byte_perm(h[0], h[1], 0x7632), __byte_perm(h[2], h[3], 0x7632));
+        }
+        uint8_t* p = dst + 2 * e8;
+        *reinterpret_cast<uint2*>(p) = lo;
+        *reinterpret_cast<uint2*>(p + 8) = hi;
+    }
+}
+
+// The k-slots' partials of tile nb summed, scaled and stored by the consumer threads.
+template <bool kGateUp>
+__device__ __forceinline__ void gv_epilogue(const GemmArgs& a, const GvSmem& m, int64_t row0,
+                                            int nt, int nb)
+{
+    const int tid = threadIdx.x;  // consumers: 0 .. 32 kGvConsumers - 1
+    if constexpr (kGateUp) {
+        // output (token t, feature 64 nb + j): gate row j % 16, up row 16 + j % 16 of unit j / 16
+        const float alpha = m.tscale[2 * kGvTok];
+        const int I = a.N / 2;
+        for (int o = tid; o < nt * 64; o += kGvConsumers * 32) {
+            const int t = o >> 6, j = o & 63;
+            const int u = j >> 4, fi = j & 15;
+            float vg = 0.0f, vu = 0.0f;
+#pragma unroll
+            for (int s = 0; s < kGvKsteps; ++s) {
+                const float* rw = m.red + (s * kGvUnits + u) * 32 * kGvTok;
+                vg += rw[fi * kGvTok + t];
+                vu += rw[(16 + fi) * kGvTok + t];
+            }
+            vg = __fmul_rn(vg, alpha);
+            vu = __fmul_rn(vu, alpha);
+            const int64_t row = row0 + t;
+            const int f = 64 * nb + j;
+            if (a.epilogue == kEpiGateUpF32) {
+                a.out_f32[row * a.N + f] = vg;
+                a.out_f32[row * a.N + I + f] = vu;
+            } else {
+                a.out_bf16[row * I + f] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_mul(vg, vu)));
+            }
+        }
+    } else {
+        // output (token t, row 128 nb + j)
+        for (int o = tid; o < nt * 128; o += kGvConsumers * 32) {
+            const int t = o >> 7, j = o & 127;
+            const int u = j >> 5, ri = j & 31;
+            float v = 0.0f;
+#pragma unroll
+            for (int s = 0; s < kGvKsteps; ++s) v += m.red[((s * kGvUnits + u) * 32 + ri) * kGvTok + t];
+            a.out_f32[(row0 + t) * a.N + 128 * nb + j] =
+                __fmul_rn(v, m.tscale[t]) * m.tscale[kGvTok + t];
+        }
+    }
+}
+
+}  // namespace
+
+size_t gemv_w4a16_smem(int K, int slots, int list_cap)
+{
+    return (size_t)slots * kNvf4TileBytes + gv_fixed_bytes(K) + 4 * (size_t)list_cap;
+}
+
+int gemv_w4a16_slots(int K, int list_cap)
+{
+    const size_t fixed = gv_fixed_bytes(K) + 4 * (size_t)list_cap;
+    if (fixed >= (size_t)kSmemLimit) return 0;
+    return (int)std::min<size_t>(kGvMaxSlots, ((size_t)kSmemLimit - fixed) / kNvf4TileBytes);
+}
+
+// kGateUp: N = 2I interleaved gate/up rows, x the fp16 rows x * gs_a, epilogue
+// kEpiGateUpSwiglu or kEpiGateUpF32.  Else N = H rows of W2 (nibble-pair blobs), x the bf16
+// intermediate, epilogue kEpiDown.  slots: weight blobs in the shared-memory ring.  Every
+// consumer warp reads every blob (its unit's rows, its k-step), so each warp waits on every
+// phase of every ring barrier in order and no parity wait can be satisfied by a stale phase.
+template <bool kGateUp>
+__global__ void __launch_bounds__(kGvThreads, 1)
+    gemv_w4a16_kernel(GemmArgs a, const uint16_t* __restrict__ xin, int list_cap, int slots)
+{
+    extern __shared__ __align__(128) uint8_t gv_smem[];
+    const int K = a.K, KB = (K + 255) / 256, NB = a.N / 128;
+    const int pitch = gv_row_pitch(KB);
+    const GvSmem m = gv_carve(gv_smem, K, slots);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < slots; ++i) {
+            mbar_init(&m.full[i], 1);
+            mbar_init(&m.empty[i], kGvConsumers);  // every consumer warp reads every blob
+        }
+        *m.abort_flag = 0;
+        *m.zero = 0;
+        fence_barrier_init();
+    }
+    pdl_wait();  // group sizes, offsets and activation rows come from the preceding kernels
+    pdl_trigger();
+    if (warp == 0) {
+        // chunks of the non-empty groups, in group order
+        int n = 0;
+        for (int g0 = 0; g0 < a.G; g0 += 32) {
+            const int g = g0 + lane;
+            const int nc = g < a.G ? (a.counts[g] + kGvTok - 1) / kGvTok : 0;
+            int incl = nc;  // inclusive scan of the chunk counts over the warp
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            for (int c = 0; c < nc; ++c) {
+                const int slot = n + incl - nc + c;
+                if (slot < list_cap) m.list[slot] = (g << 16) | (c * kGvTok);
+            }
+            n += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            if (n > list_cap) set_status(a.status, MOE_DEV_ROWS_OVERFLOW);
+            *m.n = min(n, list_cap);
+        }
+    }
+    __syncthreads();
+    // items: (chunk, 128-row tile), chunk-major; a block takes a contiguous run of them
+    const int nitems = *m.n * NB;
+    const int i0 = (int)((int64_t)blockIdx.x * nitems / gridDim.x);
+    const int i1 = (int)((int64_t)(blockIdx.x + 1) * nitems / gridDim.x);
+
+    if (warp == kGvConsumers) {
+        // copy warp: the run's blobs, in (item, k-block) order, into the ring
+        if (lane == 0) {
+            const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
+            uint32_t c = 0;   // blobs issued
+            int sl = 0;       // their ring slot
+            uint32_t ph = 0;  // the slot's phase parity
+            bool ok = true;
+            for (int item = i0; item < i1 && ok; ++item) {
+                const int g = m.list[item / NB] >> 16, nb = item % NB;
+                // the shared slot is read once per chunk: keep it in L2
+                const uint64_t pol = g == a.G - 1 ? pol_keep : pol_stream;
+                const uint8_t* src = a.b_tiles + (size_t)(g * NB + nb) * KB * kNvf4TileBytes;
+                for (int kb = 0; kb < KB; ++kb, ++c) {
+                    if (!mbar_wait(&m.empty[sl], ph ^ 1u, m.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&m.full[sl], kNvf4TileBytes);
+                    bulk_load(m.ring + (size_t)sl * kNvf4TileBytes, src + (size_t)kb * kNvf4TileBytes,
+                              kNvf4TileBytes, &m.full[sl], pol);
+                    if (++sl == slots) {
+                        sl = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                set_status(a.status, MOE_DEV_WAIT_TIMEOUT);
+                *m.abort_flag = 1;
+            }
+            // the copies in flight land before the block exits: the last min(c, slots)
+            for (uint32_t j = c > (uint32_t)slots ? c - slots : 0; j < c; ++j)
+                mbar_wait(&m.full[j % slots], (j / slots) & 1u, m.zero);
+        }
+        return;
+    }
+
+    // consumer warps: unit my_u (rows 32 my_u .. of the tile), k-step my_ks of every blob
+    const int my_u = warp % kGvUnits, my_ks = warp / kGvUnits;
+    const int g8 = lane >> 2, c4 = lane & 3;
+    bool ok = true;
+    int staged = -1;  // chunk whose rows are in sx
+    int g = 0, nt = 0;
+    int64_t row0 = 0;
+    int sl = 0;       // ring slot of the next blob
+    uint32_t ph = 0;  // its full-barrier phase parity
+    for (int item = i0; item < i1; ++item) {
+        const int ci = item / NB, nb = item % NB;
+        if (ci != staged) {
+            const int e = m.list[ci];
+            const int t0 = e & 0xFFFF;
+            g = e >> 16;
+            nt = min(kGvTok, a.counts[g] - t0);
+            row0 = (int64_t)a.offsets[g] + t0;
+        }
+        gv_consumer_sync();  // the previous item's readers of sx, red and the scales are done
+        if (ci != staged) {
+            if (warp < nt) {
+                gv_stage<kGateUp>(xin + (row0 + warp) * K, K, KB, m.sx + warp * pitch,
+                                  m.tscale + warp, lane);
+                if (lane == 0) {
+                    const float gw = a.gs_w[g];
+                    if constexpr (kGateUp) {
+                        if (warp == 0) m.tscale[2 * kGvTok] = __frcp_rn(__fmul_rn(*a.gs_a, gw));
+                    } else {
+                        const int pair = a.perm_src[row0 + warp];
+                        const float wn = pair < a.Tk ? a.topk_w[pair] : 1.0f;
+                        m.tscale[kGvTok + warp] = __fmul_rn(__frcp_rn(gw), wn);
+                    }
+                }
+            }
+            staged = ci;
+            gv_consumer_sync();
+        }
+        float d[2][2][4] = {};
+        const uint8_t* xs = m.sx + g8 * pitch + 2 * (64 * my_ks + 16 * c4);
+        for (int kb = 0; kb < KB; ++kb) {
+            if (ok && !gv_all_wait(&m.full[sl], ph, m.abort_flag)) {
+                ok = false;
+                if (lane == 0) {
+                    set_status(a.status, MOE_DEV_WAIT_TIMEOUT);
+                    *m.abort_flag = 1;
+                }
+            }
+            if (ok) {
+                GvFrag f;
+                gv_load(f, m.ring + (size_t)sl * kNvf4TileBytes, 32 * my_u, my_ks, lane);
+                gv_kstep(f, xs + 512 * kb, lane, d);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&m.empty[sl]);
+            }
+            if (++sl == slots) {
+                sl = 0;
+                ph ^= 1u;
+            }
+        }
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) d[0][mb][r] += d[1][mb][r];
+        // partial sums: red[warp][row][token], row = 16 mb + 8 hh + g, token 2c, 2c + 1
+        float* rw = m.red + warp * 32 * kGvTok;
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                *reinterpret_cast<float2*>(rw + (16 * mb + 8 * hh + g8) * kGvTok + 2 * c4) =
+                    make_float2(d[0][mb][2 * hh], d[0][mb][2 * hh + 1]);
+        gv_consumer_sync();
+        if (ok) gv_epilogue<kGateUp>(a, m, row0, nt, nb);
+    }
+}
+
+GemvKernel gemv_w4a16_kernel_for(bool gateup)
+{
+    return gateup ? gemv_w4a16_kernel<true> : gemv_w4a16_kernel<false>;
+}
+
+}  // namespace moe

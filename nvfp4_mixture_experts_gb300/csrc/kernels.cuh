@@ -171,4 +171,17 @@ inline int w4a16_smem_bytes(int raw_slots, int b_slots, int bn, int G)
 using W16Kernel = void (*)(CUtensorMap, GemmArgs);
 W16Kernel w4a16_kernel(int bn, bool f16);
 
+// ---- gemv_w4a16.cu: W4A16 for groups of a few token rows, weights decoded into mma.sync
+// fragments.  544 threads: 16 consumer warps and a copy warp streaming the weight blobs
+// through a ring of `slots` blobs in shared memory (gemv_w4a16_slots: as many as fit, at most
+// kGvMaxSlots; 0 = the shape does not fit).  list_cap bounds the work list: the chunks of up
+// to kGvChunk rows of the non-empty groups (at most G + rows / kGvChunk).
+constexpr int kGvChunk = 8;
+constexpr int kGvThreads = 544;
+constexpr int kGvMaxSlots = 12;
+using GemvKernel = void (*)(GemmArgs, const uint16_t*, int, int);
+GemvKernel gemv_w4a16_kernel_for(bool gateup);
+size_t gemv_w4a16_smem(int K, int slots, int list_cap);
+int gemv_w4a16_slots(int K, int list_cap);
+
 }  // namespace moe

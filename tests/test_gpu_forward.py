@@ -202,6 +202,33 @@ def test_w4a16_decode_sweep(big_layer, T):
     _check(got[tok], ora.out, "w4a16 T=%d" % T)
 
 
+# W4A16 at up to 64 tokens runs on the CUDA-core GEMV, above on the tensor-core kernel.
+# H = 384 and I = 320 leave the last 256-element k-block of each GEMM partly empty; the
+# shard (experts 8..15 of 24, no shared rows added) leaves most groups empty; has_shared=0
+# drops the shared slot.
+@pytest.mark.parametrize("T,E_loc,off,add_shared,has_shared", [
+    (1, None, 0, 1, 1), (7, None, 0, 1, 1), (64, None, 0, 1, 1), (65, None, 0, 1, 1),
+    (5, 8, 8, 0, 1), (40, 8, 8, 1, 1), (9, None, 0, 1, 0)])
+def test_w4a16_small_batches_ragged_k(T, E_loc, off, add_shared, has_shared):
+    H, I, E, k = 384, 320, 24, 4
+    layer = build_layer(21, H, I, E)
+    wr = synth.router_weight(21, E, H)
+    x = synth.activations(21, T, H, outlier_frac=0.01)
+    lg = synth.logits_normal(21 + T, T, E)
+    sub = layer if E_loc is None else slice_layer(layer, off, off + E_loc)
+    h = make_layer(sub, wr, H, I, E, k, E_loc=E_loc, off=off, add_shared=add_shared,
+                   act_mode=moe.MOE_W4A16, max_tokens=T, has_shared=has_shared)
+    got = _forward(h, x, T, logits_in=lg)
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, E_loc=E_loc, off=off,
+                                             has_shared=has_shared, add_shared=add_shared,
+                                             act_mode=2),
+                             x, sub, logits_in=lg)
+    if not np.any(ora.out):
+        assert not np.any(got)
+        return
+    _check(got, ora.out, "w4a16 T=%d E_loc=%s" % (T, E_loc))
+
+
 def test_prefill_chunk_sampled_parity(big_layer):
     c = synth.CONFIGS["prefill"]
     T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
