@@ -14,7 +14,9 @@ roofline: the gate_up grouped GEMM (the dominant kernel), algorithmic bytes per 
 its CUDA-event duration measured here, against the measured HBM copy bandwidth.
 The decode and prefill steps stream 2.3-2.8 GB of weights, far more than the 129 MB L2, so
 their steps run back to back; W4A16 sweep points that stream less than twice the L2 (T=1)
-flush it before every timed step and time the steps alone.
+flush it before every timed step (a write of twice the L2 size, then a read of as much, so
+that the write-backs of the flush's dirty lines are not charged to the timed step) and time
+the steps alone.
 """
 import argparse
 import hashlib
@@ -57,6 +59,10 @@ def parse():
     if args.tokens:
         synth.CONFIGS[args.workload] = dict(synth.CONFIGS[args.workload], T=args.tokens)
     return args
+
+
+W4A16_GEMV_MAX_TOKENS = 256  # the library runs W4A16 batches up to this size on the GEMV
+GPU_SLEEP_CYCLES = 400000    # ~0.2 ms at 2 GHz: longer than a staged call's host overhead
 
 
 def peaks():
@@ -388,12 +394,15 @@ def roofline(layer, c, xd, lgd, bd, ws, stream, steps, pk, workload):
     times = {"gateup": [], "down": []}
     # steps whose weights fit twice in L2 get an L2 flush before each timed launch
     small = gemm_bytes(c, counts, True)[0] + gemm_bytes(c, counts, False)[0] < L2_FLUSH_BELOW
-    flush = torch.empty(L2_FLUSH_BELOW // 4, dtype=torch.float32, device="cuda") if small else None
+    flush = L2Flush() if small else None
     with torch.cuda.stream(stream):
         for i in range(steps + 3):
             e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             if small:
-                flush.fill_(float(i))
+                flush(i)
+            # a bounded spin on the GPU lets the host enqueue the launch before its start
+            # event is reached, so the event pair times the kernel, not the host call
+            torch.cuda._sleep(GPU_SLEEP_CYCLES)
             e[0].record(stream)
             st = lib.moe_grouped_gemm_gateup(h, P("a_codes"), P("a_sf"), P("gs_a"),
                                              P("a_bf16"), P("expert_counts"),
@@ -402,7 +411,8 @@ def roofline(layer, c, xd, lgd, bd, ws, stream, steps, pk, workload):
                                              T, C.c_void_p(ws.data_ptr()), nbytes, strm)
             e[1].record(stream)
             if small:
-                flush.fill_(float(-i))
+                flush(-i)
+            torch.cuda._sleep(GPU_SLEEP_CYCLES)
             e[2].record(stream)
             st |= lib.moe_grouped_gemm_down(h, P("inter_codes"), P("inter_sf"),
                                             P("inter_bf16"),
@@ -420,9 +430,11 @@ def roofline(layer, c, xd, lgd, bd, ws, stream, steps, pk, workload):
     bytes_gu, touched, rows = gemm_bytes(c, counts, True)
     bytes_dn, _, _ = gemm_bytes(c, counts, False)
     ach = bytes_gu / gu / 1e9
-    kern = "gemm_w4a16" if a16 else "gemm_nvf4"
+    # W4A16 batches of up to 256 tokens run on the grouped GEMV (the library's dispatch rule)
+    kern = ("gemv_w4a16" if T <= W4A16_GEMV_MAX_TOKENS else "gemm_w4a16") if a16 else "gemm_nvf4"
     fl = gemm_flops(counts, c, True)
-    return {"kernel": kern + "_kernel (gate_up, fused SwiGLU+requant)", "bound": "hbm",
+    return {"kernel": kern + ("_kernel (gate_up, fused SwiGLU)" if a16 else
+                              "_kernel (gate_up, fused SwiGLU+requant)"), "bound": "hbm",
             "achieved": round(ach, 1), "peak": pk["hbm"], "unit": "GB/s",
             "frac": round(ach / pk["hbm"], 4), "peak_src": pk["src"],
             "traffic": profile_traffic(kern + "_gateup", workload),
@@ -562,16 +574,32 @@ L2_BYTES = 129 * 2 ** 20
 L2_FLUSH_BELOW = 2 * L2_BYTES
 
 
+class L2Flush:
+    """Empties L2 of the timed work's data: a write of twice the L2 size, then a read of
+    another buffer of that size.  The read evicts the written (dirty) lines, so their
+    write-back to HBM happens here and not inside the timed region that follows."""
+
+    def __init__(self):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BELOW // 4, dtype=torch.float32, device="cuda")
+        self.r = torch.zeros(L2_FLUSH_BELOW // 4, dtype=torch.float32, device="cuda")
+
+    def __call__(self, i):
+        self.w.fill_(float(i))
+        self.r.sum()
+
+
 def flushed_replays(g, stream, steps):
-    """Mean device time (ms) of `steps` graph replays, each after an L2 flush (a write of
-    twice the L2 size); only the replays are timed."""
+    """Mean device time (ms) of `steps` graph replays, each after an L2 flush (L2Flush);
+    only the replays are timed."""
     import torch
-    flush = torch.empty(L2_FLUSH_BELOW // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush()
     total = 0.0
     with torch.cuda.stream(stream):
         evs = []
         for i in range(steps):
-            flush.fill_(float(i))
+            flush(i)
+            torch.cuda._sleep(GPU_SLEEP_CYCLES)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             g.replay()
@@ -623,9 +651,10 @@ def measure_w4a16(layer, stream, steps):
         l2 = "no flush: the step streams %.0f MB, over twice the 129 MB L2" % (wbytes / 1e6)
         if wbytes < L2_FLUSH_BELOW:
             # the touched weights could stay in L2 from one step to the next: flush it before
-            # every timed step (a write larger than L2) and time only the steps
+            # every timed step (L2Flush) and time only the steps
             ms = flushed_replays(g, stream, steps)
-            l2 = "flushed before every step (the step streams %.0f MB)" % (wbytes / 1e6)
+            l2 = ("flushed before every step: a write then a read of twice the L2 size (the "
+                  "step streams %.0f MB)" % (wbytes / 1e6))
         out_rows.append({"T": T, "value": round(T / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
                          "experts_touched": roof["experts_touched"],
                          "gemm_bytes_per_step": int(wbytes),

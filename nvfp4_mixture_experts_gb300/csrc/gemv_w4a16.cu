@@ -197,19 +197,25 @@ struct GvSmem {
     int* list;
 };
 
+// Partial-sum buffers: two for short items (at most 8 k-blocks), so the next item's partial
+// sums need not wait for this item's epilogue; one otherwise, leaving the ring its space.
+__host__ __device__ __forceinline__ int gv_nred(int K) { return (K + 255) / 256 <= 8 ? 2 : 1; }
+
 __host__ __device__ __forceinline__ size_t gv_fixed_bytes(int K)
 {
-    return (size_t)kGvTok * gv_row_pitch((K + 255) / 256) + kGvConsumers * 32 * kGvTok * 4 +
+    const int nred = gv_nred(K);
+    return (size_t)kGvTok * gv_row_pitch((K + 255) / 256) + nred * kGvConsumers * 32 * kGvTok * 4 +
            kGvScales * 4 + 2 * kGvMaxSlots * 8 + 16;
 }
 
 __device__ __forceinline__ GvSmem gv_carve(uint8_t* base, int K, int slots)
 {
+    const int nred = gv_nred(K);
     GvSmem m;
     m.ring = base;
     m.sx = m.ring + (size_t)slots * kNvf4TileBytes;
     m.red = reinterpret_cast<float*>(m.sx + (size_t)kGvTok * gv_row_pitch((K + 255) / 256));
-    m.tscale = m.red + kGvConsumers * 32 * kGvTok;
+    m.tscale = m.red + nred * kGvConsumers * 32 * kGvTok;
     m.full = reinterpret_cast<uint64_t*>(m.tscale + kGvScales);
     m.empty = m.full + kGvMaxSlots;
     m.abort_flag = reinterpret_cast<volatile int*>(m.empty + kGvMaxSlots);
@@ -271,21 +277,23 @@ __device__ __forceinline__ void gv_stage(const uint16_t* src, int K, int KB, uin
 
 // The k-slots' partials of tile nb summed, scaled and stored by the consumer threads.
 template <bool kGateUp>
-__device__ __forceinline__ void gv_epilogue(const GemmArgs& a, const GvSmem& m, int64_t row0,
-                                            int nt, int nb)
+__device__ __forceinline__ void gv_epilogue(const GemmArgs& a, const GvSmem& m,
+                                            const float* red, int64_t row0, int nt, int nb)
 {
     const int tid = threadIdx.x;  // consumers: 0 .. 32 kGvConsumers - 1
     if constexpr (kGateUp) {
         // output (token t, feature 64 nb + j): gate row j % 16, up row 16 + j % 16 of unit j / 16
         const float alpha = m.tscale[2 * kGvTok];
         const int I = a.N / 2;
-        for (int o = tid; o < nt * 64; o += kGvConsumers * 32) {
-            const int t = o >> 6, j = o & 63;
+        for (int o = tid; o < 64 * kGvTok; o += kGvConsumers * 32) {
+            const int t = o & (kGvTok - 1), j = o / kGvTok;  // token fastest: every warp
+            if (t >= nt) continue;                            // takes a share
+
             const int u = j >> 4, fi = j & 15;
             float vg = 0.0f, vu = 0.0f;
 #pragma unroll
             for (int s = 0; s < kGvKsteps; ++s) {
-                const float* rw = m.red + (s * kGvUnits + u) * 32 * kGvTok;
+                const float* rw = red + (s * kGvUnits + u) * 32 * kGvTok;
                 vg += rw[fi * kGvTok + t];
                 vu += rw[(16 + fi) * kGvTok + t];
             }
@@ -302,12 +310,14 @@ __device__ __forceinline__ void gv_epilogue(const GemmArgs& a, const GvSmem& m, 
         }
     } else {
         // output (token t, row 128 nb + j)
-        for (int o = tid; o < nt * 128; o += kGvConsumers * 32) {
-            const int t = o >> 7, j = o & 127;
+        for (int o = tid; o < 128 * kGvTok; o += kGvConsumers * 32) {
+            const int t = o & (kGvTok - 1), j = o / kGvTok;  // token fastest: every warp
+            if (t >= nt) continue;                            // takes a share
+
             const int u = j >> 5, ri = j & 31;
             float v = 0.0f;
 #pragma unroll
-            for (int s = 0; s < kGvKsteps; ++s) v += m.red[((s * kGvUnits + u) * 32 + ri) * kGvTok + t];
+            for (int s = 0; s < kGvKsteps; ++s) v += red[((s * kGvUnits + u) * 32 + ri) * kGvTok + t];
             a.out_f32[(row0 + t) * a.N + 128 * nb + j] =
                 __fmul_rn(v, m.tscale[t]) * m.tscale[kGvTok + t];
         }
@@ -341,6 +351,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     const int K = a.K, KB = (K + 255) / 256, NB = a.N / 128;
     const int pitch = gv_row_pitch(KB);
     const GvSmem m = gv_carve(gv_smem, K, slots);
+    const int nred = gv_nred(K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < slots; ++i) {
@@ -354,22 +365,32 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     pdl_wait();  // group sizes, offsets and activation rows come from the preceding kernels
     pdl_trigger();
     if (warp == 0) {
-        // chunks of the non-empty groups, in group order
+        // chunks of the non-empty groups, in group order; the counts 256 at a time, so one
+        // load latency per 256 groups
         int n = 0;
-        for (int g0 = 0; g0 < a.G; g0 += 32) {
-            const int g = g0 + lane;
-            const int nc = g < a.G ? (a.counts[g] + kGvTok - 1) / kGvTok : 0;
-            int incl = nc;  // inclusive scan of the chunk counts over the warp
+        for (int g0 = 0; g0 < a.G; g0 += 256) {
+            int cnt[8];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
+            for (int j = 0; j < 8; ++j) {
+                const int g = g0 + 32 * j + lane;
+                cnt[j] = g < a.G ? a.counts[g] : 0;
             }
-            for (int c = 0; c < nc; ++c) {
-                const int slot = n + incl - nc + c;
-                if (slot < list_cap) m.list[slot] = (g << 16) | (c * kGvTok);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int g = g0 + 32 * j + lane;
+                const int nc = (cnt[j] + kGvTok - 1) / kGvTok;
+                int incl = nc;  // inclusive scan of the chunk counts over the warp
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                for (int c = 0; c < nc; ++c) {
+                    const int slot = n + incl - nc + c;
+                    if (slot < list_cap) m.list[slot] = (g << 16) | (c * kGvTok);
+                }
+                n += __shfl_sync(0xffffffffu, incl, 31);
             }
-            n += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (lane == 0) {
             if (n > list_cap) set_status(a.status, MOE_DEV_ROWS_OVERFLOW);
@@ -438,7 +459,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
             nt = min(kGvTok, a.counts[g] - t0);
             row0 = (int64_t)a.offsets[g] + t0;
         }
-        gv_consumer_sync();  // the previous item's readers of sx, red and the scales are done
+        // the previous item's readers of sx, the scales and (one buffer) red are done
+        if (nred == 1 || ci != staged) gv_consumer_sync();
         if (ci != staged) {
             if (warp < nt) {
                 gv_stage<kGateUp>(xin + (row0 + warp) * K, K, KB, m.sx + warp * pitch,
@@ -484,7 +506,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
 #pragma unroll
             for (int r = 0; r < 4; ++r) d[0][mb][r] += d[1][mb][r];
         // partial sums: red[warp][row][token], row = 16 mb + 8 hh + g, token 2c, 2c + 1
-        float* rw = m.red + warp * 32 * kGvTok;
+        float* redb = m.red + (nred == 2 ? ((item - i0) & 1) : 0) * kGvConsumers * 32 * kGvTok;
+        float* rw = redb + warp * 32 * kGvTok;
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
@@ -492,7 +515,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
                 *reinterpret_cast<float2*>(rw + (16 * mb + 8 * hh + g8) * kGvTok + 2 * c4) =
                     make_float2(d[0][mb][2 * hh], d[0][mb][2 * hh + 1]);
         gv_consumer_sync();
-        if (ok) gv_epilogue<kGateUp>(a, m, row0, nt, nb);
+        if (ok) gv_epilogue<kGateUp>(a, m, redb, row0, nt, nb);
     }
 }
 
