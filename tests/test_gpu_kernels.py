@@ -327,10 +327,11 @@ def test_gather_w4a16_rows_are_exact_fp16_copies(scale):
     assert np.max(np.abs(want.astype(np.float32))) <= 2.0 ** 15
 
 
-# W4A16 picks 16, 32 or 64 token rows per tile from T * k / E (here 15, 25 and 50 rows);
+# W4A16 runs batches of up to 256 tokens on the grouped GEMV (T = 60, 100, 200 here) and
+# larger ones on the tensor-core kernel (T = 300: 64 token rows per tile from T * k / E);
 # W4A4 sizes its activation slots from T (32 rows at T=30, 64 at T=60, 128 at T=200)
 @pytest.mark.parametrize("act_mode,T", [(0, 30), (0, 60), (0, 200), (2, 60), (2, 100),
-                                        (2, 200)])
+                                        (2, 200), (2, 300)])
 def test_grouped_gemm_gateup_unfused_matches_oracle(act_mode, T):
     layer, wr, x, lg, h, (H, I, E, k, T) = _mid_problem(act_mode, T)
     st = Staged(h, bits16(x), T, k, lg)
@@ -358,7 +359,7 @@ def test_grouped_gemm_gateup_unfused_matches_oracle(act_mode, T):
         assert np.max(err) <= 2e-5 * scale * np.sqrt(H / 64), (g, np.max(err), scale)
 
 
-@pytest.mark.parametrize("act_mode,T", [(0, 200), (2, 60), (2, 100), (2, 200)])
+@pytest.mark.parametrize("act_mode,T", [(0, 200), (2, 60), (2, 100), (2, 200), (2, 300)])
 def test_grouped_gemm_fused_and_down_match_oracle(act_mode, T):
     layer, wr, x, lg, h, (H, I, E, k, T) = _mid_problem(act_mode, T)
     st = Staged(h, bits16(x), T, k, lg)
