@@ -169,7 +169,8 @@ namespace {
 constexpr int kGvConsumers = kGvThreads / 32 - 1;  // 16 consumer warps, then the copy warp
 constexpr int kGvUnits = 4;                        // 32-row units per 128-row tile
 constexpr int kGvKsteps = 4;                       // 64-element k-steps per blob
-constexpr int kGvScales = 32;                      // per-chunk output scales (floats)
+constexpr int kGvScales = 48;                      // per-chunk output scales (floats)
+constexpr int kGvScaleWmax = 32;                   // ... and 16 words for the staging maxima
 
 // Consumer-warp wait on a full barrier: every lane polls; the vote keeps the outcome
 // warp-uniform should the lanes' time limits run out at different polls.
@@ -188,7 +189,7 @@ struct GvSmem {
     uint8_t* sx;
     float* red;
     float* tscale;  // [kGvScales]: 2^-k_t per token, then (down) rcp(gs_w) x routing weight
-                    // per token, then (gate_up) 1 / (gs_a gs_w)
+                    // per token, then (gate_up) 1 / (gs_a gs_w); 16 staging words at 32
     uint64_t* full;
     uint64_t* empty;
     volatile int* abort_flag;
@@ -225,54 +226,110 @@ __device__ __forceinline__ GvSmem gv_carve(uint8_t* base, int K, int slots)
     return m;
 }
 
-// Token row src (K 16-bit values) -> dst as fp16, zeros past K; one warp.
-// down: bf16 -> fp16 x * 2^k_t (k_t from the row's largest magnitude), 2^-k_t -> *tscale, and
-// each 8-element group stored in the blobs' nibble order 0,2,4,6,1,3,5,7.
-template <bool kGateUp>
-__device__ __forceinline__ void gv_stage(const uint16_t* src, int K, int KB, uint8_t* dst,
-                                         float* tscale, int lane)
+// bf16 pair -> two floats times `up`, rounded to an fp16 pair.
+__device__ __forceinline__ uint32_t gv_bf16x2_to_f16x2(uint32_t u, float up)
 {
+    const __half2 v = __floats2half2_rn(__uint_as_float(u << 16) * up,
+                                        __uint_as_float(u & 0xFFFF0000u) * up);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// The chunk's nt token rows (K 16-bit values each, from row row0 of xin) -> sx as fp16,
+// zeros past K, by all consumer warps: 16 / nt (rounded to a power of two) warps per row,
+// each lane four 16-byte pieces in flight at a time.  down: each row's bf16 values are taken
+// times 2^k_t (k_t from the row's largest magnitude, met across its warps in shared memory)
+// and every 8-element group is stored in the blobs' nibble order 0,2,4,6,1,3,5,7.  Also the
+// chunk's output scales: 2^-k_t, and rcp(gs_w) x the routing weight per row (down) or
+// 1 / (gs_a gs_w) (gate_up).  Ends with the staged data visible to every consumer.
+template <bool kGateUp>
+__device__ __forceinline__ void gv_stage_chunk(const GemmArgs& a, const GvSmem& m,
+                                               const uint16_t* xin, int64_t row0, int nt,
+                                               int g, int K, int KB, int pitch)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wpt = nt <= 1 ? 16 : nt <= 2 ? 8 : nt <= 4 ? 4 : 2;
+    const int t = warp / wpt, sub = warp % wpt;
+    const bool act = t < nt;
+    const int npc = KB * 32;  // 8-element pieces of a staged row
+    const int S = wpt * 32;   // the row's threads
+    const uint16_t* src = xin + (row0 + (act ? t : 0)) * K;
+    uint8_t* dst = m.sx + (act ? t : 0) * pitch;
     float up = 1.0f;  // down: 2^k_t
     if constexpr (!kGateUp) {
-        uint32_t mx = 0;
-        for (int e8 = 8 * lane; e8 < K; e8 += 256) {
-            const uint4 q = *reinterpret_cast<const uint4*>(src + e8);
-            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+        uint32_t mx = 0;  // largest bf16 magnitude (bits), this thread's pieces
+        if (act)
+            for (int p0 = sub * 32 + lane; p0 < npc; p0 += 4 * S) {
+                uint4 q[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) mx = max(mx, max(u[j] & 0x7FFFu, (u[j] >> 16) & 0x7FFFu));
-        }
+                for (int j = 0; j < 4; ++j) {
+                    const int p = p0 + j * S;
+                    q[j] = (p < npc && 8 * p < K) ? *reinterpret_cast<const uint4*>(src + 8 * p)
+                                                  : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t u[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        mx = max(mx, max(u[i] & 0x7FFFu, (u[i] >> 16) & 0x7FFFu));
+                }
+            }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        // bf16 exponent field of the largest magnitude -> k_t in [-113, 113]
-        const int ex = (int)(mx >> 7) - 127;
-        const int kt = mx ? max(-113, min(113, 14 - ex)) : 0;
-        up = __uint_as_float((uint32_t)(127 + kt) << 23);
-        if (lane == 0) *tscale = __uint_as_float((uint32_t)(127 - kt) << 23);
+        uint32_t* wmax = reinterpret_cast<uint32_t*>(m.tscale + kGvScaleWmax);
+        if (lane == 0) wmax[warp] = mx;
+        gv_consumer_sync();
+        if (act) {
+            for (int w = 0; w < wpt; ++w) mx = max(mx, wmax[t * wpt + w]);
+            // bf16 exponent field of the largest magnitude -> k_t in [-113, 113]
+            const int ex = (int)(mx >> 7) - 127;
+            const int kt = mx ? max(-113, min(113, 14 - ex)) : 0;
+            up = __uint_as_float((uint32_t)(127 + kt) << 23);
+            if (sub == 0 && lane == 0) m.tscale[t] = __uint_as_float((uint32_t)(127 - kt) << 23);
+        }
     }
-    for (int e8 = 8 * lane; e8 < KB * 256; e8 += 256) {
-        uint4 q = make_uint4(0, 0, 0, 0);
-        if (e8 < K) q = *reinterpret_cast<const uint4*>(src + e8);
-        uint2 lo, hi;  // elements (0..3, 4..7), or (0,2,4,6), (1,3,5,7) for down
-        if constexpr (kGateUp) {
-            lo = make_uint2(q.x, q.y);
-            hi = make_uint2(q.z, q.w);
-        } else {
-            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-            uint32_t h[4];
+    if (act)
+        for (int p0 = sub * 32 + lane; p0 < npc; p0 += 4 * S) {
+            uint4 q[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const __half2 v = __floats2half2_rn(__uint_as_float(u[j] << 16) * up,
-                                                    __uint_as_float(u[j] & 0xFFFF0000u) * up);
-                h[j] = *reinterpret_cast<const uint32_t*>(&v);
+                const int p = p0 + j * S;
+                q[j] = (p < npc && 8 * p < K) ? *reinterpret_cast<const uint4*>(src + 8 * p)
+                                              : make_uint4(0, 0, 0, 0);
             }
-            // h[j] = (x_2j, x_2j+1) -> (x0, x2), (x4, x6) | (x1, x3), (x5, x7)
-            lo = make_uint2(__byte_perm(h[0], h[1], 0x5410), __byte_perm(h[2], h[3], 0x5410));
-            hi = make_uint2(__byte_perm(h[0], h[1], 0x7632), __byte_perm(h[2], h[3], 0x7632));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int p = p0 + j * S;
+                if (p >= npc) break;
+                uint2 lo, hi;  // elements (0..3, 4..7), or (0,2,4,6), (1,3,5,7) for down
+                if constexpr (kGateUp) {
+                    lo = make_uint2(q[j].x, q[j].y);
+                    hi = make_uint2(q[j].z, q[j].w);
+                } else {
+                    const uint32_t h0 = gv_bf16x2_to_f16x2(q[j].x, up),
+                                   h1 = gv_bf16x2_to_f16x2(q[j].y, up),
+                                   h2 = gv_bf16x2_to_f16x2(q[j].z, up),
+                                   h3 = gv_bf16x2_to_f16x2(q[j].w, up);
+                    // h_i = (x_2i, x_2i+1) -> (x0, x2), (x4, x6) | (x1, x3), (x5, x7)
+                    lo = make_uint2(__byte_perm(h0, h1, 0x5410), __byte_perm(h2, h3, 0x5410));
+                    hi = make_uint2(__byte_perm(h0, h1, 0x7632), __byte_perm(h2, h3, 0x7632));
+                }
+                uint8_t* d = dst + 16 * p;
+                *reinterpret_cast<uint2*>(d) = lo;
+                *reinterpret_cast<uint2*>(d + 8) = hi;
+            }
         }
-        uint8_t* p = dst + 2 * e8;
-        *reinterpret_cast<uint2*>(p) = lo;
-        *reinterpret_cast<uint2*>(p + 8) = hi;
+    if (act && sub == 0 && lane == 0) {
+        const float gw = a.gs_w[g];
+        if constexpr (kGateUp) {
+            if (t == 0) m.tscale[2 * kGvTok] = __frcp_rn(__fmul_rn(*a.gs_a, gw));
+        } else {
+            const int pair = a.perm_src[row0 + t];
+            const float wn = pair < a.Tk ? a.topk_w[pair] : 1.0f;
+            m.tscale[kGvTok + t] = __fmul_rn(__frcp_rn(gw), wn);
+        }
     }
+    gv_consumer_sync();
 }
 
 // The k-slots' partials of tile nb summed, scaled and stored by the consumer threads.
@@ -462,22 +519,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         // the previous item's readers of sx, the scales and (one buffer) red are done
         if (nred == 1 || ci != staged) gv_consumer_sync();
         if (ci != staged) {
-            if (warp < nt) {
-                gv_stage<kGateUp>(xin + (row0 + warp) * K, K, KB, m.sx + warp * pitch,
-                                  m.tscale + warp, lane);
-                if (lane == 0) {
-                    const float gw = a.gs_w[g];
-                    if constexpr (kGateUp) {
-                        if (warp == 0) m.tscale[2 * kGvTok] = __frcp_rn(__fmul_rn(*a.gs_a, gw));
-                    } else {
-                        const int pair = a.perm_src[row0 + warp];
-                        const float wn = pair < a.Tk ? a.topk_w[pair] : 1.0f;
-                        m.tscale[kGvTok + warp] = __fmul_rn(__frcp_rn(gw), wn);
-                    }
-                }
-            }
+            gv_stage_chunk<kGateUp>(a, m, xin, row0, nt, g, K, KB, pitch);
             staged = ci;
-            gv_consumer_sync();
         }
         float d[2][2][4] = {};
         const uint8_t* xs = m.sx + g8 * pitch + 2 * (64 * my_ks + 16 * c4);
