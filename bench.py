@@ -349,9 +349,10 @@ def measure_ours(args, rank, world):
         torch.cuda.synchronize()
         barrier()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    ms_eager = max_over_ranks(eager_ms(fwd, stream, args.steps), world)
 
     roof = roofline(layer, c, xd, lgd, bd, ws, stream, args.steps, peaks(), name)
-    res = dict(value=value, ms=ms, ms_e2e=ms_e2e, clocks=clocks, roofline=roof,
+    res = dict(value=value, ms=ms, ms_e2e=ms_e2e, ms_eager=ms_eager, clocks=clocks, roofline=roof,
                launches=launches_per_forward(c) * args.steps)
     if "prefill" in extra and rank == 0:
         res["prefill"] = measure_prefill(handles["prefill"], stream, max(3, args.steps // 20))
@@ -363,6 +364,22 @@ def measure_ours(args, rank, world):
     if extra and rank == 0:
         res["weight_prep"] = measure_weight_prep(c, stream, 10)
     return res
+
+
+def eager_ms(fwd, stream, steps):
+    """Device time (ms) per forward launched eagerly (no graph), inputs resident."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fwd()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fwd()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
 
 
 def staged_counts(layer, ws, T):
@@ -645,6 +662,8 @@ def measure_w4a16(layer, stream, steps):
             e1.record(stream)
             torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
+        ms_eager = eager_ms(lambda: moe.moe_forward(layer.handle, xd, lgd, None, T, out, ws),
+                            stream, steps)
         roof = roofline(layer, cc, xd, lgd, None, ws, stream, min(steps, 20), pk, "w4a16")
         counts = staged_counts(layer, ws, T)
         wbytes = gemm_bytes(cc, counts, True)[0] + gemm_bytes(cc, counts, False)[0]
@@ -661,7 +680,7 @@ def measure_w4a16(layer, stream, steps):
                          "step_hbm_frac": round(wbytes / (ms / 1e3) / 1e9 / pk["hbm"], 4),
                          "gateup_us": roof["launch_us"], "gateup_frac": roof["frac"],
                          "down_us": roof["down"]["launch_us"], "down_frac": roof["down"]["frac"],
-                         "l2": l2})
+                         "eager_ms_per_step": round(ms_eager, 4), "l2": l2})
     return {"workload": "w4a16 decode sweep (bf16 x NVFP4, logits given)", "unit": "tokens/s",
             "sweep": out_rows}
 
@@ -708,14 +727,28 @@ ORACLE_SAMPLE = {"decode": 64, "prefill": 16, "shard": 16, "w4a16": 16, "tiny": 
 
 
 def cpu_baseline(name):
+    """The oracle on the host cores (all of them), and on one thread for a quarter of the
+    sample."""
     import oracle
     run, what = oracle_setup(name, ORACLE_SAMPLE[name])
     t0 = time.perf_counter()
     run()
     dt = time.perf_counter() - t0
     n = ORACLE_SAMPLE[name]
-    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": what, "seconds": round(dt, 2)}
+    cores = oracle.num_threads()
+    n1 = max(1, n // 4)
+    run1, what1 = oracle_setup(name, n1)
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        run1()
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle", "sample": what, "seconds": round(dt, 2),
+            "one_thread": {"value": round(n1 / dt1, 3), "unit": "tokens/s", "sample": what1,
+                           "seconds": round(dt1, 2)}}
 
 
 def main():
@@ -779,7 +812,9 @@ def main():
             "e2e": {"value": job_tokens_per_s(world, c["T"], r["ms_e2e"]), "unit": "tokens/s",
                     "h2d_bytes_per_step": c["T"] * c["H"] * 2,
                     "d2h_bytes_per_step": c["T"] * c["H"] * 2},
-            "gpu_launches": r["launches"], "roofline": r["roofline"]}
+            "gpu_launches": r["launches"], "roofline": r["roofline"],
+            "eager": {"ms_per_step": r["ms_eager"],
+                      "note": "the same forward launched eagerly (no CUDA graph), device time"}}
     for side in ("prefill", "w4a16", "decode_static", "decode_dyninter", "weight_prep"):
         if side in r:
             line[side] = r[side]
