@@ -419,8 +419,11 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         *m.zero = 0;
         fence_barrier_init();
     }
-    pdl_wait();  // group sizes, offsets and activation rows come from the preceding kernels
-    pdl_trigger();
+    // The group sizes and offsets come from the grouping kernels, which are complete when
+    // this kernel starts (every kernel of the forward waits for its predecessor before it
+    // lets the next one start, see pdl_wait), and the weights are constant: the work list
+    // and the weight stream go ahead of the wait, which only the consumers (reading the
+    // predecessor's activation rows) take.
     if (warp == 0) {
         // chunks of the non-empty groups, in group order; the counts 256 at a time, so one
         // load latency per 256 groups
@@ -498,6 +501,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         return;
     }
 
+    pdl_wait();
+    pdl_trigger();
     // consumer warps: unit my_u (rows 32 my_u .. of the tile), k-step my_ks of every blob
     const int my_u = warp % kGvUnits, my_ks = warp / kGvUnits;
     const int g8 = lane >> 2, c4 = lane & 3;
