@@ -230,6 +230,22 @@ def test_w4a16_forward_ragged_k(T, E_loc, off, add_shared, has_shared):
     _check(got, ora.out, "w4a16 T=%d E_loc=%s" % (T, E_loc))
 
 
+def test_w4a16_tiny_layer_short_k():
+    """The tiny layer in W4A16 mode: down's K = I = 128 is half of one 256-element k-block,
+    gate_up's K = H = 256 exactly one."""
+    c = synth.CONFIGS["tiny"]
+    T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+    layer = build_layer(0, H, I, E)
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(0, T, H)
+    lg = synth.logits_normal(3, T, E)
+    h = make_layer(layer, wr, H, I, E, k, act_mode=moe.MOE_W4A16, max_tokens=T)
+    got = _forward(h, x, T, logits_in=lg)
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, act_mode=2), x, layer,
+                             logits_in=lg)
+    _check(got, ora.out, "w4a16 tiny")
+
+
 def test_prefill_chunk_sampled_parity(big_layer):
     c = synth.CONFIGS["prefill"]
     T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
