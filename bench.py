@@ -212,10 +212,17 @@ def job_tokens_per_s(world, tokens_per_rank, ms_slowest):
 
 
 def launches_per_forward(c):
-    n = 1 + (0 if c["logits"] else 1)      # router logits (from x) + top-k
-    n += 3                                 # grouping: histogram, scan, scatter
-    n += 2 if c["act_mode"] == 0 else 1    # (amax +) gather-quantise / gather
-    n += 2 + 1                             # two grouped GEMMs + combine
+    """Kernels one forward launches, by the library's dispatch rules (api.cu)."""
+    router = not c["logits"]
+    n = (1 if router else 0) + 1           # router logits from x (unless given), top-k
+    pairs = c["T"] * c["k"]
+    n += 1 if pairs <= 1024 else 3         # grouping: one block, or histogram, scan, scatter
+    # the activation amax is folded into the top-k kernel when the router ran; with given
+    # logits a dynamic (or W4A16) forward runs its own amax pass
+    n += 1 if (c["act_mode"] != 1 and not router) else 0
+    n += 1                                 # gather (NVFP4 quantise, or fp16 copies for W4A16)
+    n += 2 if c.get("inter") == "dynamic" else 1   # gate_up (+ the intermediate requant pass)
+    n += 2                                 # down + combine
     return n
 
 
