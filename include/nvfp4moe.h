@@ -299,6 +299,15 @@ MOE_API moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int3
  * MOE_ERR_DEVICE_STATUS (other bits set). */
 MOE_API moe_status moe_get_status(moe_handle h, void* ws_d, moe_stream_t stream, uint32_t* bits);
 
+/* Self-test of the failure path of the pipelines' bounded waits: one thread waits, with the
+ * same bounded wait the kernels use, on an mbarrier phase that nothing completes, so the
+ * wait runs out after limit_ns (1 ns .. 2 s) and sets MOE_DEV_WAIT_TIMEOUT in *status_d (a
+ * caller-owned device word, cleared first), as a pipeline role would; no trap, the context
+ * stays usable.  Synchronises the stream.  Returns MOE_ERR_TIMEOUT (the expected outcome),
+ * MOE_OK (the wait completed: a broken wait), MOE_ERR_INVALID or MOE_ERR_CUDA. */
+MOE_API moe_status moe_selftest_bounded_wait(uint32_t* status_d, uint64_t limit_ns,
+                                             moe_stream_t stream);
+
 MOE_API const char* moe_status_string(moe_status s);
 
 #ifdef __cplusplus

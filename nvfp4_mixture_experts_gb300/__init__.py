@@ -61,6 +61,7 @@ SIGNATURES = {
     "moe_forward_buffers": (C.c_int, [_V, _V, _I] + [C.POINTER(_V)] * 15),
     "moe_get_status": (C.c_int, [_V, _V, _V, C.POINTER(C.c_uint32)]),
     "moe_status_string": (C.c_char_p, [C.c_int]),
+    "moe_selftest_bounded_wait": (C.c_int, [_V, C.c_uint64, _V]),
 }
 
 _lib = None
@@ -217,6 +218,12 @@ def moe_forward_buffers(h, ws, T):
     _check(load().moe_forward_buffers(h, _p(ws), T, *[C.byref(p) for p in ptrs]),
            "moe_forward_buffers")
     return {n: p.value for n, p in zip(FORWARD_BUFFERS, ptrs)}
+
+
+def moe_selftest_bounded_wait(status_word, limit_ns, stream=None):
+    """Runs the bounded-wait failure self-test (status_word: a device tensor of >= 4 bytes);
+    returns the status code (MOE_ERR_TIMEOUT expected)."""
+    return load().moe_selftest_bounded_wait(_p(status_word), int(limit_ns), _stream(stream))
 
 
 def moe_get_status(h, ws, stream=None):

@@ -1033,6 +1033,40 @@ moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
                   (const uint16_t*)nullptr, 0, (uint32_t*)nullptr);
 }
 
+namespace moe {
+namespace {
+
+// One thread waits, with the pipelines' own bounded wait, on a phase of an mbarrier that
+// nothing arrives on; when the limit runs out it sets MOE_DEV_WAIT_TIMEOUT, as a pipeline
+// role would, and returns.
+__global__ void bounded_wait_probe_kernel(uint32_t* status, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int zero;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    zero = 0;
+    fence_barrier_init();
+    if (!mbar_wait(&bar, 0, &zero, limit_ns)) set_status(status, MOE_DEV_WAIT_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace moe
+
+moe_status moe_selftest_bounded_wait(uint32_t* status_d, uint64_t limit_ns, moe_stream_t stream)
+{
+    if (!status_d || limit_ns == 0 || limit_ns > moe::kWaitLimitNs) return MOE_ERR_INVALID;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t bits = 0;
+    if (cudaMemsetAsync(status_d, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    moe::bounded_wait_probe_kernel<<<1, 32, 0, s>>>(status_d, limit_ns);
+    if (cudaGetLastError() != cudaSuccess ||
+        cudaMemcpyAsync(&bits, status_d, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return (bits & MOE_DEV_WAIT_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_OK;
+}
+
 moe_status moe_get_status(moe_handle h, void* ws_d, moe_stream_t stream, uint32_t* bits)
 {
     if (!h || !ws_d) return MOE_ERR_INVALID;

@@ -19,6 +19,26 @@ def _ws(nbytes):
     return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device="cuda")
 
 
+# ---------------------------------------------------------------- failure path of the waits
+
+def test_bounded_wait_runs_out_sets_status_and_leaves_the_context_usable():
+    """A wait on an mbarrier phase that nothing completes gives up after its limit, reports
+    MOE_DEV_WAIT_TIMEOUT through the status word, and returns (no trap); the GPU then runs
+    the quantiser bit-exactly as before."""
+    import time
+    word = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert moe.moe_selftest_bounded_wait(word, 0) == moe.MOE_ERR_INVALID
+    assert moe.moe_selftest_bounded_wait(word, 3 * 10 ** 9) == moe.MOE_ERR_INVALID
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    st = moe.moe_selftest_bounded_wait(word, 2 * 10 ** 6)  # 2 ms
+    dt = time.perf_counter() - t0
+    assert st == moe.MOE_ERR_TIMEOUT
+    assert int(host(word)[0]) & moe.MOE_DEV_WAIT_TIMEOUT
+    assert dt >= 2e-3
+    test_quant_nvfp4_dynamic_bit_exact(300, 512, 1)
+
+
 # ---------------------------------------------------------------- quantiser
 
 @pytest.mark.parametrize("R,K,layout", [(300, 512, 0), (300, 512, 1), (1, 64, 0), (129, 4096, 1),
