@@ -248,9 +248,9 @@ bool t_ok(const moe_layer* h, int T) { return T >= 0 && T <= h->cfg.max_tokens; 
 
 int grid_for(int64_t threads, int block) { return (int)std::max<int64_t>(1, (threads + block - 1) / block); }
 
-// W4A16 batches of at most this many tokens take the grouped GEMV (gemv_w4a16.cu), which
-// reads each weight once per chunk of 8 rows of a group instead of padding every group to
-// the tensor-core kernel's 128-row MMA.
+// W4A16 batches of at most this many tokens (and at most 2 x 8 expected rows per local
+// expert) take the grouped GEMV (gemv_w4a16.cu), which reads each weight once per chunk of
+// 8 rows of a group instead of padding every group to the tensor-core kernel's 128-row MMA.
 constexpr int kGemvMaxTokens = 256;
 
 // Persistent grid: one CTA per SM, or fewer when the tile list (bounded above from the
@@ -415,7 +415,10 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
         const int64_t rows = (int64_t)p.T * c.top_k + shared_rows(h, p.T);
         const int list_cap = (int)(p.G + (rows + kGvChunk - 1) / kGvChunk);
         const int slots = gemv_w4a16_slots(K, list_cap);
-        if (p.T <= kGemvMaxTokens && epilogue != kEpiGateUpSwigluF32 && slots >= 4) {
+        // (and only while the expected rows per local expert fit about two chunks: with
+        // more, the GEMV would decode every weight once per further chunk)
+        const bool few_rows = (int64_t)p.T * c.top_k <= 2LL * kGvChunk * std::max(1, p.El);
+        if (p.T <= kGemvMaxTokens && few_rows && epilogue != kEpiGateUpSwigluF32 && slots >= 4) {
             const size_t gsm = gemv_w4a16_smem(K, slots, list_cap);
             const int64_t items = (int64_t)list_cap * (N / 128);
             const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(h->num_sms, items));

@@ -202,14 +202,16 @@ def test_w4a16_decode_sweep(big_layer, T):
     _check(got[tok], ora.out, "w4a16 T=%d" % T)
 
 
-# W4A16 at up to 256 tokens runs on the grouped GEMV, above on the tensor-core kernel.
+# W4A16 at up to 256 tokens (and at most 16 expected rows per expert: T*k/E <= 16) runs on
+# the grouped GEMV, otherwise on the tensor-core kernel; here E=24 (or 8 local), k=4.
 # H = 384 and I = 320 leave the last 256-element k-block of each GEMM partly empty; the
 # shard (experts 8..15 of 24, no shared rows added) leaves most groups empty; has_shared=0
-# drops the shared slot; T = 256 gives the shared slot 32 chunks of 8 rows.
+# drops the shared slot; T = 96 gives the shared slot 12 chunks of 8 rows on the GEMV;
+# T = 40 on the shard and T >= 128 run on the tensor-core kernel.
 @pytest.mark.parametrize("T,E_loc,off,add_shared,has_shared", [
     (1, None, 0, 1, 1), (7, None, 0, 1, 1), (64, None, 0, 1, 1), (65, None, 0, 1, 1),
-    (5, 8, 8, 0, 1), (40, 8, 8, 1, 1), (9, None, 0, 1, 0), (256, None, 0, 1, 1),
-    (257, None, 0, 1, 1), (300, 8, 8, 1, 1)])
+    (96, None, 0, 1, 1), (5, 8, 8, 0, 1), (40, 8, 8, 1, 1), (9, None, 0, 1, 0),
+    (256, None, 0, 1, 1), (257, None, 0, 1, 1), (300, 8, 8, 1, 1)])
 def test_w4a16_forward_ragged_k(T, E_loc, off, add_shared, has_shared):
     H, I, E, k = 384, 320, 24, 4
     layer = build_layer(21, H, I, E)

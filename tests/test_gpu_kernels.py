@@ -347,8 +347,9 @@ def test_gather_w4a16_rows_are_exact_fp16_copies(scale):
     assert np.max(np.abs(want.astype(np.float32))) <= 2.0 ** 15
 
 
-# W4A16 runs batches of up to 256 tokens on the grouped GEMV (T = 60, 100, 200 here) and
-# larger ones on the tensor-core kernel (T = 300: 64 token rows per tile from T * k / E);
+# W4A16 runs batches of up to 256 tokens with at most 16 expected rows per expert on the
+# grouped GEMV (T = 60 here: 15 rows per expert) and the others on the tensor-core kernel
+# (T = 100, 200, 300: 32, 64, 64 token rows per tile from T * k / E = 25, 50, 75);
 # W4A4 sizes its activation slots from T (32 rows at T=30, 64 at T=60, 128 at T=200)
 @pytest.mark.parametrize("act_mode,T", [(0, 30), (0, 60), (0, 200), (2, 60), (2, 100),
                                         (2, 200), (2, 300)])
