@@ -175,12 +175,20 @@ def gpu_layer(name, seed=0, extra_handles=(), local_experts=0):
     handles = {}
     for nm in (name,) + tuple(extra_handles):
         cc = synth.CONFIGS[nm]
-        cfg = moe.make_config(H, I, E, k, E_loc=El, off=c["off"], has_shared=1,
+        ww, el, off = w, El, c["off"]
+        if not local_experts and (cc["off"], cc["E_loc"]) != (c["off"], c["E_loc"]):
+            # an expert shard of this layer: the slice of the same weights
+            lo = cc["off"] - c["off"]
+            el, off = cc["E_loc"], cc["off"]
+            ww = dict(w)
+            for key in ("w13", "w13_sf", "w13_gs", "w2", "w2_sf", "w2_gs"):
+                ww[key] = w[key][lo:lo + el]
+        cfg = moe.make_config(H, I, E, k, E_loc=el, off=off, has_shared=1,
                               add_shared=cc["add_shared"], act_mode=cc["act_mode"],
                               act_gs=INTER[nm].get("act_global_scale", 0.0),
                               inter_gs=INTER[nm]["inter_global_scale"],
                               max_tokens=cc["T"])
-        handles[nm] = moe.MoELayer(cfg, w)
+        handles[nm] = moe.MoELayer(cfg, ww)
     del w
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -274,7 +282,7 @@ def measure_ours(args, rank, world):
     c = synth.CONFIGS[name]
     T, H, k = c["T"], c["H"], c["k"]
     extra = () if (args.no_extra or name != "decode" or args.local_experts) else \
-        ("prefill", "w4a16", "decode_static", "decode_dyninter")
+        ("prefill", "w4a16", "decode_static", "decode_dyninter", "shard")
     handles = gpu_layer(name, extra_handles=extra, local_experts=args.local_experts)
     if args.local_experts:
         c = dict(c, E_loc=args.local_experts)
@@ -365,6 +373,8 @@ def measure_ours(args, rank, world):
         res["prefill"] = measure_prefill(handles["prefill"], stream, max(3, args.steps // 20))
     if "w4a16" in extra and rank == 0:
         res["w4a16"] = measure_w4a16(handles["w4a16"], stream, max(10, args.steps // 4))
+    if "shard" in extra and rank == 0:
+        res["shard"] = measure_shard(handles["shard"], stream, max(10, args.steps // 4))
     for nm in ("decode_static", "decode_dyninter"):
         if nm in extra and rank == 0:
             res[nm] = measure_variant(handles[nm], nm, stream, max(10, args.steps // 4))
@@ -558,6 +568,52 @@ def measure_variant(layer, name, stream, steps):
             "ms_per_step": round(ms, 4), "gateup_us": roof["launch_us"],
             "gateup_frac": roof["frac"], "down_us": roof["down"]["launch_us"],
             "down_frac": roof["down"]["frac"]}
+
+
+def measure_shard(layer, stream, steps):
+    """Side measurement of the expert shard (experts 160-319 of the same layer, T=2048, router
+    logits biased towards a Zipf(1.1) popularity, no shared rows): the shard's partial sum,
+    CUDA-graph replays, and its two grouped GEMM launches timed on their own."""
+    import torch
+
+    import nvfp4_mixture_experts_gb300 as moe
+    c = synth.CONFIGS["shard"]
+    T, H = c["T"], c["H"]
+    x, _, bias = inputs("shard")
+    xd = torch.from_numpy(x.view(np.int16)).cuda()
+    bd = torch.from_numpy(bias).cuda()
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    ws = layer.ensure_workspace(T)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            moe.moe_forward(layer.handle, xd, None, bd, T, out, ws)
+        torch.cuda.synchronize()
+        st, bits = moe.moe_get_status(layer.handle, ws)
+        if st != moe.MOE_OK:
+            raise RuntimeError("device status %#x" % bits)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            moe.moe_forward(layer.handle, xd, None, bd, T, out, ws)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    roof = roofline(layer, c, xd, None, bd, ws, stream, min(steps, 20), peaks(), "shard")
+    counts = staged_counts(layer, ws, T)
+    El = c["E_loc"]
+    return {"workload": "expert shard: experts 160-319 of the decode layer, T=2048, Zipf(1.1) "
+                        "popularity, partial sum (no shared rows)",
+            "value": round(T / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
+            "local_pairs": int(counts[:El].sum()), "experts_touched": roof["experts_touched"],
+            "max_rows_per_expert": int(counts[:El].max()),
+            "gateup_us": roof["launch_us"], "gateup_frac": roof["frac"],
+            "down_us": roof["down"]["launch_us"], "down_frac": roof["down"]["frac"]}
 
 
 def measure_weight_prep(c, stream, steps):
@@ -822,7 +878,7 @@ def main():
             "gpu_launches": r["launches"], "roofline": r["roofline"],
             "eager": {"ms_per_step": r["ms_eager"],
                       "note": "the same forward launched eagerly (no CUDA graph), device time"}}
-    for side in ("prefill", "w4a16", "decode_static", "decode_dyninter", "weight_prep"):
+    for side in ("prefill", "w4a16", "decode_static", "decode_dyninter", "shard", "weight_prep"):
         if side in r:
             line[side] = r[side]
     if world == 1 and not args.no_oracle and not args.local_experts:
