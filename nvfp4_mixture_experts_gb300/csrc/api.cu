@@ -61,7 +61,7 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 struct Plan {
     int T, k, E, El, G, H, I, cap, nblk, Tk;
     size_t status, amax, gs_a, gs_i, ids, w, logits, hist, blkoff, counts, offsets, mb_start,
-        perm_src, inv, a_codes, a_sf, a_bf16, i_codes, i_sf, i_bf16, s_f32, y, total;
+        perm_src, inv, a_codes, a_sf, a_bf16, i_codes, i_sf, i_bf16, s_f32, y, y_scale, total;
     // amax holds two words: the activation amax, then the intermediate amax (dynamic gs_i)
 };
 
@@ -125,7 +125,8 @@ Plan plan(const moe_config& c, int T)
     p.i_sf = take(a16 ? 0 : (size_t)p.cap * (p.I / 16));
     p.i_bf16 = take(a16 ? (size_t)p.cap * p.I * 2 : 0);
     p.s_f32 = take(dynamic_inter(c) ? (size_t)p.cap * p.I * 4 : 0);
-    p.y = take((size_t)p.cap * p.H * 4);
+    p.y = take((size_t)p.cap * p.H * 4);  // fp32 (staged calls) or fp16 (W4A4 forward)
+    p.y_scale = take((size_t)p.cap * 4);
     p.total = o;
     return p;
 }
@@ -407,7 +408,12 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     args.topk_w = topk_w;
     args.Tk = p.Tk;
     args.inter_amax = at<uint32_t>(ws, p.amax) + 1;
-    args.gs_i_dev = (epilogue == kEpiDown && dynamic_inter(c)) ? at<float>(ws, p.gs_i) : nullptr;
+    args.gs_i_dev = (is_down(epilogue) && dynamic_inter(c)) ? at<float>(ws, p.gs_i) : nullptr;
+    if (epilogue == kEpiDownF16) {  // the y buffer holds fp16 rows; their scales beside it
+        args.out_bf16 = reinterpret_cast<uint16_t*>(out_f32);
+        args.out_f32 = nullptr;
+        args.y_scale = at<float>(ws, p.y_scale);
+    }
     args.status = at<uint32_t>(ws, p.status);
     if (a16) {
         // Few token rows per group: the CUDA-core GEMV reads each weight once per chunk of
@@ -462,7 +468,7 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     // few rows per 128-row block the down epilogue stores directly and the shared memory
     // goes to one more pipeline stage; with many it stages TMA stores.
     const int64_t local_rows = (int64_t)p.T * c.top_k / std::max(1, c.num_local_experts);
-    args.staging = (epilogue == kEpiDown && local_rows >= 16) ? kDownStaging : 0;
+    args.staging = (is_down(epilogue) && local_rows >= 16) ? kDownStaging : 0;
     args.rb_cap = p.cap / 128;
     args.stages = gemm_stages(6, stage_bytes, args.staging, p.G, args.rb_cap);
     const int smem = gemm_smem_bytes(args.stages, stage_bytes, args.staging, p.G, args.rb_cap);
@@ -470,6 +476,10 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     if (epilogue == kEpiDown &&
         !make_tmap(&tmY, out_f32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, p.cap, (uint64_t)N * 4, 32,
                    32, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MOE_ERR_CUDA;
+    if (epilogue == kEpiDownF16 &&
+        !make_tmap(&tmY, out_f32, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, N, p.cap, (uint64_t)N * 2, 32,
+                   32, CU_TENSOR_MAP_SWIZZLE_64B))
         return MOE_ERR_CUDA;
     const int pitch = codes_pitch(K);
     if (!make_tmap(&tmA, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128, 128,
@@ -520,34 +530,37 @@ moe_status launch_gateup_fused(const moe_layer* h, const Plan& p, const uint8_t*
 constexpr int kCombineTmaMinTokens = 1024;
 constexpr size_t kCombineSmemBudget = 220 * 1024;
 
-moe_status launch_combine(const moe_layer* h, const float* y, const int32_t* inv,
+// y: fp32 rows, or (y_scale non-null) fp16 rows each times y_scale[row].
+moe_status launch_combine(const moe_layer* h, const void* y, const int32_t* inv,
                           const int32_t* offsets, int T, void* out, bool pdl, cudaStream_t s,
-                          uint32_t* status = nullptr)
+                          uint32_t* status = nullptr, const float* y_scale = nullptr)
 {
     const moe_config& c = h->cfg;
     const int add = shared_rows(h, T) > 0 ? 1 : 0;
     const int nrows = c.top_k + add;
+    const size_t es = y_scale ? 2 : 4;  // bytes per element of y
     if (T >= kCombineTmaMinTokens && nrows > 0 &&
         (reinterpret_cast<uintptr_t>(y) & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 7) == 0) {
-        int cw = 0;
-        for (int w : {2048, 1024, 512})
-            if (c.hidden % w == 0 && 2 * (size_t)nrows * w * 4 <= kCombineSmemBudget) {
+        int cw = 0;  // pieces of at most 8 KB (the measured best), two slots at least
+        for (int w : {4096, 2048, 1024, 512})
+            if (c.hidden % w == 0 && w * es <= 8192 &&
+                2 * (size_t)nrows * w * es <= kCombineSmemBudget) {
                 cw = w;
                 break;
             }
         if (cw) {
             const int nslots = (int)std::min<size_t>(
-                kCombineMaxSlots, kCombineSmemBudget / ((size_t)nrows * cw * 4));
+                kCombineMaxSlots, kCombineSmemBudget / ((size_t)nrows * cw * es));
             const int64_t units = (int64_t)T * (c.hidden / cw);
             return launch(combine_tma_kernel,
                           dim3((unsigned)std::min<int64_t>(units, h->num_sms)),
-                          dim3(kCombineTmaThreads), combine_tma_smem(nrows, cw, nslots), s, pdl,
-                          y, inv, offsets, c.num_local_experts, T, c.hidden, c.top_k, add, cw,
-                          nslots, static_cast<uint16_t*>(out), status);
+                          dim3(kCombineTmaThreads), combine_tma_smem(nrows, cw, nslots, (int)es),
+                          s, pdl, y, y_scale, inv, offsets, c.num_local_experts, T, c.hidden,
+                          c.top_k, add, cw, nslots, static_cast<uint16_t*>(out), status);
         }
     }
     return launch(combine_kernel, dim3(grid_for((int64_t)T * (c.hidden / 8), 256)), dim3(256), 0,
-                  s, pdl, y, inv, offsets, c.num_local_experts, T, c.hidden, c.top_k,
+                  s, pdl, y, y_scale, inv, offsets, c.num_local_experts, T, c.hidden, c.top_k,
                   shared_rows(h, T) > 0 ? 1 : 0, static_cast<uint16_t*>(out));
 }
 
@@ -957,10 +970,16 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
     if (r == MOE_OK)
         r = launch_gateup_fused(h, p, a_codes, a_sf, gs_a, a_bf16, counts, offsets, i_codes,
                                 i_sf, i_bf16, ws, true, s);
+    // W4A4: y as fp16 rows times a per-expert power of two (half the bytes of the y round
+    // trip); W4A16 (its bf16 intermediate has no a-priori bound) keeps fp32 y
+    const bool y16 = h->cfg.act_mode != MOE_W4A16;
     if (r == MOE_OK)
-        r = launch_gemm(h, p, false, kEpiDown, i_codes, i_sf, nullptr, i_bf16, counts, offsets,
-                        y, nullptr, nullptr, nullptr, perm_src, w, ws, true, s);
-    if (r == MOE_OK) r = launch_combine(h, y, inv, offsets, T, out_bf16_d, true, s, status);
+        r = launch_gemm(h, p, false, y16 ? kEpiDownF16 : kEpiDown, i_codes, i_sf, nullptr,
+                        i_bf16, counts, offsets, y, nullptr, nullptr, nullptr, perm_src, w, ws,
+                        true, s);
+    if (r == MOE_OK)
+        r = launch_combine(h, y, inv, offsets, T, out_bf16_d, true, s, status,
+                           y16 ? at<float>(ws, p.y_scale) : nullptr);
     return r;
 }
 

@@ -25,6 +25,7 @@
 // Every pipeline wait is bounded: a wait that runs out sets MOE_DEV_WAIT_TIMEOUT in the
 // status word and makes all roles stop, drain their copies in flight, free TMEM and exit.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.cuh"
 
@@ -103,9 +104,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 // Per-row epilogue constants of one tile (global loads, issued before the accumulator
 // wait so their latency overlaps the tile's mainloop).
+// Eight fp32 accumulator words times alpha -> eight fp16 (round to nearest even).
+__device__ __forceinline__ uint4 f32x8_to_f16x8(const uint32_t* r, float alpha)
+{
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 v = __floats2half2_rn(__uint_as_float(r[2 * i]) * alpha,
+                                            __uint_as_float(r[2 * i + 1]) * alpha);
+        h[i] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
 struct EpiPrep {
     int64_t prow;   // padded row of this thread
-    float alpha;    // 1 / (global scales) (x routing weight for kEpiDown)
+    float alpha;    // 1 / (global scales) (x routing weight for the down epilogues; x 2^e_g
+                    // for kEpiDownF16)
+    float yinv;     // kEpiDownF16: 2^-e_g
     int nvalid;     // valid rows in this warp's 32-row quarter (0..32)
     bool valid;
 };
@@ -118,21 +134,33 @@ __device__ __forceinline__ EpiPrep epi_prep(const GemmArgs& a, const TileInfo& t
     e.valid = m < ti.rows;
     e.prow = (int64_t)ti.arow0 + m;
     const float gw = a.gs_w[ti.g];
-    const float gs_in = a.epilogue != kEpiDown ? *a.gs_a : a.gs_i_dev ? *a.gs_i_dev : a.gs_i;
+    const float gs_in = !is_down(a.epilogue) ? *a.gs_a : a.gs_i_dev ? *a.gs_i_dev : a.gs_i;
     e.alpha = __frcp_rn(__fmul_rn(gs_in, gw));
     e.nvalid = max(0, min(32, ti.rows - q * 32));
-    if (a.epilogue == kEpiDown && e.valid) {
+    e.yinv = 1.0f;
+    float ys = 1.0f;
+    if (a.epilogue == kEpiDownF16) {
+        // 2^e_g: the largest power of two with K x 2688^2 x alpha_g x 2^e_g <= 65504
+        // (the bound rounded up, the quotient rounded down: 2^e_g never exceeds the exact one)
+        const float t = __fdiv_rd(kYF16Max,
+                                  __fmul_ru(__fmul_ru((float)a.K, kE2M1E4M3MaxSq), e.alpha));
+        const int ex = max(-126, min(126, (int)((__float_as_uint(t) >> 23) & 0xFFu) - 127));
+        ys = __uint_as_float((uint32_t)(127 + ex) << 23);
+        e.yinv = __uint_as_float((uint32_t)(127 - ex) << 23);
+    }
+    if (is_down(a.epilogue) && e.valid) {
         const int pair = a.perm_src[e.prow];
         const float wgt = pair < a.Tk ? a.topk_w[pair] : 1.0f;
-        e.alpha = __fmul_rn(e.alpha, wgt);
+        e.alpha = __fmul_rn(__fmul_rn(e.alpha, wgt), ys);
     }
     return e;
 }
 
 // Epilogue of one tile for the 32 rows of TMEM lane quarter q (thread = row).  A warp
-// whose quarter has no valid row does nothing.  kEpiDown with more than 8 valid rows
-// stages each 32 x 32 fp32 chunk in shared memory (128-byte swizzle, two buffers per warp)
-// and writes it with a TMA tensor store; sparse quarters store directly.
+// whose quarter has no valid row does nothing.  The down epilogues with more than 8 valid
+// rows stage each 32 x 32 chunk in shared memory (fp32: 128-byte swizzle; fp16: 64-byte
+// swizzle; two buffers per warp) and write it with a TMA tensor store; sparse quarters store
+// directly.
 __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& ti,
                                              const EpiPrep& ep, uint32_t tacc, int q, int lane,
                                              const CUtensorMap* tmY, uint8_t* stg, int& pp)
@@ -141,7 +169,9 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& 
     const bool valid = ep.valid;
     const int64_t prow = ep.prow;
     const float alpha = ep.alpha;
-    const bool staged = a.epilogue == kEpiDown && a.staging && ep.nvalid > 8;
+    const bool staged = is_down(a.epilogue) && a.staging && ep.nvalid > 8;
+    const bool f16 = a.epilogue == kEpiDownF16;
+    if (f16 && ti.nb == 0 && valid) a.y_scale[prow] = ep.yinv;  // one writer per row
     const int I = a.N / 2;
     uint32_t sfword = 0;
     float smax = 0.0f;  // kEpiGateUpSwigluF32: this lane's amax |s|
@@ -154,13 +184,20 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& 
             uint8_t* buf = stg + pp * 4096;
             if (lane == 0) bulk_wait_read1();  // this buffer's previous store has read it
             __syncwarp();
+            if (f16) {  // row lane: 64 bytes, 16-byte piece i at i ^ ((lane >> 1) & 3)
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                *reinterpret_cast<float4*>(buf + lane * 128 + ((i ^ (lane & 7)) << 4)) =
-                    make_float4(__uint_as_float(r[4 * i]) * alpha,
-                                __uint_as_float(r[4 * i + 1]) * alpha,
-                                __uint_as_float(r[4 * i + 2]) * alpha,
-                                __uint_as_float(r[4 * i + 3]) * alpha);
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4)) =
+                        f32x8_to_f16x8(r + 8 * i, alpha);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    *reinterpret_cast<float4*>(buf + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+                        make_float4(__uint_as_float(r[4 * i]) * alpha,
+                                    __uint_as_float(r[4 * i + 1]) * alpha,
+                                    __uint_as_float(r[4 * i + 2]) * alpha,
+                                    __uint_as_float(r[4 * i + 3]) * alpha);
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -171,7 +208,11 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& 
             continue;
         }
         if (!valid) continue;
-        if (a.epilogue == kEpiDown) {
+        if (f16) {
+            uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + prow * a.N + 128 * ti.nb + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = f32x8_to_f16x8(r + 8 * i, alpha);
+        } else if (a.epilogue == kEpiDown) {
             float4* dst = reinterpret_cast<float4*>(a.out_f32 + prow * a.N + 128 * ti.nb + 32 * c);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -279,7 +320,7 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = aligned_smem(smem_raw);
     const int NS = args.stages;
-    uint8_t* staging = stages + NS * kNvf4StageBytes;  // epilogue staging (kEpiDown)
+    uint8_t* staging = stages + NS * kNvf4StageBytes;  // epilogue staging (down epilogues)
     Ctl ctl = carve(staging + args.staging, kMaxStages);
     const Tables tb = load_tables(args, tables_smem(staging + args.staging));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -68,20 +68,23 @@ __global__ void quant_inter_kernel(const float* s, const int32_t* counts, const 
                                    const int32_t* mb_start, int G, int I,
                                    const uint32_t* amax_bits, uint8_t* codes, uint8_t* sf,
                                    float* gs_out);
-__global__ void combine_kernel(const float* y, const int32_t* inv, const int32_t* offsets,
-                               int shared_group, int T, int H, int k, int add_shared,
-                               uint16_t* out);
-// Bulk-copy combine for large batches: 160 threads (a copy thread, four adding warps), a
-// ring of nslots slots of (k + add_shared) row pieces of cw fp32 columns each.
-constexpr int kCombineTmaThreads = 160;
+// y: fp32 rows, or (y_scale non-null) fp16 rows to be multiplied by y_scale[row]
+__global__ void combine_kernel(const void* y, const float* y_scale, const int32_t* inv,
+                               const int32_t* offsets, int shared_group, int T, int H, int k,
+                               int add_shared, uint16_t* out);
+// Bulk-copy combine for large batches: 544 threads (a copy thread, sixteen adding warps), a
+// ring of nslots slots of (k + add_shared) row pieces of cw columns each.
+constexpr int kCombineTmaThreads = 544;
 constexpr int kCombineMaxSlots = 6;
-inline size_t combine_tma_smem(int nrows, int cw, int nslots)
+inline size_t combine_tma_smem(int nrows, int cw, int nslots, int esize = 4)
 {
-    return (size_t)nslots * nrows * cw * 4 + 3 * kCombineMaxSlots * 8 + 16;
+    return (size_t)nslots * nrows * cw * esize + 3 * kCombineMaxSlots * 8 + 16 +
+           (size_t)kCombineMaxSlots * (kMaxTopK + 1) * 4;
 }
-__global__ void combine_tma_kernel(const float* y, const int32_t* inv, const int32_t* offsets,
-                                   int shared_group, int T, int H, int k, int add_shared, int cw,
-                                   int nslots, uint16_t* out, uint32_t* status);
+__global__ void combine_tma_kernel(const void* y, const float* y_scale, const int32_t* inv,
+                                   const int32_t* offsets, int shared_group, int T, int H, int k,
+                                   int add_shared, int cw, int nslots, uint16_t* out,
+                                   uint32_t* status);
 __global__ void prepare_weights_kernel(const uint8_t* codes, const uint8_t* sf,
                                        const float* glob, int N, int K, int convention,
                                        float fold_target, int swap_halves, int off, int count,
@@ -94,9 +97,22 @@ enum GemmEpilogue : int {
     kEpiGateUpF32 = 0,     // G (alpha applied) -> fp32 rows, gate then up columns
     kEpiGateUpSwiglu = 1,  // silu(gate)*up -> NVFP4 (W4A4) or bf16 (W4A16)
     kEpiDown = 2,          // Y * routing weight -> fp32 rows indexed by padded row
-    kEpiGateUpSwigluF32 = 3  // silu(gate)*up -> fp32 rows [rows][I], and amax |s| into
+    kEpiGateUpSwigluF32 = 3, // silu(gate)*up -> fp32 rows [rows][I], and amax |s| into
                              // inter_amax (first pass of the dynamic intermediate scale)
+    kEpiDownF16 = 4          // as kEpiDown, as fp16 rows (out_bf16) of Y x 2^e_g, e_g per group
+                             // from a bound on |Y| (kYF16Bound); y_scale[row] = 2^-e_g
 };
+
+// |Y| of a W4A4 down row is at most K x 2688^2 x alpha_g (every code x scale factor of the
+// intermediate and of W2 is at most 6 x 448 = 2688 in magnitude, the routing weight at most
+// 1, alpha_g = 1 / (gs_i gs_w)).  The fp16 form takes Y x 2^e_g with 2^e_g the largest power
+// of two that keeps that bound within the fp16 range.
+constexpr float kYF16Max = 65504.0f;
+constexpr float kE2M1E4M3MaxSq = 2688.0f * 2688.0f;
+__host__ __device__ __forceinline__ bool is_down(int epilogue)
+{
+    return epilogue == kEpiDown || epilogue == kEpiDownF16;
+}
 
 struct GemmArgs {
     const uint8_t* a_sf;      // W4A4: activation scale atoms (tiled, K-wide)
@@ -124,6 +140,7 @@ struct GemmArgs {
     int raw_slots;            // W4A16: raw weight blobs in flight
     uint32_t* inter_amax;     // kEpiGateUpSwigluF32: fp32 bits of amax |s| (atomic max)
     const float* gs_i_dev;    // kEpiDown: device intermediate scale (dynamic), else gs_i
+    float* y_scale;           // kEpiDownF16: [rows] the inverse of each row's fp16 scale
     uint32_t* status;
 };
 

@@ -317,12 +317,26 @@ __global__ void __launch_bounds__(256) quant_inter_kernel(
 // out[t][h] = sum_{j: inv >= 0} y[inv[t*k+j]][h] + (add_shared ? y[offsets[G_s] + t][h] : 0)
 // in ascending j then the shared row, fp32, rounded to bf16.  y rows are padded rows (already
 // multiplied by their routing weight).  One thread per 8 columns of one token.
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
+// Eight fp16 (one 16-byte piece) -> fp32, exactly.
+__device__ __forceinline__ void f16x8_to_f32(uint4 q, float (&f)[8])
+{
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        f[2 * i] = p.x;
+        f[2 * i + 1] = p.y;
+    }
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y,
+                                                      const float* __restrict__ y_scale,
                                                       const int32_t* __restrict__ inv,
                                                       const int32_t* __restrict__ offsets,
                                                       int shared_group, int T, int H, int k,
                                                       int add_shared, uint16_t* __restrict__ out)
 {
+    const bool f16 = y_scale != nullptr;  // fp16 rows, each times y_scale[row]
     const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     const int per = H / 8;
     const bool live = i < (int64_t)T * per;
@@ -348,13 +362,31 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     for (int j0 = 0; j0 < nrows; j0 += 8) {
         if (j0) rows_of(j0, row);
         float4 v[8][2];
+        uint4 h[8];
+        float sc[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
             if (row[u] >= 0) {
-                const float4* src = reinterpret_cast<const float4*>(y + row[u] * H + c);
-                v[u][0] = src[0];
-                v[u][1] = src[1];
+                if (f16) {
+                    h[u] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(y) +
+                                                           row[u] * H + c);
+                    sc[u] = y_scale[row[u]];
+                } else {
+                    const float4* src =
+                        reinterpret_cast<const float4*>(static_cast<const float*>(y) + row[u] * H + c);
+                    v[u][0] = src[0];
+                    v[u][1] = src[1];
+                }
             }
+        if (f16)
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (row[u] >= 0) {
+                    float f[8];
+                    f16x8_to_f32(h[u], f);
+                    v[u][0] = make_float4(f[0] * sc[u], f[1] * sc[u], f[2] * sc[u], f[3] * sc[u]);
+                    v[u][1] = make_float4(f[4] * sc[u], f[5] * sc[u], f[6] * sc[u], f[7] * sc[u]);
+                }
 #pragma unroll
         for (int u = 0; u < 8; ++u)
             if (row[u] >= 0) {
@@ -374,7 +406,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 // The same combine for large batches, with the y rows moved by bulk copies: a work unit is
 // one token and one cw-column piece; thread 0 of warp 0 copies the piece of each of the
 // token's rows (pairs in top-k order, then its shared row; a pair outside the shard has none)
-// into a ring slot of shared memory, and warps 1-4 add them in that order (the sums of
+// into a ring slot of shared memory, and warps 1-16 add them in that order (the sums of
 // combine_kernel, bit for bit), round to bf16 and store.  Every wait is bounded; a wait that
 // runs out sets MOE_DEV_WAIT_TIMEOUT (when a status word is given) and ends the CTA's work.
 __device__ __forceinline__ bool cmb_warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort)
@@ -385,19 +417,24 @@ __device__ __forceinline__ bool cmb_warp_wait(uint64_t* bar, uint32_t parity, vo
 }
 
 __global__ void __launch_bounds__(kCombineTmaThreads, 1) combine_tma_kernel(
-    const float* __restrict__ y, const int32_t* __restrict__ inv,
-    const int32_t* __restrict__ offsets, int shared_group, int T, int H, int k, int add_shared,
-    int cw, int nslots, uint16_t* __restrict__ out, uint32_t* status)
+    const void* __restrict__ y, const float* __restrict__ y_scale,
+    const int32_t* __restrict__ inv, const int32_t* __restrict__ offsets, int shared_group,
+    int T, int H, int k, int add_shared, int cw, int nslots, uint16_t* __restrict__ out,
+    uint32_t* status)
 {
     extern __shared__ __align__(128) uint8_t smem_cmb[];
+    const bool f16 = y_scale != nullptr;  // fp16 rows, each times y_scale[row]
+    const uint32_t es = f16 ? 2u : 4u;     // bytes per element
     const int nrows = k + (add_shared ? 1 : 0);
-    const size_t slot_bytes = (size_t)nrows * cw * 4;
-    float* slots = reinterpret_cast<float*>(smem_cmb);
+    const size_t slot_bytes = (size_t)nrows * cw * es;
+    uint8_t* slots = smem_cmb;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem_cmb + nslots * slot_bytes);
     uint64_t* empty = full + kCombineMaxSlots;
     uint64_t* masks = empty + kCombineMaxSlots;  // valid rows of each slot's unit
     volatile int* abort_flag = reinterpret_cast<volatile int*>(masks + kCombineMaxSlots);
     int* zero = const_cast<int*>(reinterpret_cast<volatile int*>(abort_flag + 1));
+    // [slot][row]: the fp16 rows' scales, after the two flag words (16 bytes)
+    float* rsc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(masks + kCombineMaxSlots) + 16);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < nslots; ++i) {
@@ -421,11 +458,14 @@ __global__ void __launch_bounds__(kCombineTmaThreads, 1) combine_tma_kernel(
             int i = 0;
             // a unit's rows are read one unit ahead, so their latency hides behind the wait
             int64_t row[kMaxTopK + 1];
+            float scl[kMaxTopK + 1];
             auto rows_of = [&](int64_t uu) {
                 const int tt = (int)(uu / nchunk);
-                for (int j = 0; j < nrows; ++j)
+                for (int j = 0; j < nrows; ++j) {
                     row[j] = j < k ? (int64_t)inv[(size_t)tt * k + j]
                                    : (int64_t)offsets[shared_group] + tt;
+                    if (f16 && row[j] >= 0) scl[j] = y_scale[row[j]];
+                }
             };
             if (blockIdx.x < nunits) rows_of(blockIdx.x);
             for (int64_t u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++i) {
@@ -441,15 +481,17 @@ __global__ void __launch_bounds__(kCombineTmaThreads, 1) combine_tma_kernel(
                 for (int j = 0; j < nrows; ++j)
                     if (row[j] >= 0) {
                         mask |= 1ull << j;
-                        nbytes += (uint32_t)cw * 4u;
+                        nbytes += (uint32_t)cw * es;
+                        if (f16) rsc[sl * (kMaxTopK + 1) + j] = scl[j];
                     }
                 masks[sl] = mask;
                 mbar_arrive_expect_tx(&full[sl], nbytes);
-                float* dst = slots + (size_t)sl * nrows * cw;
+                uint8_t* dst = slots + (size_t)sl * slot_bytes;
                 for (int j = 0; j < nrows; ++j)
                     if (row[j] >= 0)
-                        bulk_load(dst + (size_t)j * cw, y + row[j] * H + c0, (uint32_t)cw * 4u,
-                                  &full[sl], pol);
+                        bulk_load(dst + (size_t)j * cw * es,
+                                  static_cast<const uint8_t*>(y) + ((size_t)row[j] * H + c0) * es,
+                                  (uint32_t)cw * es, &full[sl], pol);
                 issued |= 1u << sl;
                 issued_par = (issued_par & ~(1u << sl)) | (ph << sl);
                 if (u + gridDim.x < nunits) rows_of(u + gridDim.x);
@@ -462,7 +504,8 @@ __global__ void __launch_bounds__(kCombineTmaThreads, 1) combine_tma_kernel(
                 if ((issued >> sl) & 1u) mbar_wait(&full[sl], (issued_par >> sl) & 1u, zero);
         }
     } else {
-        const int tid = threadIdx.x - 32;  // 0..127: four columns per 512-column segment
+        // four columns per thread and segment of 4 x (consumer threads) columns
+        const int tid = threadIdx.x - 32, seg = 4 * (kCombineTmaThreads - 32);
         int i = 0;
         for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x, ++i) {
             const int sl = i % nslots;
@@ -476,12 +519,23 @@ __global__ void __launch_bounds__(kCombineTmaThreads, 1) combine_tma_kernel(
             }
             const uint64_t mask = masks[sl];
             const int t = (int)(u / nchunk), c0 = (int)(u % nchunk) * cw;
-            const float* src = slots + (size_t)sl * nrows * cw;
-            for (int col = 4 * tid; col < cw; col += 512) {
+            const uint8_t* src = slots + (size_t)sl * slot_bytes;
+            const float* sc = rsc + sl * (kMaxTopK + 1);
+            for (int col = 4 * tid; col < cw; col += seg) {
                 float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
                 for (int j = 0; j < nrows; ++j)
                     if ((mask >> j) & 1ull) {
-                        const float4 v = *reinterpret_cast<const float4*>(src + (size_t)j * cw + col);
+                        float4 v;
+                        if (f16) {
+                            const uint2 hq = *reinterpret_cast<const uint2*>(
+                                src + ((size_t)j * cw + col) * 2);
+                            const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&hq.x));
+                            const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&hq.y));
+                            const float s = sc[j];
+                            v = make_float4(lo.x * s, lo.y * s, hi.x * s, hi.y * s);
+                        } else {
+                            v = *reinterpret_cast<const float4*>(src + ((size_t)j * cw + col) * 4);
+                        }
                         a0 += v.x;
                         a1 += v.y;
                         a2 += v.z;
