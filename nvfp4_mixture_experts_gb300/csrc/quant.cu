@@ -449,53 +449,67 @@ __global__ void __launch_bounds__(kCombineTmaThreads, 1) combine_tma_kernel(
     const int nchunk = H / cw;
     const int64_t nunits = (int64_t)T * nchunk;
     if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            pdl_wait();  // y is the predecessor's output
-            pdl_trigger();
-            uint32_t issued = 0, issued_par = 0;
-            bool ok = true;
-            int i = 0;
-            // a unit's rows are read one unit ahead, so their latency hides behind the wait
-            int64_t row[kMaxTopK + 1];
-            float scl[kMaxTopK + 1];
-            auto rows_of = [&](int64_t uu) {
-                const int tt = (int)(uu / nchunk);
-                for (int j = 0; j < nrows; ++j) {
-                    row[j] = j < k ? (int64_t)inv[(size_t)tt * k + j]
-                                   : (int64_t)offsets[shared_group] + tt;
-                    if (f16 && row[j] >= 0) scl[j] = y_scale[row[j]];
-                }
-            };
-            if (blockIdx.x < nunits) rows_of(blockIdx.x);
-            for (int64_t u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++i) {
-                const int sl = i % nslots;
-                const uint32_t ph = (uint32_t)(i / nslots) & 1u;
-                if (!mbar_wait(&empty[sl], ph ^ 1u, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const int c0 = (int)(u % nchunk) * cw;
-                uint64_t mask = 0;
-                uint32_t nbytes = 0;
-                for (int j = 0; j < nrows; ++j)
-                    if (row[j] >= 0) {
-                        mask |= 1ull << j;
-                        nbytes += (uint32_t)cw * es;
-                        if (f16) rsc[sl * (kMaxTopK + 1) + j] = scl[j];
-                    }
-                masks[sl] = mask;
-                mbar_arrive_expect_tx(&full[sl], nbytes);
-                uint8_t* dst = slots + (size_t)sl * slot_bytes;
-                for (int j = 0; j < nrows; ++j)
-                    if (row[j] >= 0)
-                        bulk_load(dst + (size_t)j * cw * es,
-                                  static_cast<const uint8_t*>(y) + ((size_t)row[j] * H + c0) * es,
-                                  (uint32_t)cw * es, &full[sl], pol);
-                issued |= 1u << sl;
-                issued_par = (issued_par & ~(1u << sl)) | (ph << sl);
-                if (u + gridDim.x < nunits) rows_of(u + gridDim.x);
+        // the copy warp: lane j looks up rows j and j + 32 of a unit (its index, then its
+        // fp16 scale), so a unit's lookups take two load latencies; lane 0 issues the copies
+        const uint64_t pol = policy_evict_first();
+        pdl_wait();  // y and its scales are the predecessor's output
+        pdl_trigger();
+        uint32_t issued = 0, issued_par = 0;
+        bool ok = true;
+        int i = 0;
+        int64_t row[2] = {-1, -1};  // rows lane and lane + 32 of the next unit (-1: none)
+        float scl[2] = {1.0f, 1.0f};
+        auto rows_of = [&](int64_t uu) {
+            const int tt = (int)(uu / nchunk);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = lane + 32 * h;
+                row[h] = j >= nrows ? -1
+                         : j < k    ? (int64_t)inv[(size_t)tt * k + j]
+                                    : (int64_t)offsets[shared_group] + tt;
             }
+            if (f16)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    if (row[h] >= 0) scl[h] = y_scale[row[h]];
+        };
+        if (blockIdx.x < nunits) rows_of(blockIdx.x);
+        for (int64_t u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++i) {
+            const int sl = i % nslots;
+            const uint32_t ph = (uint32_t)(i / nslots) & 1u;
+            int okw = 1;
+            if (lane == 0) okw = mbar_wait(&empty[sl], ph ^ 1u, abort_flag) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, okw, 0)) {
+                ok = false;
+                break;
+            }
+            const int c0 = (int)(u % nchunk) * cw;
+            // the unit's valid rows (a ballot per half) and their bytes; scales to the slot
+            const uint64_t mask = (uint64_t)__ballot_sync(0xffffffffu, row[0] >= 0) |
+                                  ((uint64_t)__ballot_sync(0xffffffffu, row[1] >= 0) << 32);
+            if (f16) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    if (row[h] >= 0) rsc[sl * (kMaxTopK + 1) + lane + 32 * h] = scl[h];
+            }
+            __syncwarp();
+            if (lane == 0) {
+                masks[sl] = mask;
+                mbar_arrive_expect_tx(&full[sl], (uint32_t)__popcll(mask) * (uint32_t)cw * es);
+            }
+            uint8_t* dst = slots + (size_t)sl * slot_bytes;
+            for (int j = 0; j < nrows; ++j) {
+                const int64_t r = __shfl_sync(0xffffffffu, row[j >> 5], j & 31);
+                if (lane == 0 && r >= 0)
+                    bulk_load(dst + (size_t)j * cw * es,
+                              static_cast<const uint8_t*>(y) + ((size_t)r * H + c0) * es,
+                              (uint32_t)cw * es, &full[sl], pol);
+            }
+            issued |= 1u << sl;
+            issued_par = (issued_par & ~(1u << sl)) | (ph << sl);
+            if (u + gridDim.x < nunits) rows_of(u + gridDim.x);
+        }
+        if (lane == 0) {
             if (!ok) {
                 set_status(status, MOE_DEV_WAIT_TIMEOUT);
                 *abort_flag = 1;
