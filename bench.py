@@ -234,10 +234,12 @@ def launches_per_forward(c):
     return n
 
 
-def gemm_bytes(c, counts, gateup):
+def gemm_bytes(c, counts, gateup, y_bytes=4):
     """Algorithmic bytes of one grouped-GEMM launch: the weights of every expert that has
     rows, the activation rows it reads and the rows it writes, each once (with the dynamic
-    intermediate scale gate_up also writes and re-reads the fp32 intermediate)."""
+    intermediate scale gate_up also writes and re-reads the fp32 intermediate).  y_bytes:
+    bytes per element of down's output rows (4: the staged call's fp32; 2: the W4A4
+    forward's fp16)."""
     H, I, El = c["H"], c["I"], c["E_loc"]
     touched = int((counts[:El] > 0).sum()) + int(counts[El] > 0)
     rows = int(counts.sum())
@@ -251,7 +253,7 @@ def gemm_bytes(c, counts, gateup):
     else:
         wbytes = touched * H * I * NVFP4_BYTES
         a_in = rows * I * (2 if w4a16 else NVFP4_BYTES)
-        a_out = rows * H * 4
+        a_out = rows * H * y_bytes
     return wbytes + a_in + a_out, touched, rows
 
 
@@ -510,7 +512,8 @@ def measure_prefill(layer, stream, steps):
     # the layer against the combined roofline t = max(bytes / HBM, flops / FP4 peak): the
     # two grouped GEMMs' FP4 flops and algorithmic bytes (touched weights + activation rows);
     # FP4 peak = the measured bf16 peak x the nominal FP4 / bf16 ratio (13.5 / 2.25)
-    by = gemm_bytes(c, counts, True)[0] + gemm_bytes(c, counts, False)[0]
+    # the forward's down writes fp16 y rows (W4A4)
+    by = gemm_bytes(c, counts, True)[0] + gemm_bytes(c, counts, False, y_bytes=2)[0]
     fp4_peak = pk["bf16"] * 6.0
     t = ms / 1e3
     t_roof = max(by / (pk["hbm"] * 1e9), fl / (fp4_peak * 1e12))
