@@ -286,13 +286,17 @@ MOE_API moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* 
 /* Where moe_forward keeps its intermediates inside the workspace (device pointers into
  * ws_d), so callers can inspect them after a forward.  Any pointer may be NULL.  Unlike
  * moe_permute's, the forward's perm_src leaves padding rows unmarked (stale).  inter_gs:
- * the dynamic intermediate scale of the last forward (set only in that mode). */
+ * the dynamic intermediate scale of the last forward (set only in that mode).  y: the
+ * weighted expert outputs by padded row -- fp32 in W4A16 mode; in the W4A4 modes fp16 rows
+ * of y x 2^e (e per local expert, chosen from a bound on |y| so that no value overflows)
+ * with y_scale[row] = 2^-e (float, per padded row), which the combine multiplies back. */
 MOE_API moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** topk_ids,
                                float** topk_w, int32_t** expert_counts,
                                int32_t** expert_offsets, int32_t** perm_src, int32_t** inv,
                                float** gs_a, uint8_t** a_codes, uint8_t** a_sf,
                                void** a_bf16, uint8_t** inter_codes, uint8_t** inter_sf,
-                               void** inter_bf16, float** y, float** inter_gs);
+                               void** inter_bf16, float** y, float** inter_gs,
+                               float** y_scale);
 
 /* Reads the device status word of ws (synchronises the stream) into *bits (nullable) and
  * clears it.  Returns MOE_OK, MOE_ERR_TIMEOUT (MOE_DEV_WAIT_TIMEOUT set) or

@@ -58,7 +58,7 @@ SIGNATURES = {
     "moe_grouped_gemm_down": (C.c_int, [_V, _V, _V, _V, _V, _V, _V, _V, _V, _I, _V, _SZ, _V]),
     "moe_combine": (C.c_int, [_V, _V, _V, _V, _I, _V, _V]),
     "moe_forward": (C.c_int, [_V, _V, _V, _V, _I, _V, _V, _SZ, _V]),
-    "moe_forward_buffers": (C.c_int, [_V, _V, _I] + [C.POINTER(_V)] * 15),
+    "moe_forward_buffers": (C.c_int, [_V, _V, _I] + [C.POINTER(_V)] * 16),
     "moe_get_status": (C.c_int, [_V, _V, _V, C.POINTER(C.c_uint32)]),
     "moe_status_string": (C.c_char_p, [C.c_int]),
     "moe_selftest_bounded_wait": (C.c_int, [_V, C.c_uint64, _V]),
@@ -209,7 +209,7 @@ def moe_forward(h, x, logits_in, logit_bias, T, out, ws, stream=None):
 
 FORWARD_BUFFERS = ("topk_ids", "topk_w", "expert_counts", "expert_offsets", "perm_src", "inv",
                    "gs_a", "a_codes", "a_sf", "a_bf16", "inter_codes", "inter_sf", "inter_bf16",
-                   "y", "inter_gs")
+                   "y", "inter_gs", "y_scale")
 
 
 def moe_forward_buffers(h, ws, T):

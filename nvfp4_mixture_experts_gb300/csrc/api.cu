@@ -988,7 +988,8 @@ moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** to
                                int32_t** expert_offsets, int32_t** perm_src, int32_t** inv,
                                float** gs_a, uint8_t** a_codes, uint8_t** a_sf,
                                void** a_bf16, uint8_t** inter_codes, uint8_t** inter_sf,
-                               void** inter_bf16, float** y, float** inter_gs)
+                               void** inter_bf16, float** y, float** inter_gs,
+                               float** y_scale)
 {
     if (!h || !ws_d || !t_ok(h, T)) return MOE_ERR_INVALID;
     const Plan p = plan(h->cfg, T);
@@ -1007,6 +1008,7 @@ moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** to
     if (inter_sf) *inter_sf = at<uint8_t>(ws_d, p.i_sf);
     if (y) *y = at<float>(ws_d, p.y);
     if (inter_gs) *inter_gs = at<float>(ws_d, p.gs_i);
+    if (y_scale) *y_scale = at<float>(ws_d, p.y_scale);
     return MOE_OK;
 }
 

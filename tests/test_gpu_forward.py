@@ -248,6 +248,40 @@ def test_w4a16_tiny_layer_short_k():
     _check(got, ora.out, "w4a16 tiny")
 
 
+@pytest.mark.parametrize("T", [64, 1100])
+def test_forward_combine_of_fp16_y_is_exact(big_layer, T):
+    """The W4A4 forward's combine (the load-based kernel below 1024 tokens, the bulk-copy one
+    from 1024) against a numpy replay from the forward's own fp16 y rows and row scales:
+    out[t] = bf16(sum over the token's rows, pairs in top-k order then the shared row, of
+    fp32(y16[row]) * y_scale[row], added in fp32 in that order), bit for bit; the scales
+    are powers of two."""
+    c = synth.CONFIGS["decode"]
+    H, I, E, k = c["H"], c["I"], c["E"], c["k"]
+    gs_i = INTER["decode"]["inter_global_scale"]
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(5, T, H)
+    h = make_layer(big_layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T)
+    out = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+    h.forward(bits16(x), out=out)
+    torch.cuda.synchronize()
+    assert moe.moe_get_status(h.handle, h.ws)[0] == moe.MOE_OK
+    b = moe.moe_forward_buffers(h.handle, h.ws, T)
+    offs = _read_ws(h, b["expert_offsets"], E + 2, np.int32)
+    rows_total = int(offs[-1])
+    inv = _read_ws(h, b["inv"], T * k, np.int32).reshape(T, k)
+    y16 = _read_ws(h, b["y"], rows_total * H, np.float16).reshape(rows_total, H)
+    ysc = _read_ws(h, b["y_scale"], rows_total, np.float32)
+    rows = np.concatenate([inv, (offs[E] + np.arange(T, dtype=np.int32))[:, None]], 1)
+    used = ysc[rows.ravel()]
+    assert np.all(used > 0) and np.all(np.frexp(used)[0] == 0.5)  # powers of two
+    acc = np.zeros((T, H), np.float32)
+    for j in range(k + 1):
+        r = rows[:, j]
+        acc = acc + y16[r].astype(np.float32) * ysc[r][:, None]
+    want = torch.from_numpy(acc).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(host(out), want)
+
+
 def test_prefill_chunk_sampled_parity(big_layer):
     c = synth.CONFIGS["prefill"]
     T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
