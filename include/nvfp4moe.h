@@ -278,7 +278,11 @@ MOE_API moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* in
 
 /* The whole layer: route, permute, gather-quantise, gate_up (fused SwiGLU+requant),
  * down, combine.  logits_in_d (nullable): given router logits [T][E] instead of x.Wr^T;
- * logit_bias_d (nullable) [E].  out_bf16_d [T][H] receives this shard's partial sum. */
+ * logit_bias_d (nullable) [E].  out_bf16_d [T][H] receives this shard's partial sum.
+ * Unlike the staged calls, the W4A4 modes keep the weighted expert rows between down and
+ * combine as fp16 values of y x 2^e (e per local expert, from a bound on |y| that rules out
+ * overflow; see moe_forward_buffers), each with 11 significant bits; the combine multiplies
+ * by 2^-e and sums in the same fixed order in fp32. */
 MOE_API moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_in_d,
                        const float* logit_bias_d, int32_t T, void* out_bf16_d, void* ws_d,
                        size_t ws_bytes, moe_stream_t stream);
