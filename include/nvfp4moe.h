@@ -10,6 +10,12 @@
  * a contiguous shard of experts selected by local_expert_offset, whose output is the
  * shard's partial sum (same page, "b12x에서의 Expert Parallelism 구현 추가").
  *
+ * Passages: every declaration below names the passage that defines its operation, as
+ *   [OV] "Serving Solar Open 2 (NVFP4) on DGX Spark", section "Solar Open 2 개요";
+ *   [EP] the same page, section "b12x에서의 Expert Parallelism 구현 추가";
+ *   [CK] the same page, section "b12x 버전이 실제 NVFP4 체크포인트를 읽어들이도록 만들기";
+ *   or "none" for this library's own plumbing, which the pages have no counterpart for.
+ *
  * Conventions for every call:
  *   - Pointers named *_d are device pointers; all tensors are caller-owned unless stated.
  *     moe_create copies the weights into its own re-laid-out buffers: the caller may free
@@ -127,16 +133,23 @@ typedef struct moe_layer* moe_handle;
 /* Validates cfg, allocates the handle and device copies of the weights re-laid out for
  * the grouped GEMMs (gate/up rows interleaved in blocks of 16 inside each 128-row tile,
  * scales in 512-byte atoms, one extra expert slot for the shared expert).  Synchronises
- * the stream before returning.  *out receives the handle (NULL on error). */
+ * the stream before returning.  *out receives the handle (NULL on error).
+ * Passage: [OV] (320 routed + 1 shared experts) and [CK] (packed FP4
+ * weights, FP8 block scales, a per-expert global scale, fused gate/up rows, MMA tile layout). */
 MOE_API moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t stream,
                       moe_handle* out);
+/* Passage: none; releases what moe_create allocated (the pages have no counterpart). */
 MOE_API void moe_destroy(moe_handle h);
 
 /* Bytes of workspace a call with T tokens needs (moe_forward and the staged calls).
- * One workspace may be shared by every layer of a model (calls on one stream). */
+ * One workspace may be shared by every layer of a model (calls on one stream).
+ * Passage: [EP] (one module-level workspace pool
+ * shared by the layers instead of per-layer scratch). */
 MOE_API size_t moe_workspace_size(const moe_config* cfg, int32_t T);
 
-/* Padded-row capacity for T tokens: every buffer indexed by padded row is sized to it. */
+/* Padded-row capacity for T tokens: every buffer indexed by padded row is sized to it.
+ * Passage: [EP] (the compact pre-pass that groups the
+ * local pairs by expert); the 128-row padding is this library's GEMM tile. */
 MOE_API int32_t moe_rows_capacity(const moe_config* cfg, int32_t T);
 
 /* Router (steps: logits, softmax + top-k).  logits = x . Wr^T (+ logit_bias) in fp32, or
@@ -144,25 +157,34 @@ MOE_API int32_t moe_rows_capacity(const moe_config* cfg, int32_t T);
  * descending, ties to the lower id (-0 equals +0; a NaN ranks below every number);
  * topk_w_d[T][k]: softmax over the selected logits.
  * logits_out_d (nullable): fp32 [T][E] including the bias.  x_bf16_d may be NULL when
- * logits_in_d is set.  ws: scratch for the logits when they are computed from x. */
+ * logits_in_d is set.  ws: scratch for the logits when they are computed from x.
+ * Passage: [OV] (top-8 of 320 routed experts; the softmax over the
+ * selected logits and the tie rule are readings where the page is silent). */
 MOE_API moe_status moe_route_topk(moe_handle h, const void* x_bf16_d, const float* logits_in_d,
                           const float* logit_bias_d, int32_t T, int32_t* topk_ids_d,
                           float* topk_w_d, float* logits_out_d, void* ws_d, size_t ws_bytes,
                           moe_stream_t stream);
 
-/* Routing that allocates nothing: the same result as moe_route_topk, for callers that
- * cannot allocate device memory at call time and have no workspace to lend -- for example
- * code running while another component owns every byte of device memory through its own
- * pool, or a caller in a phase where a cudaMalloc (which may synchronise the device) is not
+/* Routing that allocates nothing: moe_route_topk's computation, for callers that cannot
+ * allocate device memory at call time and have no workspace to lend -- for example code
+ * running while another component owns every byte of device memory through its own pool,
+ * or a caller in a phase where a cudaMalloc (which may synchronise the device) is not
  * allowed.  The pages have no counterpart; it is an addition of this library.
- * The router's partial-sum planes live in one file-scope 8 MiB device array that every
- * device loading the library keeps until exit; T * E (tokens x global experts) must not
- * exceed 2,097,152, else MOE_ERR_WORKSPACE (with E = 320: T <= 6553).  The first call on a
- * device looks the array's address up (cudaGetSymbolAddress, with the handle's device
- * current) and should come before any stream capture.  All calls share the array: calls
- * whose executions overlap on the GPU race (use one stream, or serialise them).  Nothing in
- * the array needs to start at zero: each call writes every value it reads.  Given
- * logits_in_d, no scratch is touched at all. */
+ * Result: the ids are the top-k of the returned logits exactly as moe_route_topk selects
+ * them, and the logits and weights agree with moe_route_topk's to fp32 rounding (for
+ * T * E * splits beyond the scratch this call sums fewer router k-splits, in another fp32
+ * order, so near-ties may select differently).
+ * The router's partial-sum planes and a status word live in one file-scope 8 MiB device
+ * array that every device loading the library keeps until exit; T * E (tokens x global
+ * experts) must not exceed 2,097,088, else MOE_ERR_WORKSPACE (with E = 320: T <= 6553).
+ * The first call on a device (and again after the device's context changes, e.g. after a
+ * cudaDeviceReset) looks the array's address up (cudaGetSymbolAddress, with the handle's
+ * device current) and should come before any stream capture.  All calls share the array:
+ * calls whose executions overlap on the GPU race (use one stream, or serialise them).  Each
+ * call clears the status word and writes every plane value it reads.  If a bounded wait of
+ * the router runs out, every id is written as -1 and every weight as 0 (moe_permute drops
+ * such pairs and flags MOE_DEV_BAD_EXPERT_ID).  Given logits_in_d, no scratch is touched.
+ * Passage: none -- the pages have no counterpart (see above). */
 MOE_API moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
                                           const float* logits_in_d, const float* logit_bias_d,
                                           int32_t T, int32_t* topk_ids_d, float* topk_w_d,
@@ -177,7 +199,9 @@ MOE_API moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
  *   perm_src_d[rows_capacity] pair index of each padded row (T*k + t for shared rows,
  *                             -1 for padding)
  *   inv_d[T*k]                padded row of each pair, -1 if dropped
- * ws: the workspace (its tile table is filled here and read by the grouped GEMMs). */
+ * ws: the workspace (its tile table is filled here and read by the grouped GEMMs).
+ * Passage: [EP] (local_expert_offset maps global ids to the
+ * shard; pairs outside it are filtered by a CTA-uniform guard; the compact pre-pass). */
 MOE_API moe_status moe_permute(moe_handle h, const int32_t* topk_ids_d, int32_t T,
                        int32_t* expert_counts_d, int32_t* expert_offsets_d,
                        int32_t* perm_src_d, int32_t* inv_d, void* ws_d, size_t ws_bytes,
@@ -186,7 +210,9 @@ MOE_API moe_status moe_permute(moe_handle h, const int32_t* topk_ids_d, int32_t 
 /* NVFP4 quantiser of a bf16 matrix [rows][cols] (cols % 64 == 0).  gs_in_d NULL: dynamic
  * global scale 2688/amax over the whole matrix (written to gs_out_d); else the scale
  * *gs_in_d.  sf_layout 0: canonical codes [rows][cols/2], scales [rows][cols/16];
- * sf_layout 1: tiled (pitch-padded codes, 512-byte scale atoms).  ws: scratch for amax. */
+ * sf_layout 1: tiled (pitch-padded codes, 512-byte scale atoms).  ws: scratch for amax.
+ * Passage: [CK] (packed FP4 codes, FP8 E4M3 block scales
+ * clamped at 448, an FP32 global scale in reciprocal form). */
 MOE_API moe_status moe_quant_nvfp4(const void* x_bf16_d, int32_t rows, int32_t cols,
                            const float* gs_in_d, float* gs_out_d, uint8_t* codes_d,
                            uint8_t* sf_d, int32_t sf_layout, void* ws_d, size_t ws_bytes,
@@ -197,7 +223,9 @@ MOE_API moe_status moe_quant_nvfp4(const void* x_bf16_d, int32_t rows, int32_t c
  * shared row, in the tiled layout (W4A4).  W4A16: write fp16(x * gs) instead
  * (a_bf16_d [rows_capacity][H] fp16), gs = 2^(141 - e) for e the exponent field of
  * amax|x| (clamped to 2^[-126, 127]), so |x * gs| <= 2^15 and every x above amax * 2^-29
- * converts exactly.  gs_out_d receives the scale used (both modes). */
+ * converts exactly.  gs_out_d receives the scale used (both modes).
+ * Passage: [EP] (tokens reach the local experts of the
+ * shard) and [CK] (the NVFP4 format of the operands). */
 MOE_API moe_status moe_gather_activations(moe_handle h, const void* x_bf16_d, int32_t T,
                                   const int32_t* inv_d, const int32_t* expert_offsets_d,
                                   uint8_t* a_codes_d, uint8_t* a_sf_d, void* a_bf16_d,
@@ -214,7 +242,9 @@ MOE_API moe_status moe_gather_activations(moe_handle h, const void* x_bf16_d, in
  *              using the workspace for the fp32 intermediate, and leaves gs_i there for
  *              moe_grouped_gemm_down on the same workspace
  *       W4A16: bf16 -> inter_bf16_d [rows_capacity][I]
- * Padding rows of the outputs are left unwritten. */
+ * Padding rows of the outputs are left unwritten.
+ * Passage: [CK] (the fused gate/up projection, its row
+ * order, per-expert global scales) and [EP] (per-expert scales of the local experts). */
 MOE_API moe_status moe_grouped_gemm_gateup(moe_handle h, const uint8_t* a_codes_d,
                                    const uint8_t* a_sf_d, const float* gs_a_d,
                                    const void* a_bf16_d, const int32_t* expert_counts_d,
@@ -223,12 +253,11 @@ MOE_API moe_status moe_grouped_gemm_gateup(moe_handle h, const uint8_t* a_codes_
                                    uint8_t* inter_sf_d, void* inter_bf16_d, int32_t T,
                                    void* ws_d, size_t ws_bytes, moe_stream_t stream);
 
-/* Checkpoint-convention weight preparation ("Serving Solar Open 2 (NVFP4) on DGX Spark",
- * section on reading real NVFP4 checkpoints: packed FP4 weights, FP8 block scales and a
- * per-expert global scale in either convention; the reciprocal global scale inverted and
- * folded into the FP8 block scales with re-rounding, clamped at 448; the fused gate/up row
- * order; per-shard scale slicing).  One weight matrix type of num_experts experts, each
- * N x K NVFP4 in the canonical layout -- codes_d [E][N][K/2] (element 2i in the low
+/* Checkpoint-convention weight preparation.  Passage: [CK] (packed FP4 weights, FP8 block
+ * scales and a per-expert global scale in either convention; the reciprocal global scale
+ * inverted and folded into the FP8 block scales with re-rounding, clamped at 448; the fused
+ * gate/up row order; per-shard scale slicing).  One weight matrix type of num_experts
+ * experts, each N x K NVFP4 in the canonical layout -- codes_d [E][N][K/2] (element 2i in the low
  * nibble), sf_d [E][N][K/16] E4M3, glob_d [E] fp32 -- becomes the moe_weights form of
  * experts off .. off+count-1:
  *   codes_out_d [count][N][K/2]: the codes (rows reordered by swap_halves);
@@ -251,7 +280,9 @@ MOE_API moe_status moe_prepare_weights(const uint8_t* codes_d, const uint8_t* sf
 
 /* SwiGLU + NVFP4 requantisation of fp32 gate/up rows [rows][2I] (gate cols 0..I-1):
  * s = silu(g) * u in fp32, quantised with the static scale gs_i.  sf_layout as for
- * moe_quant_nvfp4 (0 canonical, 1 tiled). */
+ * moe_quant_nvfp4 (0 canonical, 1 tiled).
+ * Passage: [CK] (the fused gate/up projection whose halves
+ * feed silu(gate) * up) and [EP] (the static / dynamic W4A4 backends requantise it). */
 MOE_API moe_status moe_swiglu_requant(const float* gateup_f32_d, int32_t rows, int32_t inter,
                               float gs_i, uint8_t* codes_d, uint8_t* sf_d, int32_t sf_layout,
                               moe_stream_t stream);
@@ -260,7 +291,9 @@ MOE_API moe_status moe_swiglu_requant(const float* gateup_f32_d, int32_t rows, i
  * intermediate scale: gs_i is the one moe_grouped_gemm_gateup left in ws_d), each row
  * multiplied by its routing weight (1 for shared rows; the weight of padded row r is
  * topk_w[perm_src[r]]), written to y_d[rows_capacity][H] fp32 at the same padded row.
- * Padding rows of y may receive arbitrary values. */
+ * Padding rows of y may receive arbitrary values.
+ * Passage: [EP] (each local expert's output, weighted by its
+ * routing weight, enters the shard's partial sum). */
 MOE_API moe_status moe_grouped_gemm_down(moe_handle h, const uint8_t* inter_codes_d,
                                  const uint8_t* inter_sf_d, const void* inter_bf16_d,
                                  const int32_t* expert_counts_d,
@@ -271,7 +304,9 @@ MOE_API moe_status moe_grouped_gemm_down(moe_handle h, const uint8_t* inter_code
 /* Combine: out[t] = sum_{j: inv[t*k+j] >= 0} y[inv[t*k+j]]
  *                  + (add_shared ? y[expert_offsets[E_loc] + t] : 0),
  * y indexed by padded row (moe_grouped_gemm_down), summed in ascending j then the shared
- * term in fp32, rounded to bf16. */
+ * term in fp32, rounded to bf16.
+ * Passage: [EP] (the shard's output is the partial sum over its
+ * local experts [T, H], which an all-reduce adds across shards). */
 MOE_API moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* inv_d,
                        const int32_t* expert_offsets_d, int32_t T, void* out_bf16_d,
                        moe_stream_t stream);
@@ -282,7 +317,10 @@ MOE_API moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* in
  * Unlike the staged calls, the W4A4 modes keep the weighted expert rows between down and
  * combine as fp16 values of y x 2^e (e per local expert, from a bound on |y| that rules out
  * overflow; see moe_forward_buffers), each with 11 significant bits; the combine multiplies
- * by 2^-e and sums in the same fixed order in fp32. */
+ * by 2^-e and sums in the same fixed order in fp32.
+ * Passage: [OV] (the layer: 320 routed + 1 shared experts, top-8)
+ * and [EP] (local_expert_offset, the partial-sum output; the static W4A4, dynamic W4A4
+ * and W4A16 fused-MoE backends). */
 MOE_API moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_in_d,
                        const float* logit_bias_d, int32_t T, void* out_bf16_d, void* ws_d,
                        size_t ws_bytes, moe_stream_t stream);
@@ -293,7 +331,8 @@ MOE_API moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* 
  * the dynamic intermediate scale of the last forward (set only in that mode).  y: the
  * weighted expert outputs by padded row -- fp32 in W4A16 mode; in the W4A4 modes fp16 rows
  * of y x 2^e (e per local expert, chosen from a bound on |y| so that no value overflows)
- * with y_scale[row] = 2^-e (float, per padded row), which the combine multiplies back. */
+ * with y_scale[row] = 2^-e (float, per padded row), which the combine multiplies back.
+ * Passage: none; inspection of moe_forward's intermediates (the pages have no counterpart). */
 MOE_API moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** topk_ids,
                                float** topk_w, int32_t** expert_counts,
                                int32_t** expert_offsets, int32_t** perm_src, int32_t** inv,
@@ -304,7 +343,8 @@ MOE_API moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int3
 
 /* Reads the device status word of ws (synchronises the stream) into *bits (nullable) and
  * clears it.  Returns MOE_OK, MOE_ERR_TIMEOUT (MOE_DEV_WAIT_TIMEOUT set) or
- * MOE_ERR_DEVICE_STATUS (other bits set). */
+ * MOE_ERR_DEVICE_STATUS (other bits set).
+ * Passage: none; the device status word of this library (the pages have no counterpart). */
 MOE_API moe_status moe_get_status(moe_handle h, void* ws_d, moe_stream_t stream, uint32_t* bits);
 
 /* Self-test of the failure path of the pipelines' bounded waits: one thread waits, with the
@@ -312,10 +352,13 @@ MOE_API moe_status moe_get_status(moe_handle h, void* ws_d, moe_stream_t stream,
  * wait runs out after limit_ns (1 ns .. 2 s) and sets MOE_DEV_WAIT_TIMEOUT in *status_d (a
  * caller-owned device word, cleared first), as a pipeline role would; no trap, the context
  * stays usable.  Synchronises the stream.  Returns MOE_ERR_TIMEOUT (the expected outcome),
- * MOE_OK (the wait completed: a broken wait), MOE_ERR_INVALID or MOE_ERR_CUDA. */
+ * MOE_OK (the wait completed: a broken wait), MOE_ERR_INVALID or MOE_ERR_CUDA.
+ * Passage: none; a self-test of this library's bounded waits (the pages have no
+ * counterpart). */
 MOE_API moe_status moe_selftest_bounded_wait(uint32_t* status_d, uint64_t limit_ns,
                                              moe_stream_t stream);
 
+/* Passage: none; error text of this library (the pages have no counterpart). */
 MOE_API const char* moe_status_string(moe_status s);
 
 #ifdef __cplusplus

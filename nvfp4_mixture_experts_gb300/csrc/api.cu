@@ -569,11 +569,15 @@ moe_status launch_combine(const moe_layer* h, const void* y, const int32_t* inv,
 // ================================================================ routing without allocation
 //
 // Scratch for moe_route_topk_noalloc: the router's partial-sum logit planes live in this
-// file-scope device array instead of a caller workspace.  Every device that loads the
-// library holds it (8 MiB) until the process exits.  Host code may not pass the symbol
-// itself to a kernel (on the host it only names a stand-in); the device address is looked
-// up once per device with cudaGetSymbolAddress, with that device current.
+// file-scope device array instead of a caller workspace, and its last 256 bytes hold the
+// call's status word (set by the router when a bounded wait runs out).  Every device that
+// loads the library holds it (8 MiB) until the process exits.  Host code may not pass the
+// symbol itself to a kernel (on the host it only names a stand-in); the device address is
+// looked up with cudaGetSymbolAddress, with that device current, once per device and
+// context.
 constexpr size_t kRouteScratchBytes = size_t(8) << 20;
+constexpr size_t kRouteStatusBytes = 256;
+constexpr size_t kRoutePlaneFloats = (kRouteScratchBytes - kRouteStatusBytes) / sizeof(float);
 static __device__ __align__(256) float g_route_scratch[kRouteScratchBytes / sizeof(float)];
 
 namespace {
@@ -581,26 +585,67 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_route_scratch_mu;
 float* g_route_scratch_ptr[kMaxDevices] = {};
+void* g_route_scratch_ctx[kMaxDevices] = {};
 
-// Device address of g_route_scratch on the current device (looked up on first use).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The current driver context (nullptr if it cannot be read): the cached symbol address is
+// valid only for the context it was looked up in (a cudaDeviceReset makes a new one).
+void* current_context()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+// Device address of g_route_scratch on the current device and context (looked up on the
+// first use in each).
 moe_status route_scratch_address(float** out)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    void* ctx = current_context();
     std::lock_guard<std::mutex> lock(g_route_scratch_mu);
-    if (!g_route_scratch_ptr[dev]) {
+    if (!g_route_scratch_ptr[dev] || !ctx || ctx != g_route_scratch_ctx[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) {
             cudaGetLastError();
+            g_route_scratch_ptr[dev] = nullptr;
             return MOE_ERR_CUDA;
         }
         g_route_scratch_ptr[dev] = static_cast<float*>(p);
+        g_route_scratch_ctx[dev] = ctx;
     }
     *out = g_route_scratch_ptr[dev];
     return MOE_OK;
 }
 
 }  // namespace
+
+namespace moe {
+
+// After the top-k: if the router flagged a wait that ran out, its planes are incomplete,
+// so every id becomes -1 (a pair every later step drops) and every weight 0.
+__global__ void route_invalidate_kernel(const uint32_t* status, int n, int32_t* ids, float* w)
+{
+    if (*status == 0u) return;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        ids[i] = -1;
+        w[i] = 0.0f;
+    }
+}
+
+}  // namespace moe
 
 // ================================================================ C ABI
 
@@ -1023,38 +1068,47 @@ moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
     const moe_config& c = h->cfg;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const float* src = logits_in_d;
+    uint32_t* status = nullptr;
     int nsplit = 1;
     if (!logits_in_d) {
         if (reinterpret_cast<uintptr_t>(x_bf16_d) & 15) return MOE_ERR_INVALID;
         const size_t plane = (size_t)T * c.num_experts;          // floats per partial plane
-        const size_t capacity = kRouteScratchBytes / sizeof(float);
-        if (plane > capacity) return MOE_ERR_WORKSPACE;            // T * E beyond the scratch
+        if (plane > kRoutePlaneFloats) return MOE_ERR_WORKSPACE;  // T * E beyond the scratch
         int dev = -1;
         if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
         if (dev != h->device) return MOE_ERR_INVALID;
         float* scratch = nullptr;
         const moe_status st = route_scratch_address(&scratch);
         if (st != MOE_OK) return st;
+        status = reinterpret_cast<uint32_t*>(scratch + kRoutePlaneFloats);
         nsplit = router_splits(T, c.num_experts, c.hidden, h->num_sms);
-        while (nsplit > 1 && plane * nsplit > capacity) nsplit /= 2;
+        while (nsplit > 1 && plane * nsplit > kRoutePlaneFloats) nsplit /= 2;
         CUtensorMap tmX;
         if (!make_tmap(&tmX, x_bf16_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.hidden, T,
                        (uint64_t)c.hidden * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
             return MOE_ERR_CUDA;
+        if (cudaMemsetAsync(status, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
         const int bn = router_bn(T, c.num_experts);
         dim3 grid(ceil_div(T, 128), ceil_div(c.num_experts, bn), nsplit);
         const moe_status r = launch(router_gemm_kernel, grid, dim3(192), kRouterSmem, s, false,
                                     tmX, bn == 160 ? h->tm_router160 : h->tm_router, (int)T,
                                     c.num_experts, c.hidden, c.hidden / nsplit, bn, scratch,
-                                    (uint32_t*)nullptr, (uint32_t*)nullptr, (uint32_t*)nullptr);
+                                    status, (uint32_t*)nullptr, (uint32_t*)nullptr);
         if (r != MOE_OK) return r;
         src = scratch;
     }
-    return launch(topk_kernel_for(c.num_experts), dim3(ceil_div(T, topk_tokens_per_block(nsplit))),
-                  dim3(kTopkThreads), topk_smem(nsplit, c.num_experts), s, false, src, nsplit,
-                  logit_bias_d, (int)T, c.num_experts, c.top_k, topk_ids_d, topk_w_d,
-                  logits_out_d, (uint32_t*)nullptr, (uint32_t*)nullptr,
-                  (const uint16_t*)nullptr, 0, (uint32_t*)nullptr);
+    moe_status r = launch(topk_kernel_for(c.num_experts),
+                          dim3(ceil_div(T, topk_tokens_per_block(nsplit))), dim3(kTopkThreads),
+                          topk_smem(nsplit, c.num_experts), s, false, src, nsplit, logit_bias_d,
+                          (int)T, c.num_experts, c.top_k, topk_ids_d, topk_w_d, logits_out_d,
+                          (uint32_t*)nullptr, (uint32_t*)nullptr, (const uint16_t*)nullptr, 0,
+                          (uint32_t*)nullptr);
+    if (r == MOE_OK && status) {
+        const int n = T * c.top_k;
+        r = launch(route_invalidate_kernel, dim3(std::min(grid_for(n, 256), 4 * h->num_sms)),
+                   dim3(256), 0, s, false, (const uint32_t*)status, n, topk_ids_d, topk_w_d);
+    }
+    return r;
 }
 
 namespace moe {

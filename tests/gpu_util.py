@@ -110,3 +110,35 @@ def quant_decisions_near_boundary(s, gs, sf_a, sf_b, codes_a, codes_b, rel=2e-6)
     elem_ok = same | near_c
     ok &= diff_sf | elem_ok.all(-1)
     return ok
+
+
+def bf16_rn_from_f64(v):
+    """fp64 array -> bf16 bit patterns, one rounding to nearest even (no fp32 step).  The
+    truncation of fp32(v) is the bf16 value at or below |v| (every bf16 value is an fp32
+    value, so the fp32 rounding never crosses one); of it and the next bf16 value up the
+    nearer wins, a tie going to the even pattern."""
+    v = np.asarray(v, np.float64)
+    lo = (np.abs(v).astype(np.float32).view(np.uint32) >> 16).astype(np.uint32)
+    hi = lo + 1
+    f = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    a = np.abs(v)
+    dl, dh = a - f(lo), f(hi) - a
+    pick = np.where(dl < dh, lo, np.where(dh < dl, hi, np.where(lo & 1, hi, lo)))
+    sign = np.signbit(v).astype(np.uint32) << 15
+    return (pick | sign).astype(np.uint16)
+
+
+def bf16_adjacent_near_midpoint(got, ref64, rel):
+    """Mask of elements where the bf16 patterns got and bf16_rn(ref64) agree, or are adjacent
+    values with ref64 within rel of the midpoint between them (an fp32-accumulated value can
+    round to either side there)."""
+    want = bf16_rn_from_f64(ref64)
+    same = got == want
+    g = np.asarray(got, np.uint16).astype(np.int64)
+    w = want.astype(np.int64)
+    adjacent = (np.abs(g - w) == 1) & ((g >> 15) == (w >> 15))
+    gv = (g.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    wv = (w.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    mid = (gv + wv) / 2
+    near = np.abs(ref64 - mid) <= rel * np.maximum(np.abs(ref64), 1e-300)
+    return same | (adjacent & near)

@@ -97,3 +97,23 @@ def test_null_arguments(lib):
         moe.MOE_ERR_UNSUPPORTED
     assert lib.moe_swiglu_requant(dummy, 1, 128, C.c_float(0.0), dummy, dummy, 0, None) == \
         moe.MOE_ERR_INVALID
+
+
+def test_every_declaration_cites_its_passage():
+    """Each MOE_API declaration is preceded by a comment that names the passage of the pages
+    defining the operation ([OV], [EP], [CK]) or says it has none (library plumbing)."""
+    lines = open(HEADER).read().split("\n")
+    for i, ln in enumerate(lines):
+        m = re.match(r"MOE_API [^(]*\b(moe_[a-z_0-9]+)\s*\(", ln)
+        if not m:
+            continue
+        j = i - 1
+        assert lines[j].rstrip().endswith("*/"), m.group(1)
+        block = []
+        while True:
+            block.insert(0, lines[j])
+            if lines[j].lstrip().startswith("/*"):
+                break
+            j -= 1
+        text = " ".join(block)
+        assert re.search(r"Passage: (\[(OV|EP|CK)\]|none)", text), m.group(1)

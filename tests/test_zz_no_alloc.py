@@ -1,7 +1,9 @@
 """moe_route_topk_noalloc: routing for callers that cannot allocate device memory during a
 call and have no workspace to lend (its scratch is a static device array of the library).
 Checked through the C ABI against moe_route_topk (which uses a caller workspace), on two
-calls in a row, and its size limit is checked to fail cleanly.
+calls in a row; at sizes where it sums fewer router k-splits than moe_route_topk (T = 4096,
+and T = 6553, the largest that fits at E = 320), its ids against the oracle's top-k of the
+logits it returns; and its size limit is checked to fail cleanly.
 
 This file is collected last on purpose, and builds everything it needs itself, so it runs
 the same alone in a fresh process or after the other tests."""
@@ -50,6 +52,34 @@ def test_noalloc_routing_matches_workspace_routing(T):
         assert np.max(np.abs(host(w2) - host(w))) <= 1e-6
 
 
+@pytest.mark.parametrize("T", [4096, 6553])
+def test_noalloc_routing_at_large_batches_selects_the_topk_of_its_logits(T):
+    """Beyond 1638 tokens (E = 320) the scratch holds fewer partial planes than the
+    workspace call uses, so the logits are summed in another fp32 order: they agree with
+    moe_route_topk's to fp32 rounding, and the ids are exactly the top-k of the logits this
+    call returns (6553 x 320 fills the scratch up to its status word)."""
+    E, H, k = 320, 4096, 8
+    h = _routing_handle(E=E, H=H, k=k)
+    x = bits16(synth.activations(11, T, H))
+    ws = torch.zeros(h.workspace_bytes(T), dtype=torch.uint8, device="cuda")
+    lo = torch.zeros((T, E), dtype=torch.float32, device="cuda")
+    ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(h.handle, x, None, None, T, ids, w, lo, ws)
+    for _ in range(2):
+        ids2 = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+        w2 = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+        lo2 = torch.zeros((T, E), dtype=torch.float32, device="cuda")
+        moe.moe_route_topk_noalloc(h.handle, x, None, None, T, ids2, w2, lo2)
+        torch.cuda.synchronize()
+        l2 = host(lo2).astype(np.float64)
+        ref = host(lo).astype(np.float64)
+        assert np.max(np.abs(l2 - ref)) <= 1e-5 * np.max(np.abs(ref))
+        rid, rw = oracle.topk(l2, k)
+        assert np.array_equal(host(ids2), rid)
+        assert np.max(np.abs(host(w2) - rw)) <= 1e-6
+
+
 def test_noalloc_routing_with_given_logits_and_the_size_limit():
     E, k = 320, 8
     h = _routing_handle(E=E, k=k)
@@ -61,8 +91,8 @@ def test_noalloc_routing_with_given_logits_and_the_size_limit():
     rid, rw = oracle.topk(lg.astype(np.float64), k)
     assert np.array_equal(host(ids), rid)
     assert np.max(np.abs(host(w) - rw)) <= 1e-6
-    # T * E beyond the 8 MiB scratch: a clean error, nothing launched
-    T_big = 2 ** 21 // E + 1
+    # T * E beyond the 8 MiB scratch (less its status word): a clean error, nothing launched
+    T_big = (2 ** 21 - 64) // E + 1
     x = torch.zeros((T_big, 4096), dtype=torch.int16, device="cuda")
     ids = torch.zeros((T_big, k), dtype=torch.int32, device="cuda")
     w = torch.zeros((T_big, k), dtype=torch.float32, device="cuda")
