@@ -346,25 +346,29 @@ def measure_ours(args, rank, world):
     ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
     value = job_tokens_per_s(world, T, ms)
 
-    # ---- end to end through the C ABI: pinned host x -> device, forward, out -> host
+    # ---- end to end through the C ABI on host buffers: moe_forward_host copies the pinned
+    # host batch to the device, runs the forward and copies the output back to pinned host
+    # memory, every step inside the timed region
     xh = torch.from_numpy(x.view(np.int16)).pin_memory()
     oh = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    wsh = torch.zeros(moe.moe_workspace_size_host(layer.cfg, T), dtype=torch.uint8, device=dev)
+
+    def fwd_host():
+        moe.moe_forward_host(layer.handle, xh, lgd, bd, T, oh, wsh)
+
     with torch.cuda.stream(stream):
         for _ in range(3):
-            xd.copy_(xh, non_blocking=True)
-            fwd()
-            oh.copy_(out, non_blocking=True)
+            fwd_host()
         barrier()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.steps):
-            xd.copy_(xh, non_blocking=True)
-            fwd()
-            oh.copy_(out, non_blocking=True)
+            fwd_host()
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
+    del wsh
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     ms_eager = max_over_ranks(eager_ms(fwd, stream, args.steps), world)
 
@@ -372,11 +376,14 @@ def measure_ours(args, rank, world):
     res = dict(value=value, ms=ms, ms_e2e=ms_e2e, ms_eager=ms_eager, clocks=clocks, roofline=roof,
                launches=launches_per_forward(c) * args.steps)
     if "prefill" in extra and rank == 0:
-        res["prefill"] = measure_prefill(handles["prefill"], stream, max(3, args.steps // 20))
+        res["prefill"] = measure_prefill(handles["prefill"], stream, max(20, args.steps // 10),
+                                         with_oracle=not args.no_oracle)
     if "w4a16" in extra and rank == 0:
-        res["w4a16"] = measure_w4a16(handles["w4a16"], stream, max(10, args.steps // 4))
+        res["w4a16"] = measure_w4a16(handles["w4a16"], stream, max(20, args.steps // 4),
+                                     with_oracle=not args.no_oracle)
     if "shard" in extra and rank == 0:
-        res["shard"] = measure_shard(handles["shard"], stream, max(10, args.steps // 4))
+        res["shard"] = measure_shard(handles["shard"], stream, max(20, args.steps // 4),
+                                     with_oracle=not args.no_oracle)
     for nm in ("decode_static", "decode_dyninter"):
         if nm in extra and rank == 0:
             res[nm] = measure_variant(handles[nm], nm, stream, max(10, args.steps // 4))
@@ -482,8 +489,55 @@ def roofline(layer, c, xd, lgd, bd, ws, stream, steps, pk, workload):
                      "frac": round(bytes_dn / dn / 1e9 / pk["hbm"], 4)}}
 
 
-def measure_prefill(layer, stream, steps):
-    """Side measurement of the prefill chunk (8192 tokens, 1% outlier channels)."""
+def graph_replays(fwd, stream, steps, min_seconds=1.5):
+    """One forward captured in a CUDA graph (after 3 eager warm-ups and a status check), 3
+    warm-up replays, then `steps` replays timed with CUDA events on the stream; the clocks are
+    sampled from before the timed replays until at least min_seconds of replays have run.
+    Returns (mean ms per replay, clock summary)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fwd()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fwd()
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        t_end = time.time() + max(0.0, min_seconds - ev0.elapsed_time(ev1) / 1e3)
+        while time.time() < t_end:
+            for _ in range(20):
+                g.replay()
+            torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / steps, summarise_clocks(sampler.stop())
+
+
+def cpu_side(name):
+    """The oracle on all host cores for a bounded sample of a side workload."""
+    import oracle
+    run, what = oracle_setup(name, ORACLE_SAMPLE[name])
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    return {"value": round(ORACLE_SAMPLE[name] / dt, 3), "unit": "tokens/s",
+            "cores": oracle.num_threads(), "kind": "oracle", "sample": what,
+            "seconds": round(dt, 2)}
+
+
+def measure_prefill(layer, stream, steps, with_oracle=True):
+    """Side measurement of the prefill chunk (8192 tokens, 1% outlier channels): CUDA-graph
+    replays with their own clock record, the two grouped GEMMs timed on their own, the layer
+    against its combined roofline, and the oracle on a 16-token sample."""
     import torch
 
     import nvfp4_mixture_experts_gb300 as moe
@@ -494,17 +548,14 @@ def measure_prefill(layer, stream, steps):
     xd = torch.from_numpy(x.view(np.int16)).to(dev)
     out = torch.empty((T, H), dtype=torch.int16, device=dev)
     ws = layer.ensure_workspace(T)
+    fwd = lambda: moe.moe_forward(layer.handle, xd, None, None, T, out, ws)
     with torch.cuda.stream(stream):
-        for _ in range(3):
-            moe.moe_forward(layer.handle, xd, None, None, T, out, ws)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            moe.moe_forward(layer.handle, xd, None, None, T, out, ws)
-        e1.record(stream)
-        torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+        fwd()
+    torch.cuda.synchronize()
+    st, bits = moe.moe_get_status(layer.handle, ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError("device status %#x" % bits)
+    ms, clocks = graph_replays(fwd, stream, steps)
     pk = peaks()
     roof = roofline(layer, c, xd, None, None, ws, stream, steps, pk, "prefill")
     counts = staged_counts(layer, ws, T)
@@ -523,9 +574,14 @@ def measure_prefill(layer, stream, steps):
                   "fp4_frac": round(fl / t / 1e12 / fp4_peak, 4),
                   "bound": "hbm" if by / (pk["hbm"] * 1e9) >= fl / (fp4_peak * 1e12) else "tensor",
                   "roof_us": round(t_roof * 1e6, 1), "roof_frac": round(t_roof / t, 4)}
-    return {"workload": "prefill T=8192", "value": T / (ms / 1e3), "ms_per_step": ms,
-            "roofline": roof, "expert_fp4_tflops": round(fl / (ms / 1e3) / 1e12, 2),
-            "layer": layer_roof}
+    res = {"workload": "prefill T=8192", "value": T / (ms / 1e3), "ms_per_step": ms,
+           "steps": steps, "timing": "CUDA-graph replays, inputs resident (2.8 GB of weights "
+           "per step: no L2 flush)", "clocks": clocks,
+           "roofline": roof, "expert_fp4_tflops": round(fl / (ms / 1e3) / 1e12, 2),
+           "layer": layer_roof}
+    if with_oracle:
+        res["cpu_baseline"] = cpu_side("prefill")
+    return res
 
 
 VARIANTS = {
@@ -573,7 +629,7 @@ def measure_variant(layer, name, stream, steps):
             "down_frac": roof["down"]["frac"]}
 
 
-def measure_shard(layer, stream, steps):
+def measure_shard(layer, stream, steps, with_oracle=True):
     """Side measurement of the expert shard (experts 160-319 of the same layer, T=2048, router
     logits biased towards a Zipf(1.1) popularity, no shared rows): the shard's partial sum,
     CUDA-graph replays, and its two grouped GEMM launches timed on their own."""
@@ -587,26 +643,14 @@ def measure_shard(layer, stream, steps):
     bd = torch.from_numpy(bias).cuda()
     out = torch.empty((T, H), dtype=torch.int16, device="cuda")
     ws = layer.ensure_workspace(T)
+    fwd = lambda: moe.moe_forward(layer.handle, xd, None, bd, T, out, ws)
     with torch.cuda.stream(stream):
-        for _ in range(3):
-            moe.moe_forward(layer.handle, xd, None, bd, T, out, ws)
-        torch.cuda.synchronize()
-        st, bits = moe.moe_get_status(layer.handle, ws)
-        if st != moe.MOE_OK:
-            raise RuntimeError("device status %#x" % bits)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            moe.moe_forward(layer.handle, xd, None, bd, T, out, ws)
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            g.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+        fwd()
+    torch.cuda.synchronize()
+    st, bits = moe.moe_get_status(layer.handle, ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError("device status %#x" % bits)
+    ms, clocks = graph_replays(fwd, stream, steps)
     roof = roofline(layer, c, xd, None, bd, ws, stream, min(steps, 20), peaks(), "shard")
     counts = staged_counts(layer, ws, T)
     El = c["E_loc"]
@@ -616,7 +660,9 @@ def measure_shard(layer, stream, steps):
             "local_pairs": int(counts[:El].sum()), "experts_touched": roof["experts_touched"],
             "max_rows_per_expert": int(counts[:El].max()),
             "gateup_us": roof["launch_us"], "gateup_frac": roof["frac"],
-            "down_us": roof["down"]["launch_us"], "down_frac": roof["down"]["frac"]}
+            "down_us": roof["down"]["launch_us"], "down_frac": roof["down"]["frac"],
+            "steps": steps, "clocks": clocks,
+            "cpu_baseline": cpu_side("shard") if with_oracle else None}
 
 
 def measure_weight_prep(c, stream, steps):
@@ -693,7 +739,7 @@ def flushed_replays(g, stream, steps):
     return total / steps
 
 
-def measure_w4a16(layer, stream, steps):
+def measure_w4a16(layer, stream, steps, with_oracle=True):
     """Side measurement of the W4A16 path (bf16 activations x NVFP4 weights, router logits
     given ~ N(0,1)) over the decode sweep T in {1, 8, 32, 128, 256}: CUDA-graph replays."""
     import torch
@@ -747,8 +793,11 @@ def measure_w4a16(layer, stream, steps):
                          "gateup_us": roof["launch_us"], "gateup_frac": roof["frac"],
                          "down_us": roof["down"]["launch_us"], "down_frac": roof["down"]["frac"],
                          "eager_ms_per_step": round(ms_eager, 4), "l2": l2})
-    return {"workload": "w4a16 decode sweep (bf16 x NVFP4, logits given)", "unit": "tokens/s",
-            "sweep": out_rows}
+    res = {"workload": "w4a16 decode sweep (bf16 x NVFP4, logits given)", "unit": "tokens/s",
+           "sweep": out_rows}
+    if with_oracle:  # the oracle's W4A16 layer on a 16-token sample of the T=256 point
+        res["cpu_baseline"] = cpu_side("w4a16")
+    return res
 
 
 # ---------------------------------------------------------------- CPU oracle

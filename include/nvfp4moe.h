@@ -91,6 +91,9 @@ typedef enum {
 #define MOE_DEV_BAD_EXPERT_ID  0x1u   /* a top-k id outside [0, num_experts): pair dropped */
 #define MOE_DEV_WAIT_TIMEOUT   0x2u   /* a pipeline wait ran out: that tile was abandoned */
 #define MOE_DEV_ROWS_OVERFLOW  0x4u   /* padded rows exceeded capacity: pairs dropped */
+#define MOE_DEV_BAD_INDEX      0x8u   /* library built with MOE_DEBUG only: a padded-row or
+                                         pair index read from a buffer was out of range; the
+                                         access was skipped */
 
 typedef struct {
     int32_t hidden;               /* H: multiple of 128 */
@@ -109,6 +112,11 @@ typedef struct {
                                      every row the call computes, in two passes (gate_up
                                      writes fp32 s and its amax, then s is quantised) */
     int32_t max_tokens;           /* largest T a call may pass */
+    int32_t gemm_tiling;          /* W4A4 grouped GEMM form: 0 the library's choice (row
+                                     blocks, the faster form at every measured size); 1 row
+                                     blocks: 128 padded rows x 128 weight rows per MMA tile;
+                                     2 token tiles: 128 weight rows x up to 208 token rows of
+                                     one expert (no padding rows in the MMA) */
 } moe_config;
 
 /* Device pointers, canonical layouts (see above). */
@@ -324,6 +332,23 @@ MOE_API moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* in
 MOE_API moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_in_d,
                        const float* logit_bias_d, int32_t T, void* out_bf16_d, void* ws_d,
                        size_t ws_bytes, moe_stream_t stream);
+
+/* The whole layer on host buffers: x_bf16_h [T][H] is copied to the device, the layer runs
+ * as moe_forward, and out_bf16_h [T][H] is copied back, all ordered on the stream -- the
+ * call returns before the copies finish (pinned host memory; with pageable memory the
+ * copies are synchronous): synchronise the stream before reading out_bf16_h.  The device
+ * copies of x and out live at the end of the workspace, which must hold
+ * moe_workspace_size_host(cfg, T) bytes.  logits_in_d / logit_bias_d as for moe_forward
+ * (device pointers).
+ * Passage: [OV] and [EP], as moe_forward. */
+MOE_API moe_status moe_forward_host(moe_handle h, const void* x_bf16_h, const float* logits_in_d,
+                                    const float* logit_bias_d, int32_t T, void* out_bf16_h,
+                                    void* ws_d, size_t ws_bytes, moe_stream_t stream);
+
+/* Workspace bytes for moe_forward_host: moe_workspace_size plus room for the device copies
+ * of x and out (0 for an invalid cfg).
+ * Passage: none; buffer sizing of this library (the pages have no counterpart). */
+MOE_API size_t moe_workspace_size_host(const moe_config* cfg, int32_t T);
 
 /* Where moe_forward keeps its intermediates inside the workspace (device pointers into
  * ws_d), so callers can inspect them after a forward.  Any pointer may be NULL.  Unlike

@@ -17,7 +17,9 @@ MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE, \
     MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_STATUS = range(7)
 MOE_W4A4_DYNAMIC, MOE_W4A4_STATIC, MOE_W4A16 = 0, 1, 2
 MOE_GS_ENCODE, MOE_GS_DEQUANT = 0, 1
+MOE_TILING_AUTO, MOE_TILING_ROWS, MOE_TILING_TOKENS = 0, 1, 2
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_WAIT_TIMEOUT, MOE_DEV_ROWS_OVERFLOW = 1, 2, 4
+MOE_DEV_BAD_INDEX = 8
 
 
 class moe_config(C.Structure):
@@ -26,7 +28,8 @@ class moe_config(C.Structure):
                 ("local_expert_offset", C.c_int32), ("has_shared", C.c_int32),
                 ("shared_inter", C.c_int32), ("add_shared", C.c_int32),
                 ("act_mode", C.c_int32), ("act_global_scale", C.c_float),
-                ("inter_global_scale", C.c_float), ("max_tokens", C.c_int32)]
+                ("inter_global_scale", C.c_float), ("max_tokens", C.c_int32),
+                ("gemm_tiling", C.c_int32)]
 
 
 class moe_weights(C.Structure):
@@ -58,6 +61,8 @@ SIGNATURES = {
     "moe_grouped_gemm_down": (C.c_int, [_V, _V, _V, _V, _V, _V, _V, _V, _V, _I, _V, _SZ, _V]),
     "moe_combine": (C.c_int, [_V, _V, _V, _V, _I, _V, _V]),
     "moe_forward": (C.c_int, [_V, _V, _V, _V, _I, _V, _V, _SZ, _V]),
+    "moe_forward_host": (C.c_int, [_V, _V, _V, _V, _I, _V, _V, _SZ, _V]),
+    "moe_workspace_size_host": (_SZ, [C.POINTER(moe_config), _I]),
     "moe_forward_buffers": (C.c_int, [_V, _V, _I] + [C.POINTER(_V)] * 16),
     "moe_get_status": (C.c_int, [_V, _V, _V, C.POINTER(C.c_uint32)]),
     "moe_status_string": (C.c_char_p, [C.c_int]),
@@ -65,22 +70,36 @@ SIGNATURES = {
 }
 
 _lib = None
+_lib_debug = None
+
+
+def _open(p):
+    if not os.path.exists(p):
+        raise OSError("%s not built: run __graft_entry__.build()" % p)
+    lib = C.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
 
 
 def load(path=None):
     """Loads the compiled library (raises OSError if it is not there)."""
     global _lib
     if _lib is None:
-        p = path or LIB_PATH
-        if not os.path.exists(p):
-            raise OSError("libnvfp4moe.so not built (%s): run __graft_entry__.build()" % p)
-        lib = C.CDLL(p)
-        for name, (res, args) in SIGNATURES.items():
-            f = getattr(lib, name)
-            f.restype = res
-            f.argtypes = args
-        _lib = lib
+        _lib = _open(path or LIB_PATH)
     return _lib
+
+
+def load_debug():
+    """The MOE_DEBUG flavour of the library (same entry points; every index read from a
+    buffer is bounds-checked on the device and a bad one flags MOE_DEV_BAD_INDEX).  Handles
+    of one flavour are used with that flavour's calls only."""
+    global _lib_debug
+    if _lib_debug is None:
+        _lib_debug = _open(_build.LIB_DEBUG)
+    return _lib_debug
 
 
 class MoEError(RuntimeError):
@@ -205,6 +224,18 @@ def moe_combine(h, y, inv, offsets, T, out, stream=None):
 def moe_forward(h, x, logits_in, logit_bias, T, out, ws, stream=None):
     _check(load().moe_forward(h, _p(x), _p(logits_in), _p(logit_bias), T, _p(out), _p(ws),
                               ws.numel() * ws.element_size(), _stream(stream)), "moe_forward")
+
+
+def moe_forward_host(h, x_host, logits_in, logit_bias, T, out_host, ws, stream=None):
+    """x_host / out_host: CPU tensors (pinned for asynchronous copies); ws: a device workspace
+    of moe_workspace_size_host bytes."""
+    _check(load().moe_forward_host(h, _p(x_host), _p(logits_in), _p(logit_bias), T,
+                                   _p(out_host), _p(ws), ws.numel() * ws.element_size(),
+                                   _stream(stream)), "moe_forward_host")
+
+
+def moe_workspace_size_host(cfg, T):
+    return load().moe_workspace_size_host(C.byref(cfg), T)
 
 
 FORWARD_BUFFERS = ("topk_ids", "topk_w", "expert_counts", "expert_offsets", "perm_src", "inv",

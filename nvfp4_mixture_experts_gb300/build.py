@@ -9,6 +9,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnvfp4moe.so")
+# the MOE_DEBUG flavour: bounds checks on every index read from a buffer (a bad one sets
+# MOE_DEV_BAD_INDEX and its access is skipped); same symbols, separate file
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libnvfp4moe_debug.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
@@ -24,21 +28,24 @@ def _deps():
         [os.path.join(os.path.dirname(HERE), "include", "nvfp4moe.h"), __file__]
 
 
-def up_to_date():
-    if not os.path.exists(LIB):
+def up_to_date(lib=LIB):
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force=False, verbose=False):
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force=False, verbose=False, debug=False):
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose else []
+    if debug:
+        extra.append("-DMOE_DEBUG")
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = [NVCC, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -49,13 +56,23 @@ def build(force=False, verbose=False):
 
     with ThreadPoolExecutor(len(_sources())) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + ".%d.tmp" % os.getpid()
-    r = subprocess.run([NVCC, *FLAGS, "-shared", *objs, "-o", tmp], capture_output=True, text=True)
+    tmp = lib + ".%d.tmp" % os.getpid()
+    r = subprocess.run([NVCC, *FLAGS, "-shared", *objs, "-ldl", "-o", tmp], capture_output=True,
+                       text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_all(force=False):
+    """Both flavours, side by side."""
+    with ThreadPoolExecutor(2) as ex:
+        return list(ex.map(lambda d: build(force=force, debug=d), (False, True)))
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    if "--debug" in sys.argv:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug=True))
+    else:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -3,6 +3,7 @@
 // runs in this library's kernels; there is no host or library fallback.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdio>
 #include <cmath>
@@ -15,6 +16,26 @@
 using namespace moe;
 
 namespace {
+
+// ---------------------------------------------------------------- NVTX ranges
+// Every C-ABI call that launches work opens a range named after itself in the "nvfp4moe"
+// domain (host-side; a profiler attributes the call's launches to it).  With no tool
+// attached an NVTX call returns at once.
+struct NvtxRange {
+    explicit NvtxRange(const char* name)
+    {
+        static const nvtxDomainHandle_t domain = nvtxDomainCreateA("nvfp4moe");
+        nvtxEventAttributes_t a = {};
+        a.version = NVTX_VERSION;
+        a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+        a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+        a.message.ascii = name;
+        nvtxDomainRangePushEx(domain, &a);
+        dom = domain;
+    }
+    ~NvtxRange() { nvtxDomainRangePop(dom); }
+    nvtxDomainHandle_t dom;
+};
 
 // ---------------------------------------------------------------- driver entry point
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -228,6 +249,7 @@ bool valid_cfg(const moe_config* c, moe_status* why)
     if (c->act_mode < 0 || c->act_mode > 2) return false;
     if (c->act_mode == MOE_W4A4_STATIC && !(c->act_global_scale > 0.0f)) return false;
     if (c->act_mode != MOE_W4A16 && !(c->inter_global_scale >= 0.0f)) return false;
+    if (c->gemm_tiling < 0 || c->gemm_tiling > 2) return false;
     *why = MOE_ERR_UNSUPPORTED;
     if (c->hidden % 128 || c->inter % 64) return false;
     if (c->num_experts > kMaxExperts || c->top_k > kMaxTopK) return false;
@@ -253,6 +275,15 @@ int grid_for(int64_t threads, int block) { return (int)std::max<int64_t>(1, (thr
 // expert) take the grouped GEMV (gemv_w4a16.cu), which reads each weight once per chunk of
 // 8 rows of a group instead of padding every group to the tensor-core kernel's 128-row MMA.
 constexpr int kGemvMaxTokens = 256;
+
+// W4A4 grouped GEMM form: row blocks (gemm.cu) unless the configuration asks for token
+// tiles (gemm_swap.cu).  Measured on the prefill chunk (8192 tokens, ~205 rows per expert):
+// row blocks 1.375 ms per forward (gate_up 690 us, down 440 us), token tiles of up to 208 /
+// 160 / 128 rows 1.63 / 1.84 / 1.91 ms (gate_up 843 / 980 / 1027 us); at decode both forms
+// stream the weights.  So the automatic choice is row blocks at every size.
+constexpr int kTokenTileRows = 208;  // token rows per tile at most (gemm_swap.cu)
+
+bool use_token_tiles(const moe_layer* h, int /*T*/) { return h->cfg.gemm_tiling == 2; }
 
 // Persistent grid: one CTA per SM, or fewer when the tile list (bounded above from the
 // pair count, with row blocks of `rows` rows) is shorter.
@@ -369,10 +400,11 @@ moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T
         return launch(gather_f16_kernel,
                       dim3(grid_for((int64_t)T * ((c.hidden + 255) / 256) * 32, 256)), dim3(256),
                       0, s, pdl, xb, T, c.hidden, c.top_k, inv, offsets, p.El, add,
-                      (const uint32_t*)amax, static_cast<uint16_t*>(a_bf16), gs_out);
+                      (const uint32_t*)amax, static_cast<uint16_t*>(a_bf16), gs_out,
+                      (int64_t)p.cap, at<uint32_t>(ws, p.status));
     return launch(gather_quant_kernel_for(bpl), grid, dim3(256), 0, s, pdl, xb, T, c.hidden,
                   c.top_k, inv, offsets, p.El, add, gs_static, (const uint32_t*)amax, a_codes,
-                  a_sf, gs_out);
+                  a_sf, gs_out, (int64_t)p.cap, at<uint32_t>(ws, p.status));
 }
 
 moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilogue,
@@ -462,6 +494,29 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     CUtensorMap tmA, tmA16, tmY;
     memset(&tmY, 0, sizeof(tmY));
     const int grid = gemm_grid(h, p.T, N, 128);
+    const int pitch = codes_pitch(K);
+    if (use_token_tiles(h, p.T)) {
+        args.rb_cap = p.cap / 128;
+        args.tile_n = kTokenTileRows;
+        args.stages = kMaxStages;
+        while (args.stages > 2 &&
+               gemm_swap_smem_bytes(args.stages, args.tile_n, p.G) > kSmemLimit)
+            --args.stages;
+        const int smem = gemm_swap_smem_bytes(args.stages, args.tile_n, p.G);
+        if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
+        if (!make_tmap(&tmA, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
+                       128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_tmap(&tmA16, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
+                       16, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MOE_ERR_CUDA;
+        // kEpiDownF16 stores y in 32 x 32 fp16 boxes (64-byte rows, 64-byte swizzle)
+        if (epilogue == kEpiDownF16 &&
+            !make_tmap(&tmY, out_f32, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, N, p.cap, (uint64_t)N * 2,
+                       32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+            return MOE_ERR_CUDA;
+        return launch(gemm_nvf4_swap_kernel, dim3(grid), dim3(kSwThreads), smem, s, pdl, tmA,
+                      tmA16, tmY, args);
+    }
     const int stage_bytes = kNvf4StageBytes;
     // Kernel configuration from the expected LOCAL load (rows per local expert), as the
     // pages' backend choice is re-tuned on the local rather than the global workload: with
@@ -481,7 +536,6 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
         !make_tmap(&tmY, out_f32, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, N, p.cap, (uint64_t)N * 2, 32,
                    32, CU_TENSOR_MAP_SWIZZLE_64B))
         return MOE_ERR_CUDA;
-    const int pitch = codes_pitch(K);
     if (!make_tmap(&tmA, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap(&tmA16, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128, 16,
@@ -556,12 +610,14 @@ moe_status launch_combine(const moe_layer* h, const void* y, const int32_t* inv,
                           dim3((unsigned)std::min<int64_t>(units, h->num_sms)),
                           dim3(kCombineTmaThreads), combine_tma_smem(nrows, cw, nslots, (int)es),
                           s, pdl, y, y_scale, inv, offsets, c.num_local_experts, T, c.hidden,
-                          c.top_k, add, cw, nslots, static_cast<uint16_t*>(out), status);
+                          c.top_k, add, cw, nslots, static_cast<uint16_t*>(out), status,
+                          (int64_t)rows_cap(c, T));
         }
     }
     return launch(combine_kernel, dim3(grid_for((int64_t)T * (c.hidden / 8), 256)), dim3(256), 0,
                   s, pdl, y, y_scale, inv, offsets, c.num_local_experts, T, c.hidden, c.top_k,
-                  shared_rows(h, T) > 0 ? 1 : 0, static_cast<uint16_t*>(out));
+                  shared_rows(h, T) > 0 ? 1 : 0, static_cast<uint16_t*>(out),
+                  (int64_t)rows_cap(c, T), status);
 }
 
 }  // namespace
@@ -693,6 +749,7 @@ void moe_destroy(moe_handle h)
 moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t stream,
                       moe_handle* out)
 {
+    const NvtxRange nvtx_range("moe_create");
     if (!out) return MOE_ERR_INVALID;
     *out = nullptr;
     moe_status why;
@@ -771,6 +828,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
          set_topk_smem_limits() &&
          cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemLimit) == cudaSuccess &&
+         cudaFuncSetAttribute(gemm_nvf4_swap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemLimit) == cudaSuccess &&
          set_w4a16_smem_limits();
     if (!ok) {
         cudaGetLastError();
@@ -786,6 +845,7 @@ moe_status moe_route_topk(moe_handle h, const void* x_bf16_d, const float* logit
                           float* topk_w_d, float* logits_out_d, void* ws_d, size_t ws_bytes,
                           moe_stream_t stream)
 {
+    const NvtxRange nvtx_range("moe_route_topk");
     if (!h || !t_ok(h, T) || !topk_ids_d || !topk_w_d) return MOE_ERR_INVALID;
     if (!logits_in_d && !x_bf16_d) return MOE_ERR_INVALID;
     if (T == 0) return MOE_OK;
@@ -809,6 +869,7 @@ moe_status moe_permute(moe_handle h, const int32_t* topk_ids_d, int32_t T,
                        int32_t* perm_src_d, int32_t* inv_d, void* ws_d, size_t ws_bytes,
                        moe_stream_t stream)
 {
+    const NvtxRange nvtx_range("moe_permute");
     if (!h || !t_ok(h, T) || !topk_ids_d || !expert_counts_d || !expert_offsets_d ||
         !perm_src_d || !inv_d)
         return MOE_ERR_INVALID;
@@ -825,6 +886,7 @@ moe_status moe_quant_nvfp4(const void* x_bf16_d, int32_t rows, int32_t cols,
                            uint8_t* sf_d, int32_t sf_layout, void* ws_d, size_t ws_bytes,
                            moe_stream_t stream)
 {
+    const NvtxRange nvtx_range("moe_quant_nvfp4");
     if (!x_bf16_d || !codes_d || !sf_d || rows < 0 || cols <= 0) return MOE_ERR_INVALID;
     if (sf_layout != 0 && sf_layout != 1) return MOE_ERR_INVALID;
     if (cols % 64) return MOE_ERR_UNSUPPORTED;
@@ -853,6 +915,7 @@ moe_status moe_gather_activations(moe_handle h, const void* x_bf16_d, int32_t T,
                                   float* gs_out_d, void* ws_d, size_t ws_bytes,
                                   moe_stream_t stream)
 {
+    const NvtxRange nvtx_range("moe_gather_activations");
     if (!h || !t_ok(h, T) || !x_bf16_d || !inv_d || !expert_offsets_d) return MOE_ERR_INVALID;
     if (h->cfg.act_mode == MOE_W4A16 ? !a_bf16_d : (!a_codes_d || !a_sf_d || !gs_out_d))
         return MOE_ERR_INVALID;
@@ -873,6 +936,7 @@ moe_status moe_grouped_gemm_gateup(moe_handle h, const uint8_t* a_codes_d,
                                    uint8_t* inter_sf_d, void* inter_bf16_d, int32_t T,
                                    void* ws_d, size_t ws_bytes, moe_stream_t stream)
 {
+    const NvtxRange nvtx_range("moe_grouped_gemm_gateup");
     if (!h || !t_ok(h, T) || !expert_counts_d || !expert_offsets_d) return MOE_ERR_INVALID;
     const bool a16 = h->cfg.act_mode == MOE_W4A16;
     if (a16 ? !a_bf16_d : (!a_codes_d || !a_sf_d || !gs_a_d)) return MOE_ERR_INVALID;
@@ -904,6 +968,7 @@ moe_status moe_prepare_weights(const uint8_t* codes_d, const uint8_t* sf_d, cons
                                int32_t count, uint8_t* codes_out_d, uint8_t* sf_out_d,
                                float* gs_out_d, moe_stream_t stream)
 {
+    const NvtxRange nvtx_range("moe_prepare_weights");
     if (N <= 0 || K <= 0 || num_experts < 0 || off < 0 || count < 0 ||
         (int64_t)off + count > num_experts)
         return MOE_ERR_INVALID;
@@ -929,6 +994,7 @@ moe_status moe_swiglu_requant(const float* gateup_f32_d, int32_t rows, int32_t i
                               float gs_i, uint8_t* codes_d, uint8_t* sf_d, int32_t sf_layout,
                               moe_stream_t stream)
 {
+    const NvtxRange nvtx_range("moe_swiglu_requant");
     if (!gateup_f32_d || !codes_d || !sf_d || rows < 0 || inter <= 0 || !(gs_i > 0.0f))
         return MOE_ERR_INVALID;
     if (sf_layout != 0 && sf_layout != 1) return MOE_ERR_INVALID;
@@ -947,6 +1013,7 @@ moe_status moe_grouped_gemm_down(moe_handle h, const uint8_t* inter_codes_d,
                                  const float* topk_w_d, float* y_d, int32_t T, void* ws_d,
                                  size_t ws_bytes, moe_stream_t stream)
 {
+    const NvtxRange nvtx_range("moe_grouped_gemm_down");
     if (!h || !t_ok(h, T) || !expert_counts_d || !expert_offsets_d || !perm_src_d ||
         !topk_w_d || !y_d)
         return MOE_ERR_INVALID;
@@ -965,6 +1032,7 @@ moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* inv_d,
                        const int32_t* expert_offsets_d, int32_t T, void* out_bf16_d,
                        moe_stream_t stream)
 {
+    const NvtxRange nvtx_range("moe_combine");
     if (!h || !t_ok(h, T) || !y_d || !inv_d || !expert_offsets_d || !out_bf16_d)
         return MOE_ERR_INVALID;
     if (T == 0) return MOE_OK;
@@ -976,6 +1044,7 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
                        const float* logit_bias_d, int32_t T, void* out_bf16_d, void* ws_d,
                        size_t ws_bytes, moe_stream_t stream)
 {
+    const NvtxRange nvtx_range("moe_forward");
     if (!h || !t_ok(h, T) || !x_bf16_d || !out_bf16_d) return MOE_ERR_INVALID;
     if (reinterpret_cast<uintptr_t>(x_bf16_d) & 15) return MOE_ERR_INVALID;
     if (T == 0) return MOE_OK;  // nothing to do: no workspace needed
@@ -1028,6 +1097,37 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
     return r;
 }
 
+size_t moe_workspace_size_host(const moe_config* cfg, int32_t T)
+{
+    const size_t base = moe_workspace_size(cfg, T);
+    if (!base) return 0;
+    return base + 2 * align256((size_t)T * cfg->hidden * 2);
+}
+
+moe_status moe_forward_host(moe_handle h, const void* x_bf16_h, const float* logits_in_d,
+                            const float* logit_bias_d, int32_t T, void* out_bf16_h, void* ws_d,
+                            size_t ws_bytes, moe_stream_t stream)
+{
+    const NvtxRange nvtx_range("moe_forward_host");
+    if (!h || !t_ok(h, T) || !x_bf16_h || !out_bf16_h) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;  // nothing to do: no workspace needed
+    const size_t base = plan(h->cfg, T).total;
+    const size_t xb = (size_t)T * h->cfg.hidden * 2;
+    moe_status st = check_ws(h, T, ws_d, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (ws_bytes < base + 2 * align256(xb)) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* xd = static_cast<uint8_t*>(ws_d) + base;
+    uint8_t* od = xd + align256(xb);
+    if (cudaMemcpyAsync(xd, x_bf16_h, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    st = moe_forward(h, xd, logits_in_d, logit_bias_d, T, od, ws_d, base, stream);
+    if (st != MOE_OK) return st;
+    return cudaMemcpyAsync(out_bf16_h, od, xb, cudaMemcpyDeviceToHost, s) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}
+
 moe_status moe_forward_buffers(moe_handle h, void* ws_d, int32_t T, int32_t** topk_ids,
                                float** topk_w, int32_t** expert_counts,
                                int32_t** expert_offsets, int32_t** perm_src, int32_t** inv,
@@ -1062,6 +1162,7 @@ moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
                                   int32_t T, int32_t* topk_ids_d, float* topk_w_d,
                                   float* logits_out_d, moe_stream_t stream)
 {
+    const NvtxRange nvtx_range("moe_route_topk_noalloc");
     if (!h || !t_ok(h, T) || !topk_ids_d || !topk_w_d) return MOE_ERR_INVALID;
     if (!logits_in_d && !x_bf16_d) return MOE_ERR_INVALID;
     if (T == 0) return MOE_OK;
@@ -1133,6 +1234,7 @@ __global__ void bounded_wait_probe_kernel(uint32_t* status, uint64_t limit_ns)
 
 moe_status moe_selftest_bounded_wait(uint32_t* status_d, uint64_t limit_ns, moe_stream_t stream)
 {
+    const NvtxRange nvtx_range("moe_selftest_bounded_wait");
     if (!status_d || limit_ns == 0 || limit_ns > moe::kWaitLimitNs) return MOE_ERR_INVALID;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint32_t bits = 0;
@@ -1147,6 +1249,7 @@ moe_status moe_selftest_bounded_wait(uint32_t* status_d, uint64_t limit_ns, moe_
 
 moe_status moe_get_status(moe_handle h, void* ws_d, moe_stream_t stream, uint32_t* bits)
 {
+    const NvtxRange nvtx_range("moe_get_status");
     if (!h || !ws_d) return MOE_ERR_INVALID;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint32_t v = 0;

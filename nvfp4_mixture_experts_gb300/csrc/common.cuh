@@ -184,6 +184,12 @@ __device__ __forceinline__ void bulk_wait_read1()
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
+// Wait until no committed bulk store still reads its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Wait until every committed bulk store has completed (writes performed).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 

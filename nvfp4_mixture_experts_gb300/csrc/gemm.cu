@@ -150,7 +150,7 @@ __device__ __forceinline__ EpiPrep epi_prep(const GemmArgs& a, const TileInfo& t
     }
     if (is_down(a.epilogue) && e.valid) {
         const int pair = a.perm_src[e.prow];
-        const float wgt = pair < a.Tk ? a.topk_w[pair] : 1.0f;
+        const float wgt = !pair_ok(pair, a.status) ? 0.0f : pair < a.Tk ? a.topk_w[pair] : 1.0f;
         e.alpha = __fmul_rn(__fmul_rn(e.alpha, wgt), ys);
     }
     return e;

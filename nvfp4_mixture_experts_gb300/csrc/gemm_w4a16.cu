@@ -455,7 +455,9 @@ __global__ void __launch_bounds__(kW16Threads, 1)
                 const int n = lane + 32 * i;
                 if (args.epilogue == kEpiDown && n < ti.rows) {
                     const int pair = args.perm_src[ti.brow0 + n];
-                    wl[i] = pair < args.Tk ? args.topk_w[pair] : 1.0f;
+                    wl[i] = !pair_ok(pair, args.status) ? 0.0f
+                            : pair < args.Tk            ? args.topk_w[pair]
+                                                        : 1.0f;
                 }
             }
             int okw = 1;  // (a whole tile: the lane sleeps between polls)

@@ -325,7 +325,7 @@ __device__ __forceinline__ void gv_stage_chunk(const GemmArgs& a, const GvSmem& 
             if (t == 0) m.tscale[2 * kGvTok] = __frcp_rn(__fmul_rn(*a.gs_a, gw));
         } else {
             const int pair = a.perm_src[row0 + t];
-            const float wn = pair < a.Tk ? a.topk_w[pair] : 1.0f;
+            const float wn = !pair_ok(pair, a.status) ? 0.0f : pair < a.Tk ? a.topk_w[pair] : 1.0f;
             m.tscale[kGvTok + t] = __fmul_rn(__frcp_rn(gw), wn);
         }
     }

@@ -7,6 +7,35 @@ namespace moe {
 
 constexpr int kPairsPerBlock = 1024;   // grouping: pairs per block of the counting sort
 
+// Debug builds (MOE_DEBUG defined) check every padded-row index and pair index that a
+// kernel reads from a buffer before using it: a bad one sets MOE_DEV_BAD_INDEX in the status
+// word and the access is skipped (never a trap).  Release builds compile the checks away.
+#ifdef MOE_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+// A padded row r (-1: none) read from a buffer, against the row capacity.
+__device__ __forceinline__ int64_t checked_row(int64_t r, int64_t cap, uint32_t* status)
+{
+    if (kDebugChecks && (r < -1 || r >= cap)) {
+        set_status(status, MOE_DEV_BAD_INDEX);
+        return -1;
+    }
+    return r;
+}
+
+// A pair index read from perm_src (>= T*k: a shared row), for a valid row: never negative.
+__device__ __forceinline__ bool pair_ok(int pair, uint32_t* status)
+{
+    if (kDebugChecks && pair < 0) {
+        set_status(status, MOE_DEV_BAD_INDEX);
+        return false;
+    }
+    return true;
+}
+
 // silu(g) * u in fp32: g / (1 + exp(-g)) * u, each step an IEEE fp32 operation.
 __device__ __forceinline__ float silu_mul(float g, float u)
 {
@@ -54,11 +83,12 @@ __global__ void amax_bf16_kernel(const uint16_t* x, int64_t n, uint32_t* amax_bi
 // per destination row, for large batches).
 using GatherKernel = void (*)(const uint16_t*, int, int, int, const int32_t*, const int32_t*,
                               int, int, const float*, const uint32_t*, uint8_t*, uint8_t*,
-                              float*);
+                              float*, int64_t, uint32_t*);
 GatherKernel gather_quant_kernel_for(int blocks_per_lane);
 __global__ void gather_f16_kernel(const uint16_t* x, int T, int H, int k, const int32_t* inv,
                                   const int32_t* offsets, int shared_group, int add_shared,
-                                  const uint32_t* amax_bits, uint16_t* out, float* gs_out);
+                                  const uint32_t* amax_bits, uint16_t* out, float* gs_out,
+                                  int64_t rows_cap, uint32_t* status);
 __global__ void quant_rows_kernel(const uint16_t* x, int rows, int cols, const float* gs_static,
                                   const uint32_t* amax_bits, uint8_t* codes, uint8_t* sf,
                                   int layout, float* gs_out);
@@ -71,7 +101,8 @@ __global__ void quant_inter_kernel(const float* s, const int32_t* counts, const 
 // y: fp32 rows, or (y_scale non-null) fp16 rows to be multiplied by y_scale[row]
 __global__ void combine_kernel(const void* y, const float* y_scale, const int32_t* inv,
                                const int32_t* offsets, int shared_group, int T, int H, int k,
-                               int add_shared, uint16_t* out);
+                               int add_shared, uint16_t* out, int64_t rows_cap,
+                               uint32_t* status);
 // Bulk-copy combine for large batches: 544 threads (a copy thread, sixteen adding warps), a
 // ring of nslots slots of (k + add_shared) row pieces of cw columns each.
 constexpr int kCombineTmaThreads = 544;
@@ -84,7 +115,7 @@ inline size_t combine_tma_smem(int nrows, int cw, int nslots, int esize = 4)
 __global__ void combine_tma_kernel(const void* y, const float* y_scale, const int32_t* inv,
                                    const int32_t* offsets, int shared_group, int T, int H, int k,
                                    int add_shared, int cw, int nslots, uint16_t* out,
-                                   uint32_t* status);
+                                   uint32_t* status, int64_t rows_cap);
 __global__ void prepare_weights_kernel(const uint8_t* codes, const uint8_t* sf,
                                        const float* glob, int N, int K, int convention,
                                        float fold_target, int swap_halves, int off, int count,
@@ -142,6 +173,7 @@ struct GemmArgs {
     const float* gs_i_dev;    // kEpiDown: device intermediate scale (dynamic), else gs_i
     float* y_scale;           // kEpiDownF16: [rows] the inverse of each row's fp16 scale
     uint32_t* status;
+    int tile_n;               // gemm_swap: token rows per tile at most (16..kSwNmax, % 16 == 0)
 };
 
 // W4A4: warp 0 TMA, warp 1 MMA, warps 2..5 epilogue, warps 6..9 scale factors
@@ -171,6 +203,32 @@ inline int gemm_stages(int want, int stage_bytes, int staging, int G, int rb_cap
 __global__ void gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
                                  const __grid_constant__ CUtensorMap tmA16,
                                  const __grid_constant__ CUtensorMap tmY, GemmArgs args);
+
+// ---- gemm_swap.cu: W4A4 with weight rows as the MMA's M side and up to kSwNmax token rows
+// of one expert as its N side (many rows per expert).  448 threads: producer, MMA, eight
+// epilogue warps, four scale warps.
+constexpr int kSwThreads = 448;
+constexpr int kSwNmax = 208;         // token rows per tile at most (GemmArgs::tile_n <= this)
+// a stage: weight blob, token codes (tile_n rows of 128 bytes), token scale atoms of two
+// 128-row blocks; a multiple of 1024 bytes for tile_n a multiple of 8
+__host__ __device__ constexpr int sw_stage_bytes(int tile_n)
+{
+    return kNvf4TileBytes + tile_n * 128 + 2 * 2048;
+}
+// scale slots in TMEM beside two accumulators of tile_n columns (at columns 0 and 256): each
+// slot holds a stage's weight scales (16 columns) and token scales (4 or 8 columns per
+// 64-element k-step)
+__host__ __device__ constexpr int sw_sfb_stride(int tile_n) { return tile_n <= 128 ? 4 : 8; }
+__host__ __device__ constexpr int sw_slot_cols(int tile_n) { return 16 + 4 * sw_sfb_stride(tile_n); }
+__host__ __device__ constexpr int sw_sf_slots(int tile_n)
+{
+    return 2 * ((256 - tile_n) / sw_slot_cols(tile_n));
+}
+__global__ void gemm_nvf4_swap_kernel(const __grid_constant__ CUtensorMap tmA,
+                                      const __grid_constant__ CUtensorMap tmA16,
+                                      const __grid_constant__ CUtensorMap tmY, GemmArgs args);
+// dynamic shared memory of a launch with `stages` stages and G groups
+int gemm_swap_smem_bytes(int stages, int tile_n, int G);
 
 // ---- gemm_w4a16.cu: swap-AB weight stream, BN token rows per tile (16, 32 or 64)
 constexpr int kW16Threads = 480;        // 15 warps: see the kernel's role table

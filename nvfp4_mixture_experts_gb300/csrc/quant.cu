@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(
     const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, int shared_group, int add_shared,
     const float* gs_static, const uint32_t* amax_bits, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ sf, float* gs_out)
+    uint8_t* __restrict__ sf, float* gs_out, int64_t rows_cap, uint32_t* status)
 {
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -99,8 +99,9 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(
         for (int u = 0; u < 8; ++u) {
             const int j = j0 + u;
             row[u] = !act || j >= nrows ? -1
-                     : j < k            ? (int64_t)inv[(size_t)t * k + j]
-                                        : (int64_t)offsets[shared_group] + t;
+                     : checked_row(j < k ? (int64_t)inv[(size_t)t * k + j]
+                                         : (int64_t)offsets[shared_group] + t,
+                                   rows_cap, status);
         }
     };
     // the layer input is complete before the forward starts: its load goes out before the
@@ -172,7 +173,8 @@ __device__ __forceinline__ float f16_prescale(const uint32_t* amax_bits)
 __global__ void __launch_bounds__(256) gather_f16_kernel(
     const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, int shared_group, int add_shared,
-    const uint32_t* amax_bits, uint16_t* __restrict__ out, float* gs_out)
+    const uint32_t* amax_bits, uint16_t* __restrict__ out, float* gs_out, int64_t rows_cap,
+    uint32_t* status)
 {
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -204,8 +206,9 @@ __global__ void __launch_bounds__(256) gather_f16_kernel(
         for (int u = 0; u < 8; ++u) {
             const int j = j0 + u;
             row[u] = j >= nrows ? -1
-                     : j < k    ? (int64_t)inv[(size_t)t * k + j]
-                                : (int64_t)offsets[shared_group] + t;
+                     : checked_row(j < k ? (int64_t)inv[(size_t)t * k + j]
+                                         : (int64_t)offsets[shared_group] + t,
+                                   rows_cap, status);
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u)
@@ -334,7 +337,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
                                                       const int32_t* __restrict__ inv,
                                                       const int32_t* __restrict__ offsets,
                                                       int shared_group, int T, int H, int k,
-                                                      int add_shared, uint16_t* __restrict__ out)
+                                                      int add_shared, uint16_t* __restrict__ out,
+                                                      int64_t rows_cap, uint32_t* status)
 {
     const bool f16 = y_scale != nullptr;  // fp16 rows, each times y_scale[row]
     const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
@@ -349,8 +353,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
         for (int u = 0; u < 8; ++u) {
             const int j = j0 + u;
             row[u] = !live || j >= nrows ? -1
-                     : j < k             ? (int64_t)inv[(size_t)t * k + j]
-                                         : (int64_t)offsets[shared_group] + t;
+                     : checked_row(j < k ? (int64_t)inv[(size_t)t * k + j]
+                                         : (int64_t)offsets[shared_group] + t,
+                                   rows_cap, status);
         }
     };
     int64_t row[8];
@@ -420,7 +425,7 @@ __global__ void __launch_bounds__(kCombineTmaThreads, 1) combine_tma_kernel(
     const void* __restrict__ y, const float* __restrict__ y_scale,
     const int32_t* __restrict__ inv, const int32_t* __restrict__ offsets, int shared_group,
     int T, int H, int k, int add_shared, int cw, int nslots, uint16_t* __restrict__ out,
-    uint32_t* status)
+    uint32_t* status, int64_t rows_cap)
 {
     extern __shared__ __align__(128) uint8_t smem_cmb[];
     const bool f16 = y_scale != nullptr;  // fp16 rows, each times y_scale[row]
@@ -465,8 +470,9 @@ __global__ void __launch_bounds__(kCombineTmaThreads, 1) combine_tma_kernel(
             for (int h = 0; h < 2; ++h) {
                 const int j = lane + 32 * h;
                 row[h] = j >= nrows ? -1
-                         : j < k    ? (int64_t)inv[(size_t)tt * k + j]
-                                    : (int64_t)offsets[shared_group] + tt;
+                         : checked_row(j < k ? (int64_t)inv[(size_t)tt * k + j]
+                                             : (int64_t)offsets[shared_group] + tt,
+                                       rows_cap, status);
             }
             if (f16)
 #pragma unroll

@@ -6,9 +6,10 @@ from . import (MOE_W4A4_DYNAMIC, moe_config, moe_create, moe_destroy, moe_forwar
 
 
 def make_config(H, I, E, k, E_loc=None, off=0, has_shared=1, add_shared=1,
-                act_mode=MOE_W4A4_DYNAMIC, act_gs=0.0, inter_gs=1.0, max_tokens=8192):
+                act_mode=MOE_W4A4_DYNAMIC, act_gs=0.0, inter_gs=1.0, max_tokens=8192,
+                gemm_tiling=0):
     return moe_config(H, I, E, k, E if E_loc is None else E_loc, off, has_shared, I,
-                      add_shared, act_mode, act_gs, inter_gs, max_tokens)
+                      add_shared, act_mode, act_gs, inter_gs, max_tokens, gemm_tiling)
 
 
 def _ptr(t):

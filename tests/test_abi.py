@@ -117,3 +117,13 @@ def test_every_declaration_cites_its_passage():
             j -= 1
         text = " ".join(block)
         assert re.search(r"Passage: (\[(OV|EP|CK)\]|none)", text), m.group(1)
+
+
+def test_debug_flavour_builds_and_exports_the_same_symbols():
+    """The MOE_DEBUG flavour (device bounds checks on indices read from buffers) compiles
+    from the same sources and exports every declared call."""
+    path = moe_build.build(debug=True)
+    assert path == moe_build.LIB_DEBUG and os.path.exists(path)
+    dbg = moe.load_debug()
+    for n in _declared_functions():
+        assert C.cast(getattr(dbg, n), C.c_void_p).value, n

@@ -110,14 +110,15 @@ def _forward_buffers_check(h, T, ora, clear, x, wr, bias=None):
         assert np.array_equal(s[valid], ora.x_sf[tok])
 
 
-def test_tiny_layer_full_parity():
+@pytest.mark.parametrize("tiling", [0, 2])
+def test_tiny_layer_full_parity(tiling):
     c = synth.CONFIGS["tiny"]
     T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
     gs_i = INTER["tiny"]["inter_global_scale"]
     layer = build_layer(0, H, I, E)
     wr = synth.router_weight(0, E, H)
     x = synth.activations(0, T, H)
-    h = make_layer(layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T)
+    h = make_layer(layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T, gemm_tiling=tiling)
     got = _forward(h, x, T)
     ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, inter_gs=gs_i), x, layer, router_w=wr)
     clear, _ = _routing_clear(x, wr, None, k)
@@ -137,13 +138,14 @@ def test_empty_batch_is_a_no_op():
     torch.cuda.synchronize()
 
 
-def test_decode_layer_full_parity(big_layer):
+@pytest.mark.parametrize("tiling", [0, 2])
+def test_decode_layer_full_parity(big_layer, tiling):
     c = synth.CONFIGS["decode"]
     T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
     gs_i = INTER["decode"]["inter_global_scale"]
     wr = synth.router_weight(0, E, H)
     x = synth.activations(0, T, H)
-    h = make_layer(big_layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T)
+    h = make_layer(big_layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T, gemm_tiling=tiling)
     got = _forward(h, x, T)
     clear, _ = _routing_clear(x, wr, None, k)
     ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, inter_gs=gs_i), x, big_layer,
@@ -248,8 +250,8 @@ def test_w4a16_tiny_layer_short_k():
     _check(got, ora.out, "w4a16 tiny")
 
 
-@pytest.mark.parametrize("T", [64, 1100])
-def test_forward_combine_of_fp16_y_is_exact(big_layer, T):
+@pytest.mark.parametrize("T,tiling", [(64, 0), (1100, 0), (1100, 2)])
+def test_forward_combine_of_fp16_y_is_exact(big_layer, T, tiling):
     """The W4A4 forward's combine (the load-based kernel below 1024 tokens, the bulk-copy one
     from 1024) against a numpy replay from the forward's own fp16 y rows and row scales:
     out[t] = bf16(sum over the token's rows, pairs in top-k order then the shared row, of
@@ -260,7 +262,7 @@ def test_forward_combine_of_fp16_y_is_exact(big_layer, T):
     gs_i = INTER["decode"]["inter_global_scale"]
     wr = synth.router_weight(0, E, H)
     x = synth.activations(5, T, H)
-    h = make_layer(big_layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T)
+    h = make_layer(big_layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T, gemm_tiling=tiling)
     out = torch.zeros((T, H), dtype=torch.int16, device="cuda")
     h.forward(bits16(x), out=out)
     torch.cuda.synchronize()
@@ -282,13 +284,15 @@ def test_forward_combine_of_fp16_y_is_exact(big_layer, T):
     assert np.array_equal(host(out), want)
 
 
-def test_prefill_chunk_sampled_parity(big_layer):
+@pytest.mark.parametrize("tiling", [0, 2])
+def test_prefill_chunk_sampled_parity(big_layer, tiling):
+    """The prefill chunk (the default row blocks, and token tiles), on sampled tokens."""
     c = synth.CONFIGS["prefill"]
     T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
     gs_i = INTER["prefill"]["inter_global_scale"]
     wr = synth.router_weight(0, E, H)
     x = synth.activations(0, T, H, outlier_frac=c["outlier_frac"])
-    h = make_layer(big_layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T)
+    h = make_layer(big_layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T, gemm_tiling=tiling)
     got = _forward(h, x, T)
     clear, _ = _routing_clear(x, wr, None, k)
     tok = np.sort(np.random.default_rng(1).choice(T, 96, replace=False)).astype(np.int32)
@@ -310,13 +314,14 @@ def _dyn_scale_check(h, T, ora):
     assert abs(float(gs) - ora.gs_i) <= 1e-5 * ora.gs_i, (gs, ora.gs_i)
 
 
-def test_tiny_layer_dynamic_intermediate_scale():
+@pytest.mark.parametrize("tiling", [0, 2])
+def test_tiny_layer_dynamic_intermediate_scale(tiling):
     c = synth.CONFIGS["tiny"]
     T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
     layer = build_layer(0, H, I, E)
     wr = synth.router_weight(0, E, H)
     x = synth.activations(0, T, H)
-    h = make_layer(layer, wr, H, I, E, k, inter_gs=0.0, max_tokens=T)
+    h = make_layer(layer, wr, H, I, E, k, inter_gs=0.0, max_tokens=T, gemm_tiling=tiling)
     got = _forward(h, x, T)
     ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, inter_gs=0.0), x, layer, router_w=wr)
     _dyn_scale_check(h, T, ora)
@@ -358,3 +363,58 @@ def test_decode_layer_static_activation_scale(big_layer):
     assert ora.gs_a == np.float32(gs_a)
     _check(got[clear], ora.out[clear], "decode static activation scale")
     _forward_buffers_check(h, T, ora, clear, x, wr)
+
+
+@pytest.mark.parametrize("tiling", [1, 2])
+def test_fp16_y_envelope_heavy_tails_and_small_tokens(big_layer, tiling):
+    """The W4A4 forward keeps the expert outputs y as fp16 rows of y x 2^e_g, 2^e_g from the
+    bound K x 2688^2 / (gs_i gs_w) on |y|.  Heavy tails (1 % of the input channels x200) and
+    tokens whose input is 2^-2, 2^-4 and 2^-6 of the others' (their y rows down to ~2^-26 of
+    the bound: s is about quadratic in the input's scale) stay within the whole-layer bar,
+    each small token also against its own rms."""
+    c = synth.CONFIGS["decode"]
+    T, H, I, E, k = 64, c["H"], c["I"], c["E"], c["k"]
+    gs_i = INTER["decode"]["inter_global_scale"]
+    wr = synth.router_weight(0, E, H)
+    xf = synth.bf16_to_f32(synth.activations(13, T, H, outlier_frac=0.01,
+                                              outlier_scale=200.0)).astype(np.float32)
+    small = {5: 2.0 ** -2, 6: 2.0 ** -4, 7: 2.0 ** -6}
+    for t, f in small.items():
+        xf[t] *= np.float32(f)
+    x = synth.bf16_bits(xf)
+    h = make_layer(big_layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T, gemm_tiling=tiling)
+    got = _forward(h, x, T)
+    clear, _ = _routing_clear(x, wr, None, k)
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, inter_gs=gs_i), x, big_layer,
+                             router_w=wr)
+    _check(got[clear], ora.out[clear], "heavy-tailed input")
+    for t in small:
+        if clear[t]:
+            _check(got[t:t + 1], ora.out[t:t + 1], "token scaled by %g" % small[t])
+
+
+def test_forward_on_host_buffers_matches_the_device_call():
+    """moe_forward_host (x and out in pinned host memory, copies ordered on the stream)
+    gives the device call's output bit for bit; a workspace without room for the copies is
+    refused before anything runs."""
+    c = synth.CONFIGS["tiny"]
+    T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+    gs_i = INTER["tiny"]["inter_global_scale"]
+    layer = build_layer(0, H, I, E)
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(0, T, H)
+    h = make_layer(layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T)
+    want = host(h.forward(bits16(x)))
+    torch.cuda.synchronize()
+    ws = torch.zeros(moe.moe_workspace_size_host(h.cfg, T), dtype=torch.uint8, device="cuda")
+    assert ws.numel() >= h.workspace_bytes(T) + 2 * T * H * 2
+    xh = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
+    oh = torch.zeros((T, H), dtype=torch.int16).pin_memory()
+    for _ in range(2):
+        moe.moe_forward_host(h.handle, xh, None, None, T, oh, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(oh.numpy(), want)
+    small = ws[:h.workspace_bytes(T)]
+    with pytest.raises(moe.MoEError) as err:
+        moe.moe_forward_host(h.handle, xh, None, None, T, oh, small)
+    assert err.value.status == moe.MOE_ERR_WORKSPACE

@@ -295,14 +295,15 @@ class Staged:
         return np.array(out, dtype=np.int64).reshape(-1, 3)
 
 
-def _mid_problem(act_mode, T=200):
+def _mid_problem(act_mode, T=200, tiling=0):
     H, I, E, k = 512, 256, 8, 2
     layer = build_layer(12, H, I, E)
     wr = synth.router_weight(12, E, H)
     x = synth.activations(12, T, H, outlier_frac=0.01)
     lg = synth.logits_normal(12, T, E)
-    lg[:, 3] += 2.5   # one popular expert: > 128 rows -> two row blocks
-    h = make_layer(layer, wr, H, I, E, k, act_mode=act_mode, inter_gs=32.0)
+    lg[:, 3] += 2.5   # one popular expert: > 128 rows at T=200 (> 208 at T=600)
+    h = make_layer(layer, wr, H, I, E, k, act_mode=act_mode, inter_gs=32.0,
+                   gemm_tiling=tiling)
     return layer, wr, x, lg, h, (H, I, E, k, T)
 
 
@@ -350,16 +351,25 @@ def test_gather_w4a16_rows_are_exact_fp16_copies(scale):
 
 # W4A16 runs batches of up to 256 tokens with at most 16 expected rows per expert on the
 # grouped GEMV (T = 60 here: 15 rows per expert) and the others on the tensor-core kernel
-# (T = 100, 200, 300: 32, 64, 64 token rows per tile from T * k / E = 25, 50, 75);
-# W4A4 sizes its activation slots from T (32 rows at T=30, 64 at T=60, 128 at T=200)
-@pytest.mark.parametrize("act_mode,T", [(0, 30), (0, 60), (0, 200), (2, 60), (2, 100),
-                                        (2, 200), (2, 300)])
-def test_grouped_gemm_gateup_unfused_matches_oracle(act_mode, T):
-    layer, wr, x, lg, h, (H, I, E, k, T) = _mid_problem(act_mode, T)
+# (T = 100, 200, 300: 32, 64, 64 token rows per tile from T * k / E = 25, 50, 75).
+# W4A4 runs both GEMM forms (tiling 1: 128-row blocks, activation slots of 32 rows at T=30,
+# 64 at T=60, 128 at T=200; tiling 2: token tiles of up to 208 rows -- one tile with two
+# scale row blocks for the > 128-row group at T=200, three tiles (128 + 128 + rest) for the
+# > 256-row group at T=600)
+W4A4_CASES = [(0, 30, 1), (0, 30, 2), (0, 60, 1), (0, 60, 2), (0, 200, 1), (0, 200, 2),
+              (0, 600, 2)]
+W4A16_CASES = [(2, 60, 0), (2, 100, 0), (2, 200, 0), (2, 300, 0)]
+
+
+@pytest.mark.parametrize("act_mode,T,tiling", W4A4_CASES + W4A16_CASES)
+def test_grouped_gemm_gateup_unfused_matches_oracle(act_mode, T, tiling):
+    layer, wr, x, lg, h, (H, I, E, k, T) = _mid_problem(act_mode, T, tiling)
     st = Staged(h, bits16(x), T, k, lg)
     rows = st.rows()
     if T == 200:
         assert (np.bincount(rows[:, 2], minlength=E + 1) > 128).any()
+    if T == 600:
+        assert (np.bincount(rows[:, 2], minlength=E + 1) > 256).any()
     G = torch.zeros((st.cap, 2 * I), dtype=torch.float32, device="cuda")
     moe.moe_grouped_gemm_gateup(h.handle, st.a_codes, st.a_sf, st.gs, st.a_bf16, st.counts,
                                 st.offsets, 0, G, None, None, None, T, st.ws)
@@ -381,9 +391,10 @@ def test_grouped_gemm_gateup_unfused_matches_oracle(act_mode, T):
         assert np.max(err) <= 2e-5 * scale * np.sqrt(H / 64), (g, np.max(err), scale)
 
 
-@pytest.mark.parametrize("act_mode,T", [(0, 200), (2, 60), (2, 100), (2, 200), (2, 300)])
-def test_grouped_gemm_fused_and_down_match_oracle(act_mode, T):
-    layer, wr, x, lg, h, (H, I, E, k, T) = _mid_problem(act_mode, T)
+@pytest.mark.parametrize("act_mode,T,tiling", [(0, 200, 1), (0, 200, 2), (0, 600, 2)] +
+                         W4A16_CASES)
+def test_grouped_gemm_fused_and_down_match_oracle(act_mode, T, tiling):
+    layer, wr, x, lg, h, (H, I, E, k, T) = _mid_problem(act_mode, T, tiling)
     st = Staged(h, bits16(x), T, k, lg)
     rows = st.rows()
     ic = torch.zeros(st.cap * ((I // 2 + 127) // 128 * 128), dtype=torch.uint8, device="cuda")
@@ -480,16 +491,17 @@ def test_combine_sums_pairs_and_shared(T, H, k):
     assert np.array_equal(host(out), want_bits)
 
 
-def test_grouped_gemms_with_the_dynamic_intermediate_scale():
+@pytest.mark.parametrize("tiling", [1, 2])
+def test_grouped_gemms_with_the_dynamic_intermediate_scale(tiling):
     """Staged gate_up (both passes) and down with inter_global_scale 0: gs_i is 2688 / amax
     of the fp32 intermediate of the computed rows, and the down output matches the oracle's
-    expert MLP quantising the intermediate with that scale."""
+    expert MLP quantising the intermediate with that scale (both GEMM forms)."""
     H, I, E, k, T = 512, 256, 8, 2, 200
     layer = build_layer(12, H, I, E)
     wr = synth.router_weight(12, E, H)
     x = synth.activations(12, T, H, outlier_frac=0.01)
     lg = synth.logits_normal(12, T, E)
-    h = make_layer(layer, wr, H, I, E, k, act_mode=0, inter_gs=0.0)
+    h = make_layer(layer, wr, H, I, E, k, act_mode=0, inter_gs=0.0, gemm_tiling=tiling)
     st = Staged(h, bits16(x), T, k, lg)
     rows = st.rows()
     ic = torch.zeros(st.cap * ((I // 2 + 127) // 128 * 128), dtype=torch.uint8, device="cuda")
