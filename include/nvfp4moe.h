@@ -242,7 +242,8 @@ MOE_API moe_status moe_gather_activations(moe_handle h, const void* x_bf16_d, in
 
 /* Grouped GEMM gate_up over the padded rows: for group g with expert weights W13_g,
  * G = A_g . W13_g^T / (gs_a * gs13_g), A_g the NVFP4 rows (W4A4) or the fp16 rows of
- * moe_gather_activations (W4A16, gs_a its fp16 prescale).
+ * moe_gather_activations (W4A16, gs_a its fp16 prescale).  gs_a_d (a device scalar) is
+ * required in both modes.
  *   fuse_epilogue 0: gateup_f32_d [rows_capacity][2I] fp32 (gate cols 0..I-1, up I..2I-1)
  *   fuse_epilogue 1: s = silu(gate) * up, then
  *       W4A4 : NVFP4 with inter_global_scale -> inter_codes_d / inter_sf_d (tiled, K = I);

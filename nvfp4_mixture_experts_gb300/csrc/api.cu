@@ -939,7 +939,9 @@ moe_status moe_grouped_gemm_gateup(moe_handle h, const uint8_t* a_codes_d,
     const NvtxRange nvtx_range("moe_grouped_gemm_gateup");
     if (!h || !t_ok(h, T) || !expert_counts_d || !expert_offsets_d) return MOE_ERR_INVALID;
     const bool a16 = h->cfg.act_mode == MOE_W4A16;
-    if (a16 ? !a_bf16_d : (!a_codes_d || !a_sf_d || !gs_a_d)) return MOE_ERR_INVALID;
+    // gs_a: the activation global scale (W4A4) or the fp16 prescale (W4A16); both modes
+    // read it on the device
+    if (!gs_a_d || (a16 ? !a_bf16_d : (!a_codes_d || !a_sf_d))) return MOE_ERR_INVALID;
     if (fuse_epilogue) {
         if (a16 ? !inter_bf16_d : (!inter_codes_d || !inter_sf_d)) return MOE_ERR_INVALID;
     } else if (!gateup_f32_d) {

@@ -127,3 +127,4 @@ def test_debug_flavour_builds_and_exports_the_same_symbols():
     dbg = moe.load_debug()
     for n in _declared_functions():
         assert C.cast(getattr(dbg, n), C.c_void_p).value, n
+

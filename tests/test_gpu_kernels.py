@@ -531,3 +531,16 @@ def test_grouped_gemms_with_the_dynamic_intermediate_scale(tiling):
         w = np.where(pair < T * k, wts[np.minimum(pair, T * k - 1)], 1.0)
         rel, mx = within_layer_tolerance(Yg[sel[:, 0]], Y * w[:, None])
         assert rel <= 1e-2 and mx <= 5e-2, (g, rel, mx)
+
+
+@pytest.mark.parametrize("act_mode", [0, 2])
+def test_gateup_refuses_a_missing_activation_scale(act_mode):
+    """gs_a is read on the device in both modes (W4A4: the activation global scale; W4A16:
+    the fp16 prescale), so a null gs_a is refused before anything is launched."""
+    layer, wr, x, lg, h, (H, I, E, k, T) = _mid_problem(act_mode, 60)
+    st = Staged(h, bits16(x), T, k, lg)
+    G = torch.zeros((st.cap, 2 * I), dtype=torch.float32, device="cuda")
+    with pytest.raises(moe.MoEError) as err:
+        moe.moe_grouped_gemm_gateup(h.handle, st.a_codes, st.a_sf, None, st.a_bf16, st.counts,
+                                    st.offsets, 0, G, None, None, None, T, st.ws)
+    assert err.value.status == moe.MOE_ERR_INVALID
