@@ -116,7 +116,9 @@ typedef struct {
                                      blocks, the faster form at every measured size); 1 row
                                      blocks: 128 padded rows x 128 weight rows per MMA tile;
                                      2 token tiles: 128 weight rows x up to 208 token rows of
-                                     one expert (no padding rows in the MMA) */
+                                     one expert (no padding rows in the MMA); 3 row blocks on
+                                     CTA pairs: 256 padded rows x 128 weight rows per pair,
+                                     each CTA streaming half of the weight tile */
 } moe_config;
 
 /* Device pointers, canonical layouts (see above). */

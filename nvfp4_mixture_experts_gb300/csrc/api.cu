@@ -184,6 +184,30 @@ moe_status launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cu
                : MOE_ERR_CUDA;
 }
 
+// As launch, for a kernel whose blocks run as clusters of two (CTA pairs).
+template <typename... KArgs, typename... Args>
+moe_status launch_pairs(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                        bool pdl, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- the handle
@@ -197,6 +221,7 @@ struct moe_layer {
     float* act_gs = nullptr;                   // static activation scale (device copy)
     CUtensorMap tm_router;                     // Wr [E][H] bf16, 64 x 64 boxes
     CUtensorMap tm_router160;                  // Wr [E][H] bf16, 64 x 160 boxes
+    int max_pairs = 0;                         // CTA pairs that can be resident at once
 };
 
 namespace {
@@ -249,7 +274,7 @@ bool valid_cfg(const moe_config* c, moe_status* why)
     if (c->act_mode < 0 || c->act_mode > 2) return false;
     if (c->act_mode == MOE_W4A4_STATIC && !(c->act_global_scale > 0.0f)) return false;
     if (c->act_mode != MOE_W4A16 && !(c->inter_global_scale >= 0.0f)) return false;
-    if (c->gemm_tiling < 0 || c->gemm_tiling > 2) return false;
+    if (c->gemm_tiling < 0 || c->gemm_tiling > 3) return false;
     *why = MOE_ERR_UNSUPPORTED;
     if (c->hidden % 128 || c->inter % 64) return false;
     if (c->num_experts > kMaxExperts || c->top_k > kMaxTopK) return false;
@@ -284,6 +309,9 @@ constexpr int kGemvMaxTokens = 256;
 constexpr int kTokenTileRows = 208;  // token rows per tile at most (gemm_swap.cu)
 
 bool use_token_tiles(const moe_layer* h, int /*T*/) { return h->cfg.gemm_tiling == 2; }
+
+// Row blocks on CTA pairs (gemm_nvf4_pair_kernel): each CTA streams half of every weight tile.
+bool use_pairs(const moe_layer* h, int /*T*/) { return h->cfg.gemm_tiling == 3; }
 
 // Persistent grid: one CTA per SM, or fewer when the tile list (bounded above from the
 // pair count, with row blocks of `rows` rows) is shorter.
@@ -525,9 +553,6 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     const int64_t local_rows = (int64_t)p.T * c.top_k / std::max(1, c.num_local_experts);
     args.staging = (is_down(epilogue) && local_rows >= 16) ? kDownStaging : 0;
     args.rb_cap = p.cap / 128;
-    args.stages = gemm_stages(6, stage_bytes, args.staging, p.G, args.rb_cap);
-    const int smem = gemm_smem_bytes(args.stages, stage_bytes, args.staging, p.G, args.rb_cap);
-    if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
     if (epilogue == kEpiDown &&
         !make_tmap(&tmY, out_f32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, p.cap, (uint64_t)N * 4, 32,
                    32, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -536,6 +561,25 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
         !make_tmap(&tmY, out_f32, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, N, p.cap, (uint64_t)N * 2, 32,
                    32, CU_TENSOR_MAP_SWIZZLE_64B))
         return MOE_ERR_CUDA;
+    if (use_pairs(h, p.T)) {
+        args.stages = kMaxStages;
+        while (args.stages > 2 && gemm_pair_smem_bytes(args.stages, args.staging, p.G,
+                                                       args.rb_cap) > kSmemLimit)
+            --args.stages;
+        const int smem = gemm_pair_smem_bytes(args.stages, args.staging, p.G, args.rb_cap);
+        if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
+        if (!make_tmap(&tmA, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
+                       128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_tmap(&tmA16, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
+                       16, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MOE_ERR_CUDA;
+        const int pairs = std::max(1, std::min(std::min(grid, h->num_sms) / 2, h->max_pairs));
+        return launch_pairs(gemm_nvf4_pair_kernel, dim3(2 * pairs), dim3(kNvf4Threads), smem, s,
+                            pdl, tmA, tmA16, tmY, args);
+    }
+    args.stages = gemm_stages(6, stage_bytes, args.staging, p.G, args.rb_cap);
+    const int smem = gemm_smem_bytes(args.stages, stage_bytes, args.staging, p.G, args.rb_cap);
+    if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
     if (!make_tmap(&tmA, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap(&tmA16, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128, 16,
@@ -830,7 +874,28 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
                               kSmemLimit) == cudaSuccess &&
          cudaFuncSetAttribute(gemm_nvf4_swap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemLimit) == cudaSuccess &&
+         cudaFuncSetAttribute(gemm_nvf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemLimit) == cudaSuccess &&
          set_w4a16_smem_limits();
+    if (ok) {  // how many CTA pairs of the pair kernel fit the GPU at once (its grid)
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(2 * (h->num_sms / 2));
+        lc.blockDim = dim3(kNvf4Threads);
+        lc.dynamicSmemBytes = kSmemLimit;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        lc.attrs = at;
+        lc.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvf4_pair_kernel, &lc) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = h->num_sms / 2;
+        }
+        h->max_pairs = n;
+    }
     if (!ok) {
         cudaGetLastError();
         moe_destroy(h);

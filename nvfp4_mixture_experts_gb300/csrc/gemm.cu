@@ -555,4 +555,361 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
     }
 }
 
+// ============================================================== W4A4 on CTA pairs
+//
+// Two CTAs of a cluster share one 256-row tile: each holds its own 128-row block of an
+// expert group's rows (the MMA's A, 128 of M = 256) and half of the 128-row weight tile (the
+// MMA's B: weight rows 64 r .. 64 r + 63 of CTA r), so each CTA loads and keeps half of the
+// weight bytes the one-CTA kernel does for the same work.  The leader (cluster rank 0) issues
+// tcgen05.mma.cta_group::2 (M = 256, N = 128); each CTA's TMEM receives its own 128 rows x 128
+// weight columns, so the epilogue is the one-CTA kernel's.  Each CTA's TMEM holds its own
+// rows' activation scales and all 128 weight rows' scales (its scale warps write both).
+//
+// Synchronisation across the pair: the leader's MMA thread waits on its ready barrier, which
+// the scale warps of both CTAs arrive on (the peer's remotely, after its stage has landed);
+// its accumulator-empty barrier likewise counts the epilogue warps of both CTAs; the MMA
+// commits arrive on the stage-empty and accumulator-full barriers of both CTAs (multicast).
+// A group with an odd number of row blocks leaves the second CTA's half of its last pair
+// empty (no rows loaded, nothing stored).
+
+struct PairTables {
+    const int32_t* mb_start;  // [G+1]
+    const int32_t* counts;    // [G]
+    const int32_t* offsets;   // [G+1]
+    const int32_t* pb_start;  // [G+1] first pair block of each group
+    const int32_t* pb_group;  // [pair blocks] group of each pair block
+};
+
+__host__ __device__ inline int pair_table_ints(int G, int rb_cap) { return 4 * G + 4 + rb_cap + 32; }
+
+// Builds the pair tables in shared memory (all threads; ends with __syncthreads).
+__device__ __forceinline__ PairTables load_pair_tables(const GemmArgs& a, int32_t* sm)
+{
+    const int G = a.G;
+    int32_t* m = sm;
+    int32_t* c = m + (G + 1);
+    int32_t* o = c + G;
+    int32_t* ps = o + (G + 1);
+    int32_t* pg = ps + (G + 1);
+    int32_t* ws = pg + a.rb_cap;
+    const int nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i <= G; i += nthr) {
+        m[i] = a.mb_start[i];
+        o[i] = a.offsets[i];
+        if (i < G) c[i] = a.counts[i];
+    }
+    __syncthreads();
+    const int per = (G + nthr - 1) / nthr;
+    const int g0 = min(G, tid * per), g1 = min(G, g0 + per);
+    auto npb = [&](int g) {  // pair blocks of group g (its row blocks within the capacity)
+        const int nmb = max(0, min(m[g + 1], a.rb_cap) - max(m[g], 0));
+        return (nmb + 1) >> 1;
+    };
+    int sum = 0;
+    for (int g = g0; g < g1; ++g) sum += npb(g);
+    int v = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += t;
+    }
+    if (lane == 31) ws[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = nthr >> 5;
+        int w = lane < nw ? ws[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, w, d);
+            if (lane >= d) w += t;
+        }
+        if (lane < nw) ws[lane] = w;
+    }
+    __syncthreads();
+    int pre = v - sum + (warp > 0 ? ws[warp - 1] : 0);
+    for (int g = g0; g < g1; ++g) {
+        ps[g] = pre;
+        const int n = npb(g);
+        for (int b = 0; b < n; ++b) pg[pre + b] = g;
+        pre += n;
+    }
+    if (tid == nthr - 1) ps[G] = pre;
+    __syncthreads();
+    PairTables tb;
+    tb.mb_start = m;
+    tb.counts = c;
+    tb.offsets = o;
+    tb.pb_start = ps;
+    tb.pb_group = pg;
+    return tb;
+}
+
+// Pair tile t (groups in order; inside a group, weight tiles in order; inside a weight tile,
+// the group's pair blocks) as seen by the CTA of cluster rank `rank`: its row block is
+// 2 mbp + rank of the group (rows 0 when the group has no such block).
+__device__ __forceinline__ TileInfo decode_pair_tile(const GemmArgs& a, const PairTables& tb,
+                                                     int NB, int t, int rank)
+{
+    const int g = tb.pb_group[t / NB];
+    const int npb = tb.pb_start[g + 1] - tb.pb_start[g];
+    const int local = t - tb.pb_start[g] * NB;
+    const int nb = npb == 1 ? local : local / npb, mbp = npb == 1 ? 0 : local % npb;
+    const int mb = 2 * mbp + rank;
+    const int nmb = max(0, min(tb.mb_start[g + 1], a.rb_cap) - max(tb.mb_start[g], 0));
+    TileInfo ti;
+    ti.g = g;
+    ti.nb = nb;
+    ti.rows = mb < nmb ? min(128, tb.counts[g] - 128 * mb) : 0;
+    ti.arow0 = tb.offsets[g] + 128 * mb;
+    ti.brow0 = g * a.N + 128 * nb;
+    return ti;
+}
+
+__global__ void __launch_bounds__(kNvf4Threads, 1)
+    gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmA16,
+                          const __grid_constant__ CUtensorMap tmY, GemmArgs args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* stages = aligned_smem(smem_raw);
+    const int NS = args.stages;
+    uint8_t* staging = stages + NS * kPairStageBytes;  // epilogue staging (down epilogues)
+    Ctl ctl = carve(staging + args.staging, kMaxStages);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = (int)cluster_ctarank();
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int NB = args.N / 128;
+    const int KB = (args.K + 255) / 256;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&ctl.full[s], 1);
+            mbar_init(&ctl.empty[s], 1);
+            mbar_init(&ctl.ready[s], 8);  // the scale warps of both CTAs (the leader's)
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl.acc_full[b], 1);
+            mbar_init(&ctl.acc_empty[b], 8);  // the epilogue warps of both CTAs (leader's)
+        }
+        mbar_init(ctl.drain, 1);
+        *ctl.abort_flag = 0;
+        *ctl.zero = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmA16);
+    }
+    if (warp == 1) tmem_alloc_pair(ctl.tmem_slot, 512);
+    const PairTables tb = load_pair_tables(args, tables_smem(staging + args.staging));
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before any arrives across the pair
+    tc_fence_after();
+    const uint32_t tmem = *ctl.tmem_slot;
+    const int ntiles = tb.pb_start[args.G] * NB;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+            auto arm = [&](const TileInfo& ti, int nk, uint64_t* bar) {
+                const int nbox = (ti.rows + 15) >> 4;
+                const uint32_t a_bytes = ti.rows == 0 ? 0u : nbox > 4 ? 16384u : (uint32_t)nbox * 2048u;
+                mbar_arrive_expect_tx(bar, a_bytes + 8192u + 2048u + (ti.rows ? 512u * nk : 0u));
+            };
+            auto weights = [&](const TileInfo& ti, int kb, uint8_t* sB, uint64_t* bar) {
+                const uint8_t* blob = args.b_tiles +
+                                      (((size_t)ti.g * NB + ti.nb) * KB + kb) * (size_t)kNvf4TileBytes;
+                bulk_load(sB, blob + rank * 8192, 8192u, bar, pol_w);     // this CTA's 64 rows
+                bulk_load(sB + 8192, blob + 16384, 2048u, bar, pol_w);    // all 128 rows' scales
+            };
+            // the first NS stages' weights (constant) go out before the predecessor is done
+            int i = 0;
+            for (int t = pair; t < ntiles && i < NS; t += npairs) {
+                const TileInfo ti = decode_pair_tile(args, tb, NB, t, rank);
+                for (int kb = 0; kb < KB && i < NS; ++kb, ++i) {
+                    arm(ti, min(4, (args.K - kb * 256) / 64), &ctl.full[i]);
+                    weights(ti, kb, stages + i * kPairStageBytes + 16384, &ctl.full[i]);
+                }
+            }
+            pdl_wait();
+            pdl_trigger();
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            i = 0;
+            for (int t = pair; t < ntiles && ok; t += npairs) {
+                const TileInfo ti = decode_pair_tile(args, tb, NB, t, rank);
+                const int nbox = (ti.rows + 15) >> 4;
+                const bool big = nbox > 4;
+                const uint8_t* sfa = args.a_sf + (size_t)(ti.arow0 >> 7) * (args.K / 64) * 512;
+                for (int kb = 0; kb < KB; ++kb, ++i) {
+                    const int nk = min(4, (args.K - kb * 256) / 64);
+                    uint8_t* sA = stages + stage * kPairStageBytes;
+                    uint8_t* sB = sA + 16384;     // weight codes (64 rows), then all their scales
+                    uint8_t* sSFA = sB + 8192 + 2048;
+                    if (i >= NS) {  // (the first NS stages were armed above)
+                        if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, ctl.abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        arm(ti, nk, &ctl.full[stage]);
+                        weights(ti, kb, sB, &ctl.full[stage]);
+                    }
+                    if (ti.rows) {
+                        if (big) {
+                            tma_load_2d(sA, &tmA, &ctl.full[stage], kb * 128, ti.arow0, pol_a);
+                        } else {
+                            for (int b = 0; b < nbox; ++b)
+                                tma_load_2d(sA + b * 2048, &tmA16, &ctl.full[stage], kb * 128,
+                                            ti.arow0 + 16 * b, pol_a);
+                        }
+                        bulk_load(sSFA, sfa + kb * 2048, 512u * nk, &ctl.full[stage], pol_a);
+                    }
+                    issued |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == NS) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+                *ctl.abort_flag = 1;
+            }
+            for (int s = 0; s < NS; ++s)  // copies in flight land before exit
+                if ((issued >> s) & 1u) mbar_wait(&ctl.full[s], (issued_par >> s) & 1u, ctl.zero);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_nvf4(256, 128);
+            int stage = 0, it = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = pair; t < ntiles && ok; t += npairs, ++it) {
+                const int buf = it & 1;
+                const uint32_t acc_par = (it >> 1) & 1;
+                if (!mbar_wait_cluster(&ctl.acc_empty[buf], acc_par ^ 1u, ctl.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_t = tmem + buf * 128;
+                for (int kb = 0; kb < KB; ++kb) {
+                    // both CTAs' operands in smem and their stage scales in TMEM
+                    if (!mbar_wait_cluster(&ctl.ready[stage], phase, ctl.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nk = min(4, (args.K - kb * 256) / 64);
+                    uint8_t* sA = stages + stage * kPairStageBytes;
+                    uint8_t* sB = sA + 16384;
+                    const uint32_t sfa_t = tmem + 256 + stage * 32, sfb_t = sfa_t + 16;
+                    const uint64_t ad = sdesc_sw128(smem_u32(sA)), bd = sdesc_sw128(smem_u32(sB));
+                    for (int j = 0; j < nk; ++j)
+                        tc_mma_nvf4_pair(d_t, ad + 2 * j, bd + 2 * j, idesc, sfa_t + 4 * j,
+                                         sfb_t + 4 * j, (kb | j) != 0);
+                    tc_commit_pair(&ctl.empty[stage], 3);
+                    if (++stage == NS) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair(&ctl.acc_full[buf], 3);
+            }
+            if (!ok) {
+                set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+                *ctl.abort_flag = 1;
+            }
+            tc_commit_pair(ctl.drain, 1);  // every MMA issued above is complete after this
+            mbar_wait(ctl.drain, 0, ctl.zero);
+        }
+        __syncwarp();
+    } else if (warp >= 6) {
+        // scale warps (one per TMEM lane quarter): this CTA's activation scales and all 128
+        // weight rows' scales of each stage, smem -> registers -> TMEM columns 256 + 32 stage,
+        // then an arrival on the leader's ready barrier
+        const int q = warp & 3;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = pair; t < ntiles && ok; t += npairs) {
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!warp_wait(&ctl.full[stage], phase, ctl.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* sSFB = stages + stage * kPairStageBytes + 16384 + 8192;
+                const uint8_t* sSFA = sSFB + 2048;
+                uint32_t r[32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(sSFA + 512 * j + 16 * lane);
+                    const uint4 b = *reinterpret_cast<const uint4*>(sSFB + 512 * j + 16 * lane);
+                    r[4 * j] = a.x;
+                    r[4 * j + 1] = a.y;
+                    r[4 * j + 2] = a.z;
+                    r[4 * j + 3] = a.w;
+                    r[16 + 4 * j] = b.x;
+                    r[16 + 4 * j + 1] = b.y;
+                    r[16 + 4 * j + 2] = b.z;
+                    r[16 + 4 * j + 3] = b.w;
+                }
+                tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + 256 + stage * 32, r);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(&ctl.ready[stage], 0);
+                if (++stage == NS) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+            *ctl.abort_flag = 1;
+        }
+    } else {
+        const int q = warp & 3;
+        int it = 0, pp = 0;
+        pdl_wait();
+        for (int t = pair; t < ntiles; t += npairs, ++it) {
+            const TileInfo ti = decode_pair_tile(args, tb, NB, t, rank);
+            const EpiPrep ep = epi_prep(args, ti, q, lane);
+            const int buf = it & 1;
+            const uint32_t acc_par = (it >> 1) & 1;
+            if (!warp_wait(&ctl.acc_full[buf], acc_par, ctl.abort_flag)) {
+                if (lane == 0) {
+                    set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+                    *ctl.abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            run_epilogue(args, ti, ep, tmem + buf * 128, q, lane, &tmY,
+                         staging + (warp - 2) * 8192, pp);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(&ctl.acc_empty[buf], 0);
+        }
+        if (lane == 0) bulk_wait_all();  // staged stores complete before the CTA exits
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the leader's MMAs have read this CTA's smem; both CTAs leave together
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
+    }
+}
+
+int gemm_pair_smem_bytes(int stages, int staging, int G, int rb_cap)
+{
+    return stages * kPairStageBytes + staging + 1024 + kCtlBytes + 4 * pair_table_ints(G, rb_cap);
+}
+
 }  // namespace moe

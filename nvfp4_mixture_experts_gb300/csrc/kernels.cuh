@@ -203,6 +203,14 @@ inline int gemm_stages(int want, int stage_bytes, int staging, int G, int rb_cap
 __global__ void gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
                                  const __grid_constant__ CUtensorMap tmA16,
                                  const __grid_constant__ CUtensorMap tmY, GemmArgs args);
+// The same grouped GEMM on CTA pairs (clusters of 2, tcgen05.mma.cta_group::2, M = 256): each
+// CTA holds its own 128-row block and half of the 128-row weight tile.  A stage: activation
+// tile 16 KB, 64 weight rows 8 KB, all 128 weight rows' scales 2 KB, activation scales 2 KB.
+constexpr int kPairStageBytes = 16384 + 8192 + 2048 + 2048;
+__global__ void gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                                      const __grid_constant__ CUtensorMap tmA16,
+                                      const __grid_constant__ CUtensorMap tmY, GemmArgs args);
+int gemm_pair_smem_bytes(int stages, int staging, int G, int rb_cap);
 
 // ---- gemm_swap.cu: W4A4 with weight rows as the MMA's M side and up to kSwNmax token rows
 // of one expert as its N side (many rows per expert).  448 threads: producer, MMA, eight
