@@ -176,14 +176,17 @@ __device__ __forceinline__ void cluster_sync()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Arrive on the mbarrier at the same shared-memory offset in CTA `rank` of the cluster
-// (release at cluster scope: this thread's earlier writes are visible to its waiters).
+// Arrive on the mbarrier at the same shared-memory offset in CTA `rank` of the cluster.  The
+// callers' data is complete before they arrive (TMA transfers their barrier has counted, TMEM
+// stores waited for with tcgen05.wait::st), so the arrive carries only the default release:
+// a cluster-scope release would wait for every outstanding memory operation of the thread
+// and put a cross-SM round trip into every pipeline stage.
 __device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, uint32_t rank)
 {
     asm volatile(
         "{\n\t.reg .b32 ra;\n\t"
         "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
-        "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
+        "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
         "r"(rank)
         : "memory");
 }
