@@ -118,7 +118,9 @@ typedef struct {
                                      2 token tiles: 128 weight rows x up to 208 token rows of
                                      one expert (no padding rows in the MMA); 3 row blocks on
                                      CTA pairs: 256 padded rows x 128 weight rows per pair,
-                                     each CTA streaming half of the weight tile */
+                                     each CTA streaming half of the weight tile; 4 row blocks
+                                     x 256 weight rows per MMA (weight matrices of a multiple of
+                                     256 rows; others take form 1) */
 } moe_config;
 
 /* Device pointers, canonical layouts (see above). */

@@ -17,7 +17,8 @@ MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE, \
     MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_STATUS = range(7)
 MOE_W4A4_DYNAMIC, MOE_W4A4_STATIC, MOE_W4A16 = 0, 1, 2
 MOE_GS_ENCODE, MOE_GS_DEQUANT = 0, 1
-MOE_TILING_AUTO, MOE_TILING_ROWS, MOE_TILING_TOKENS, MOE_TILING_PAIRS = 0, 1, 2, 3
+MOE_TILING_AUTO, MOE_TILING_ROWS, MOE_TILING_TOKENS, MOE_TILING_PAIRS, MOE_TILING_WIDE = \
+    0, 1, 2, 3, 4
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_WAIT_TIMEOUT, MOE_DEV_ROWS_OVERFLOW = 1, 2, 4
 MOE_DEV_BAD_INDEX = 8
 

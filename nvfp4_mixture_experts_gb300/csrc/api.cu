@@ -274,7 +274,7 @@ bool valid_cfg(const moe_config* c, moe_status* why)
     if (c->act_mode < 0 || c->act_mode > 2) return false;
     if (c->act_mode == MOE_W4A4_STATIC && !(c->act_global_scale > 0.0f)) return false;
     if (c->act_mode != MOE_W4A16 && !(c->inter_global_scale >= 0.0f)) return false;
-    if (c->gemm_tiling < 0 || c->gemm_tiling > 3) return false;
+    if (c->gemm_tiling < 0 || c->gemm_tiling > 4) return false;
     *why = MOE_ERR_UNSUPPORTED;
     if (c->hidden % 128 || c->inter % 64) return false;
     if (c->num_experts > kMaxExperts || c->top_k > kMaxTopK) return false;
@@ -312,6 +312,13 @@ bool use_token_tiles(const moe_layer* h, int /*T*/) { return h->cfg.gemm_tiling 
 
 // Row blocks on CTA pairs (gemm_nvf4_pair_kernel): each CTA streams half of every weight tile.
 bool use_pairs(const moe_layer* h, int /*T*/) { return h->cfg.gemm_tiling == 3; }
+
+// Row blocks x 256 weight rows per MMA (gemm_nvf4_wide_kernel), for weight matrices of a
+// multiple of 256 rows.
+bool use_wide(const moe_layer* h, int /*T*/, int N)
+{
+    return h->cfg.gemm_tiling == 4 && N % 256 == 0;
+}
 
 // Persistent grid: one CTA per SM, or fewer when the tile list (bounded above from the
 // pair count, with row blocks of `rows` rows) is shorter.
@@ -561,6 +568,21 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
         !make_tmap(&tmY, out_f32, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, N, p.cap, (uint64_t)N * 2, 32,
                    32, CU_TENSOR_MAP_SWIZZLE_64B))
         return MOE_ERR_CUDA;
+    if (use_wide(h, p.T, N)) {
+        // fp16 y is staged through shared memory (2 KB boxes); fp32 y is stored directly
+        args.staging = (epilogue == kEpiDownF16 && local_rows >= 16) ? kWideDownStaging : 0;
+        args.stages = gemm_stages(5, kWideStageBytes, args.staging, p.G, args.rb_cap);
+        const int smem =
+            gemm_smem_bytes(args.stages, kWideStageBytes, args.staging, p.G, args.rb_cap);
+        if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
+        if (!make_tmap(&tmA, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
+                       128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_tmap(&tmA16, a_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, pitch, p.cap, pitch, 128,
+                       16, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MOE_ERR_CUDA;
+        return launch(gemm_nvf4_wide_kernel, dim3(gemm_grid(h, p.T, N / 2, 128)),
+                      dim3(kWideThreads), smem, s, pdl, tmA, tmA16, tmY, args);
+    }
     if (use_pairs(h, p.T)) {
         args.stages = kMaxStages;
         while (args.stages > 2 && gemm_pair_smem_bytes(args.stages, args.staging, p.G,
@@ -875,6 +897,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
          cudaFuncSetAttribute(gemm_nvf4_swap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemLimit) == cudaSuccess &&
          cudaFuncSetAttribute(gemm_nvf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemLimit) == cudaSuccess &&
+         cudaFuncSetAttribute(gemm_nvf4_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemLimit) == cudaSuccess &&
          set_w4a16_smem_limits();
     if (ok) {  // how many CTA pairs of the pair kernel fit the GPU at once (its grid)

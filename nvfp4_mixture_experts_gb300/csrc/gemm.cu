@@ -163,7 +163,8 @@ __device__ __forceinline__ EpiPrep epi_prep(const GemmArgs& a, const TileInfo& t
 // directly.
 __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& ti,
                                              const EpiPrep& ep, uint32_t tacc, int q, int lane,
-                                             const CUtensorMap* tmY, uint8_t* stg, int& pp)
+                                             const CUtensorMap* tmY, uint8_t* stg, int& pp,
+                                             int stg_stride = 4096)
 {
     if (ep.nvalid == 0) return;
     const bool valid = ep.valid;
@@ -181,7 +182,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const TileInfo& 
         tmem_ld32(tacc + ((uint32_t)(q * 32) << 16) + 32 * c, r);
         tmem_ld_wait();
         if (staged) {
-            uint8_t* buf = stg + pp * 4096;
+            uint8_t* buf = stg + pp * stg_stride;
             if (lane == 0) bulk_wait_read1();  // this buffer's previous store has read it
             __syncwarp();
             if (f16) {  // row lane: 64 bytes, 16-byte piece i at i ^ ((lane >> 1) & 3)
@@ -544,6 +545,281 @@ __global__ void __launch_bounds__(kNvf4Threads, 1)
                              staging + (warp - 2) * 8192, pp);
             tc_fence_before();
             mbar_arrive(&ctl.acc_empty[buf]);
+        }
+        if (lane == 0) bulk_wait_all();  // staged stores complete before the CTA exits
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ============================================================== W4A4 with 256-column tiles
+//
+// The row-block kernel with each MMA covering two weight tiles (N = 256): measured in the
+// row-block kernel, a block-scaled MMA holds its issuing thread about as long at N = 256 as at
+// N = 128, so twice the columns per instruction halve the main loop's time per FLOP.  Two
+// 256-column accumulators would fill TMEM, so there is one, beside the stage scale slots
+// (256 + 48 s: the activation scales, 4 columns per k-step, then the 256 weight rows' scales,
+// 8 columns per k-step); eight epilogue warps (two per TMEM lane quarter, one per weight tile)
+// drain it while the producer and the scale warps fill the next tile's stages.  A stage holds
+// the activation tile, the two weight tiles' codes back to back (the B operand's 256 rows),
+// their scales, and the activation scales.  Tiles: groups in order; inside a group, pairs of
+// weight tiles in order; inside those, the group's row blocks.
+//   warp 0 producer, warp 1 TMEM + MMA, warps 2..9 epilogue, warps 10..13 scale warps
+
+__device__ __forceinline__ TileInfo decode_wide_tile(const GemmArgs& a, const Tables& tb, int NB2,
+                                                     int t)
+{
+    const int g = tb.rb_group[t / NB2];
+    const int nmb = tb.mb_start[g + 1] - tb.mb_start[g];
+    const int local = t - tb.mb_start[g] * NB2;
+    const int nb2 = nmb == 1 ? local : local / nmb, mb = nmb == 1 ? 0 : local % nmb;
+    TileInfo ti;
+    ti.g = g;
+    ti.nb = 2 * nb2;  // the first of the two weight tiles
+    ti.rows = min(128, tb.counts[g] - 128 * mb);
+    ti.arow0 = tb.offsets[g] + 128 * mb;
+    ti.brow0 = g * a.N + 128 * ti.nb;
+    return ti;
+}
+
+__global__ void __launch_bounds__(kWideThreads, 1)
+    gemm_nvf4_wide_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmA16,
+                          const __grid_constant__ CUtensorMap tmY, GemmArgs args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* stages = aligned_smem(smem_raw);
+    const int NS = args.stages;
+    uint8_t* staging = stages + NS * kWideStageBytes;  // epilogue staging (fp16 down)
+    Ctl ctl = carve(staging + args.staging, kMaxStages);
+    const Tables tb = load_tables(args, tables_smem(staging + args.staging));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NB = args.N / 128, NB2 = NB / 2;
+    const int KB = (args.K + 255) / 256;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&ctl.full[s], 1);
+            mbar_init(&ctl.empty[s], 1);
+            mbar_init(&ctl.ready[s], 4);  // one arrival per scale warp
+        }
+        mbar_init(&ctl.acc_full[0], 1);
+        mbar_init(&ctl.acc_empty[0], 8);  // one arrival per epilogue warp
+        mbar_init(ctl.drain, 1);
+        *ctl.abort_flag = 0;
+        *ctl.zero = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmA16);
+    }
+    if (warp == 1) {
+        tmem_alloc(ctl.tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *ctl.tmem_slot;
+    const int ntiles = min(tb.mb_start[args.G], args.rb_cap) * NB2;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+            // the two weight tiles' k-stage blobs: codes back to back, then their scales
+            auto weights = [&](const TileInfo& ti, int kb, uint8_t* sB, uint64_t* bar) {
+                const uint8_t* b0 = args.b_tiles +
+                                    (((size_t)ti.g * NB + ti.nb) * KB + kb) * (size_t)kNvf4TileBytes;
+                const uint8_t* b1 = b0 + (size_t)KB * kNvf4TileBytes;
+                bulk_load(sB, b0, 16384u, bar, pol_w);
+                bulk_load(sB + 16384, b1, 16384u, bar, pol_w);
+                bulk_load(sB + 32768, b0 + 16384, 2048u, bar, pol_w);
+                bulk_load(sB + 34816, b1 + 16384, 2048u, bar, pol_w);
+            };
+            int i = 0;
+            for (int t = blockIdx.x; t < ntiles && i < NS; t += gridDim.x) {
+                const TileInfo ti = decode_wide_tile(args, tb, NB2, t);
+                const int nbox = (ti.rows + 15) >> 4;
+                const uint32_t a_bytes = nbox > 4 ? 16384u : (uint32_t)nbox * 2048u;
+                for (int kb = 0; kb < KB && i < NS; ++kb, ++i) {
+                    const int nk = min(4, (args.K - kb * 256) / 64);
+                    mbar_arrive_expect_tx(&ctl.full[i], a_bytes + 36864u + 512u * nk);
+                    weights(ti, kb, stages + i * kWideStageBytes + 16384, &ctl.full[i]);
+                }
+            }
+            pdl_wait();
+            pdl_trigger();
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            i = 0;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const TileInfo ti = decode_wide_tile(args, tb, NB2, t);
+                const int nbox = (ti.rows + 15) >> 4;
+                const bool big = nbox > 4;
+                const uint32_t a_bytes = big ? 16384u : (uint32_t)nbox * 2048u;
+                const uint8_t* sfa = args.a_sf + (size_t)(ti.arow0 >> 7) * (args.K / 64) * 512;
+                for (int kb = 0; kb < KB; ++kb, ++i) {
+                    const int nk = min(4, (args.K - kb * 256) / 64);
+                    uint8_t* sA = stages + stage * kWideStageBytes;
+                    uint8_t* sB = sA + 16384;
+                    uint8_t* sSFA = sB + 36864;
+                    if (i >= NS) {
+                        if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, ctl.abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&ctl.full[stage], a_bytes + 36864u + 512u * nk);
+                        weights(ti, kb, sB, &ctl.full[stage]);
+                    }
+                    if (big) {
+                        tma_load_2d(sA, &tmA, &ctl.full[stage], kb * 128, ti.arow0, pol_a);
+                    } else {
+                        for (int b = 0; b < nbox; ++b)
+                            tma_load_2d(sA + b * 2048, &tmA16, &ctl.full[stage], kb * 128,
+                                        ti.arow0 + 16 * b, pol_a);
+                    }
+                    bulk_load(sSFA, sfa + kb * 2048, 512u * nk, &ctl.full[stage], pol_a);
+                    issued |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == NS) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+                *ctl.abort_flag = 1;
+            }
+            for (int s = 0; s < NS; ++s)  // copies in flight land before exit
+                if ((issued >> s) & 1u) mbar_wait(&ctl.full[s], (issued_par >> s) & 1u, ctl.zero);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_nvf4(128, 256);
+            int stage = 0, it = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+                if (!mbar_wait(&ctl.acc_empty[0], (it & 1) ^ 1u, ctl.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&ctl.ready[stage], phase, ctl.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nk = min(4, (args.K - kb * 256) / 64);
+                    uint8_t* sA = stages + stage * kWideStageBytes;
+                    uint8_t* sB = sA + 16384;
+                    const uint32_t sfa_t = tmem + 256 + stage * 48, sfb_t = sfa_t + 16;
+                    const uint64_t ad = sdesc_sw128(smem_u32(sA)), bd = sdesc_sw128(smem_u32(sB));
+                    for (int j = 0; j < nk; ++j)
+                        tc_mma_nvf4(tmem, ad + 2 * j, bd + 2 * j, idesc, sfa_t + 4 * j,
+                                    sfb_t + 8 * j, (kb | j) != 0);
+                    tc_commit(&ctl.empty[stage]);
+                    if (++stage == NS) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&ctl.acc_full[0]);
+            }
+            if (!ok) {
+                set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+                *ctl.abort_flag = 1;
+            }
+            tc_commit(ctl.drain);  // every MMA issued above is complete after this
+            mbar_wait(ctl.drain, 0, ctl.zero);
+        }
+        __syncwarp();
+    } else if (warp >= 10) {
+        // scale warps (one per TMEM lane quarter): the stage's activation scales (columns
+        // 256 + 48 s + 4 j + c: rows 32 c + lane) and the 256 weight rows' scales (columns
+        // + 16 + 8 j + c: weight rows 32 c + lane, c < 4 from the first tile's atoms, c >= 4
+        // from the second's)
+        const int q = warp & 3;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!warp_wait(&ctl.full[stage], phase, ctl.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* sSFB = stages + stage * kWideStageBytes + 16384 + 32768;
+                const uint8_t* sSFA = sSFB + 4096;
+                uint32_t ra[16], rb[32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(sSFA + 512 * j + 16 * lane);
+                    const uint4 b0 = *reinterpret_cast<const uint4*>(sSFB + 512 * j + 16 * lane);
+                    const uint4 b1 =
+                        *reinterpret_cast<const uint4*>(sSFB + 2048 + 512 * j + 16 * lane);
+                    ra[4 * j] = a.x;
+                    ra[4 * j + 1] = a.y;
+                    ra[4 * j + 2] = a.z;
+                    ra[4 * j + 3] = a.w;
+                    rb[8 * j] = b0.x;
+                    rb[8 * j + 1] = b0.y;
+                    rb[8 * j + 2] = b0.z;
+                    rb[8 * j + 3] = b0.w;
+                    rb[8 * j + 4] = b1.x;
+                    rb[8 * j + 5] = b1.y;
+                    rb[8 * j + 6] = b1.z;
+                    rb[8 * j + 7] = b1.w;
+                }
+                const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + 256 + stage * 48;
+                tmem_st16(base, ra);
+                tmem_st32(base + 16, rb);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl.ready[stage]);
+                if (++stage == NS) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+            *ctl.abort_flag = 1;
+        }
+    } else {
+        // epilogue: quarter q, weight tile nb + h of the pair (accumulator columns 128 h ..)
+        const int q = warp & 3, h = (warp - 2) >> 2;
+        int it = 0, pp = 0;
+        pdl_wait();
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+            TileInfo ti = decode_wide_tile(args, tb, NB2, t);
+            ti.nb += h;
+            ti.brow0 += 128 * h;
+            const EpiPrep ep = epi_prep(args, ti, q, lane);
+            if (!warp_wait(&ctl.acc_full[0], it & 1, ctl.abort_flag)) {
+                if (lane == 0) {
+                    set_status(args.status, MOE_DEV_WAIT_TIMEOUT);
+                    *ctl.abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            run_epilogue(args, ti, ep, tmem + 128 * h, q, lane, &tmY,
+                         staging + (warp - 2) * 4096, pp, 2048);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.acc_empty[0]);
         }
         if (lane == 0) bulk_wait_all();  // staged stores complete before the CTA exits
     }

@@ -203,6 +203,16 @@ inline int gemm_stages(int want, int stage_bytes, int staging, int G, int rb_cap
 __global__ void gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
                                  const __grid_constant__ CUtensorMap tmA16,
                                  const __grid_constant__ CUtensorMap tmY, GemmArgs args);
+// The row-block grouped GEMM with 256-column tiles (two weight tiles per MMA, one
+// accumulator, eight epilogue warps): 448 threads; a stage holds the activation tile 16 KB,
+// the two weight tiles' codes 32 KB and scales 4 KB, the activation scales 2 KB.  The fp16 down
+// epilogue stages 32 x 32 boxes, two 2 KB buffers per epilogue warp.
+constexpr int kWideThreads = 448;
+constexpr int kWideStageBytes = 16384 + 32768 + 4096 + 2048;
+constexpr int kWideDownStaging = 8 * 2 * 2048;
+__global__ void gemm_nvf4_wide_kernel(const __grid_constant__ CUtensorMap tmA,
+                                      const __grid_constant__ CUtensorMap tmA16,
+                                      const __grid_constant__ CUtensorMap tmY, GemmArgs args);
 // The same grouped GEMM on CTA pairs (clusters of 2, tcgen05.mma.cta_group::2, M = 256): each
 // CTA holds its own 128-row block and half of the 128-row weight tile.  A stage: activation
 // tile 16 KB, 64 weight rows 8 KB, all 128 weight rows' scales 2 KB, activation scales 2 KB.

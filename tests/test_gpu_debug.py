@@ -50,7 +50,7 @@ def _status(lib, h, ws, s):
     return st, bits.value
 
 
-@pytest.mark.parametrize("tiling", [1, 2, 3])
+@pytest.mark.parametrize("tiling", [1, 2, 3, 4])
 def test_debug_build_flags_bad_indices_without_a_trap(dbg, tiling):
     h, cfg, layer, s = _handle(dbg, tiling)
     try:

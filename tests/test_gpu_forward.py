@@ -110,7 +110,7 @@ def _forward_buffers_check(h, T, ora, clear, x, wr, bias=None):
         assert np.array_equal(s[valid], ora.x_sf[tok])
 
 
-@pytest.mark.parametrize("tiling", [0, 2, 3])
+@pytest.mark.parametrize("tiling", [0, 2, 3, 4])
 def test_tiny_layer_full_parity(tiling):
     c = synth.CONFIGS["tiny"]
     T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
@@ -138,7 +138,7 @@ def test_empty_batch_is_a_no_op():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("tiling", [0, 2, 3])
+@pytest.mark.parametrize("tiling", [0, 2, 3, 4])
 def test_decode_layer_full_parity(big_layer, tiling):
     c = synth.CONFIGS["decode"]
     T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
@@ -250,7 +250,7 @@ def test_w4a16_tiny_layer_short_k():
     _check(got, ora.out, "w4a16 tiny")
 
 
-@pytest.mark.parametrize("T,tiling", [(64, 0), (1100, 0), (1100, 2), (1100, 3)])
+@pytest.mark.parametrize("T,tiling", [(64, 0), (1100, 0), (1100, 2), (1100, 3), (1100, 4)])
 def test_forward_combine_of_fp16_y_is_exact(big_layer, T, tiling):
     """The W4A4 forward's combine (the load-based kernel below 1024 tokens, the bulk-copy one
     from 1024) against a numpy replay from the forward's own fp16 y rows and row scales:
@@ -284,10 +284,10 @@ def test_forward_combine_of_fp16_y_is_exact(big_layer, T, tiling):
     assert np.array_equal(host(out), want)
 
 
-@pytest.mark.parametrize("tiling", [0, 2, 3])
+@pytest.mark.parametrize("tiling", [0, 2, 3, 4])
 def test_prefill_chunk_sampled_parity(big_layer, tiling):
-    """The prefill chunk (the default, token tiles, row blocks on CTA pairs), on sampled
-    tokens."""
+    """The prefill chunk (the default, token tiles, row blocks on CTA pairs, 256-column
+    tiles), on sampled tokens."""
     c = synth.CONFIGS["prefill"]
     T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
     gs_i = INTER["prefill"]["inter_global_scale"]
@@ -315,7 +315,7 @@ def _dyn_scale_check(h, T, ora):
     assert abs(float(gs) - ora.gs_i) <= 1e-5 * ora.gs_i, (gs, ora.gs_i)
 
 
-@pytest.mark.parametrize("tiling", [0, 2, 3])
+@pytest.mark.parametrize("tiling", [0, 2, 3, 4])
 def test_tiny_layer_dynamic_intermediate_scale(tiling):
     c = synth.CONFIGS["tiny"]
     T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
@@ -366,7 +366,7 @@ def test_decode_layer_static_activation_scale(big_layer):
     _forward_buffers_check(h, T, ora, clear, x, wr)
 
 
-@pytest.mark.parametrize("tiling", [1, 2, 3])
+@pytest.mark.parametrize("tiling", [1, 2, 3, 4])
 def test_fp16_y_envelope_heavy_tails_and_small_tokens(big_layer, tiling):
     """The W4A4 forward keeps the expert outputs y as fp16 rows of y x 2^e_g, 2^e_g from the
     bound K x 2688^2 / (gs_i gs_w) on |y|.  Heavy tails (1 % of the input channels x200) and

@@ -356,9 +356,11 @@ def test_gather_w4a16_rows_are_exact_fp16_copies(scale):
 # 64 at T=60, 128 at T=200; tiling 2: token tiles of up to 208 rows -- one tile with two
 # scale row blocks for the > 128-row group at T=200, three tiles (128 + 128 + rest) for the
 # > 256-row group at T=600; tiling 3: row blocks on CTA pairs, a group's blocks two at a time,
-# the second CTA of an odd group's last pair empty)
-W4A4_CASES = [(0, 30, 1), (0, 30, 2), (0, 30, 3), (0, 60, 1), (0, 60, 2), (0, 200, 1),
-              (0, 200, 2), (0, 200, 3), (0, 600, 2), (0, 600, 3)]
+# the second CTA of an odd group's last pair empty; tiling 4: row blocks x 256 weight rows
+# per MMA)
+W4A4_CASES = [(0, 30, 1), (0, 30, 2), (0, 30, 3), (0, 30, 4), (0, 60, 1), (0, 60, 2),
+              (0, 200, 1), (0, 200, 2), (0, 200, 3), (0, 200, 4), (0, 600, 2), (0, 600, 3),
+              (0, 600, 4)]
 W4A16_CASES = [(2, 60, 0), (2, 100, 0), (2, 200, 0), (2, 300, 0)]
 
 
@@ -393,7 +395,8 @@ def test_grouped_gemm_gateup_unfused_matches_oracle(act_mode, T, tiling):
 
 
 @pytest.mark.parametrize("act_mode,T,tiling", [(0, 200, 1), (0, 200, 2), (0, 200, 3),
-                                               (0, 600, 2), (0, 600, 3)] + W4A16_CASES)
+                                               (0, 200, 4), (0, 600, 2), (0, 600, 3),
+                                               (0, 600, 4)] + W4A16_CASES)
 def test_grouped_gemm_fused_and_down_match_oracle(act_mode, T, tiling):
     layer, wr, x, lg, h, (H, I, E, k, T) = _mid_problem(act_mode, T, tiling)
     st = Staged(h, bits16(x), T, k, lg)
@@ -492,7 +495,7 @@ def test_combine_sums_pairs_and_shared(T, H, k):
     assert np.array_equal(host(out), want_bits)
 
 
-@pytest.mark.parametrize("tiling", [1, 2, 3])
+@pytest.mark.parametrize("tiling", [1, 2, 3, 4])
 def test_grouped_gemms_with_the_dynamic_intermediate_scale(tiling):
     """Staged gate_up (both passes) and down with inter_global_scale 0: gs_i is 2688 / amax
     of the fp32 intermediate of the computed rows, and the down output matches the oracle's
