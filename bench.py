@@ -225,9 +225,10 @@ def launches_per_forward(c):
     n = (1 if router else 0) + 1           # router logits from x (unless given), top-k
     pairs = c["T"] * c["k"]
     n += 1 if pairs <= 1024 else 3         # grouping: one block, or histogram, scan, scatter
-    # the activation amax is folded into the top-k kernel when the router ran; with given
-    # logits a dynamic (or W4A16) forward runs its own amax pass
-    n += 1 if (c["act_mode"] != 1 and not router) else 0
+    # the activation amax is folded into the top-k kernel when the router ran, or when given
+    # logits fit one top-k block (16 tokens); otherwise a dynamic (or W4A16) forward with
+    # given logits runs its own amax pass
+    n += 1 if (c["act_mode"] != 1 and not router and c["T"] > 16) else 0
     n += 1                                 # gather (NVFP4 quantise, or fp16 copies for W4A16)
     n += 2 if c.get("inter") == "dynamic" else 1   # gate_up (+ the intermediate requant pass)
     n += 2                                 # down + combine

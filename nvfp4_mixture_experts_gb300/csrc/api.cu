@@ -365,8 +365,10 @@ moe_status launch_route(const moe_layer* h, const void* x, const float* logits_i
         if (r != MOE_OK) return r;
         src = logits_scratch;
         clear0 = clear1 = nullptr;  // done by the router
-    } else {
-        amax_out = nullptr;  // nothing clears it before the top-k blocks would fold into it
+    } else if (ceil_div(T, topk_tokens_per_block(1)) > 1) {
+        // given logits and several top-k blocks: nothing would clear the word before the
+        // other blocks fold into it (a single block clears it first itself)
+        amax_out = nullptr;
     }
     if (amax_done) *amax_done = amax_out != nullptr;
     return launch(topk_kernel_for(c.num_experts), dim3(ceil_div(T, topk_tokens_per_block(nsplit))),

@@ -254,6 +254,19 @@ __device__ __forceinline__ void gv_stage_chunk(const GemmArgs& a, const GvSmem& 
     const int S = wpt * 32;   // the row's threads
     const uint16_t* src = xin + (row0 + (act ? t : 0)) * K;
     uint8_t* dst = m.sx + (act ? t : 0) * pitch;
+    // the chunk's output scales are loaded first, so their latency (a dependent pair of loads
+    // for down: the pair index, then its routing weight) overlaps the row staging
+    const bool scl = act && sub == 0 && lane == 0;
+    float gw = 1.0f, sc = 1.0f;
+    if (scl) {
+        gw = a.gs_w[g];
+        if constexpr (kGateUp) {
+            if (t == 0) sc = *a.gs_a;
+        } else {
+            const int pair = a.perm_src[row0 + t];
+            sc = !pair_ok(pair, a.status) ? 0.0f : pair < a.Tk ? a.topk_w[pair] : 1.0f;
+        }
+    }
     float up = 1.0f;  // down: 2^k_t
     if constexpr (!kGateUp) {
         uint32_t mx = 0;  // largest bf16 magnitude (bits), this thread's pieces
@@ -319,14 +332,11 @@ __device__ __forceinline__ void gv_stage_chunk(const GemmArgs& a, const GvSmem& 
                 *reinterpret_cast<uint2*>(d + 8) = hi;
             }
         }
-    if (act && sub == 0 && lane == 0) {
-        const float gw = a.gs_w[g];
+    if (scl) {
         if constexpr (kGateUp) {
-            if (t == 0) m.tscale[2 * kGvTok] = __frcp_rn(__fmul_rn(*a.gs_a, gw));
+            if (t == 0) m.tscale[2 * kGvTok] = __frcp_rn(__fmul_rn(sc, gw));
         } else {
-            const int pair = a.perm_src[row0 + t];
-            const float wn = !pair_ok(pair, a.status) ? 0.0f : pair < a.Tk ? a.topk_w[pair] : 1.0f;
-            m.tscale[kGvTok + t] = __fmul_rn(__frcp_rn(gw), wn);
+            m.tscale[kGvTok + t] = __fmul_rn(__frcp_rn(gw), sc);
         }
     }
     gv_consumer_sync();

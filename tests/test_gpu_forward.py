@@ -419,3 +419,25 @@ def test_forward_on_host_buffers_matches_the_device_call():
     with pytest.raises(moe.MoEError) as err:
         moe.moe_forward_host(h.handle, xh, None, None, T, oh, small)
     assert err.value.status == moe.MOE_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("T", [16, 17])
+def test_given_logits_forward_folds_the_activation_amax(T):
+    """W4A4 with router logits given: at up to 16 tokens one top-k block clears the activation
+    amax word and folds max |x| into it (no separate amax pass); from 17 on a separate pass
+    runs.  Both give the oracle's activation scale exactly and the layer within the bar."""
+    c = synth.CONFIGS["tiny"]
+    H, I, E, k = c["H"], c["I"], c["E"], c["k"]
+    gs_i = INTER["tiny"]["inter_global_scale"]
+    layer = build_layer(0, H, I, E)
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(2, T, H, outlier_frac=0.02)
+    lg = synth.logits_normal(2, T, E)
+    h = make_layer(layer, wr, H, I, E, k, inter_gs=gs_i, max_tokens=T)
+    for _ in range(2):  # twice: the word is cleared by each forward
+        got = _forward(h, x, T, logits_in=lg)
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, inter_gs=gs_i), x, layer,
+                             logits_in=lg)
+    gs = _read_ws(h, moe.moe_forward_buffers(h.handle, h.ws, T)["gs_a"], 1, np.float32)[0]
+    assert float(gs) == ora.gs_a
+    _check(got, ora.out, "given logits, T=%d" % T)
