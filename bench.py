@@ -229,6 +229,8 @@ def launches_per_forward(c):
     # logits fit one top-k block (16 tokens); otherwise a dynamic (or W4A16) forward with
     # given logits runs its own amax pass
     n += 1 if (c["act_mode"] != 1 and not router and c["T"] > 16) else 0
+    if c["act_mode"] == 2 and c["T"] <= W4A16_GEMV_MAX_TOKENS and pairs <= 16 * c["E_loc"]:
+        return n + 2                       # the fused GEMV (gate_up + down, rows from x) + combine
     n += 1                                 # gather (NVFP4 quantise, or fp16 copies for W4A16)
     n += 2 if c.get("inter") == "dynamic" else 1   # gate_up (+ the intermediate requant pass)
     n += 2                                 # down + combine
@@ -436,6 +438,12 @@ def roofline(layer, c, xd, lgd, bd, ws, stream, steps, pk, workload):
     a16 = c["act_mode"] == 2
     P = lambda n: C.c_void_p(b[n])
     times = {"gateup": [], "down": []}
+    if a16:  # the forward's fused GEMV takes its rows from x: the staged calls need the gather
+        st = lib.moe_gather_activations(h, C.c_void_p(xd.data_ptr()), T, P("inv"),
+                                        P("expert_offsets"), None, None, P("a_bf16"), P("gs_a"),
+                                        C.c_void_p(ws.data_ptr()), nbytes, strm)
+        if st:
+            raise RuntimeError("gather failed: %d" % st)
     # steps whose weights fit twice in L2 get an L2 flush before each timed launch
     small = gemm_bytes(c, counts, True)[0] + gemm_bytes(c, counts, False)[0] < L2_FLUSH_BELOW
     flush = L2Flush() if small else None

@@ -81,10 +81,18 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // ---------------------------------------------------------------- workspace plan
 struct Plan {
     int T, k, E, El, G, H, I, cap, nblk, Tk;
+    int gv_list_cap;  // W4A16 grouped GEMV: chunks of up to kGvChunk rows at most
     size_t status, amax, gs_a, gs_i, ids, w, logits, hist, blkoff, counts, offsets, mb_start,
-        perm_src, inv, a_codes, a_sf, a_bf16, i_codes, i_sf, i_bf16, s_f32, y, y_scale, total;
-    // amax holds two words: the activation amax, then the intermediate amax (dynamic gs_i)
+        perm_src, inv, a_codes, a_sf, a_bf16, i_codes, i_sf, i_bf16, s_f32, y, y_scale, gv_sync,
+        gv_part, total;
+    // amax holds two words: the activation amax, then the intermediate amax (dynamic gs_i);
+    // gv_sync: the fused GEMV's ready counts [gv_list_cap]; gv_part: its split partial sums
 };
+
+// W4A16 batches of at most this many tokens (and at most 2 x 8 expected rows per local
+// expert) take the grouped GEMV (gemv_w4a16.cu), which reads each weight once per chunk of
+// 8 rows of a group instead of padding every group to the tensor-core kernel's 128-row MMA.
+constexpr int kGemvMaxTokens = 256;
 
 // W4A4 with inter_global_scale == 0: the intermediate scale is computed per call.
 bool dynamic_inter(const moe_config& c)
@@ -148,6 +156,11 @@ Plan plan(const moe_config& c, int T)
     p.s_f32 = take(dynamic_inter(c) ? (size_t)p.cap * p.I * 4 : 0);
     p.y = take((size_t)p.cap * p.H * 4);  // fp32 (staged calls) or fp16 (W4A4 forward)
     p.y_scale = take((size_t)p.cap * 4);
+    const int64_t rows = (int64_t)T * p.k + ((c.has_shared && c.add_shared) ? T : 0);
+    p.gv_list_cap = (int)std::min<int64_t>(0x7fffffff, p.G + (rows + kGvChunk - 1) / kGvChunk);
+    const bool gemv = a16 && T <= kGemvMaxTokens;
+    p.gv_sync = take(gemv ? (size_t)p.gv_list_cap * 4 : 0);
+    p.gv_part = take(gemv ? (size_t)kGvSplitItems * 128 * kGvChunk * 4 : 0);
     p.total = o;
     return p;
 }
@@ -233,6 +246,9 @@ bool set_w4a16_smem_limits()
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemLimit) != cudaSuccess)
             return false;
+    if (cudaFuncSetAttribute(gemv_w4a16_fused_kernel_ptr(),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess)
+        return false;
     for (int bn : {16, 32, 64})
         for (bool f16 : {false, true})
             if (cudaFuncSetAttribute(w4a16_kernel(bn, f16),
@@ -296,11 +312,6 @@ bool t_ok(const moe_layer* h, int T) { return T >= 0 && T <= h->cfg.max_tokens; 
 
 int grid_for(int64_t threads, int block) { return (int)std::max<int64_t>(1, (threads + block - 1) / block); }
 
-// W4A16 batches of at most this many tokens (and at most 2 x 8 expected rows per local
-// expert) take the grouped GEMV (gemv_w4a16.cu), which reads each weight once per chunk of
-// 8 rows of a group instead of padding every group to the tensor-core kernel's 128-row MMA.
-constexpr int kGemvMaxTokens = 256;
-
 // W4A4 grouped GEMM form: row blocks (gemm.cu) unless the configuration asks for token
 // tiles (gemm_swap.cu).  Measured on the prefill chunk (8192 tokens, ~205 rows per expert):
 // row blocks 1.375 ms per forward (gate_up 690 us, down 440 us), token tiles of up to 208 /
@@ -339,13 +350,15 @@ int shared_rows(const moe_layer* h, int T)
 
 // ---- launch pieces (no argument checks; callers validated)
 
-// amax_out: with the router GEMM (no logits_in), the top-k kernel also folds max |x| into
-// *amax_out (cleared by the router); returns in *amax_done whether it did.
+// amax_out: the top-k kernel also folds max |x| into *amax_out (cleared by the router, or
+// by the single top-k block when logits are given); returns in *amax_done whether it did.
+// zero_words: nzero words the top-k kernel sets to zero (after its wait).
 moe_status launch_route(const moe_layer* h, const void* x, const float* logits_in,
                         const float* bias, int T, int32_t* ids, float* w, float* logits_out,
                         float* logits_scratch, uint32_t* status, uint32_t* clear0,
                         uint32_t* clear1, bool pdl, cudaStream_t s, uint32_t* amax_out = nullptr,
-                        bool* amax_done = nullptr)
+                        bool* amax_done = nullptr, int32_t* zero_words = nullptr,
+                        int nzero = 0)
 {
     const moe_config& c = h->cfg;
     const float* src = logits_in;
@@ -374,7 +387,7 @@ moe_status launch_route(const moe_layer* h, const void* x, const float* logits_i
     return launch(topk_kernel_for(c.num_experts), dim3(ceil_div(T, topk_tokens_per_block(nsplit))),
                   dim3(kTopkThreads), topk_smem(nsplit, c.num_experts), s, pdl, src, nsplit,
                   bias, T, c.num_experts, c.top_k, ids, w, logits_out, clear0, clear1,
-                  static_cast<const uint16_t*>(x), c.hidden, amax_out);
+                  static_cast<const uint16_t*>(x), c.hidden, amax_out, zero_words, nzero);
 }
 
 // write_padding: mark padding rows of perm_src with -1 (the staged call's contract; the
@@ -407,6 +420,16 @@ moe_status launch_permute(const moe_layer* h, const Plan& p, const int32_t* ids,
     return r;
 }
 
+// max |x| over the T x H input into the (zeroed) amax word.
+moe_status launch_amax(const moe_layer* h, const void* x, int T, uint32_t* amax, bool pdl,
+                       cudaStream_t s)
+{
+    const int64_t n = (int64_t)T * h->cfg.hidden;
+    const int blocks = (int)std::min<int64_t>(2 * h->num_sms, std::max<int64_t>(1, n / 2048));
+    return launch(amax_bf16_kernel, dim3(blocks), dim3(256), 0, s, pdl,
+                  static_cast<const uint16_t*>(x), n, amax);
+}
+
 // amax_zeroed: the amax word is zero (no memset); amax_ready: it already holds max |x|
 // (folded by the top-k kernel), so no amax pass runs.
 moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T,
@@ -425,10 +448,7 @@ moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T
     const float* gs_static = nullptr;
     if (c.act_mode != MOE_W4A4_STATIC && !amax_ready) {
         if (!amax_zeroed && cudaMemsetAsync(amax, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
-        const int64_t n = (int64_t)T * c.hidden;
-        const int blocks = (int)std::min<int64_t>(2 * h->num_sms, std::max<int64_t>(1, n / 2048));
-        const moe_status r = launch(amax_bf16_kernel, dim3(blocks), dim3(256), 0, s, pdl, xb, n,
-                                    amax);
+        const moe_status r = launch_amax(h, x, T, amax, pdl, s);
         if (r != MOE_OK) return r;
     } else if (c.act_mode == MOE_W4A4_STATIC) {
         gs_static = h->act_gs;  // the handle's device copy of act_global_scale
@@ -442,6 +462,15 @@ moe_status launch_gather(const moe_layer* h, const Plan& p, const void* x, int T
     return launch(gather_quant_kernel_for(bpl), grid, dim3(256), 0, s, pdl, xb, T, c.hidden,
                   c.top_k, inv, offsets, p.El, add, gs_static, (const uint32_t*)amax, a_codes,
                   a_sf, gs_out, (int64_t)p.cap, at<uint32_t>(ws, p.status));
+}
+
+// The grouped GEMV takes a W4A16 GEMM when the batch is small and the groups' expected rows
+// fit about two chunks (with more rows per group it would decode every weight once per
+// further chunk, while the tensor-core kernel's cost does not grow).
+bool gemv_shape(const moe_layer* h, const Plan& p)
+{
+    return p.T <= kGemvMaxTokens &&
+           (int64_t)p.T * h->cfg.top_k <= 2LL * kGvChunk * std::max(1, p.El);
 }
 
 moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilogue,
@@ -487,13 +516,9 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
     if (a16) {
         // Few token rows per group: the CUDA-core GEMV reads each weight once per chunk of
         // kGvChunk rows, where a 128-row MMA per 16 k would be mostly padding.
-        const int64_t rows = (int64_t)p.T * c.top_k + shared_rows(h, p.T);
-        const int list_cap = (int)(p.G + (rows + kGvChunk - 1) / kGvChunk);
+        const int list_cap = p.gv_list_cap;
         const int slots = gemv_w4a16_slots(K, list_cap);
-        // (and only while the expected rows per local expert fit about two chunks: with
-        // more, the GEMV would decode every weight once per further chunk)
-        const bool few_rows = (int64_t)p.T * c.top_k <= 2LL * kGvChunk * std::max(1, p.El);
-        if (p.T <= kGemvMaxTokens && few_rows && epilogue != kEpiGateUpSwigluF32 && slots >= 4) {
+        if (gemv_shape(h, p) && epilogue != kEpiGateUpSwigluF32 && slots >= 4) {
             const size_t gsm = gemv_w4a16_smem(K, slots, list_cap);
             const int64_t items = (int64_t)list_cap * (N / 128);
             const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(h->num_sms, items));
@@ -611,6 +636,62 @@ moe_status launch_gemm(const moe_layer* h, const Plan& p, bool gateup, int epilo
         return MOE_ERR_CUDA;
     return launch(gemm_nvf4_kernel, dim3(grid), dim3(kNvf4Threads), smem, s, pdl, tmA, tmA16,
                   tmY, args);
+}
+
+// Ring slots of the fused W4A16 GEMV (gemv_w4a16_fused_kernel: the forward's gate_up and
+// down in one launch) for this forward, or 0 when the forward runs them as separate kernels.
+int fused_gemv_slots(const moe_layer* h, const Plan& p)
+{
+    const moe_config& c = h->cfg;
+    if (c.act_mode != MOE_W4A16 || p.T < 1 || !gemv_shape(h, p)) return 0;
+    const int slots = gemv_w4a16_fused_slots(c.hidden, std::min(kGvChunk, p.T), p.gv_list_cap);
+    return slots >= 4 ? slots : 0;
+}
+
+// The fused W4A16 GEMV: activation rows from x (prescaled by max |x| in the workspace), the
+// intermediate into i_bf16, the weighted expert outputs into y (fp32 rows).  The ready counts
+// (gv_sync) were zeroed by the routing kernel of the same forward.
+moe_status launch_gemv_fused(const moe_layer* h, const Plan& p, const void* x, void* ws,
+                             int slots, bool pdl, cudaStream_t s)
+{
+    const moe_config& c = h->cfg;
+    GvFusedArgs f;
+    memset(&f, 0, sizeof(f));
+    for (GemmArgs* a : {&f.gu, &f.dn}) {
+        a->counts = at<int32_t>(ws, p.counts);
+        a->offsets = at<int32_t>(ws, p.offsets);
+        a->G = p.G;
+        a->perm_src = at<int32_t>(ws, p.perm_src);
+        a->Tk = p.Tk;
+        a->status = at<uint32_t>(ws, p.status);
+    }
+    f.gu.b_tiles = h->w13;
+    f.gu.gs_w = h->gs13;
+    f.gu.N = 2 * c.inter;
+    f.gu.K = c.hidden;
+    f.gu.epilogue = kEpiGateUpSwiglu;
+    f.gu.out_bf16 = at<uint16_t>(ws, p.i_bf16);
+    f.dn.b_tiles = h->w2;
+    f.dn.gs_w = h->gs2;
+    f.dn.N = c.hidden;
+    f.dn.K = c.inter;
+    f.dn.epilogue = kEpiDown;
+    f.dn.out_f32 = at<float>(ws, p.y);
+    f.dn.topk_w = at<float>(ws, p.w);
+    f.x = static_cast<const uint16_t*>(x);
+    f.amax = at<uint32_t>(ws, p.amax);
+    f.gs_out = at<float>(ws, p.gs_a);
+    f.T = p.T;
+    f.k = p.k;
+    f.tok_rows = std::min(kGvChunk, p.T);
+    f.ready = at<int32_t>(ws, p.gv_sync);
+    f.part = at<float>(ws, p.gv_part);
+    const int64_t items =
+        (int64_t)p.gv_list_cap * ((2 * c.inter / 128) * kGvMaxSplit + c.hidden / 128);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(h->num_sms, items));
+    return launch(gemv_w4a16_fused_kernel_ptr(), dim3(grid), dim3(kGvFusedThreads),
+                  gemv_w4a16_fused_smem(c.hidden, f.tok_rows, slots, p.gv_list_cap), s, pdl, f,
+                  p.gv_list_cap, slots);
 }
 
 }  // namespace
@@ -1166,11 +1247,22 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
     uint32_t* amax = at<uint32_t>(ws, p.amax);
     const bool need_amax = h->cfg.act_mode != MOE_W4A4_STATIC;
     bool amax_done = false;
+    // W4A16 batches of a few tokens: gate_up and down in one GEMV launch that takes the
+    // activation rows from x itself (no gather); the routing kernel zeroes its counters
+    const int fused_slots = fused_gemv_slots(h, p);
     moe_status r = launch_route(h, x_bf16_d, logits_in_d, logit_bias_d, T, ids, w, nullptr,
                                 at<float>(ws, p.logits), status, status, amax, true, s,
-                                need_amax ? amax : nullptr, &amax_done);
+                                need_amax ? amax : nullptr, &amax_done,
+                                fused_slots ? at<int32_t>(ws, p.gv_sync) : nullptr,
+                                fused_slots ? p.gv_list_cap : 0);
     if (r == MOE_OK)
         r = launch_permute(h, p, ids, T, counts, offsets, perm_src, inv, ws, true, s, false);
+    if (fused_slots) {
+        if (r == MOE_OK && !amax_done) r = launch_amax(h, x_bf16_d, T, amax, true, s);
+        if (r == MOE_OK) r = launch_gemv_fused(h, p, x_bf16_d, ws, fused_slots, true, s);
+        if (r == MOE_OK) r = launch_combine(h, y, inv, offsets, T, out_bf16_d, true, s, status);
+        return r;
+    }
     if (r == MOE_OK)
         r = launch_gather(h, p, x_bf16_d, T, inv, offsets, a_codes, a_sf, a_bf16, gs_a, ws, true,
                           true, s, amax_done);
@@ -1296,7 +1388,7 @@ moe_status moe_route_topk_noalloc(moe_handle h, const void* x_bf16_d,
                           topk_smem(nsplit, c.num_experts), s, false, src, nsplit, logit_bias_d,
                           (int)T, c.num_experts, c.top_k, topk_ids_d, topk_w_d, logits_out_d,
                           (uint32_t*)nullptr, (uint32_t*)nullptr, (const uint16_t*)nullptr, 0,
-                          (uint32_t*)nullptr);
+                          (uint32_t*)nullptr, (int32_t*)nullptr, 0);
     if (r == MOE_OK && status) {
         const int n = T * c.top_k;
         r = launch(route_invalidate_kernel, dim3(std::min(grid_for(n, 256), 4 * h->num_sms)),

@@ -36,6 +36,22 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits)
     if (status) atomicOr(status, bits);
 }
 
+// Adds v to *p with release semantics at GPU scope: writes this thread has made, or has
+// observed (through a block barrier it passed), are visible to a thread that sees the sum.
+__device__ __forceinline__ void red_release_gpu(int32_t* p, int v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// A 32-bit load with acquire semantics at GPU scope: reads that follow it in this thread see
+// the writes released (a fence, then an atomic) by the thread whose value it observed.
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Programmatic dependent launch.  The forward's kernels are launched so that each may start
 // while its predecessor finishes.  pdl_wait() blocks the calling thread until the preceding
 // kernel has completed and its writes are visible (a no-op without the launch attribute);

@@ -195,6 +195,7 @@ struct GvSmem {
     volatile int* abort_flag;
     int* zero;
     int* n;
+    volatile int* done;  // fused kernel: gate_up items whose stores are complete (consumers)
     int* list;
 };
 
@@ -202,28 +203,77 @@ struct GvSmem {
 // sums need not wait for this item's epilogue; one otherwise, leaving the ring its space.
 __host__ __device__ __forceinline__ int gv_nred(int K) { return (K + 255) / 256 <= 8 ? 2 : 1; }
 
+// Bytes of sx for `rows` staged rows, rounded up to 128 so that the buffers after it start
+// 16-byte aligned.
+__host__ __device__ __forceinline__ size_t gv_sx_bytes(int rows, int pitch)
+{
+    return ((size_t)rows * pitch + 127) / 128 * 128;
+}
+
 __host__ __device__ __forceinline__ size_t gv_fixed_bytes(int K)
 {
     const int nred = gv_nred(K);
-    return (size_t)kGvTok * gv_row_pitch((K + 255) / 256) + nred * kGvConsumers * 32 * kGvTok * 4 +
-           kGvScales * 4 + 2 * kGvMaxSlots * 8 + 16;
+    return gv_sx_bytes(kGvTok, gv_row_pitch((K + 255) / 256)) +
+           nred * kGvConsumers * 32 * kGvTok * 4 + kGvScales * 4 + 2 * kGvMaxSlots * 8 + 16;
 }
 
-__device__ __forceinline__ GvSmem gv_carve(uint8_t* base, int K, int slots)
+// ring | sx (sx_bytes: the staged activation rows) | nred partial-sum buffers | scales |
+// barriers | flags | work list
+__device__ __forceinline__ GvSmem gv_carve(uint8_t* base, size_t sx_bytes, int nred, int slots)
 {
-    const int nred = gv_nred(K);
     GvSmem m;
     m.ring = base;
     m.sx = m.ring + (size_t)slots * kNvf4TileBytes;
-    m.red = reinterpret_cast<float*>(m.sx + (size_t)kGvTok * gv_row_pitch((K + 255) / 256));
+    m.red = reinterpret_cast<float*>(m.sx + sx_bytes);  // sx_bytes from gv_sx_bytes
     m.tscale = m.red + nred * kGvConsumers * 32 * kGvTok;
     m.full = reinterpret_cast<uint64_t*>(m.tscale + kGvScales);
     m.empty = m.full + kGvMaxSlots;
     m.abort_flag = reinterpret_cast<volatile int*>(m.empty + kGvMaxSlots);
     m.zero = const_cast<int*>(m.abort_flag + 1);
     m.n = m.zero + 1;
+    m.done = m.n + 1;
     m.list = m.n + 2;
     return m;
+}
+
+// The work list: the chunks of up to kGvTok rows of the non-empty groups, in group order,
+// each (group << 16) | first row; *m.n = their number.  Called by warp 0.  Each lane takes a
+// contiguous range of groups and loads their counts 16 at a time (one load latency for up to
+// 512 groups) into tmp, then a warp scan places the lanes' chunks.
+__device__ __forceinline__ void gv_build_list(const GemmArgs& a, const GvSmem& m, int list_cap,
+                                              int* tmp)
+{
+    const int lane = threadIdx.x & 31;
+    const int per = (a.G + 31) / 32;
+    const int gb = lane * per, ge = min(a.G, gb + per);
+    int nc = 0;  // chunks of this lane's groups
+    for (int g0 = gb; g0 < ge; g0 += 16) {
+        int c[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) c[j] = g0 + j < ge ? a.counts[g0 + j] : 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (g0 + j < ge) {
+                c[j] = max(c[j], 0);
+                tmp[g0 + j] = c[j];
+                nc += (c[j] + kGvTok - 1) / kGvTok;
+            }
+    }
+    int incl = nc;  // inclusive scan of the chunk counts over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const int n = __shfl_sync(0xffffffffu, incl, 31);
+    int slot = incl - nc;
+    for (int g = gb; g < ge; ++g)
+        for (int r = 0; r < tmp[g]; r += kGvTok, ++slot)
+            if (slot < list_cap) m.list[slot] = (g << 16) | r;
+    if (lane == 0) {
+        if (n > list_cap) set_status(a.status, MOE_DEV_ROWS_OVERFLOW);
+        *m.n = min(n, list_cap);
+    }
 }
 
 // bf16 pair -> two floats times `up`, rounded to an fp16 pair.
@@ -241,19 +291,48 @@ __device__ __forceinline__ uint32_t gv_bf16x2_to_f16x2(uint32_t u, float up)
 // and every 8-element group is stored in the blobs' nibble order 0,2,4,6,1,3,5,7.  Also the
 // chunk's output scales: 2^-k_t, and rcp(gs_w) x the routing weight per row (down) or
 // 1 / (gs_a gs_w) (gate_up).  Ends with the staged data visible to every consumer.
-template <bool kGateUp>
+// kSrc: where row t of the chunk comes from -- kGvSrcRows: row row0 + t of xin;
+// kGvSrcRowsL2: the same through L2 (ld.global.cg: rows written earlier in the same launch);
+// kGvSrcTokens (gate_up): the layer input row of the row's token (from perm_src: pair / k,
+// or pair - T k for a shared row) in bf16, times the prescale gs, rounded to fp16 -- the row
+// the gather kernel would have written; kGvSrcSmem: row t of xin in shared memory.
+constexpr int kGvSrcRows = 0, kGvSrcRowsL2 = 1, kGvSrcTokens = 2, kGvSrcSmem = 3;
+template <bool kGateUp, int kSrc = kGvSrcRows>
 __device__ __forceinline__ void gv_stage_chunk(const GemmArgs& a, const GvSmem& m,
                                                const uint16_t* xin, int64_t row0, int nt,
-                                               int g, int K, int KB, int pitch)
+                                               int g, int K, int KB, int pitch, int T = 0,
+                                               int k = 1, float gs = 1.0f)
 {
+    static_assert(kSrc != kGvSrcTokens || kGateUp, "token rows are gate_up's input");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wpt = nt <= 1 ? 16 : nt <= 2 ? 8 : nt <= 4 ? 4 : 2;
     const int t = warp / wpt, sub = warp % wpt;
     const bool act = t < nt;
     const int npc = KB * 32;  // 8-element pieces of a staged row
     const int S = wpt * 32;   // the row's threads
-    const uint16_t* src = xin + (row0 + (act ? t : 0)) * K;
+    int64_t srow = (kSrc == kGvSrcSmem ? 0 : row0) + (act ? t : 0);
+    bool rd = act;  // the row has a source (else it is staged as zeros)
+    if constexpr (kSrc == kGvSrcTokens) {
+        srow = 0;
+        if (act) {
+            const int pair = a.perm_src[row0 + t];
+            const int tok = pair >= a.Tk ? pair - a.Tk : pair / k;
+            if (pair < 0 || tok >= T) {  // not a row of this batch
+                if (sub == 0 && lane == 0) set_status(a.status, MOE_DEV_BAD_INDEX);
+                rd = false;
+            } else {
+                srow = tok;
+            }
+        }
+    }
+    const uint16_t* src = xin + srow * K;
     uint8_t* dst = m.sx + (act ? t : 0) * pitch;
+    auto ld16 = [](const uint16_t* q) {
+        if constexpr (kSrc == kGvSrcRowsL2)
+            return __ldcg(reinterpret_cast<const uint4*>(q));
+        else
+            return *reinterpret_cast<const uint4*>(q);
+    };
     // the chunk's output scales are loaded first, so their latency (a dependent pair of loads
     // for down: the pair index, then its routing weight) overlaps the row staging
     const bool scl = act && sub == 0 && lane == 0;
@@ -261,7 +340,7 @@ __device__ __forceinline__ void gv_stage_chunk(const GemmArgs& a, const GvSmem& 
     if (scl) {
         gw = a.gs_w[g];
         if constexpr (kGateUp) {
-            if (t == 0) sc = *a.gs_a;
+            if (t == 0) sc = kSrc == kGvSrcTokens ? gs : *a.gs_a;
         } else {
             const int pair = a.perm_src[row0 + t];
             sc = !pair_ok(pair, a.status) ? 0.0f : pair < a.Tk ? a.topk_w[pair] : 1.0f;
@@ -276,8 +355,7 @@ __device__ __forceinline__ void gv_stage_chunk(const GemmArgs& a, const GvSmem& 
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int p = p0 + j * S;
-                    q[j] = (p < npc && 8 * p < K) ? *reinterpret_cast<const uint4*>(src + 8 * p)
-                                                  : make_uint4(0, 0, 0, 0);
+                    q[j] = (rd && p < npc && 8 * p < K) ? ld16(src + 8 * p) : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -307,15 +385,17 @@ __device__ __forceinline__ void gv_stage_chunk(const GemmArgs& a, const GvSmem& 
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int p = p0 + j * S;
-                q[j] = (p < npc && 8 * p < K) ? *reinterpret_cast<const uint4*>(src + 8 * p)
-                                              : make_uint4(0, 0, 0, 0);
+                q[j] = (rd && p < npc && 8 * p < K) ? ld16(src + 8 * p) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int p = p0 + j * S;
                 if (p >= npc) break;
                 uint2 lo, hi;  // elements (0..3, 4..7), or (0,2,4,6), (1,3,5,7) for down
-                if constexpr (kGateUp) {
+                if constexpr (kSrc == kGvSrcTokens) {
+                    lo = make_uint2(gv_bf16x2_to_f16x2(q[j].x, gs), gv_bf16x2_to_f16x2(q[j].y, gs));
+                    hi = make_uint2(gv_bf16x2_to_f16x2(q[j].z, gs), gv_bf16x2_to_f16x2(q[j].w, gs));
+                } else if constexpr (kGateUp) {
                     lo = make_uint2(q[j].x, q[j].y);
                     hi = make_uint2(q[j].z, q[j].w);
                 } else {
@@ -343,7 +423,8 @@ __device__ __forceinline__ void gv_stage_chunk(const GemmArgs& a, const GvSmem& 
 }
 
 // The k-slots' partials of tile nb summed, scaled and stored by the consumer threads.
-template <bool kGateUp>
+// kNks: partial-sum sets in red (the k-step warps' 4, or 1 already summed).
+template <bool kGateUp, int kNks = kGvKsteps>
 __device__ __forceinline__ void gv_epilogue(const GemmArgs& a, const GvSmem& m,
                                             const float* red, int64_t row0, int nt, int nb)
 {
@@ -359,7 +440,7 @@ __device__ __forceinline__ void gv_epilogue(const GemmArgs& a, const GvSmem& m,
             const int u = j >> 4, fi = j & 15;
             float vg = 0.0f, vu = 0.0f;
 #pragma unroll
-            for (int s = 0; s < kGvKsteps; ++s) {
+            for (int s = 0; s < kNks; ++s) {
                 const float* rw = red + (s * kGvUnits + u) * 32 * kGvTok;
                 vg += rw[fi * kGvTok + t];
                 vu += rw[(16 + fi) * kGvTok + t];
@@ -417,8 +498,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     extern __shared__ __align__(128) uint8_t gv_smem[];
     const int K = a.K, KB = (K + 255) / 256, NB = a.N / 128;
     const int pitch = gv_row_pitch(KB);
-    const GvSmem m = gv_carve(gv_smem, K, slots);
     const int nred = gv_nred(K);
+    const GvSmem m = gv_carve(gv_smem, gv_sx_bytes(kGvTok, pitch), nred, slots);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < slots; ++i) {
@@ -434,39 +515,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     // lets the next one start, see pdl_wait), and the weights are constant: the work list
     // and the weight stream go ahead of the wait, which only the consumers (reading the
     // predecessor's activation rows) take.
-    if (warp == 0) {
-        // chunks of the non-empty groups, in group order; the counts 256 at a time, so one
-        // load latency per 256 groups
-        int n = 0;
-        for (int g0 = 0; g0 < a.G; g0 += 256) {
-            int cnt[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int g = g0 + 32 * j + lane;
-                cnt[j] = g < a.G ? a.counts[g] : 0;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int g = g0 + 32 * j + lane;
-                const int nc = (cnt[j] + kGvTok - 1) / kGvTok;
-                int incl = nc;  // inclusive scan of the chunk counts over the warp
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += v;
-                }
-                for (int c = 0; c < nc; ++c) {
-                    const int slot = n + incl - nc + c;
-                    if (slot < list_cap) m.list[slot] = (g << 16) | (c * kGvTok);
-                }
-                n += __shfl_sync(0xffffffffu, incl, 31);
-            }
-        }
-        if (lane == 0) {
-            if (n > list_cap) set_status(a.status, MOE_DEV_ROWS_OVERFLOW);
-            *m.n = min(n, list_cap);
-        }
-    }
+    if (warp == 0) gv_build_list(a, m, list_cap, reinterpret_cast<int*>(m.red));
     __syncthreads();
     // items: (chunk, 128-row tile), chunk-major; a block takes a contiguous run of them
     const int nitems = *m.n * NB;
@@ -576,6 +625,395 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         if (ok) gv_epilogue<kGateUp>(a, m, redb, row0, nt, nb);
     }
 }
+
+// ---------------------------------------------------------------- fused gate_up + down
+//
+// The forward's two grouped GEMVs in one launch, for batches of a few tokens.  With one
+// token the layer streams about 80 MB of weights in a few microseconds, and what two launches
+// cost is their seams: the down launch's blocks cannot start until the gate_up blocks leave
+// (each holds most of an SM's shared memory), then rebuild the work list and refill the ring,
+// all while the stream is idle.  Here each block's copy warp streams its gate_up blobs and
+// then its down blobs without a break, and a down item waits only for its own chunk: the
+// chunk's intermediate rows are complete when all N1 / 128 of its gate_up tiles have been
+// stored (ready[chunk] counts them: a block barrier after the stores, then one release add;
+// the reader polls with acquire loads).  The activation rows are taken from the layer input
+// directly (the gather kernel's fp16 rows x * gs, formed while staging).
+//
+// Few items: with one token the gate_up work is 9 chunks x 20 tiles = 180 items of 16 blobs
+// on 152 SMs, and the SMs with two set the pace.  So when there are few items the contraction
+// of each tile is cut into S parts (items of 16 / S blobs); each part stores its partial sums
+// (fp32, 128 rows per token) and counts itself in ready[chunk], and the down stager of the
+// chunk adds the S parts in the order of their k ranges and applies the gate_up epilogue's
+// scale and SwiGLU (so the result does not depend on the order the parts finished in).
+//
+// Items: gate_up (chunk, tile, part), then down (chunk, tile), each list split evenly over the
+// blocks in contiguous runs; a block takes its gate_up run, then its down run backwards
+// (GvCursor).  Warps: 16
+// consumers, a copy warp, and a signal warp that publishes the finished gate_up items (a
+// release add waits for the stores to land; the consumers go on meanwhile).  Every block
+// is resident at once (one block per SM, grid <= SMs), so every wait ends; each wait is
+// bounded all the same, and one that runs out sets MOE_DEV_WAIT_TIMEOUT and stops the
+// block's work.  The ready words are zeroed before the launch by the routing kernel.
+__device__ __forceinline__ bool gv_wait_count(const int32_t* p, int target, volatile int* abort)
+{
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        __nanosleep(100);
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// After the consumers' stores of gate_up item `it` (a tile or a part): the barrier orders every
+// consumer's stores before thread 0's release of the block's count of finished items, which
+// the signal warp turns into release adds on the chunks' ready words (so no consumer waits
+// for its stores to land).
+__device__ __forceinline__ void gv_item_done(const GvSmem& m, int it)
+{
+    gv_consumer_sync();
+    if (threadIdx.x == 0) {
+        __threadfence_block();
+        *m.done = it + 1;
+    }
+}
+
+// Split gate_up tiles: the chunk's intermediate rows from its parts' partial sums (part
+// [tile][s][token][128 rows], s in k order), as the gate_up epilogue would form them: gate and
+// up sums times alpha = 1 / (gs gs_w), SwiGLU, rounded to bf16 -> rows t < nt of dst (shared
+// memory, I per row).  Each thread takes 4 features (adjacent gate rows, and their up rows).
+__device__ __forceinline__ void gv_split_rows(const float* part, int ci, int NBg, int S, int nt,
+                                              int I, float alpha, uint16_t* dst)
+{
+    const int q4 = I / 4;
+    for (int e = threadIdx.x; e < nt * q4; e += kGvConsumers * 32) {
+        const int t = e / q4, f0 = 4 * (e % q4);
+        const int nb = f0 / 64, j = f0 % 64, u = j / 16, fi = j % 16;
+        const float* base = part + (size_t)(ci * NBg + nb) * S * (128 * kGvTok) + t * 128 + u * 32 + fi;
+        float4 vg = make_float4(0.f, 0.f, 0.f, 0.f), vu = vg;
+        for (int q = 0; q < S; ++q) {
+            const float4 pg = __ldcg(reinterpret_cast<const float4*>(base + (size_t)q * (128 * kGvTok)));
+            const float4 pu = __ldcg(reinterpret_cast<const float4*>(base + (size_t)q * (128 * kGvTok) + 16));
+            vg.x += pg.x; vg.y += pg.y; vg.z += pg.z; vg.w += pg.w;
+            vu.x += pu.x; vu.y += pu.y; vu.z += pu.z; vu.w += pu.w;
+        }
+        const float g4[4] = {vg.x, vg.y, vg.z, vg.w}, u4[4] = {vu.x, vu.y, vu.z, vu.w};
+        uint16_t* o = dst + t * I + f0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = __bfloat16_as_ushort(__float2bfloat16_rn(
+                silu_mul(__fmul_rn(g4[i], alpha), __fmul_rn(u4[i], alpha))));
+    }
+}
+
+// A block's items in order, decoded one step at a time: its gate_up run ascending (chunk,
+// tile, part), then its down run descending (chunk, tile).  Descending, because the runs are
+// contiguous and chunk-major: the block's first down chunk is then its last gate_up chunk,
+// whose other tiles the next block took first -- complete as soon as this block's own
+// gate_up run is -- while the chunk it shares with the previous block (finished last there)
+// comes last.
+struct GvCursor {
+    int ci, nb, s;  // the current item: chunk, tile, part
+    bool isg;       // gate_up (else down)
+    int left;       // gate_up items left, the current one included
+    int S, NBg, NBd, d1;
+    __device__ __forceinline__ void init(int u0, int nu, int d1_, int S_, int NBg_, int NBd_)
+    {
+        S = S_;
+        NBg = NBg_;
+        NBd = NBd_;
+        d1 = d1_;
+        left = nu;
+        if (nu > 0) {
+            isg = true;
+            ci = u0 / (NBg * S);
+            nb = (u0 / S) % NBg;
+            s = u0 % S;
+        } else {
+            to_down();
+        }
+    }
+    __device__ __forceinline__ void to_down()
+    {
+        isg = false;
+        s = 0;
+        ci = (d1 - 1) / NBd;  // (d1 - 1 < 0 only when the run is empty: never read)
+        nb = (d1 - 1) % NBd;
+    }
+    __device__ __forceinline__ void next()
+    {
+        if (isg) {
+            if (--left == 0) {
+                to_down();
+            } else if (++s == S) {
+                s = 0;
+                if (++nb == NBg) {
+                    nb = 0;
+                    ++ci;
+                }
+            }
+        } else if (--nb < 0) {
+            nb = NBd - 1;
+            --ci;
+        }
+    }
+};
+
+// sx holds up to tok_rows staged rows of the gate_up width; one partial-sum buffer (a second
+// one, letting warps start the next item before the slowest has read this item's sums, made
+// every size slower: 321 vs 315 us at 32 tokens, 714 vs 699 us at 256)
+__host__ __device__ __forceinline__ size_t gv_fused_fixed_bytes(int H, int tok_rows)
+{
+    return gv_sx_bytes(tok_rows, gv_row_pitch((H + 255) / 256)) +
+           kGvConsumers * 32 * kGvTok * 4 + kGvScales * 4 + 2 * kGvMaxSlots * 8 + 16;
+}
+
+__global__ void __launch_bounds__(kGvFusedThreads, 1)
+    gemv_w4a16_fused_kernel(GvFusedArgs f, int list_cap, int slots)
+{
+    extern __shared__ __align__(128) uint8_t gv_smem[];
+    const GemmArgs& gu = f.gu;
+    const GemmArgs& dn = f.dn;
+    const int KBg = (gu.K + 255) / 256, NBg = gu.N / 128;
+    const int KBd = (dn.K + 255) / 256, NBd = dn.N / 128;
+    const int pg = gv_row_pitch(KBg), pd = gv_row_pitch(KBd);
+    const GvSmem m = gv_carve(gv_smem, gv_sx_bytes(f.tok_rows, pg), 1, slots);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < slots; ++i) {
+            mbar_init(&m.full[i], 1);
+            mbar_init(&m.empty[i], kGvConsumers);  // every consumer warp reads every blob
+        }
+        *m.abort_flag = 0;
+        *m.zero = 0;
+        *m.done = 0;
+        fence_barrier_init();
+    }
+    // the group counts and the rows' pairs come from the predecessor (the grouping kernel)
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
+    if (warp == 0) gv_build_list(gu, m, list_cap, reinterpret_cast<int*>(m.red));
+    __syncthreads();
+    const int n = *m.n;
+    // parts per gate_up tile (uniform over the grid: it depends on n only); the down stager
+    // forms a split chunk's rows in the partial-sum buffer (16 KB)
+    int S = 1;
+    const bool rows_fit = (int64_t)f.tok_rows * dn.K * 2 <= kGvConsumers * 32 * kGvTok * 4;
+    while (rows_fit && 2 * S <= kGvMaxSplit && KBg % (2 * S) == 0 &&
+           (int64_t)n * NBg * 2 * S <= min(6LL * gridDim.x, (long long)kGvSplitItems))
+        S *= 2;
+    const int nkg = KBg / S;
+    const int64_t Ngu = (int64_t)n * NBg * S, Ndn = (int64_t)n * NBd;
+    const int64_t b = blockIdx.x, P = gridDim.x;
+    const int u0 = (int)(b * Ngu / P), nu = (int)((b + 1) * Ngu / P) - u0;
+    const int d0 = (int)(b * Ndn / P), d1 = (int)((b + 1) * Ndn / P), nd = d1 - d0;
+    GvCursor cur;
+    cur.init(u0, nu, d1, S, NBg, NBd);
+
+    if (warp == kGvConsumers + 1) {
+        // signal warp: as the consumers finish gate_up items, adds them to their chunks'
+        // ready words (runs of one chunk in one add).  Bounded: it gives up when the
+        // consumers stop (abort) or finish no item for the wait limit.
+        if (lane == 0) {
+            int j = 0;  // gate_up items published; cur is item j
+            uint64_t t0 = globaltimer();
+            while (j < nu) {
+                const int dn_ = *m.done;
+                if (dn_ > j) {
+                    __threadfence_block();
+                    while (j < dn_) {
+                        const int ci = cur.ci;
+                        int cnt = 0;
+                        for (; j < dn_ && cur.isg && cur.ci == ci; ++j, ++cnt) cur.next();
+                        red_release_gpu(f.ready + ci, cnt);
+                    }
+                    t0 = globaltimer();
+                } else {
+                    if (*m.abort_flag) break;
+                    if (globaltimer() - t0 > kWaitLimitNs) {
+                        set_status(gu.status, MOE_DEV_WAIT_TIMEOUT);
+                        *m.abort_flag = 1;
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+            }
+        }
+        return;
+    }
+    if (warp == kGvConsumers) {
+        // copy warp: the blobs of the block's gate_up run, then of its down run
+        if (lane == 0) {
+            const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
+            uint32_t c = 0;
+            int sl = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int it = 0; it < nu + nd && ok; ++it, cur.next()) {
+                const int ci = cur.ci, nb = cur.nb, s = cur.s;
+                const bool isg = cur.isg;
+                const int g = m.list[ci] >> 16;
+                const uint64_t pol = g == gu.G - 1 ? pol_keep : pol_stream;
+                const uint8_t* src =
+                    isg ? gu.b_tiles + ((size_t)(g * NBg + nb) * KBg + (size_t)s * nkg) * kNvf4TileBytes
+                        : dn.b_tiles + (size_t)(g * NBd + nb) * KBd * kNvf4TileBytes;
+                const int nkb = isg ? nkg : KBd;
+                for (int kb = 0; kb < nkb; ++kb, ++c) {
+                    if (!mbar_wait(&m.empty[sl], ph ^ 1u, m.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&m.full[sl], kNvf4TileBytes);
+                    bulk_load(m.ring + (size_t)sl * kNvf4TileBytes, src + (size_t)kb * kNvf4TileBytes,
+                              kNvf4TileBytes, &m.full[sl], pol);
+                    if (++sl == slots) {
+                        sl = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                set_status(gu.status, MOE_DEV_WAIT_TIMEOUT);
+                *m.abort_flag = 1;
+            }
+            for (uint32_t j = c > (uint32_t)slots ? c - slots : 0; j < c; ++j)
+                mbar_wait(&m.full[j % slots], (j / slots) & 1u, m.zero);
+        }
+        return;
+    }
+
+    const int my_u = warp % kGvUnits, my_ks = warp / kGvUnits;
+    const int g8 = lane >> 2, c4 = lane & 3;
+    const int xr = min(g8, f.tok_rows - 1);  // the B-fragment row (rows past tok_rows repeat)
+    const float gs = f16_prescale(f.amax);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && f.gs_out) *f.gs_out = gs;
+    bool ok = true;
+    int staged = -1;  // 2 chunk + (1 for down) of the rows in sx
+    int nt = 0;
+    int64_t row0 = 0;
+    int sl = 0;
+    uint32_t ph = 0;
+    for (int it = 0; it < nu + nd; ++it, cur.next()) {
+        const int ci = cur.ci, nb = cur.nb, s = cur.s;
+        const bool isg = cur.isg;
+        const int key = 2 * ci + (isg ? 0 : 1);
+        if (key != staged) {
+            const int e = m.list[ci];
+            const int t0 = e & 0xFFFF, g = e >> 16;
+            nt = min(kGvTok, gu.counts[g] - t0);
+            if (nt > f.tok_rows) {  // more rows in a group than the batch has tokens
+                if (threadIdx.x == 0) set_status(gu.status, MOE_DEV_ROWS_OVERFLOW);
+                nt = f.tok_rows;
+            }
+            row0 = (int64_t)gu.offsets[g] + t0;
+            gv_consumer_sync();  // the previous chunk's readers of sx and the scales are done
+            if (!isg) {
+                // the chunk's intermediate rows: all NBg gate_up tiles (all their S parts)
+                if (threadIdx.x == 0 && !*m.abort_flag &&
+                    !gv_wait_count(f.ready + ci, NBg * S, m.abort_flag)) {
+                    set_status(dn.status, MOE_DEV_WAIT_TIMEOUT);
+                    *m.abort_flag = 1;
+                }
+                gv_consumer_sync();
+                if (*m.abort_flag) ok = false;
+                if (S == 1) {
+                    gv_stage_chunk<false, kGvSrcRowsL2>(dn, m, gu.out_bf16, row0, nt, g, dn.K,
+                                                        KBd, pd);
+                } else {
+                    uint16_t* rows = reinterpret_cast<uint16_t*>(m.red);
+                    gv_split_rows(f.part, ci, NBg, S, nt, dn.K,
+                                  __frcp_rn(__fmul_rn(gs, gu.gs_w[g])), rows);
+                    gv_consumer_sync();
+                    gv_stage_chunk<false, kGvSrcSmem>(dn, m, rows, row0, nt, g, dn.K, KBd, pd);
+                }
+            } else {
+                gv_stage_chunk<true, kGvSrcTokens>(gu, m, f.x, row0, nt, g, gu.K, KBg, pg, f.T,
+                                                   f.k, gs);
+            }
+            staged = key;
+        } else {
+            gv_consumer_sync();  // the previous item's readers of red are done
+        }
+        float d[2][2][4] = {};
+        const int nkb = isg ? nkg : KBd;
+        const uint8_t* xs = m.sx + xr * (isg ? pg : pd) + 2 * (64 * my_ks + 16 * c4) +
+                            512 * (isg ? s * nkg : 0);
+        for (int kb = 0; kb < nkb; ++kb) {
+            if (ok && !gv_all_wait(&m.full[sl], ph, m.abort_flag)) {
+                ok = false;
+                if (lane == 0) {
+                    set_status(gu.status, MOE_DEV_WAIT_TIMEOUT);
+                    *m.abort_flag = 1;
+                }
+            }
+            if (ok) {
+                GvFrag fr;
+                gv_load(fr, m.ring + (size_t)sl * kNvf4TileBytes, 32 * my_u, my_ks, lane);
+                gv_kstep(fr, xs + 512 * kb, lane, d);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&m.empty[sl]);
+            }
+            if (++sl == slots) {
+                sl = 0;
+                ph ^= 1u;
+            }
+        }
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) d[0][mb][r] += d[1][mb][r];
+        float* redb = m.red;
+        float* rw = redb + warp * 32 * kGvTok;
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                *reinterpret_cast<float2*>(rw + (16 * mb + 8 * hh + g8) * kGvTok + 2 * c4) =
+                    make_float2(d[0][mb][2 * hh], d[0][mb][2 * hh + 1]);
+        gv_consumer_sync();
+        if (!isg) {
+            if (ok) gv_epilogue<false>(dn, m, redb, row0, nt, nb);
+        } else if (S == 1) {
+            if (ok) gv_epilogue<true>(gu, m, redb, row0, nt, nb);
+            gv_item_done(m, it);
+        } else {
+            // this part's sums over its k range -> part[tile][s][token][row]; the down stagers
+            // of the chunk add the parts
+            float* mine = f.part + ((size_t)(ci * NBg + nb) * S + s) * (128 * kGvTok);
+            for (int o = threadIdx.x; o < 128 * nt; o += kGvConsumers * 32) {
+                const int t = o / 128, row = o % 128, u = row / 32, ri = row % 32;
+                float v = 0.0f;
+#pragma unroll
+                for (int q = 0; q < kGvKsteps; ++q)
+                    v += redb[((q * kGvUnits + u) * 32 + ri) * kGvTok + t];
+                mine[o] = v;
+            }
+            gv_item_done(m, it);
+        }
+    }
+}
+
+size_t gemv_w4a16_fused_smem(int H, int tok_rows, int slots, int list_cap)
+{
+    return (size_t)slots * kNvf4TileBytes + gv_fused_fixed_bytes(H, tok_rows) +
+           4 * (size_t)list_cap;
+}
+
+// At most 6 blobs in flight per block: with one token (where shared memory would allow 12)
+// the deeper ring was slower (46.6 vs 45.2 us a forward; 8 tokens: 123.5 vs 123.1 us), as
+// its first burst of requests delays every block's first blob; 32 and 256 tokens, where at
+// most 7-8 fit, ran the same at 6.
+constexpr int kGvFusedMaxSlots = 6;
+
+int gemv_w4a16_fused_slots(int H, int tok_rows, int list_cap)
+{
+    const size_t fixed = gv_fused_fixed_bytes(H, tok_rows) + 4 * (size_t)list_cap;
+    if (fixed >= (size_t)kSmemLimit) return 0;
+    return (int)std::min<size_t>(kGvFusedMaxSlots, ((size_t)kSmemLimit - fixed) / kNvf4TileBytes);
+}
+
+FusedGemvKernel gemv_w4a16_fused_kernel_ptr() { return gemv_w4a16_fused_kernel; }
 
 GemvKernel gemv_w4a16_kernel_for(bool gateup)
 {

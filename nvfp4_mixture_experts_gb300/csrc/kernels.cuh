@@ -36,6 +36,19 @@ __device__ __forceinline__ bool pair_ok(int pair, uint32_t* status)
     return true;
 }
 
+// W4A16 activation rows: x (bf16) times the power of two gs = 2^(141 - exponent field of
+// amax(x)), clamped to 2^[-126, 127], rounded to fp16.  amax <= 2^(e - 126) for exponent
+// field e, so |x * gs| <= 2^15 < 65504 and every bf16 value x with |x * gs| >= 2^-14 (all but
+// values below amax * 2^-29) converts exactly; the GEMM divides by gs in its epilogue.
+__device__ __forceinline__ float f16_prescale(const uint32_t* amax_bits)
+{
+    const uint32_t bits = *amax_bits;
+    if (bits == 0u) return 1.0f;
+    const int e = (int)((bits >> 23) & 0xFFu);
+    const int p = min(127, max(-126, 141 - e));
+    return __uint_as_float((uint32_t)(p + 127) << 23);
+}
+
 // silu(g) * u in fp32: g / (1 + exp(-g)) * u, each step an IEEE fp32 operation.
 __device__ __forceinline__ float silu_mul(float g, float u)
 {
@@ -56,7 +69,8 @@ __host__ __device__ int topk_tokens_per_block(int nsplit);
 size_t topk_smem(int nsplit, int E);
 constexpr int kTopkThreads = 512;
 using TopkKernel = void (*)(const float*, int, const float*, int, int, int, int32_t*, float*,
-                            float*, uint32_t*, uint32_t*, const uint16_t*, int, uint32_t*);
+                            float*, uint32_t*, uint32_t*, const uint16_t*, int, uint32_t*,
+                            int32_t*, int);
 // the top-k kernel instantiated for E experts (E <= kMaxExperts)
 TopkKernel topk_kernel_for(int E);
 __global__ void perm_hist_kernel(const int32_t* ids, int P, int E, int off, int El,
@@ -276,5 +290,29 @@ using GemvKernel = void (*)(GemmArgs, const uint16_t*, int, int);
 GemvKernel gemv_w4a16_kernel_for(bool gateup);
 size_t gemv_w4a16_smem(int K, int slots, int list_cap);
 int gemv_w4a16_slots(int K, int list_cap);
+
+// The forward's gate_up and down GEMVs in one launch (gemv_w4a16.cu: items of both, a down
+// chunk waiting for its gate_up tiles; activation rows taken from the layer input).  With few
+// gate_up items each tile's contraction is cut into up to kGvMaxSplit parts, whose partial
+// sums (kGvSplitItems parts at most) meet in `part`.  ready ([list_cap]) is zero at launch.
+constexpr int kGvMaxSplit = 4;
+constexpr int kGvFusedThreads = kGvThreads + 32;  // + the signal warp
+constexpr int kGvSplitItems = 1024;
+struct GvFusedArgs {
+    GemmArgs gu;           // gate_up: W13 blobs, gs_w, counts/offsets/G, perm_src, Tk, status,
+                           // out_bf16 = the intermediate rows [rows][I]
+    GemmArgs dn;           // down: W2 blobs, gs_w, perm_src, topk_w, Tk, out_f32 = y [rows][H]
+    const uint16_t* x;     // the layer input [T][H], bf16
+    const uint32_t* amax;  // fp32 bits of max |x|
+    float* gs_out;         // receives the prescale gs (the forward's record of gs_a)
+    int T, k;
+    int tok_rows;          // rows of a chunk at most: min(kGvChunk, T)
+    int32_t* ready;        // [list_cap] gate_up tiles (or tile parts) stored per chunk
+    float* part;           // [kGvSplitItems][kGvChunk tokens][128 rows] partial sums
+};
+using FusedGemvKernel = void (*)(GvFusedArgs, int, int);
+FusedGemvKernel gemv_w4a16_fused_kernel_ptr();
+size_t gemv_w4a16_fused_smem(int H, int tok_rows, int slots, int list_cap);
+int gemv_w4a16_fused_slots(int H, int tok_rows, int list_cap);
 
 }  // namespace moe

@@ -156,20 +156,8 @@ GatherKernel gather_quant_kernel_for(int blocks_per_lane)
     return blocks_per_lane == 4 ? gather_quant_kernel<4> : gather_quant_kernel<1>;
 }
 
-// W4A16: copy token rows (bf16) to the padded rows of their pairs and shared row; a warp
-// copies 256 elements of one token.
-// W4A16 activation rows: x (bf16) times the power of two gs = 2^(141 - exponent field of
-// amax(x)), clamped to 2^[-126, 127], rounded to fp16.  amax <= 2^(e - 126) for exponent
-// field e, so |x * gs| <= 2^15 < 65504 and every bf16 value x with |x * gs| >= 2^-14 (all but
-// values below amax * 2^-29) converts exactly; the GEMM divides by gs in its epilogue.
-__device__ __forceinline__ float f16_prescale(const uint32_t* amax_bits)
-{
-    const int e = (int)((*amax_bits >> 23) & 0xFFu);
-    if (*amax_bits == 0u) return 1.0f;
-    const int p = min(127, max(-126, 141 - e));
-    return __uint_as_float((uint32_t)(p + 127) << 23);
-}
-
+// W4A16: copy token rows (bf16) times the prescale (f16_prescale), as fp16, to the padded
+// rows of their pairs and shared row; a warp copies 256 elements of one token.
 __global__ void __launch_bounds__(256) gather_f16_kernel(
     const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, int shared_group, int add_shared,

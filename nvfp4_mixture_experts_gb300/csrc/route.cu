@@ -208,7 +208,8 @@ __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(
     const float* __restrict__ logits_src, int nsplit, const float* __restrict__ bias, int T,
     int E, int k, int32_t* __restrict__ ids, float* __restrict__ wts,
     float* __restrict__ logits_out, uint32_t* clear0, uint32_t* clear1,
-    const uint16_t* __restrict__ x_amax, int H, uint32_t* amax_out)
+    const uint16_t* __restrict__ x_amax, int H, uint32_t* amax_out, int32_t* zero_words,
+    int nzero)
 {
     extern __shared__ float s_part[];  // [nsplit][tokens of this block][E]
     __shared__ float s_xm[kTopkWarps];
@@ -247,6 +248,9 @@ __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(
             if (clear1) clear1[0] = clear1[1] = 0u;  // both amax accumulators
         }
     }
+    // counters a later kernel of the forward starts from zero (the fused W4A16 GEMV's)
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero_words[i] = 0;
     const int per = nt * E;  // floats of this block in one plane
     uint32_t dyn_smem;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_smem));

@@ -204,6 +204,27 @@ def test_w4a16_decode_sweep(big_layer, T):
     _check(got[tok], ora.out, "w4a16 T=%d" % T)
 
 
+@pytest.mark.parametrize("T", [1, 3])
+def test_w4a16_small_batch_forward_is_deterministic(big_layer, T):
+    """Small W4A16 batches run gate_up and down in one GEMV launch that cuts each gate_up
+    tile's contraction into parts when there are few tiles (one token: 180 tiles on the
+    SMs); the part that arrives last adds all parts' sums in k order, so the result does not
+    depend on which part came last: repeated forwards give the same bits (and the oracle's
+    result within the bar)."""
+    c = synth.CONFIGS["w4a16"]
+    H, I, E, k = c["H"], c["I"], c["E"], c["k"]
+    wr = synth.router_weight(0, E, H)
+    x = synth.activations(5, T, H)
+    lg = synth.logits_normal(5, T, E)
+    h = make_layer(big_layer, wr, H, I, E, k, act_mode=moe.MOE_W4A16, max_tokens=T)
+    first = _forward(h, x, T, logits_in=lg)
+    for _ in range(4):
+        assert np.array_equal(_forward(h, x, T, logits_in=lg), first)
+    ora = oracle.moe_forward(oracle.make_cfg(T, H, I, E, k, act_mode=2), x, big_layer,
+                             logits_in=lg)
+    _check(first, ora.out, "w4a16 T=%d repeated" % T)
+
+
 # W4A16 at up to 256 tokens (and at most 16 expected rows per expert: T*k/E <= 16) runs on
 # the grouped GEMV, otherwise on the tensor-core kernel; here E=24 (or 8 local), k=4.
 # H = 384 and I = 320 leave the last 256-element k-block of each GEMM partly empty; the
