@@ -651,8 +651,11 @@ int fused_gemv_slots(const moe_layer* h, const Plan& p)
 // The fused W4A16 GEMV: activation rows from x (prescaled by max |x| in the workspace), the
 // intermediate into i_bf16, the weighted expert outputs into y (fp32 rows).  The ready counts
 // (gv_sync) were zeroed by the routing kernel of the same forward.
+// one_block_pred: the kernel before it is the one-block grouping kernel; the grid then leaves
+// one SM free for it, so that no block of this launch starts after it (one token: 41.3 vs
+// 42.4 us a forward; with more blocks before it, all SMs: 256 tokens 702 vs 704 us).
 moe_status launch_gemv_fused(const moe_layer* h, const Plan& p, const void* x, void* ws,
-                             int slots, bool pdl, cudaStream_t s)
+                             int slots, bool one_block_pred, bool pdl, cudaStream_t s)
 {
     const moe_config& c = h->cfg;
     GvFusedArgs f;
@@ -678,6 +681,10 @@ moe_status launch_gemv_fused(const moe_layer* h, const Plan& p, const void* x, v
     f.dn.epilogue = kEpiDown;
     f.dn.out_f32 = at<float>(ws, p.y);
     f.dn.topk_w = at<float>(ws, p.w);
+    f.ids = at<int32_t>(ws, p.ids);
+    f.E = c.num_experts;
+    f.off = c.local_expert_offset;
+    f.shared_rows = shared_rows(h, p.T);
     f.x = static_cast<const uint16_t*>(x);
     f.amax = at<uint32_t>(ws, p.amax);
     f.gs_out = at<float>(ws, p.gs_a);
@@ -688,7 +695,8 @@ moe_status launch_gemv_fused(const moe_layer* h, const Plan& p, const void* x, v
     f.part = at<float>(ws, p.gv_part);
     const int64_t items =
         (int64_t)p.gv_list_cap * ((2 * c.inter / 128) * kGvMaxSplit + c.hidden / 128);
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(h->num_sms, items));
+    const int sms = one_block_pred && h->num_sms > 1 ? h->num_sms - 1 : h->num_sms;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, items));
     return launch(gemv_w4a16_fused_kernel_ptr(), dim3(grid), dim3(kGvFusedThreads),
                   gemv_w4a16_fused_smem(c.hidden, f.tok_rows, slots, p.gv_list_cap), s, pdl, f,
                   p.gv_list_cap, slots);
@@ -1259,7 +1267,9 @@ moe_status moe_forward(moe_handle h, const void* x_bf16_d, const float* logits_i
         r = launch_permute(h, p, ids, T, counts, offsets, perm_src, inv, ws, true, s, false);
     if (fused_slots) {
         if (r == MOE_OK && !amax_done) r = launch_amax(h, x_bf16_d, T, amax, true, s);
-        if (r == MOE_OK) r = launch_gemv_fused(h, p, x_bf16_d, ws, fused_slots, true, s);
+        if (r == MOE_OK)
+            r = launch_gemv_fused(h, p, x_bf16_d, ws, fused_slots, p.nblk == 1 && amax_done,
+                                  true, s);
         if (r == MOE_OK) r = launch_combine(h, y, inv, offsets, T, out_bf16_d, true, s, status);
         return r;
     }

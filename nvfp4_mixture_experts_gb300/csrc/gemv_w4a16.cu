@@ -237,28 +237,17 @@ __device__ __forceinline__ GvSmem gv_carve(uint8_t* base, size_t sx_bytes, int n
 }
 
 // The work list: the chunks of up to kGvTok rows of the non-empty groups, in group order,
-// each (group << 16) | first row; *m.n = their number.  Called by warp 0.  Each lane takes a
-// contiguous range of groups and loads their counts 16 at a time (one load latency for up to
-// 512 groups) into tmp, then a warp scan places the lanes' chunks.
-__device__ __forceinline__ void gv_build_list(const GemmArgs& a, const GvSmem& m, int list_cap,
-                                              int* tmp)
+// each (group << 16) | first row; *m.n = their number.  Called by warp 0 with the G group
+// counts in tmp (shared memory): each lane takes a contiguous range of groups, then a warp
+// scan places the lanes' chunks.
+__device__ __forceinline__ void gv_list_from_counts(const GemmArgs& a, const GvSmem& m,
+                                                    int list_cap, const int* tmp)
 {
     const int lane = threadIdx.x & 31;
     const int per = (a.G + 31) / 32;
     const int gb = lane * per, ge = min(a.G, gb + per);
     int nc = 0;  // chunks of this lane's groups
-    for (int g0 = gb; g0 < ge; g0 += 16) {
-        int c[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) c[j] = g0 + j < ge ? a.counts[g0 + j] : 0;
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            if (g0 + j < ge) {
-                c[j] = max(c[j], 0);
-                tmp[g0 + j] = c[j];
-                nc += (c[j] + kGvTok - 1) / kGvTok;
-            }
-    }
+    for (int g = gb; g < ge; ++g) nc += (tmp[g] + kGvTok - 1) / kGvTok;
     int incl = nc;  // inclusive scan of the chunk counts over the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -274,6 +263,54 @@ __device__ __forceinline__ void gv_build_list(const GemmArgs& a, const GvSmem& m
         if (n > list_cap) set_status(a.status, MOE_DEV_ROWS_OVERFLOW);
         *m.n = min(n, list_cap);
     }
+}
+
+// gv_list_from_counts from the grouping's counts (a.counts), loaded 16 per lane at a time
+// (one load latency for up to 512 groups).
+__device__ __forceinline__ void gv_build_list(const GemmArgs& a, const GvSmem& m, int list_cap,
+                                              int* tmp)
+{
+    const int lane = threadIdx.x & 31;
+    const int per = (a.G + 31) / 32;
+    const int gb = lane * per, ge = min(a.G, gb + per);
+    for (int g0 = gb; g0 < ge; g0 += 16) {
+        int c[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) c[j] = g0 + j < ge ? a.counts[g0 + j] : 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (g0 + j < ge) tmp[g0 + j] = max(c[j], 0);
+    }
+    __syncwarp();
+    gv_list_from_counts(a, m, list_cap, tmp);
+}
+
+// The same list from the top-k ids (P <= 32 * kGvIdsLanePairs pairs): the counts the grouping
+// kernel forms from them (an id outside [0, E) or outside the shard's experts off .. off +
+// G - 2 has no row; the shared group, the last, has shared_rows), so the list needs nothing
+// the grouping writes.
+constexpr int kGvIdsLanePairs = 2;
+__device__ __forceinline__ void gv_build_list_ids(const GemmArgs& a, const GvSmem& m,
+                                                  int list_cap, int* tmp, const int32_t* ids,
+                                                  int P, int E, int off, int shared_rows)
+{
+    const int lane = threadIdx.x & 31;
+    const int El = a.G - 1;
+    int id[kGvIdsLanePairs];
+#pragma unroll
+    for (int j = 0; j < kGvIdsLanePairs; ++j) {
+        const int i = 32 * j + lane;
+        id[j] = i < P ? ids[i] : -1;
+    }
+    for (int g = lane; g < a.G; g += 32) tmp[g] = g < El ? 0 : shared_rows;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kGvIdsLanePairs; ++j) {
+        const int le = id[j] - off;
+        if (id[j] >= 0 && id[j] < E && le >= 0 && le < El) atomicAdd(&tmp[le], 1);
+    }
+    __syncwarp();
+    gv_list_from_counts(a, m, list_cap, tmp);
 }
 
 // bf16 pair -> two floats times `up`, rounded to an fp16 pair.
@@ -790,10 +827,21 @@ __global__ void __launch_bounds__(kGvFusedThreads, 1)
         *m.done = 0;
         fence_barrier_init();
     }
-    // the group counts and the rows' pairs come from the predecessor (the grouping kernel)
-    pdl_wait();
-    if (threadIdx.x == 0) pdl_trigger();
-    if (warp == 0) gv_build_list(gu, m, list_cap, reinterpret_cast<int*>(m.red));
+    // The work list.  The group counts and the rows' pairs come from the predecessor (the
+    // grouping kernel); with few pairs the list is formed from the top-k ids instead, which
+    // the kernel before the predecessor wrote (complete when this kernel starts), so the copy
+    // warp streams weights while the grouping kernel runs.  The consumers wait (pdl_wait)
+    // before they read its output.
+    const int npairs = f.T * f.k;
+    const bool list_from_ids = npairs <= 32 * kGvIdsLanePairs;
+    if (!list_from_ids) pdl_wait();
+    if (warp == 0) {
+        if (list_from_ids)
+            gv_build_list_ids(gu, m, list_cap, reinterpret_cast<int*>(m.red), f.ids, npairs,
+                              f.E, f.off, f.shared_rows);
+        else
+            gv_build_list(gu, m, list_cap, reinterpret_cast<int*>(m.red));
+    }
     __syncthreads();
     const int n = *m.n;
     // parts per gate_up tile (uniform over the grid: it depends on n only); the down stager
@@ -883,6 +931,8 @@ __global__ void __launch_bounds__(kGvFusedThreads, 1)
         return;
     }
 
+    if (list_from_ids) pdl_wait();
+    if (threadIdx.x == 0) pdl_trigger();
     const int my_u = warp % kGvUnits, my_ks = warp / kGvUnits;
     const int g8 = lane >> 2, c4 = lane & 3;
     const int xr = min(g8, f.tok_rows - 1);  // the B-fragment row (rows past tok_rows repeat)

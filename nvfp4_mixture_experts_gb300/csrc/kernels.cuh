@@ -302,6 +302,9 @@ struct GvFusedArgs {
     GemmArgs gu;           // gate_up: W13 blobs, gs_w, counts/offsets/G, perm_src, Tk, status,
                            // out_bf16 = the intermediate rows [rows][I]
     GemmArgs dn;           // down: W2 blobs, gs_w, perm_src, topk_w, Tk, out_f32 = y [rows][H]
+    const int32_t* ids;    // the top-k ids [T][k] (the work list is formed from them)
+    int E, off;            // experts, and the shard's first expert
+    int shared_rows;       // rows of the shared group (T, or 0)
     const uint16_t* x;     // the layer input [T][H], bf16
     const uint32_t* amax;  // fp32 bits of max |x|
     float* gs_out;         // receives the prescale gs (the forward's record of gs_a)

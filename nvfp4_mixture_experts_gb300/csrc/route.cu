@@ -566,8 +566,9 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(
     extern __shared__ uint16_t s_wtab[];  // [32][G]: pairs of group g in warp w, then prefix
     const int G = El + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nw = (P + 31) / 32;  // warps that hold pairs: only their rows of the table
     for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = g < El ? 0 : shared_rows;
-    for (int x = threadIdx.x; x < 32 * G; x += blockDim.x) s_wtab[x] = 0;
+    for (int x = threadIdx.x; x < nw * G; x += blockDim.x) s_wtab[x] = 0;
     __syncthreads();
     // local expert of pair i (-1: dropped), per-expert counts, per-warp counts and ranks
     const int i = threadIdx.x;
@@ -606,7 +607,7 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(
     // per group: exclusive prefix of its per-warp counts over the warps
     if (threadIdx.x < G) {
         int run = 0;
-        for (int w = 0; w < 32; ++w) {
+        for (int w = 0; w < nw; ++w) {
             const int c = s_wtab[w * G + threadIdx.x];
             s_wtab[w * G + threadIdx.x] = (uint16_t)run;
             run += c;
