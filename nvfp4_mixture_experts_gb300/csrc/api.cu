@@ -198,6 +198,30 @@ moe_status launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cu
 }
 
 // As launch, for a kernel whose blocks run as clusters of two (CTA pairs).
+// A launch whose blocks wait on one another (the fused W4A16 GEMV's down items wait for gate_up
+// tiles of other blocks): cooperative, so that every block is resident at once or the launch
+// fails.
+template <typename... KArgs, typename... Args>
+moe_status launch_coop(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, bool pdl, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}
+
 template <typename... KArgs, typename... Args>
 moe_status launch_pairs(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                         bool pdl, Args... args)
@@ -697,7 +721,7 @@ moe_status launch_gemv_fused(const moe_layer* h, const Plan& p, const void* x, v
         (int64_t)p.gv_list_cap * ((2 * c.inter / 128) * kGvMaxSplit + c.hidden / 128);
     const int sms = one_block_pred && h->num_sms > 1 ? h->num_sms - 1 : h->num_sms;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, items));
-    return launch(gemv_w4a16_fused_kernel_ptr(), dim3(grid), dim3(kGvFusedThreads),
+    return launch_coop(gemv_w4a16_fused_kernel_ptr(), dim3(grid), dim3(kGvFusedThreads),
                   gemv_w4a16_fused_smem(c.hidden, f.tok_rows, slots, p.gv_list_cap), s, pdl, f,
                   p.gv_list_cap, slots);
 }

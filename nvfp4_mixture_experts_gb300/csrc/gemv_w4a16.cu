@@ -685,12 +685,11 @@ __global__ void __launch_bounds__(kGvThreads, 1)
 //
 // Items: gate_up (chunk, tile, part), then down (chunk, tile), each list split evenly over the
 // blocks in contiguous runs; a block takes its gate_up run, then its down run backwards
-// (GvCursor).  Warps: 16
-// consumers, a copy warp, and a signal warp that publishes the finished gate_up items (a
-// release add waits for the stores to land; the consumers go on meanwhile).  Every block
-// is resident at once (one block per SM, grid <= SMs), so every wait ends; each wait is
-// bounded all the same, and one that runs out sets MOE_DEV_WAIT_TIMEOUT and stops the
-// block's work.  The ready words are zeroed before the launch by the routing kernel.
+// (GvCursor).  Warps: 16 consumers, a copy warp, and a signal warp that publishes the
+// finished gate_up items (a release add waits for the stores to land; the consumers go on
+// meanwhile).  The launch is cooperative, so every block is resident at once (one block per
+// SM, grid <= SMs) and every wait ends; each wait is bounded all the same, and one that runs
+// out sets MOE_DEV_WAIT_TIMEOUT and stops the block's work.  The ready words are zeroed before the launch by the routing kernel.
 __device__ __forceinline__ bool gv_wait_count(const int32_t* p, int target, volatile int* abort)
 {
     if (ld_acquire_gpu(p) >= target) return true;
