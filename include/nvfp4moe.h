@@ -327,6 +327,9 @@ MOE_API moe_status moe_combine(moe_handle h, const float* y_d, const int32_t* in
 /* The whole layer: route, permute, gather-quantise, gate_up (fused SwiGLU+requant),
  * down, combine.  logits_in_d (nullable): given router logits [T][E] instead of x.Wr^T;
  * logit_bias_d (nullable) [E].  out_bf16_d [T][H] receives this shard's partial sum.
+ * W4A16 batches of up to 256 tokens run gate_up and down as one cooperative launch that
+ * forms the fp16 activation rows from x itself (no gather launch); the results are those
+ * of the staged calls up to the fp32 summation order of the expert rows.
  * Unlike the staged calls, the W4A4 modes keep the weighted expert rows between down and
  * combine as fp16 values of y x 2^e (e per local expert, from a bound on |y| that rules out
  * overflow; see moe_forward_buffers), each with 11 significant bits; the combine multiplies
@@ -357,7 +360,10 @@ MOE_API size_t moe_workspace_size_host(const moe_config* cfg, int32_t T);
 
 /* Where moe_forward keeps its intermediates inside the workspace (device pointers into
  * ws_d), so callers can inspect them after a forward.  Any pointer may be NULL.  Unlike
- * moe_permute's, the forward's perm_src leaves padding rows unmarked (stale).  inter_gs:
+ * moe_permute's, the forward's perm_src leaves padding rows unmarked (stale).  W4A16
+ * forwards of up to 256 tokens write no a_bf16 rows (the fused GEMV forms them while
+ * staging), and with one or a few tokens, where it splits each gate_up tile's contraction,
+ * no inter_bf16 rows either.  inter_gs:
  * the dynamic intermediate scale of the last forward (set only in that mode).  y: the
  * weighted expert outputs by padded row -- fp32 in W4A16 mode; in the W4A4 modes fp16 rows
  * of y x 2^e (e per local expert, chosen from a bound on |y| so that no value overflows)
