@@ -125,17 +125,27 @@ __global__ void __launch_bounds__(192, 1) router_gemm_kernel(
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok && !flags[0]) {
             tc_fence_after();
-            const int t = m0 + q * 32 + lane;
-            float* dst = part + ((size_t)blockIdx.z * T + t) * E + n0;
+            // each 32 x 32 piece (a lane per token) goes through shared memory, so that the
+            // stores run along the rows (a lane per expert: 128 bytes a store) instead of one
+            // 4-byte store per row.  The pipeline stages are free once acc completed (every
+            // load they received was consumed by an MMA the commit covers).
+            float* pc = reinterpret_cast<float*>(st) + (warp - 2) * 32 * 33;
+            const int t0 = m0 + q * 32;
+            float* dst = part + (size_t)blockIdx.z * T * E;
 #pragma unroll 1
             for (int c = 0; c < bn / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + 32 * c, r);
                 tmem_ld_wait();
-                if (t < T)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (n0 + 32 * c + i < E) dst[32 * c + i] = __uint_as_float(r[i]);
+                for (int i = 0; i < 32; ++i) pc[lane * 33 + i] = __uint_as_float(r[i]);
+                __syncwarp();
+                const int col = n0 + 32 * c + lane;
+                if (col < E)
+#pragma unroll 4
+                    for (int i = 0; i < 32 && t0 + i < T; ++i)
+                        dst[(size_t)(t0 + i) * E + col] = pc[i * 33 + lane];
+                __syncwarp();
             }
         } else if (lane == 0) {
             set_status(status, MOE_DEV_WAIT_TIMEOUT);

@@ -163,9 +163,10 @@ def test_topk_nan_logits_rank_below_every_number():
     assert np.max(np.abs(host(w) - rw)) <= 1e-6
 
 
-def test_router_logits_and_topk_from_x():
-    T, E, H, k = 200, 320, 4096, 8
-    h, wr = _tiny_layer_handle(E=E, H=H, k=k)
+@pytest.mark.parametrize("T", [200, 1100])  # 64-expert tiles; 160-expert tiles, ragged rows
+def test_router_logits_and_topk_from_x(T):
+    E, H, k = 320, 4096, 8
+    h, wr = _tiny_layer_handle(E=E, H=H, k=k, max_tokens=max(T, 256))
     x = synth.activations(6, T, H)
     ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
     w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
