@@ -671,10 +671,12 @@ __global__ void __launch_bounds__(kGvThreads, 1)
 // (each holds most of an SM's shared memory), then rebuild the work list and refill the ring,
 // all while the stream is idle.  Here each block's copy warp streams its gate_up blobs and
 // then its down blobs without a break, and a down item waits only for its own chunk: the
-// chunk's intermediate rows are complete when all N1 / 128 of its gate_up tiles have been
+// chunk's intermediate rows are complete when all 2I / 128 of its gate_up tiles have been
 // stored (ready[chunk] counts them: a block barrier after the stores, then one release add;
 // the reader polls with acquire loads).  The activation rows are taken from the layer input
-// directly (the gather kernel's fp16 rows x * gs, formed while staging).
+// directly (the gather kernel's fp16 rows x * gs, formed while staging).  With at most 64
+// pairs the work list is formed from the top-k ids before the dependency wait (they are two
+// launches back, so complete), and the weight stream starts while the grouping kernel runs.
 //
 // Few items: with one token the gate_up work is 9 chunks x 20 tiles = 180 items of 16 blobs
 // on 152 SMs, and the SMs with two set the pace.  So when there are few items the contraction
@@ -689,7 +691,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
 // finished gate_up items (a release add waits for the stores to land; the consumers go on
 // meanwhile).  The launch is cooperative, so every block is resident at once (one block per
 // SM, grid <= SMs) and every wait ends; each wait is bounded all the same, and one that runs
-// out sets MOE_DEV_WAIT_TIMEOUT and stops the block's work.  The ready words are zeroed before the launch by the routing kernel.
+// out sets MOE_DEV_WAIT_TIMEOUT and stops the block's work.  The ready words are zeroed
+// before the launch by the routing kernel.
 __device__ __forceinline__ bool gv_wait_count(const int32_t* p, int target, volatile int* abort)
 {
     if (ld_acquire_gpu(p) >= target) return true;
