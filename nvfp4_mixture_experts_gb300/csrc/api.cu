@@ -408,8 +408,13 @@ moe_status launch_route(const moe_layer* h, const void* x, const float* logits_i
         amax_out = nullptr;
     }
     if (amax_done) *amax_done = amax_out != nullptr;
+    // with given logits the top-k kernel is the first of the chain and reads the inputs (x,
+    // the logits) before its wait: it starts only when the work before it on the stream is
+    // complete (no programmatic launch), so an input written by a kernel that let its
+    // dependents start early (a chained forward's combine) is never read too soon
     return launch(topk_kernel_for(c.num_experts), dim3(ceil_div(T, topk_tokens_per_block(nsplit))),
-                  dim3(kTopkThreads), topk_smem(nsplit, c.num_experts), s, pdl, src, nsplit,
+                  dim3(kTopkThreads), topk_smem(nsplit, c.num_experts), s,
+                  pdl && !logits_in, src, nsplit,
                   bias, T, c.num_experts, c.top_k, ids, w, logits_out, clear0, clear1,
                   static_cast<const uint16_t*>(x), c.hidden, amax_out, zero_words, nzero);
 }

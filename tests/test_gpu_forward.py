@@ -204,6 +204,31 @@ def test_w4a16_decode_sweep(big_layer, T):
     _check(got[tok], ora.out, "w4a16 T=%d" % T)
 
 
+@pytest.mark.parametrize("act_mode", [0, moe.MOE_W4A16])
+def test_chained_forwards_read_complete_inputs(act_mode):
+    """Two forwards chained on one stream, the first one's output the second one's input,
+    with given logits and no synchronisation between them.  The second forward's first
+    kernel reads its input before its dependency wait, so it may start only when the first
+    forward (whose last kernel lets its dependents start early) is complete: the second
+    output equals the same forward run after a synchronisation, bit for bit."""
+    c = synth.CONFIGS["tiny"]
+    T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+    layer = build_layer(0, H, I, E)
+    wr = synth.router_weight(0, E, H)
+    h = make_layer(layer, wr, H, I, E, k, act_mode=act_mode, inter_gs=1024.0, max_tokens=T)
+    x = bits16(synth.activations(4, T, H))
+    lg = dev(synth.logits_normal(4, T, E))
+    for _ in range(3):
+        out1 = h.forward(x, logits_in=lg)
+        out2 = h.forward(out1, logits_in=lg)
+        torch.cuda.synchronize()
+        st, bits = moe.moe_get_status(h.handle, h.ws)
+        assert st == moe.MOE_OK, bits
+        ref = h.forward(out1.clone(), logits_in=lg)
+        torch.cuda.synchronize()
+        assert torch.equal(out2, ref)
+
+
 @pytest.mark.parametrize("T", [1, 3])
 def test_w4a16_small_batch_forward_is_deterministic(big_layer, T):
     """Small W4A16 batches run gate_up and down in one GEMV launch that cuts each gate_up
