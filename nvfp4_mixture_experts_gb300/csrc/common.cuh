@@ -284,13 +284,19 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
 }
 
 // 2-D tiled tensor store shared -> global (bulk-group completion).
+// The tensor stores are the down GEMMs' y rows: stored with the L2 evict-first policy, so that
+// a large y (a prefill chunk's 0.6 GB) is written back while the GEMM runs rather than under
+// the combine's reads (prefill forward 1.357 -> 1.344 ms; decode and the expert shard, whose
+// y stays in L2 either way, unchanged; evict-last: 1.357 -> 1.353 ms).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int32_t x,
                                              int32_t y)
 {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(m)),
-        "r"(smem_u32(src)), "r"(x), "r"(y)
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+        " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(m)),
+        "r"(smem_u32(src)), "r"(x), "r"(y), "l"(pol)
         : "memory");
 }
 
